@@ -1,0 +1,180 @@
+"""fp64 CPU oracle for row-wise normalization -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg
+(``cpu_baseline`` and ``--impl reference``) may import this package. The CUDA
+library and its Python binding never import it, and it imports nothing from
+them: the two share no code.
+
+The arithmetic lives in ``norm_oracle.c`` (plain single-threaded C, fp64, built
+with ``-ffp-contract=off``); this module only compiles it with gcc, widens the
+fp16 inputs to fp64 (exact) and marshals numpy arrays through ctypes. Every
+output is fp64 and unrounded.
+
+Sources for the formulas (page title, section):
+  * meTile, "Kernel coverage and training scope", "Exact native normalization
+    contract" -- RMSNorm, LayerNorm (centred population variance), fused
+    residual-add + RMSNorm (unrounded sum normalised; residual-output cotangent
+    added to both input gradients), backward at the saved statistics.
+  * tensorcore, "Training kernels", "RMSnorm -- Llama-style" (Math) and
+    "LayerNorm -- standard".
+
+Parity pins: tests/test_oracle_pins.py pins every function here against finite
+differences, closed forms, invariants, the worked LayerNorm example of the
+meTile contract and torch's fp64 CPU layer_norm / rms_norm with autograd.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "norm_oracle.c")
+BUILD_DIR = os.path.join(_HERE, "_build")
+LIB_PATH = os.path.join(BUILD_DIR, "liboracle.so")
+CFLAGS = ["-O2", "-std=c99", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
+
+_lock = threading.Lock()
+_lib = None
+
+_dp = ctypes.POINTER(ctypes.c_double)
+_i64 = ctypes.c_int64
+
+
+def compile_oracle(source: str = SOURCE, out: str = LIB_PATH) -> str:
+    """Compile the C oracle with gcc; return the path of the shared object."""
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    tmp = out + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", *CFLAGS, "-o", tmp, source, "-lm"], check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def _declare(lib):
+    lib.oracle_rmsnorm_forward.argtypes = [_dp, _dp, _dp, _dp, _i64, _i64, ctypes.c_double]
+    lib.oracle_rmsnorm_backward.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _dp, _i64, _i64]
+    lib.oracle_layernorm_forward.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _i64, _i64, ctypes.c_double]
+    lib.oracle_layernorm_backward.argtypes = [_dp] * 10 + [_i64, _i64]
+    lib.oracle_add_rmsnorm_forward.argtypes = [_dp] * 6 + [_i64, _i64, ctypes.c_double]
+    lib.oracle_add_rmsnorm_backward.argtypes = [_dp] * 8 + [_i64, _i64]
+    for name in ("oracle_rmsnorm_forward", "oracle_rmsnorm_backward",
+                 "oracle_layernorm_forward", "oracle_layernorm_backward",
+                 "oracle_add_rmsnorm_forward", "oracle_add_rmsnorm_backward"):
+        getattr(lib, name).restype = None
+    return lib
+
+
+def load_library(path: str | None = None):
+    """Load a compiled oracle. With no path: the default build, compiled on first use."""
+    global _lib
+    if path is not None:
+        return _declare(ctypes.CDLL(path))
+    with _lock:
+        if _lib is None:
+            stale = (not os.path.exists(LIB_PATH)
+                     or os.path.getmtime(LIB_PATH) < os.path.getmtime(SOURCE))
+            if stale:
+                compile_oracle()
+            _lib = _declare(ctypes.CDLL(LIB_PATH))
+    return _lib
+
+
+def _f64(a) -> np.ndarray:
+    """Widen to a C-contiguous fp64 array (exact for fp16 and fp32 inputs)."""
+    if hasattr(a, "detach"):  # a torch CPU tensor
+        a = a.detach().cpu().numpy()
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _p(a: np.ndarray):
+    return a.ctypes.data_as(_dp)
+
+
+def _shape(X) -> tuple[int, int]:
+    if X.ndim != 2:
+        raise ValueError("expected a 2-D [N, D] array")
+    return int(X.shape[0]), int(X.shape[1])
+
+
+def rmsnorm_forward(X, gamma, eps, lib=None):
+    """RMSNorm forward -> (Y [N,D], rstd [N]), fp64."""
+    lib = lib or load_library()
+    X, gamma = _f64(X), _f64(gamma)
+    N, D = _shape(X)
+    Y = np.empty((N, D)); rstd = np.empty(N)
+    lib.oracle_rmsnorm_forward(_p(X), _p(gamma), _p(Y), _p(rstd), N, D, float(eps))
+    return Y, rstd
+
+
+def rmsnorm_backward(X, gamma, dY, rstd, lib=None):
+    """RMSNorm backward -> (dX [N,D], dgamma [D], dgamma_abs [D]), fp64."""
+    lib = lib or load_library()
+    X, gamma, dY, rstd = _f64(X), _f64(gamma), _f64(dY), _f64(rstd)
+    N, D = _shape(X)
+    dX = np.empty((N, D)); dg = np.empty(D); dga = np.empty(D)
+    lib.oracle_rmsnorm_backward(_p(X), _p(gamma), _p(dY), _p(rstd), _p(dX), _p(dg), _p(dga), N, D)
+    return dX, dg, dga
+
+
+def layernorm_forward(X, gamma, beta, eps, lib=None):
+    """LayerNorm forward -> (Y [N,D], mean [N], rstd [N]), fp64."""
+    lib = lib or load_library()
+    X, gamma, beta = _f64(X), _f64(gamma), _f64(beta)
+    N, D = _shape(X)
+    Y = np.empty((N, D)); mean = np.empty(N); rstd = np.empty(N)
+    lib.oracle_layernorm_forward(_p(X), _p(gamma), _p(beta), _p(Y), _p(mean), _p(rstd),
+                                 N, D, float(eps))
+    return Y, mean, rstd
+
+
+def layernorm_backward(X, gamma, dY, mean, rstd, lib=None):
+    """LayerNorm backward -> (dX, dgamma, dbeta, dgamma_abs, dbeta_abs), fp64."""
+    lib = lib or load_library()
+    X, gamma, dY, mean, rstd = _f64(X), _f64(gamma), _f64(dY), _f64(mean), _f64(rstd)
+    N, D = _shape(X)
+    dX = np.empty((N, D)); dg = np.empty(D); db = np.empty(D)
+    dga = np.empty(D); dba = np.empty(D)
+    lib.oracle_layernorm_backward(_p(X), _p(gamma), _p(dY), _p(mean), _p(rstd), _p(dX),
+                                  _p(dg), _p(db), _p(dga), _p(dba), N, D)
+    return dX, dg, db, dga, dba
+
+
+def add_rmsnorm_forward(X, R, gamma, eps, lib=None):
+    """Fused residual-add + RMSNorm forward -> (Y [N,D], S_exact [N,D], rstd [N]), fp64.
+
+    S_exact is the exact sum X + R; the stored residual output is its
+    round-to-nearest-even fp16 value, which the caller forms.
+    """
+    lib = lib or load_library()
+    X, R, gamma = _f64(X), _f64(R), _f64(gamma)
+    N, D = _shape(X)
+    if R.shape != X.shape:
+        raise ValueError("R must match X")
+    Y = np.empty((N, D)); S = np.empty((N, D)); rstd = np.empty(N)
+    lib.oracle_add_rmsnorm_forward(_p(X), _p(R), _p(gamma), _p(S), _p(Y), _p(rstd),
+                                   N, D, float(eps))
+    return Y, S, rstd
+
+
+def add_rmsnorm_backward(S, gamma, dY, dS, rstd, lib=None):
+    """Fused residual-add + RMSNorm backward -> (dX [N,D], dgamma [D], dgamma_abs [D]).
+
+    dX is both d(source) and d(residual). dS may be None (treated as zero).
+    """
+    lib = lib or load_library()
+    S, gamma, dY, rstd = _f64(S), _f64(gamma), _f64(dY), _f64(rstd)
+    N, D = _shape(S)
+    dS_arr = None if dS is None else _f64(dS)
+    dX = np.empty((N, D)); dg = np.empty(D); dga = np.empty(D)
+    lib.oracle_add_rmsnorm_backward(_p(S), _p(gamma), _p(dY),
+                                    None if dS_arr is None else _p(dS_arr),
+                                    _p(rstd), _p(dX), _p(dg), _p(dga), N, D)
+    return dX, dg, dga
+
+
+def round_fp16(a) -> np.ndarray:
+    """Round fp64 values to IEEE binary16, round-to-nearest-even (numpy's conversion)."""
+    return np.asarray(a, dtype=np.float64).astype(np.float16)

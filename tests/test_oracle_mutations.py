@@ -1,0 +1,49 @@
+"""Plant plausible mistakes in copies of the oracle (CPU only) and check that a pin fails.
+
+Each mutation is a one-token slip of the kind the pins are meant to catch: a dropped
+term, a flipped sign, a wrong index, a transposed operand, a misplaced eps, the sample
+instead of the population variance. The committed oracle is never modified; each
+mutant is compiled from a patched copy in a temporary directory.
+"""
+import pytest
+
+import oracle
+from oracle_pins import ALL_PINS
+
+MUTATIONS = {
+    "rms_eps_outside_sqrt": ("double r = 1.0 / sqrt(ms + eps);", "double r = 1.0 / (sqrt(ms) + eps);"),
+    "rms_gamma_index": ("Y[i * D + j] = x[j] * r * gamma[j];", "Y[i * D + j] = x[j] * r * gamma[D - 1 - j];"),
+    "rms_bwd_sign": ("dX[i * D + j] = r * (g - xhat * c);", "dX[i * D + j] = r * (g + xhat * c);"),
+    "rms_bwd_dropped_c": ("dX[i * D + j] = r * (g - xhat * c);", "dX[i * D + j] = r * g;"),
+    "rms_bwd_missing_r": ("dX[i * D + j] = r * (g - xhat * c);", "dX[i * D + j] = (g - xhat * c);"),
+    "rms_dgamma_uses_g": ("double term = dy[j] * xhat;\n            dgamma[j] += term;\n            dgamma_abs[j] += fabs(term);\n        }\n    }\n}",
+                          "double term = g * xhat;\n            dgamma[j] += term;\n            dgamma_abs[j] += fabs(term);\n        }\n    }\n}"),
+    "ln_sample_variance": ("double var = sum_sq / (double)D;", "double var = sum_sq / (double)(D - 1);"),
+    "ln_uncentred_variance": ("sum_sq += (x[j] - mu) * (x[j] - mu);", "sum_sq += x[j] * x[j];"),
+    "ln_bias_dropped": ("Y[i * D + j] = (x[j] - mu) * r * gamma[j] + beta[j];", "Y[i * D + j] = (x[j] - mu) * r * gamma[j];"),
+    "ln_bwd_dropped_mean_g": ("dX[i * D + j] = r * (g - a - xhat * c);", "dX[i * D + j] = r * (g - xhat * c);"),
+    "ln_dbeta_uses_g": ("dbeta[j] += dy[j];", "dbeta[j] += g;"),
+    "ln_dgamma_transposed": ("double term = dy[j] * xhat;\n            dgamma[j] += term;\n            dgamma_abs[j] += fabs(term);\n            dbeta",
+                             "double term = dy[j] * ((x[D - 1 - j] - mu) * r);\n            dgamma[j] += term;\n            dgamma_abs[j] += fabs(term);\n            dbeta"),
+    "add_residual_dropped": ("S[i] = X[i] + R[i];", "S[i] = X[i];"),
+    "add_ds_subtracted": ("dX[i] += dS[i];", "dX[i] -= dS[i];"),
+    "add_ds_ignored": ("dX[i] += dS[i];", "dX[i] += 0.0 * dS[i];"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_mutation_is_caught(tmp_path, name):
+    old, new = MUTATIONS[name]
+    with open(oracle.SOURCE) as f:
+        src = f.read()
+    assert src.count(old) >= 1, f"mutation anchor not found: {old!r}"
+    mutated = tmp_path / "mutant.c"
+    mutated.write_text(src.replace(old, new, 1))
+    lib = oracle.load_library(oracle.compile_oracle(str(mutated), str(tmp_path / "libmutant.so")))
+    failures = []
+    for pin in ALL_PINS:
+        try:
+            pin(lib)
+        except AssertionError as e:
+            failures.append(f"{pin.__name__}: {str(e).splitlines()[0]}")
+    assert failures, f"no pin caught mutation {name}"

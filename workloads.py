@@ -1,0 +1,144 @@
+"""Seeded synthetic workloads for row-wise normalization (inputs only).
+
+This module draws the inputs that both the CUDA path and the fp64 oracle are fed.
+It holds none of the normalization arithmetic: only shapes, distributions, the
+seed and the draw order, plus the byte accounting used to express throughput.
+
+Every tensor is drawn from ONE seeded torch generator in the fixed order
+X, R, s_row, gamma, beta, dY, dS (absent entries are skipped), as fp32, then
+rounded to fp16 (round-to-nearest-even) before either side sees it. ``N(m, s)``
+means mean m and standard deviation s.
+
+The five workloads (name: op, N x D, recipe):
+  rmsnorm_17x257        RMSNorm, ragged width. X, dY ~ N(0,1); gamma = 1 + 0.1 N(0,1); eps 1e-6.
+  layernorm_128x1024    LayerNorm. X, dY ~ N(0,1); gamma = 1 + 0.1 N(0,1);
+                        beta = 0.1 N(0,1); eps 1e-5.
+  rmsnorm_16384x4096    RMSNorm at the Llama-7B activation shape (batch 4 x seq 4096,
+                        hidden 4096). X = N(0,1) * s_row, s_row ~ U(0.5, 4) per row;
+                        dY ~ N(0, 0.01); gamma = 1 + 0.1 N(0,1); eps 1e-6.
+  add_rmsnorm_32768x4096  fused residual-add + RMSNorm. X, R ~ N(0,1); dY, dS ~ N(0, 0.01);
+                        gamma = 1 + 0.1 N(0,1); eps 1e-6.
+  layernorm_2048x16384  wide-row LayerNorm with a large mean (cancellation stress).
+                        X = 50 + N(0,1); gamma = 1 + 0.1 N(0,1); beta = N(0, 0.1);
+                        dY ~ N(0, 0.01); eps 1e-5.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+RMSNORM = "rmsnorm"
+LAYERNORM = "layernorm"
+ADD_RMSNORM = "add_rmsnorm"
+OPS = (RMSNORM, LAYERNORM, ADD_RMSNORM)
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    op: str
+    N: int
+    D: int
+    eps: float
+    x_kind: str          # "normal", "row_scaled", "shifted"
+    dy_std: float
+    beta_std: float = 0.0  # LayerNorm only
+
+    @property
+    def shape(self) -> tuple[int, int]:
+        return (self.N, self.D)
+
+
+WORKLOADS = {
+    w.name: w
+    for w in (
+        Workload("rmsnorm_17x257", RMSNORM, 17, 257, 1e-6, "normal", 1.0),
+        Workload("layernorm_128x1024", LAYERNORM, 128, 1024, 1e-5, "normal", 1.0, beta_std=0.1),
+        Workload("rmsnorm_16384x4096", RMSNORM, 16384, 4096, 1e-6, "row_scaled", 0.01),
+        Workload("add_rmsnorm_32768x4096", ADD_RMSNORM, 32768, 4096, 1e-6, "normal", 0.01),
+        Workload("layernorm_2048x16384", LAYERNORM, 2048, 16384, 1e-5, "shifted", 0.01,
+                 beta_std=0.1),
+    )
+}
+WORKLOAD_ORDER = list(WORKLOADS)
+
+
+def make_generator(device, seed: int = 0) -> torch.Generator:
+    g = torch.Generator(device=torch.device(device))
+    g.manual_seed(seed)
+    return g
+
+
+def generate(op: str, N: int, D: int, *, device="cpu", seed: int = 0,
+             x_kind: str = "normal", dy_std: float = 1.0, beta_std: float = 0.1,
+             with_ds: bool = True) -> dict[str, torch.Tensor]:
+    """Draw one op's inputs as fp16 tensors on ``device``.
+
+    Returns a dict with X, gamma, dY and, by op: R and dS (fused add), beta (LayerNorm).
+    ``with_ds=False`` leaves out dS for the fused op (the absent-cotangent case).
+    """
+    if op not in OPS:
+        raise ValueError(f"unknown op {op!r}")
+    dev = torch.device(device)
+    g = make_generator(dev, seed)
+
+    def normal(shape, mean=0.0, std=1.0):
+        t = torch.randn(shape, generator=g, device=dev, dtype=torch.float32)
+        if std != 1.0:
+            t.mul_(std)
+        if mean != 0.0:
+            t.add_(mean)
+        return t
+
+    out: dict[str, torch.Tensor] = {}
+    X = normal((N, D), mean=50.0 if x_kind == "shifted" else 0.0)
+    R = normal((N, D)) if op == ADD_RMSNORM else None
+    if x_kind == "row_scaled":
+        s_row = torch.rand((N, 1), generator=g, device=dev, dtype=torch.float32)
+        s_row.mul_(3.5).add_(0.5)          # U(0.5, 4)
+        X.mul_(s_row)
+    gamma = normal((D,), mean=1.0, std=0.1)
+    beta = normal((D,), std=beta_std) if op == LAYERNORM else None
+    dY = normal((N, D), std=dy_std)
+    dS = normal((N, D), std=dy_std) if (op == ADD_RMSNORM and with_ds) else None
+
+    out["X"] = X.half()
+    if R is not None:
+        out["R"] = R.half()
+    out["gamma"] = gamma.half()
+    if beta is not None:
+        out["beta"] = beta.half()
+    out["dY"] = dY.half()
+    if dS is not None:
+        out["dS"] = dS.half()
+    return out
+
+
+def generate_workload(name: str, *, device="cpu", seed: int = 0, rows: int | None = None,
+                      with_ds: bool = True) -> dict[str, torch.Tensor]:
+    """Draw a named workload's inputs; ``rows`` overrides N (same recipe, fewer rows)."""
+    w = WORKLOADS[name]
+    return generate(w.op, rows if rows is not None else w.N, w.D, device=device, seed=seed,
+                    x_kind=w.x_kind, dy_std=w.dy_std, beta_std=w.beta_std, with_ds=with_ds)
+
+
+def compulsory_bytes(op: str, direction: str, N: int, D: int, with_ds: bool = True) -> int:
+    """Bytes that any implementation must move (fp16 activations, fp32 stats/grads).
+
+    forward:  RMSNorm 4ND + 4N + 2D; LayerNorm 4ND + 8N + 4D; fused add 8ND + 4N + 2D.
+    backward: RMSNorm 6ND + 4N + 6D; LayerNorm 6ND + 8N + 10D; fused add 8ND + 4N + 6D
+              (6ND + 4N + 6D when the residual-output cotangent is absent).
+    Workspace traffic (dgamma/dbeta partials) is not compulsory.
+    """
+    if direction == "forward":
+        return {RMSNORM: 4 * N * D + 4 * N + 2 * D,
+                LAYERNORM: 4 * N * D + 8 * N + 4 * D,
+                ADD_RMSNORM: 8 * N * D + 4 * N + 2 * D}[op]
+    if direction == "backward":
+        if op == ADD_RMSNORM and not with_ds:
+            return 6 * N * D + 4 * N + 6 * D
+        return {RMSNORM: 6 * N * D + 4 * N + 6 * D,
+                LAYERNORM: 6 * N * D + 8 * N + 10 * D,
+                ADD_RMSNORM: 8 * N * D + 4 * N + 6 * D}[op]
+    raise ValueError(direction)
