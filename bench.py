@@ -1,0 +1,493 @@
+"""Benchmark: row-wise normalization forward + backward on one GB300 (or N replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl mine|reference]
+
+A step is one forward and one backward of the workload's op (every stage of the path:
+row load, reduction, statistics, apply, backward row pass, dgamma/dbeta partials and
+their fixed-order reduction) on device-resident inputs. The metric is achieved HBM
+throughput: compulsory bytes (fp16 activations read and written once, fp32 stats and
+parameter gradients) divided by the CUDA-event time of the two calls, plus rows/s.
+L2 is flushed before every call by reading a buffer twice the L2 size (clean lines,
+so no write-back leaks into the timed call).
+
+One JSON line is printed by rank 0. Under torchrun (N > 1) every rank runs its own
+replica of the workload (weak scaling; the path has no cross-rank exchange in this
+build) and the time is the max over ranks.
+
+``--impl reference`` times the fp64 CPU oracle instead, on host cores, over a bounded
+row sample of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = ("achieved HBM GB/s (% of ~8 TB/s) and rows/s, norm fwd+bwd at N×D fp16")
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+DEFAULT_WORKLOAD = "rmsnorm_16384x4096"
+LARGE_WORKLOADS = ["rmsnorm_16384x4096", "add_rmsnorm_32768x4096", "layernorm_2048x16384"]
+CSRC = os.path.join(ROOT, "row_wise_rmsnorm_gb300", "csrc")
+
+
+# --------------------------------------------------------------- helpers ---
+
+def measured_peak_gbs():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured (MEASURED_PEAKS.json hbm_gbs, copy, burst)"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, earlier GB300 measurement)"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(CSRC)):
+        if f.endswith((".cu", ".cuh")):
+            with open(os.path.join(CSRC, f), "rb") as fh:
+                h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch from a committed ncu summary, if taken on this kernel source."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
+    entry = rec.get("entries", {}).get(f"{workload}:{kernel}")
+    return None if entry is None else entry.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for r in csv.reader(io.StringIO(getattr(self, "out", "") or "")):
+            if len(r) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(r[1]), smax=float(r[2]), power=float(r[3]),
+                                 hw=r[5].strip(), hwt=r[6].strip(), swt=r[7].strip(),
+                                 pcap=r[8].strip()))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        reasons = []
+        for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                          ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+            if any(x[key].lower() == "active" for x in rows):
+                reasons.append(name)
+        return {"sm_mhz": statistics.median(x["sm"] for x in rows),
+                "sm_max_mhz": max(x["smax"] for x in rows),
+                "power_w_max": max(x["power"] for x in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------ GPU arm ---
+
+class OpRunner:
+    """Holds one workload's device buffers and issues its forward/backward C-ABI calls."""
+
+    def __init__(self, name: str, device, seed: int):
+        import torch
+        import row_wise_rmsnorm_gb300 as mt
+        self.mt = mt
+        self.w = W.WORKLOADS[name]
+        self.dev = device
+        w = self.w
+        self.t = W.generate_workload(name, device=device, seed=seed)
+        N, D = w.N, w.D
+        h = dict(dtype=torch.float16, device=device)
+        f = dict(dtype=torch.float32, device=device)
+        self.Y = torch.empty((N, D), **h)
+        self.rstd = torch.empty(N, **f)
+        self.dX = torch.empty((N, D), **h)
+        self.dg = torch.empty(D, **f)
+        self.mean = torch.empty(N, **f) if w.op == W.LAYERNORM else None
+        self.db = torch.empty(D, **f) if w.op == W.LAYERNORM else None
+        self.S = torch.empty((N, D), **h) if w.op == W.ADD_RMSNORM else None
+        opcode = {W.RMSNORM: mt.MT_OP_RMSNORM, W.LAYERNORM: mt.MT_OP_LAYERNORM,
+                  W.ADD_RMSNORM: mt.MT_OP_ADD_RMSNORM}[w.op]
+        self.ws_bytes = mt.mt_norm_backward_workspace_size(opcode, N, D, device.index or 0)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
+        self.fwd_bytes = W.compulsory_bytes(w.op, "forward", N, D)
+        self.bwd_bytes = W.compulsory_bytes(w.op, "backward", N, D)
+
+    def forward(self, stream):
+        w, t, mt = self.w, self.t, self.mt
+        if w.op == W.RMSNORM:
+            mt.mt_rmsnorm_forward(t["X"], t["gamma"], self.Y, self.rstd, w.N, w.D, w.eps, stream)
+        elif w.op == W.LAYERNORM:
+            mt.mt_layernorm_forward(t["X"], t["gamma"], t["beta"], self.Y, self.mean, self.rstd,
+                                    w.N, w.D, w.eps, stream)
+        else:
+            mt.mt_add_rmsnorm_forward(t["X"], t["R"], t["gamma"], self.S, self.Y, self.rstd,
+                                      w.N, w.D, w.eps, stream)
+
+    def backward(self, stream):
+        w, t, mt = self.w, self.t, self.mt
+        if w.op == W.RMSNORM:
+            mt.mt_rmsnorm_backward_ws(t["X"], t["gamma"], t["dY"], self.rstd, self.dX, self.dg,
+                                      w.N, w.D, self.ws, self.ws_bytes, stream)
+        elif w.op == W.LAYERNORM:
+            mt.mt_layernorm_backward_ws(t["X"], t["gamma"], t["dY"], self.mean, self.rstd,
+                                        self.dX, self.dg, self.db, w.N, w.D, self.ws,
+                                        self.ws_bytes, stream)
+        else:
+            mt.mt_add_rmsnorm_backward_ws(self.S, t["gamma"], t["dY"], t["dS"], self.rstd,
+                                          self.dX, self.dg, w.N, w.D, self.ws, self.ws_bytes,
+                                          stream)
+
+
+def time_ops(runner: OpRunner, steps: int, warmup: int, flush, stream):
+    """Per-call CUDA-event times (ms) of forward and backward, L2 flushed before each."""
+    import torch
+    for _ in range(warmup):
+        flush()
+        runner.forward(stream)
+        flush()
+        runner.backward(stream)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    torch.cuda.synchronize()
+    for e in ev:
+        flush()
+        e[0].record(stream)
+        runner.forward(stream)
+        e[1].record(stream)
+        flush()
+        e[2].record(stream)
+        runner.backward(stream)
+        e[3].record(stream)
+    torch.cuda.synchronize()
+    fwd = [e[0].elapsed_time(e[1]) for e in ev]
+    bwd = [e[2].elapsed_time(e[3]) for e in ev]
+    return fwd, bwd
+
+
+def e2e_run(name: str, device, steps: int, warmup: int, seed: int):
+    """Same metric through the public API with pinned-host inputs/outputs: every step
+    copies X, gamma, dY (and R, dS / beta) host->device, runs forward + backward, and
+    copies Y, stats, dX, dgamma (and S / dbeta) back. CUDA events bracket the step."""
+    import torch
+    r = OpRunner(name, device, seed)
+    ins = {k: v.cpu().pin_memory() for k, v in r.t.items()}
+    outs_dev = [r.Y, r.rstd, r.dX, r.dg] + [x for x in (r.mean, r.db, r.S) if x is not None]
+    outs_host = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in outs_dev]
+    h2d = sum(v.numel() * v.element_size() for v in ins.values())
+    d2h = sum(x.numel() * x.element_size() for x in outs_dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for k, v in ins.items():
+            r.t[k].copy_(v, non_blocking=True)
+        r.forward(stream)
+        r.backward(stream)
+        for hd, dv in zip(outs_host, outs_dev):
+            hd.copy_(dv, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    gbs = (r.fwd_bytes + r.bwd_bytes) / (ms * 1e-3) / 1e9
+    del r
+    return {"value": round(gbs, 2), "unit": "GB/s", "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
+
+
+# ------------------------------------------------------------ CPU oracle ---
+
+def oracle_step_seconds(name: str, rows: int, seed: int = 0):
+    """Wall time of one oracle forward + backward over `rows` rows of the workload."""
+    import numpy as np
+    sys.path.insert(0, ROOT)
+    import oracle
+    w = W.WORKLOADS[name]
+    t = W.generate_workload(name, rows=rows, seed=seed)
+    a = {k: v.double().numpy() for k, v in t.items()}
+    eps = float(np.float32(w.eps))
+    t0 = time.perf_counter()
+    if w.op == W.RMSNORM:
+        _, rstd = oracle.rmsnorm_forward(a["X"], a["gamma"], eps)
+        oracle.rmsnorm_backward(a["X"], a["gamma"], a["dY"], rstd)
+    elif w.op == W.LAYERNORM:
+        _, mean, rstd = oracle.layernorm_forward(a["X"], a["gamma"], a["beta"], eps)
+        oracle.layernorm_backward(a["X"], a["gamma"], a["dY"], mean, rstd)
+    else:
+        _, s, rstd = oracle.add_rmsnorm_forward(a["X"], a["R"], a["gamma"], eps)
+        s16 = oracle.round_fp16(s).astype(np.float64)
+        oracle.add_rmsnorm_backward(s16, a["gamma"], a["dY"], a["dS"], rstd)
+    return time.perf_counter() - t0
+
+
+def oracle_baseline(name: str, budget_s: float = 10.0):
+    """The oracle, as it stands, on a bounded sample sized to about `budget_s` of CPU
+    work: the first rows of the workload (all of them if they fit), repeated."""
+    w = W.WORKLOADS[name]
+    probe = min(w.N, 64)
+    t_probe = oracle_step_seconds(name, probe)
+    rows = int(min(w.N, max(probe, probe * budget_s / max(t_probe, 1e-6))))
+    secs, reps = 0.0, 0
+    while reps == 0 or (secs < 0.8 * budget_s and reps < 10):
+        secs += oracle_step_seconds(name, rows)
+        reps += 1
+    nbytes = reps * (W.compulsory_bytes(w.op, "forward", rows, w.D)
+                     + W.compulsory_bytes(w.op, "backward", rows, w.D))
+    return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {rows} of {w.N} rows of {name}, forward + backward, {reps} "
+                      f"pass(es), fp64 single-threaded C, {secs:.2f} s",
+            "rows_per_s": round(reps * rows / secs, 1)}
+
+
+def run_reference(args):
+    """--impl reference: the oracle on host cores, K steps of a bounded row sample."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    name = args.workload
+    w = W.WORKLOADS[name]
+    t1 = oracle_step_seconds(name, min(w.N, 16))
+    per_row = t1 / min(w.N, 16)
+    per_step_budget = max(0.02, 60.0 / max(1, args.steps + args.warmup))
+    rows = int(max(1, min(w.N, per_step_budget / max(per_row, 1e-9))))
+    for _ in range(args.warmup):
+        oracle_step_seconds(name, rows)
+    times = [oracle_step_seconds(name, rows) for _ in range(args.steps)]
+    secs = sum(times)
+    nbytes = args.steps * (W.compulsory_bytes(w.op, "forward", rows, w.D)
+                           + W.compulsory_bytes(w.op, "backward", rows, w.D))
+    gbs = nbytes / secs / 1e9
+    sample = (f"first {rows} of {w.N} rows of {name} per step, forward + backward, fp64 "
+              f"single-threaded C oracle")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+        "rows_per_s": round(args.steps * rows / secs, 2), "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * secs / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": name, "op": w.op, "N": w.N, "D": w.D, "eps": w.eps,
+                   "rows_per_step": rows},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# --------------------------------------------------------------- main ---
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["mine", "reference"], default="mine")
+    ap.add_argument("--workload", choices=W.WORKLOAD_ORDER, default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-others", action="store_true",
+                    help="skip the per-op numbers of the other large workloads")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=device)
+
+    import row_wise_rmsnorm_gb300 as mt
+    mt.load()  # fails loudly if the CUDA library is not built
+
+    stream = torch.cuda.current_stream()
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush_buf = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=device)
+    flush_buf.fill_(1.0)
+
+    def flush():
+        flush_buf.sum()
+
+    peak, peak_src = measured_peak_gbs()
+    runner = OpRunner(args.workload, device, seed=rank)
+    w = runner.w
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    barrier()
+    with ClockSampler(local) as clocks:
+        t0 = time.perf_counter()
+        fwd, bwd = time_ops(runner, args.steps, args.warmup, flush, stream)
+        barrier()
+        wall = time.perf_counter() - t0
+    fwd_ms = statistics.mean(fwd)
+    bwd_ms = statistics.mean(bwd)
+    step_ms = fwd_ms + bwd_ms
+    if world > 1:
+        tt = torch.tensor([step_ms], device=device, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        step_ms = float(tt.item())
+
+    step_bytes = runner.fwd_bytes + runner.bwd_bytes
+    value = world * step_bytes / (step_ms * 1e-3) / 1e9
+    rows_s = world * w.N / (step_ms * 1e-3)
+
+    def op_line(nbytes, times):
+        ms = statistics.mean(times)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        return {"us": round(1e3 * ms, 3), "us_median": round(1e3 * statistics.median(times), 3),
+                "gbs": round(gbs, 2), "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
+                "frac_of_measured": round(gbs / peak, 4), "rows_per_s": round(w.N / (ms * 1e-3), 1),
+                "compulsory_bytes": nbytes}
+
+    ops = {"forward": op_line(runner.fwd_bytes, fwd), "backward": op_line(runner.bwd_bytes, bwd)}
+    dom = "backward" if bwd_ms >= fwd_ms else "forward"
+    dom_name = {"forward": f"{w.op} forward (norm_fwd_kernel, 1 launch)",
+                "backward": f"{w.op} backward (norm_bwd_kernel + param_reduce_kernel, 2 launches)"}
+    del runner
+    torch.cuda.empty_cache()
+
+    others = {}
+    if not args.no_others and rank == 0:
+        for name in LARGE_WORKLOADS:
+            if name == args.workload:
+                continue
+            r2 = OpRunner(name, device, seed=0)
+            f2, b2 = time_ops(r2, max(50, args.steps // 10), args.warmup, flush, stream)
+            others[name] = {
+                "forward_gbs": round(r2.fwd_bytes / (statistics.mean(f2) * 1e-3) / 1e9, 2),
+                "backward_gbs": round(r2.bwd_bytes / (statistics.mean(b2) * 1e-3) / 1e9, 2),
+                "forward_us": round(1e3 * statistics.mean(f2), 3),
+                "backward_us": round(1e3 * statistics.mean(b2), 3)}
+            del r2
+            torch.cuda.empty_cache()
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = e2e_run(args.workload, device, max(5, min(50, args.steps // 40)), 3, seed=rank)
+        if world > 1:
+            tt = torch.tensor([e2e["ms_per_step"]], device=device, dtype=torch.float64)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e2e["ms_per_step"] = round(float(tt.item()), 4)
+            e2e["value"] = round(world * step_bytes / (e2e["ms_per_step"] * 1e-3) / 1e9, 2)
+
+    cpu = None
+    if rank == 0 and world >= 1 and not args.no_cpu_baseline and args.gpus == 1:
+        cpu = oracle_baseline(args.workload)
+
+    dom_line = ops[dom]
+    traffic = recorded_traffic(args.workload, dom)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "rows_per_s": round(rows_s, 1),
+        "frac_of_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
+        "frac_of_measured": round(value / world / peak, 4),
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "storage": "f16",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "op": w.op, "N": w.N, "D": w.D, "eps": w.eps,
+                   "step": "forward + backward",
+                   "l2": "flushed before every timed call (read of a 2x L2 buffer)",
+                   "parallelism": f"{world} independent replica(s)"},
+        "ops": ops,
+        "roofline": {"bound": "hbm", "kernel": dom_name[dom], "achieved": dom_line["gbs"],
+                     "peak": peak, "peak_source": peak_src, "unit": "GB/s",
+                     "frac": dom_line["frac_of_measured"], "traffic": traffic,
+                     "algorithmic_bytes_per_launch": dom_line["compulsory_bytes"]},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps * 3,
+        "clocks": clocks.summary(),
+        "timed_region_wall_s": round(wall, 3),
+        "other_workloads": others,
+    }
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

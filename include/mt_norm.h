@@ -1,0 +1,188 @@
+/*
+ * mt_norm.h -- C ABI of the GB300 (sm_103a) row-wise normalization library.
+ *
+ * Three training operations, each a forward and a backward entry point:
+ *   RMSNorm                       mt_rmsnorm_forward / mt_rmsnorm_backward
+ *   LayerNorm                     mt_layernorm_forward / mt_layernorm_backward
+ *   fused residual-add + RMSNorm  mt_add_rmsnorm_forward / mt_add_rmsnorm_backward
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Layout.   Activations (X, R, S, Y, dY, dS, dX) are dense row-major [N, D] arrays of
+ *           IEEE binary16 (fp16), row i starting at element i*D. gamma and beta are [D]
+ *           fp16. mean and rstd are [N] fp32. dgamma and dbeta are [D] fp32.
+ * Memory.   Every pointer is a device pointer on the CUDA device current on the calling
+ *           thread. The caller owns every buffer; the library keeps no pointer after the
+ *           call returns. Any alignment is accepted (16-byte aligned rows with D a
+ *           multiple of 8 take the vectorised path).
+ * Streams.  `stream` is a cudaStream_t (NULL = the legacy default stream). Calls are
+ *           asynchronous: work is enqueued on `stream` and the function returns.
+ * Outputs.  Outputs are overwritten, never accumulated into. Outputs may not overlap any
+ *           input or any other output (no in-place operation).
+ * Saved state. The forward's saved tensors (X or S, mean, rstd) must not be modified
+ *           between a forward and the backward that consumes them.
+ * Arithmetic. All arithmetic is fp32; fp16 results are rounded to nearest even.
+ *           dgamma/dbeta are reduced in a fixed order without atomics, so every output
+ *           is bitwise identical from run to run on the same device and shape.
+ * Bounds.   1 <= N <= 2^31 - 1 and 1 <= D <= MT_MAX_COLS. eps must be finite and > 0.
+ * Errors.   Arguments are validated before any CUDA call is made:
+ *             MT_ERR_INVALID_ARG  a required pointer is NULL, N < 1, D < 1, eps not
+ *                                 finite or not > 0, or an output overlaps an input or
+ *                                 another output;
+ *             MT_ERR_UNSUPPORTED  D > MT_MAX_COLS, N > 2^31 - 1, or a caller-supplied
+ *                                 workspace smaller than the size query returns;
+ *             MT_ERR_CUDA         a CUDA call or kernel launch failed;
+ *                                 mt_last_cuda_error() returns its cudaError_t value.
+ *           Non-finite input values are not repaired: a NaN or Inf propagates to its
+ *           row's outputs and to the dgamma/dbeta columns it touches.
+ *
+ * Sources (page title, section):
+ *   [meTile] "Kernel coverage and training scope", "Exact native normalization contract".
+ *   [tc]     "Training kernels" (tensorcore docs), "RMSnorm -- Llama-style" and
+ *            "LayerNorm -- standard": the C signatures, buffer dtypes and saved statistics.
+ */
+#ifndef MT_NORM_H
+#define MT_NORM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes; the [tc] API returns a status code the same way. */
+typedef enum mt_status {
+    MT_OK = 0,
+    MT_ERR_INVALID_ARG = 1,
+    MT_ERR_UNSUPPORTED = 2,
+    MT_ERR_CUDA = 3
+} mt_status_t;
+
+/* Operation selector for the workspace-size query. */
+typedef enum mt_norm_op {
+    MT_OP_RMSNORM = 0,
+    MT_OP_LAYERNORM = 1,
+    MT_OP_ADD_RMSNORM = 2
+} mt_norm_op_t;
+
+/* ABI-identical to cudaStream_t, so this header needs no CUDA header. */
+struct CUstream_st;
+typedef struct CUstream_st *mt_stream_t;
+
+/* Widest supported row. [meTile] bounds rows to 1..8192 columns; this library
+ * extends the bound to 16384 so that 16384-wide LayerNorm rows are covered. */
+#define MT_MAX_COLS 16384
+
+/* ---------------------------------------------------------------- RMSNorm ---
+ * [tc] "RMSnorm -- Llama-style", Math; [meTile] contract (zero-offset weight):
+ *   rstd_i = 1 / sqrt(mean_j(X_ij^2) + eps),   Y_ij = X_ij * rstd_i * gamma_j.
+ * In:  X [N,D] fp16, gamma [D] fp16, eps.
+ * Out: Y [N,D] fp16, rstd [N] fp32 (saved for the backward).                     */
+mt_status_t mt_rmsnorm_forward(const void *X, const void *gamma, void *Y, float *rstd,
+                               int64_t N, int64_t D, float eps, mt_stream_t stream);
+
+/* Backward of mt_rmsnorm_forward at the saved rstd (no eps argument: [tc]
+ * signature). With xhat = X*rstd, g = dY*gamma, c_i = mean_j(g_ij*xhat_ij):
+ *   dX_ij = rstd_i * (g_ij - xhat_ij*c_i),   dgamma_j = sum_i dY_ij*xhat_ij.
+ * In:  X, dY [N,D] fp16, gamma [D] fp16, rstd [N] fp32.
+ * Out: dX [N,D] fp16, dgamma [D] fp32.
+ * Scratch: a stream-ordered allocation (cudaMallocAsync on `stream`) of
+ * mt_norm_backward_workspace_size() bytes, freed on `stream` before returning.   */
+mt_status_t mt_rmsnorm_backward(const void *X, const void *gamma, const void *dY,
+                                const float *rstd, void *dX, float *dgamma,
+                                int64_t N, int64_t D, mt_stream_t stream);
+
+/* As mt_rmsnorm_backward, with caller-owned scratch: `workspace` is a device buffer of
+ * at least mt_norm_backward_workspace_size(MT_OP_RMSNORM, N, D, device) bytes, used
+ * only for the duration of the enqueued work. No allocation is made.               */
+mt_status_t mt_rmsnorm_backward_ws(const void *X, const void *gamma, const void *dY,
+                                   const float *rstd, void *dX, float *dgamma,
+                                   int64_t N, int64_t D, void *workspace,
+                                   size_t workspace_bytes, mt_stream_t stream);
+
+/* -------------------------------------------------------------- LayerNorm ---
+ * [meTile] contract: centre each row by its mean, population variance of the
+ * centred values, then weight and bias; [tc] "LayerNorm -- standard": mean and
+ * rstd saved for backward.
+ *   mean_i = mean_j X_ij,  rstd_i = 1/sqrt(mean_j (X_ij - mean_i)^2 + eps),
+ *   Y_ij = (X_ij - mean_i) * rstd_i * gamma_j + beta_j.
+ * In:  X [N,D] fp16, gamma, beta [D] fp16, eps.
+ * Out: Y [N,D] fp16, mean [N] fp32, rstd [N] fp32.                               */
+mt_status_t mt_layernorm_forward(const void *X, const void *gamma, const void *beta,
+                                 void *Y, float *mean, float *rstd,
+                                 int64_t N, int64_t D, float eps, mt_stream_t stream);
+
+/* Backward of mt_layernorm_forward at the saved mean and rstd. With
+ * xhat = (X - mean)*rstd, g = dY*gamma, a_i = mean_j g_ij, c_i = mean_j g_ij*xhat_ij:
+ *   dX_ij = rstd_i * (g_ij - a_i - xhat_ij*c_i),
+ *   dgamma_j = sum_i dY_ij*xhat_ij,   dbeta_j = sum_i dY_ij.
+ * [tc]'s printed signature has no parameter gradients; [meTile] returns both, and
+ * so does this entry point.
+ * In:  X, dY [N,D] fp16, gamma [D] fp16, mean, rstd [N] fp32.
+ * Out: dX [N,D] fp16, dgamma, dbeta [D] fp32. Scratch as mt_rmsnorm_backward.      */
+mt_status_t mt_layernorm_backward(const void *X, const void *gamma, const void *dY,
+                                  const float *mean, const float *rstd, void *dX,
+                                  float *dgamma, float *dbeta,
+                                  int64_t N, int64_t D, mt_stream_t stream);
+
+mt_status_t mt_layernorm_backward_ws(const void *X, const void *gamma, const void *dY,
+                                     const float *mean, const float *rstd, void *dX,
+                                     float *dgamma, float *dbeta, int64_t N, int64_t D,
+                                     void *workspace, size_t workspace_bytes,
+                                     mt_stream_t stream);
+
+/* ------------------------------------------------- fused residual add + RMSNorm ---
+ * [meTile] contract: the sum is formed in fp32 and the UNROUNDED sum is normalised;
+ * the residual sum is also returned, rounded to fp16.
+ *   s_ij = X_ij + R_ij (fp32),  S_ij = fp16(s_ij),
+ *   rstd_i = 1/sqrt(mean_j s_ij^2 + eps),  Y_ij = s_ij * rstd_i * gamma_j.
+ * In:  X, R [N,D] fp16, gamma [D] fp16, eps.
+ * Out: S [N,D] fp16 (the residual stream), Y [N,D] fp16, rstd [N] fp32.            */
+mt_status_t mt_add_rmsnorm_forward(const void *X, const void *R, const void *gamma,
+                                   void *S, void *Y, float *rstd,
+                                   int64_t N, int64_t D, float eps, mt_stream_t stream);
+
+/* Backward of mt_add_rmsnorm_forward. [meTile] contract: takes both output
+ * cotangents; the residual-output cotangent dS is added to both input gradients,
+ * and a NULL dS means zero. With xhat = S*rstd (S the saved fp16 residual sum),
+ * g = dY*gamma, c_i = mean_j g_ij*xhat_ij:
+ *   dX_ij = rstd_i * (g_ij - xhat_ij*c_i) + dS_ij,   dgamma_j = sum_i dY_ij*xhat_ij.
+ * dX is both d(source) and d(residual): the two are equal, so one buffer is written.
+ * In:  S, dY [N,D] fp16, dS [N,D] fp16 or NULL, gamma [D] fp16, rstd [N] fp32.
+ * Out: dX [N,D] fp16, dgamma [D] fp32. Scratch as mt_rmsnorm_backward.              */
+mt_status_t mt_add_rmsnorm_backward(const void *S, const void *gamma, const void *dY,
+                                    const void *dS, const float *rstd, void *dX,
+                                    float *dgamma, int64_t N, int64_t D,
+                                    mt_stream_t stream);
+
+mt_status_t mt_add_rmsnorm_backward_ws(const void *S, const void *gamma, const void *dY,
+                                       const void *dS, const float *rstd, void *dX,
+                                       float *dgamma, int64_t N, int64_t D,
+                                       void *workspace, size_t workspace_bytes,
+                                       mt_stream_t stream);
+
+/* ------------------------------------------------------------------ utilities --- */
+
+/* Scratch bytes a backward of `op` at [N, D] needs on CUDA device `device`: the
+ * fixed-order dgamma (and dbeta) partials, one fp32 row of D per persistent CTA.
+ * Writes the size to *bytes. Errors: MT_ERR_INVALID_ARG / MT_ERR_UNSUPPORTED as the
+ * backward would return them, MT_ERR_INVALID_ARG for a NULL `bytes` or an unknown
+ * op, MT_ERR_CUDA if the device cannot be queried.                                */
+mt_status_t mt_norm_backward_workspace_size(mt_norm_op_t op, int64_t N, int64_t D,
+                                            int device, size_t *bytes);
+
+/* cudaError_t value of the most recent MT_ERR_CUDA on the calling thread (0 if none). */
+int mt_last_cuda_error(void);
+
+/* Static, human-readable name of a status code. */
+const char *mt_status_string(mt_status_t status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int mt_norm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MT_NORM_H */

@@ -1,0 +1,272 @@
+"""ctypes binding of libmt_norm.so (the C ABI in include/mt_norm.h).
+
+Two layers, both argument marshalling only -- every step of the computation runs in
+the CUDA kernels behind the C ABI:
+
+* ``mt_*`` functions with the C names and the C argument order. Tensor arguments may
+  be torch tensors (their ``data_ptr()`` is passed) or raw integer addresses; the
+  stream may be a ``torch.cuda.Stream``, a raw ``cudaStream_t`` integer, or None for
+  torch's current stream. A non-zero status raises ``MtNormError``.
+* ``rmsnorm_forward`` & co.: allocate outputs (and the backward workspace) with
+  torch on the input's device and call the ``mt_*`` function on the current stream.
+
+There is no fallback: if the library has not been built, or is loaded without a
+CUDA device, the calls fail loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+LIB_PATH = _build.LIB
+
+MT_OK, MT_ERR_INVALID_ARG, MT_ERR_UNSUPPORTED, MT_ERR_CUDA = 0, 1, 2, 3
+MT_OP_RMSNORM, MT_OP_LAYERNORM, MT_OP_ADD_RMSNORM = 0, 1, 2
+MT_MAX_COLS = 16384
+
+# Every exported symbol of include/mt_norm.h.
+EXPORTED = (
+    "mt_rmsnorm_forward", "mt_rmsnorm_backward", "mt_rmsnorm_backward_ws",
+    "mt_layernorm_forward", "mt_layernorm_backward", "mt_layernorm_backward_ws",
+    "mt_add_rmsnorm_forward", "mt_add_rmsnorm_backward", "mt_add_rmsnorm_backward_ws",
+    "mt_norm_backward_workspace_size", "mt_last_cuda_error", "mt_status_string",
+    "mt_norm_version",
+)
+
+
+class MtNormError(RuntimeError):
+    def __init__(self, status: int, func: str, lib):
+        self.status = status
+        msg = lib.mt_status_string(status).decode()
+        if status == MT_ERR_CUDA:
+            msg += f" (cudaError {lib.mt_last_cuda_error()})"
+        super().__init__(f"{func}: {msg}")
+
+
+_lib = None
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_F = ctypes.c_float
+_SZ = ctypes.c_size_t
+_SIGS = {
+    "mt_rmsnorm_forward": [_P, _P, _P, _P, _I64, _I64, _F, _P],
+    "mt_rmsnorm_backward": [_P, _P, _P, _P, _P, _P, _I64, _I64, _P],
+    "mt_rmsnorm_backward_ws": [_P, _P, _P, _P, _P, _P, _I64, _I64, _P, _SZ, _P],
+    "mt_layernorm_forward": [_P, _P, _P, _P, _P, _P, _I64, _I64, _F, _P],
+    "mt_layernorm_backward": [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P],
+    "mt_layernorm_backward_ws": [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P, _SZ, _P],
+    "mt_add_rmsnorm_forward": [_P, _P, _P, _P, _P, _P, _I64, _I64, _F, _P],
+    "mt_add_rmsnorm_backward": [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P],
+    "mt_add_rmsnorm_backward_ws": [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P, _SZ, _P],
+    "mt_norm_backward_workspace_size": [ctypes.c_int, _I64, _I64, ctypes.c_int,
+                                        ctypes.POINTER(_SZ)],
+    "mt_last_cuda_error": [],
+    "mt_status_string": [ctypes.c_int],
+    "mt_norm_version": [],
+}
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def load():
+    """Load libmt_norm.so (built by ``row_wise_rmsnorm_gb300.build``); raise if absent."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"CUDA library not built: {LIB_PATH} is missing. Build it with "
+                "`python -m row_wise_rmsnorm_gb300.build` (needs nvcc); there is no "
+                "CPU fallback.")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, args in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = ctypes.c_int
+        lib.mt_status_string.restype = ctypes.c_char_p
+        _lib = lib
+    return _lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(s):
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _check(status: int, func: str):
+    if status != MT_OK:
+        raise MtNormError(status, func, load())
+
+
+# ------------------------------------------------------------ C-named calls ---
+
+def mt_rmsnorm_forward(X, gamma, Y, rstd, N, D, eps, stream=None):
+    _check(load().mt_rmsnorm_forward(_ptr(X), _ptr(gamma), _ptr(Y), _ptr(rstd), N, D, eps,
+                                     _stream(stream)), "mt_rmsnorm_forward")
+
+
+def mt_rmsnorm_backward(X, gamma, dY, rstd, dX, dgamma, N, D, stream=None):
+    _check(load().mt_rmsnorm_backward(_ptr(X), _ptr(gamma), _ptr(dY), _ptr(rstd), _ptr(dX),
+                                      _ptr(dgamma), N, D, _stream(stream)), "mt_rmsnorm_backward")
+
+
+def mt_rmsnorm_backward_ws(X, gamma, dY, rstd, dX, dgamma, N, D, workspace, workspace_bytes,
+                           stream=None):
+    _check(load().mt_rmsnorm_backward_ws(_ptr(X), _ptr(gamma), _ptr(dY), _ptr(rstd), _ptr(dX),
+                                         _ptr(dgamma), N, D, _ptr(workspace), workspace_bytes,
+                                         _stream(stream)), "mt_rmsnorm_backward_ws")
+
+
+def mt_layernorm_forward(X, gamma, beta, Y, mean, rstd, N, D, eps, stream=None):
+    _check(load().mt_layernorm_forward(_ptr(X), _ptr(gamma), _ptr(beta), _ptr(Y), _ptr(mean),
+                                       _ptr(rstd), N, D, eps, _stream(stream)),
+           "mt_layernorm_forward")
+
+
+def mt_layernorm_backward(X, gamma, dY, mean, rstd, dX, dgamma, dbeta, N, D, stream=None):
+    _check(load().mt_layernorm_backward(_ptr(X), _ptr(gamma), _ptr(dY), _ptr(mean), _ptr(rstd),
+                                        _ptr(dX), _ptr(dgamma), _ptr(dbeta), N, D,
+                                        _stream(stream)), "mt_layernorm_backward")
+
+
+def mt_layernorm_backward_ws(X, gamma, dY, mean, rstd, dX, dgamma, dbeta, N, D, workspace,
+                             workspace_bytes, stream=None):
+    _check(load().mt_layernorm_backward_ws(_ptr(X), _ptr(gamma), _ptr(dY), _ptr(mean),
+                                           _ptr(rstd), _ptr(dX), _ptr(dgamma), _ptr(dbeta), N, D,
+                                           _ptr(workspace), workspace_bytes, _stream(stream)),
+           "mt_layernorm_backward_ws")
+
+
+def mt_add_rmsnorm_forward(X, R, gamma, S, Y, rstd, N, D, eps, stream=None):
+    _check(load().mt_add_rmsnorm_forward(_ptr(X), _ptr(R), _ptr(gamma), _ptr(S), _ptr(Y),
+                                         _ptr(rstd), N, D, eps, _stream(stream)),
+           "mt_add_rmsnorm_forward")
+
+
+def mt_add_rmsnorm_backward(S, gamma, dY, dS, rstd, dX, dgamma, N, D, stream=None):
+    _check(load().mt_add_rmsnorm_backward(_ptr(S), _ptr(gamma), _ptr(dY), _ptr(dS), _ptr(rstd),
+                                          _ptr(dX), _ptr(dgamma), N, D, _stream(stream)),
+           "mt_add_rmsnorm_backward")
+
+
+def mt_add_rmsnorm_backward_ws(S, gamma, dY, dS, rstd, dX, dgamma, N, D, workspace,
+                               workspace_bytes, stream=None):
+    _check(load().mt_add_rmsnorm_backward_ws(_ptr(S), _ptr(gamma), _ptr(dY), _ptr(dS),
+                                             _ptr(rstd), _ptr(dX), _ptr(dgamma), N, D,
+                                             _ptr(workspace), workspace_bytes, _stream(stream)),
+           "mt_add_rmsnorm_backward_ws")
+
+
+def mt_norm_backward_workspace_size(op, N, D, device=0) -> int:
+    out = _SZ(0)
+    _check(load().mt_norm_backward_workspace_size(op, N, D, device, ctypes.byref(out)),
+           "mt_norm_backward_workspace_size")
+    return int(out.value)
+
+
+def mt_last_cuda_error() -> int:
+    return load().mt_last_cuda_error()
+
+
+def mt_status_string(status: int) -> str:
+    return load().mt_status_string(status).decode()
+
+
+def mt_norm_version() -> int:
+    return load().mt_norm_version()
+
+
+# ---------------------------------------------------- allocating wrappers ---
+
+def _new(like, shape, dtype):
+    import torch
+    return torch.empty(shape, dtype=dtype, device=like.device)
+
+
+def _workspace(op, x):
+    import torch
+    n, d = x.shape
+    nbytes = mt_norm_backward_workspace_size(op, n, d, x.device.index or 0)
+    return torch.empty(nbytes, dtype=torch.uint8, device=x.device), nbytes
+
+
+def rmsnorm_forward(x, gamma, eps=1e-5):
+    """-> (y fp16 [N,D], rstd fp32 [N])"""
+    import torch
+    n, d = x.shape
+    y = _new(x, (n, d), torch.float16)
+    rstd = _new(x, (n,), torch.float32)
+    mt_rmsnorm_forward(x, gamma, y, rstd, n, d, eps)
+    return y, rstd
+
+
+def rmsnorm_backward(x, gamma, dy, rstd):
+    """-> (dx fp16 [N,D], dgamma fp32 [D])"""
+    import torch
+    n, d = x.shape
+    dx = _new(x, (n, d), torch.float16)
+    dgamma = _new(x, (d,), torch.float32)
+    ws, nbytes = _workspace(MT_OP_RMSNORM, x)
+    mt_rmsnorm_backward_ws(x, gamma, dy, rstd, dx, dgamma, n, d, ws, nbytes)
+    return dx, dgamma
+
+
+def layernorm_forward(x, gamma, beta, eps=1e-5):
+    """-> (y fp16 [N,D], mean fp32 [N], rstd fp32 [N])"""
+    import torch
+    n, d = x.shape
+    y = _new(x, (n, d), torch.float16)
+    mean = _new(x, (n,), torch.float32)
+    rstd = _new(x, (n,), torch.float32)
+    mt_layernorm_forward(x, gamma, beta, y, mean, rstd, n, d, eps)
+    return y, mean, rstd
+
+
+def layernorm_backward(x, gamma, dy, mean, rstd):
+    """-> (dx fp16 [N,D], dgamma fp32 [D], dbeta fp32 [D])"""
+    import torch
+    n, d = x.shape
+    dx = _new(x, (n, d), torch.float16)
+    dgamma = _new(x, (d,), torch.float32)
+    dbeta = _new(x, (d,), torch.float32)
+    ws, nbytes = _workspace(MT_OP_LAYERNORM, x)
+    mt_layernorm_backward_ws(x, gamma, dy, mean, rstd, dx, dgamma, dbeta, n, d, ws, nbytes)
+    return dx, dgamma, dbeta
+
+
+def add_rmsnorm_forward(x, r, gamma, eps=1e-5):
+    """-> (y fp16 [N,D], s fp16 [N,D] residual sum, rstd fp32 [N])"""
+    import torch
+    n, d = x.shape
+    y = _new(x, (n, d), torch.float16)
+    s = _new(x, (n, d), torch.float16)
+    rstd = _new(x, (n,), torch.float32)
+    mt_add_rmsnorm_forward(x, r, gamma, s, y, rstd, n, d, eps)
+    return y, s, rstd
+
+
+def add_rmsnorm_backward(s, gamma, dy, ds, rstd):
+    """-> (dx fp16 [N,D] (= d source = d residual), dgamma fp32 [D]); ds may be None."""
+    import torch
+    n, d = s.shape
+    dx = _new(s, (n, d), torch.float16)
+    dgamma = _new(s, (d,), torch.float32)
+    ws, nbytes = _workspace(MT_OP_ADD_RMSNORM, s)
+    mt_add_rmsnorm_backward_ws(s, gamma, dy, ds, rstd, dx, dgamma, n, d, ws, nbytes)
+    return dx, dgamma

@@ -1,0 +1,405 @@
+// kernels.cuh -- sm_103a kernels for row-wise normalization (RMSNorm, LayerNorm,
+// fused residual-add + RMSNorm), forward and backward.
+//
+// The work is HBM-bound (a few flops per 2-byte element), so there are no tensor
+// cores here; the design goal is to stream every byte exactly once:
+//
+//  * A row group of TPR threads (TPR = 32: one warp per row; TPR > 32: several warps
+//    per row) owns one row at a time. Thread t owns CH chunks of VEC contiguous
+//    elements, chunk k starting at column (k*TPR + t)*VEC, so a warp's loads of
+//    chunk k are contiguous and coalesced (VEC = 8: one 16-byte load per chunk).
+//  * The row stays in registers between the reduction and the apply, so X (and R,
+//    dY, S) is read from HBM exactly once.
+//  * Row reductions: warp butterfly (shfl.xor), then, when a row spans several
+//    warps, one shared-memory slot per warp summed by every thread in a fixed
+//    order. The butterfly leaves bitwise-identical sums on every lane, and every
+//    order is fixed, so results are reproducible bit for bit.
+//  * Backward: a persistent grid; CTA b takes row slots b, b + G, b + 2G, ... (a
+//    static assignment). Each thread keeps its columns' dgamma (and dbeta) sums in
+//    fp32 registers across its rows; at the end the CTA's row groups are combined in
+//    a fixed order and one fp32 partial row per CTA is written. A second small
+//    kernel sums the partials column by column in ascending CTA order. No atomics.
+//
+// Formulas (page title, section): meTile "Kernel coverage and training scope",
+// "Exact native normalization contract"; tensorcore "Training kernels",
+// "RMSnorm -- Llama-style" and "LayerNorm -- standard".
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mt {
+
+enum NormOp : int { kRms = 0, kLayer = 1, kAddRms = 2 };
+
+struct FwdArgs {
+    const __half *X;      // [N, D]
+    const __half *R;      // [N, D] residual (fused op only)
+    const __half *gamma;  // [D]
+    const __half *beta;   // [D] (LayerNorm only)
+    __half *S;            // [N, D] residual sum out (fused op only)
+    __half *Y;            // [N, D]
+    float *mean;          // [N] (LayerNorm only)
+    float *rstd;          // [N]
+    int64_t N;
+    int D;
+    float eps;
+};
+
+struct BwdArgs {
+    const __half *X;      // [N, D]: X (RMSNorm, LayerNorm) or the saved S (fused op)
+    const __half *gamma;  // [D]
+    const __half *dY;     // [N, D]
+    const __half *dS;     // [N, D] or nullptr (fused op only)
+    const float *mean;    // [N] (LayerNorm only)
+    const float *rstd;    // [N]
+    __half *dX;           // [N, D]
+    float *part_g;        // [P, D] dgamma partials, one row per CTA
+    float *part_b;        // [P, D] dbeta partials (LayerNorm only)
+    int64_t N;
+    int D;
+};
+
+// ------------------------------------------------------------------ helpers ---
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float2 half2_bits_to_float2(uint32_t w) {
+    __half2 h = *reinterpret_cast<const __half2 *>(&w);
+    return __half22float2(h);
+}
+
+__device__ __forceinline__ uint32_t float2_to_half2_bits(float a, float b) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// Raw storage of one chunk of VEC fp16 values, kept packed in registers.
+template <int VEC> struct Raw;
+template <> struct Raw<8> { uint4 v; };
+template <> struct Raw<1> { unsigned short v; };
+
+// Streaming (evict-first) load of one activation chunk; columns at or past D read 0.
+template <int VEC>
+__device__ __forceinline__ void load_act(const __half *row, int col, int D, Raw<VEC> &r) {
+    if constexpr (VEC == 8) {
+        if (col < D) r.v = __ldcs(reinterpret_cast<const uint4 *>(row + col));
+        else r.v = make_uint4(0u, 0u, 0u, 0u);
+    } else {
+        r.v = (col < D) ? __half_as_ushort(__ldcs(row + col)) : (unsigned short)0;
+    }
+}
+
+template <int VEC>
+__device__ __forceinline__ float elem(const Raw<VEC> &r, int e) {
+    if constexpr (VEC == 8) {
+        const uint32_t w = (e < 2) ? r.v.x : (e < 4) ? r.v.y : (e < 6) ? r.v.z : r.v.w;
+        const float2 f = half2_bits_to_float2(w);
+        return (e & 1) ? f.y : f.x;
+    } else {
+        return __half2float(__ushort_as_half(r.v));
+    }
+}
+
+template <int VEC>
+__device__ __forceinline__ void unpack(const Raw<VEC> &r, float (&f)[VEC]) {
+    if constexpr (VEC == 8) {
+        float2 a = half2_bits_to_float2(r.v.x), b = half2_bits_to_float2(r.v.y);
+        float2 c = half2_bits_to_float2(r.v.z), d = half2_bits_to_float2(r.v.w);
+        f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+        f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
+    } else {
+        f[0] = __half2float(__ushort_as_half(r.v));
+    }
+}
+
+// Read-only cached load of a parameter chunk (gamma/beta); past D reads 0.
+template <int VEC>
+__device__ __forceinline__ void load_param(const __half *p, int col, int D, float (&f)[VEC]) {
+    Raw<VEC> r;
+    if constexpr (VEC == 8) {
+        if (col < D) r.v = __ldg(reinterpret_cast<const uint4 *>(p + col));
+        else r.v = make_uint4(0u, 0u, 0u, 0u);
+    } else {
+        r.v = (col < D) ? __half_as_ushort(__ldg(p + col)) : (unsigned short)0;
+    }
+    unpack<VEC>(r, f);
+}
+
+// Round VEC fp32 values to fp16 (nearest even) and store; nothing is stored past D.
+template <int VEC>
+__device__ __forceinline__ void store_act(__half *row, int col, int D, const float (&f)[VEC]) {
+    if (col >= D) return;
+    if constexpr (VEC == 8) {
+        uint4 u;
+        u.x = float2_to_half2_bits(f[0], f[1]);
+        u.y = float2_to_half2_bits(f[2], f[3]);
+        u.z = float2_to_half2_bits(f[4], f[5]);
+        u.w = float2_to_half2_bits(f[6], f[7]);
+        *reinterpret_cast<uint4 *>(row + col) = u;
+    } else {
+        row[col] = __float2half_rn(f[0]);
+    }
+}
+
+// Sum NV values over the TPR threads of one row group. `red` holds
+// 2 (buffers) x RPC x WPR x NV floats; alternate `buf` between consecutive calls so
+// one __syncthreads per call suffices. Every thread of the CTA must call it when
+// WPR > 1 (it contains a CTA-wide barrier).
+template <int TPR, int RPC, int NV>
+__device__ __forceinline__ void row_sum(float (&v)[NV], float *red, int buf, int rg, int wir,
+                                        int lane) {
+    constexpr int WPR = TPR / 32;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) v[i] = warp_sum(v[i]);
+    if constexpr (WPR > 1) {
+        float *s = red + ((buf * RPC + rg) * WPR) * NV;
+        if (lane == 0) {
+#pragma unroll
+            for (int i = 0; i < NV; ++i) s[wir * NV + i] = v[i];
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            float t = 0.f;
+#pragma unroll
+            for (int w = 0; w < WPR; ++w) t += s[w * NV + i];
+            v[i] = t;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ forward ---
+// One row group per row; grid = ceil(N / RPC) CTAs of TPR*RPC threads.
+template <int OP, int TPR, int RPC, int CH, int VEC>
+__global__ void __launch_bounds__(TPR * RPC)
+norm_fwd_kernel(const FwdArgs a) {
+    static_assert(TPR % 32 == 0 && TPR * RPC <= 1024, "bad launch shape");
+    constexpr int WPR = TPR / 32;
+    __shared__ float red[2 * RPC * WPR];
+
+    const int tid = threadIdx.x;
+    const int rg = tid / TPR, t = tid % TPR, wir = t / 32, lane = tid % 32;
+    const int D = a.D;
+    const int64_t row = (int64_t)blockIdx.x * RPC + rg;
+    const bool ok = row < a.N;
+    // A single-warp row group has no CTA barrier, so it may leave early; wider row
+    // groups run masked (all loads read 0, nothing is stored) to reach the barriers.
+    if (WPR == 1 && !ok) return;
+    const int64_t off = (ok ? row : 0) * (int64_t)D;
+    const int lim = ok ? D : 0;  // masked row: every column counts as past the end
+
+    float x[CH][VEC];
+#pragma unroll
+    for (int k = 0; k < CH; ++k) {
+        const int col = (k * TPR + t) * VEC;
+        Raw<VEC> r;
+        load_act<VEC>(a.X + off, col, lim, r);
+        unpack<VEC>(r, x[k]);
+        if constexpr (OP == kAddRms) {
+            // fused op: s = x + r in fp32, normalise the unrounded s, store fp16(s)
+            Raw<VEC> rr;
+            float res[VEC];
+            load_act<VEC>(a.R + off, col, lim, rr);
+            unpack<VEC>(rr, res);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) x[k][e] += res[e];
+            store_act<VEC>(a.S + off, col, lim, x[k]);
+        }
+    }
+
+    float mu = 0.f;
+    if constexpr (OP == kLayer) {
+        float s[1] = {0.f};
+#pragma unroll
+        for (int k = 0; k < CH; ++k)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) s[0] += x[k][e];
+        row_sum<TPR, RPC, 1>(s, red, 0, rg, wir, lane);
+        mu = s[0] / (float)D;
+    }
+    float q[1] = {0.f};
+#pragma unroll
+    for (int k = 0; k < CH; ++k) {
+        const int col = (k * TPR + t) * VEC;
+        const bool valid = col < lim;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+            // LayerNorm: centred second moment (two-pass, from registers)
+            const float d = (OP == kLayer) ? (valid ? x[k][e] - mu : 0.f) : x[k][e];
+            q[0] += d * d;
+        }
+    }
+    row_sum<TPR, RPC, 1>(q, red, 1, rg, wir, lane);
+    const float rs = rsqrtf(q[0] / (float)D + a.eps);
+    if (!ok) return;  // after the last barrier
+    if (t == 0) {
+        a.rstd[row] = rs;
+        if constexpr (OP == kLayer) a.mean[row] = mu;
+    }
+
+#pragma unroll
+    for (int k = 0; k < CH; ++k) {
+        const int col = (k * TPR + t) * VEC;
+        if (col >= D) continue;
+        float g[VEC], y[VEC];
+        load_param<VEC>(a.gamma, col, D, g);
+        if constexpr (OP == kLayer) {
+            float b[VEC];
+            load_param<VEC>(a.beta, col, D, b);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) y[e] = (x[k][e] - mu) * rs * g[e] + b[e];
+        } else {
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) y[e] = x[k][e] * rs * g[e];
+        }
+        store_act<VEC>(a.Y + off, col, D, y);
+    }
+}
+
+// ----------------------------------------------------------------- backward ---
+// Persistent: grid = P CTAs of TPR*RPC threads; CTA b processes row slots
+// b*RPC + j*G*RPC (G = gridDim.x), row group rg taking row slot + rg.
+// Dynamic shared memory (RPC > 1): NV x D floats for the fixed-order combine.
+template <int OP, int TPR, int RPC, int CH, int VEC, bool HAS_DS>
+__global__ void __launch_bounds__(TPR * RPC)
+norm_bwd_kernel(const BwdArgs a) {
+    static_assert(TPR % 32 == 0 && TPR * RPC <= 1024, "bad launch shape");
+    constexpr int WPR = TPR / 32;
+    constexpr int NV = (OP == kLayer) ? 2 : 1;
+    __shared__ float red[2 * RPC * WPR * NV];
+    extern __shared__ float comb[];
+
+    const int tid = threadIdx.x;
+    const int rg = tid / TPR, t = tid % TPR, wir = t / 32, lane = tid % 32;
+    const int D = a.D;
+    const float inv_d = 1.0f / (float)D;
+
+    float accg[CH][VEC];
+    float accb[CH][(OP == kLayer) ? VEC : 1];
+#pragma unroll
+    for (int k = 0; k < CH; ++k) {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) accg[k][e] = 0.f;
+#pragma unroll
+        for (int e = 0; e < ((OP == kLayer) ? VEC : 1); ++e) accb[k][e] = 0.f;
+    }
+
+    int buf = 0;
+    for (int64_t base = (int64_t)blockIdx.x * RPC; base < a.N;
+         base += (int64_t)gridDim.x * RPC, buf ^= 1) {
+        const int64_t row = base + rg;
+        const bool ok = row < a.N;
+        if (WPR == 1 && !ok) continue;  // single-warp row group: no CTA barrier inside
+        const int64_t off = (ok ? row : 0) * (int64_t)D;
+        const int lim = ok ? D : 0;
+        const float r = ok ? a.rstd[row] : 0.f;
+        const float mu = (OP == kLayer && ok) ? a.mean[row] : 0.f;
+
+        Raw<VEC> xr[CH], dyr[CH];
+#pragma unroll
+        for (int k = 0; k < CH; ++k) {
+            const int col = (k * TPR + t) * VEC;
+            load_act<VEC>(a.X + off, col, lim, xr[k]);
+            load_act<VEC>(a.dY + off, col, lim, dyr[k]);
+        }
+
+        // pass 1 (registers): sum_j g*xhat and, for LayerNorm, sum_j g
+        float v[NV];
+#pragma unroll
+        for (int i = 0; i < NV; ++i) v[i] = 0.f;
+#pragma unroll
+        for (int k = 0; k < CH; ++k) {
+            const int col = (k * TPR + t) * VEC;
+            float gm[VEC], xv[VEC], dv[VEC];
+            load_param<VEC>(a.gamma, col, lim, gm);
+            unpack<VEC>(xr[k], xv);
+            unpack<VEC>(dyr[k], dv);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                const float xh = (xv[e] - mu) * r;
+                const float g = dv[e] * gm[e];
+                v[0] += g * xh;
+                if constexpr (OP == kLayer) v[NV - 1] += g;
+            }
+        }
+        row_sum<TPR, RPC, NV>(v, red, buf, rg, wir, lane);
+        const float c = v[0] * inv_d;
+        const float am = (OP == kLayer) ? v[NV - 1] * inv_d : 0.f;
+        if (!ok) continue;
+
+        // pass 2: dX and the parameter-gradient sums
+#pragma unroll
+        for (int k = 0; k < CH; ++k) {
+            const int col = (k * TPR + t) * VEC;
+            if (col >= D) continue;
+            float gm[VEC], xv[VEC], dv[VEC], o[VEC];
+            load_param<VEC>(a.gamma, col, D, gm);
+            unpack<VEC>(xr[k], xv);
+            unpack<VEC>(dyr[k], dv);
+            float ds[VEC];
+            if constexpr (HAS_DS) {
+                Raw<VEC> dsr;
+                load_act<VEC>(a.dS + off, col, D, dsr);
+                unpack<VEC>(dsr, ds);
+            }
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                const float xh = (xv[e] - mu) * r;
+                const float g = dv[e] * gm[e];
+                float dx = r * ((g - am) - xh * c);
+                if constexpr (HAS_DS) dx += ds[e];
+                o[e] = dx;
+                accg[k][e] += dv[e] * xh;
+                if constexpr (OP == kLayer) accb[k][e] += dv[e];
+            }
+            store_act<VEC>(a.dX + off, col, D, o);
+        }
+    }
+
+    // Combine this CTA's row groups in the fixed order rg = 0, 1, ..., RPC-1 and
+    // write one partial row per CTA. Thread t owns the same columns in every group.
+    float *pg = a.part_g + (size_t)blockIdx.x * D;
+    float *pb = (OP == kLayer) ? a.part_b + (size_t)blockIdx.x * D : nullptr;
+    if constexpr (RPC == 1) {
+#pragma unroll
+        for (int k = 0; k < CH; ++k) {
+            const int col = (k * TPR + t) * VEC;
+            if (col >= D) continue;
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                pg[col + e] = accg[k][e];
+                if constexpr (OP == kLayer) pb[col + e] = accb[k][e];
+            }
+        }
+    } else {
+        float *cg = comb;
+        float *cb = comb + D;
+        for (int j = 0; j < RPC; ++j) {
+            if (rg == j) {
+#pragma unroll
+                for (int k = 0; k < CH; ++k) {
+                    const int col = (k * TPR + t) * VEC;
+                    if (col >= D) continue;
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) {
+                        const float sg = (j == 0) ? accg[k][e] : cg[col + e] + accg[k][e];
+                        if (j == RPC - 1) pg[col + e] = sg; else cg[col + e] = sg;
+                        if constexpr (OP == kLayer) {
+                            const float sb = (j == 0) ? accb[k][e] : cb[col + e] + accb[k][e];
+                            if (j == RPC - 1) pb[col + e] = sb; else cb[col + e] = sb;
+                        }
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
+}  // namespace mt

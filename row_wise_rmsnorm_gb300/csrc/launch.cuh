@@ -1,0 +1,140 @@
+// launch.cuh -- launch shapes and per-op planning for the normalization kernels.
+//
+// A launch shape is (TPR threads per row, RPC rows per CTA, CH chunks per thread,
+// VEC fp16 elements per chunk). VEC = 8 (one 16-byte access per chunk) is legal when
+// D % 8 == 0 and every row base is 16-byte aligned; VEC = 1 covers everything else.
+// The first shape whose width covers D is taken. Forward rows up to 1024 wide get one
+// warp each (four rows per CTA); wider rows get one CTA each. The backward uses the
+// same split with more rows per CTA, so that few persistent CTAs cover the device
+// and the dgamma/dbeta partials stay small.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "kernels.cuh"
+
+namespace mt {
+
+// X(max_D, TPR, RPC, CH)
+#define MT_FWD_SHAPES_VEC8(X) \
+    X(256, 32, 4, 1)          \
+    X(512, 32, 4, 2)          \
+    X(1024, 32, 4, 4)         \
+    X(2048, 128, 1, 2)        \
+    X(4096, 256, 1, 2)        \
+    X(8192, 512, 1, 2)        \
+    X(16384, 1024, 1, 2)
+
+#define MT_FWD_SHAPES_VEC1(X) \
+    X(64, 32, 4, 2)           \
+    X(128, 32, 4, 4)          \
+    X(256, 32, 4, 8)          \
+    X(512, 32, 4, 16)         \
+    X(1024, 32, 4, 32)        \
+    X(2048, 128, 1, 16)       \
+    X(4096, 256, 1, 16)       \
+    X(8192, 512, 1, 16)       \
+    X(16384, 1024, 1, 16)
+
+#define MT_BWD_SHAPES_VEC8(X) \
+    X(256, 32, 8, 1)          \
+    X(512, 32, 8, 2)          \
+    X(1024, 32, 8, 4)         \
+    X(2048, 128, 4, 2)        \
+    X(4096, 256, 2, 2)        \
+    X(8192, 512, 1, 2)        \
+    X(16384, 512, 1, 4)
+
+#define MT_BWD_SHAPES_VEC1(X) \
+    X(64, 32, 8, 2)           \
+    X(128, 32, 8, 4)          \
+    X(256, 32, 8, 8)          \
+    X(512, 32, 8, 16)         \
+    X(1024, 64, 4, 16)        \
+    X(2048, 128, 4, 16)       \
+    X(4096, 256, 2, 16)       \
+    X(8192, 512, 1, 16)       \
+    X(16384, 512, 1, 32)
+
+struct LaunchPlan {
+    const void *kernel = nullptr;
+    int threads = 0;
+    int grid = 0;       // forward: ceil(N / RPC); backward: persistent CTA count P
+    size_t smem = 0;    // dynamic shared memory bytes
+    int rows_per_cta = 0;
+};
+
+// Host helpers defined in api.cu (cached per device; thread-safe).
+cudaError_t device_sm_count(int device, int *sms);
+cudaError_t cached_occupancy(const void *kernel, int threads, size_t smem, int device,
+                             int *blocks_per_sm);
+
+template <int OP, int TPR, int RPC, int CH, int VEC>
+LaunchPlan fwd_plan_shape(int64_t N) {
+    LaunchPlan p;
+    p.kernel = reinterpret_cast<const void *>(&norm_fwd_kernel<OP, TPR, RPC, CH, VEC>);
+    p.threads = TPR * RPC;
+    p.grid = (int)((N + RPC - 1) / RPC);
+    p.rows_per_cta = RPC;
+    return p;
+}
+
+template <int OP>
+LaunchPlan fwd_plan(int64_t N, int D, bool vec8) {
+#define MT_TRY(maxd, tpr, rpc, ch) \
+    if (D <= maxd) return fwd_plan_shape<OP, tpr, rpc, ch, VEC>(N);
+    if (vec8) {
+        constexpr int VEC = 8;
+        MT_FWD_SHAPES_VEC8(MT_TRY)
+    } else {
+        constexpr int VEC = 1;
+        MT_FWD_SHAPES_VEC1(MT_TRY)
+    }
+#undef MT_TRY
+    return LaunchPlan{};
+}
+
+template <int OP, int TPR, int RPC, int CH, int VEC, bool HAS_DS>
+cudaError_t bwd_plan_shape(int64_t N, int D, int device, LaunchPlan *p) {
+    constexpr int NV = (OP == kLayer) ? 2 : 1;
+    p->kernel = reinterpret_cast<const void *>(&norm_bwd_kernel<OP, TPR, RPC, CH, VEC, HAS_DS>);
+    p->threads = TPR * RPC;
+    p->smem = (RPC > 1) ? (size_t)NV * (size_t)D * sizeof(float) : 0;
+    p->rows_per_cta = RPC;
+    int per_sm = 0, sms = 0;
+    cudaError_t e = cached_occupancy(p->kernel, p->threads, p->smem, device, &per_sm);
+    if (e != cudaSuccess) return e;
+    e = device_sm_count(device, &sms);
+    if (e != cudaSuccess) return e;
+    const int64_t slots = (N + RPC - 1) / RPC;
+    const int64_t cap = (int64_t)sms * (int64_t)std::max(per_sm, 1);
+    p->grid = (int)std::min(slots, cap);
+    return cudaSuccess;
+}
+
+template <int OP, bool HAS_DS>
+cudaError_t bwd_plan(int64_t N, int D, bool vec8, int device, LaunchPlan *p) {
+#define MT_TRY(maxd, tpr, rpc, ch) \
+    if (D <= maxd) return bwd_plan_shape<OP, tpr, rpc, ch, VEC, HAS_DS>(N, D, device, p);
+    if (vec8) {
+        constexpr int VEC = 8;
+        MT_BWD_SHAPES_VEC8(MT_TRY)
+    } else {
+        constexpr int VEC = 1;
+        MT_BWD_SHAPES_VEC1(MT_TRY)
+    }
+#undef MT_TRY
+    return cudaErrorInvalidValue;
+}
+
+// Per-op entry points, one translation unit each (compiled in parallel).
+LaunchPlan fwd_plan_rms(int64_t N, int D, bool vec8);
+LaunchPlan fwd_plan_layer(int64_t N, int D, bool vec8);
+LaunchPlan fwd_plan_add(int64_t N, int D, bool vec8);
+cudaError_t bwd_plan_rms(int64_t N, int D, bool vec8, int device, LaunchPlan *p);
+cudaError_t bwd_plan_layer(int64_t N, int D, bool vec8, int device, LaunchPlan *p);
+cudaError_t bwd_plan_add(int64_t N, int D, bool vec8, bool has_ds, int device, LaunchPlan *p);
+
+}  // namespace mt

@@ -1,0 +1,140 @@
+"""The C ABI on the host (no GPU): the library builds, exports every symbol that
+include/mt_norm.h declares, and rejects bad arguments before any CUDA call.
+
+Only calls whose arguments fail validation are made here, with fake addresses
+that are never dereferenced: validation returns before any CUDA call.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import row_wise_rmsnorm_gb300 as mt
+from row_wise_rmsnorm_gb300 import build as mtbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mt_norm.h")
+INV, UNS = mt.MT_ERR_INVALID_ARG, mt.MT_ERR_UNSUPPORTED
+
+# fake, distinct, 16-byte-aligned addresses: validation never dereferences them
+A, B, C, E, F, G, H, K, L = (0x10000 * (i + 1) for i in range(9))
+BIG = 1 << 40
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mtbuild.build()
+    return mt.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:mt_status_t|int|const char \*)\s*(mt_\w+)\(", text,
+                                 re.M)))
+
+
+def test_header_is_plain_c():
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-fsyntax-only", "-x", "c", HEADER],
+                   check=True)
+
+
+def test_exports_every_declared_symbol(lib):
+    decl = declared_functions()
+    assert len(decl) == 13
+    assert sorted(mt.EXPORTED) == decl
+    out = subprocess.run(["nm", "-D", "--defined-only", mt.library_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (mt_\w+)$", out, re.M))
+    assert set(decl) <= exported
+    for name in decl:
+        assert getattr(lib, name) is not None
+
+
+def test_library_targets_sm_103a_only():
+    assert "arch=compute_103a,code=sm_103a" in " ".join(mtbuild.NVCC_FLAGS)
+    assert not any("fast-math" in f or "use_fast_math" in f for f in mtbuild.NVCC_FLAGS)
+
+
+def test_status_strings(lib):
+    for code in range(4):
+        assert lib.mt_status_string(code)
+    assert lib.mt_norm_version() >= 100
+    assert lib.mt_last_cuda_error() == 0
+
+
+@pytest.mark.parametrize("case", ["null", "n0", "d0", "nneg", "dwide", "nhuge", "eps0", "epsneg",
+                                  "epsnan", "epsinf", "alias", "overlap_stats"])
+def test_rmsnorm_forward_validation(lib, case):
+    args = dict(X=A, g=B, Y=C, r=E, N=4, D=64, eps=1e-5)
+    expect = INV
+    if case == "null": args["X"] = None
+    if case == "n0": args["N"] = 0
+    if case == "d0": args["D"] = 0
+    if case == "nneg": args["N"] = -3
+    if case == "dwide": args["D"], expect = mt.MT_MAX_COLS + 1, UNS
+    if case == "nhuge": args["N"], expect = 2 ** 31, UNS
+    if case == "eps0": args["eps"] = 0.0
+    if case == "epsneg": args["eps"] = -1e-5
+    if case == "epsnan": args["eps"] = float("nan")
+    if case == "epsinf": args["eps"] = float("inf")
+    if case == "alias": args["Y"] = args["X"]
+    if case == "overlap_stats": args["r"] = args["X"] + 8  # rstd inside X
+    st = lib.mt_rmsnorm_forward(args["X"], args["g"], args["Y"], args["r"], args["N"],
+                                args["D"], args["eps"], None)
+    assert st == expect
+
+
+def test_backward_validation(lib):
+    N, D = 8, 64
+    # RMSNorm backward: NULLs, shapes, dX aliasing dY, dgamma aliasing gamma
+    assert lib.mt_rmsnorm_backward(A, B, C, E, F, None, N, D, None) == INV
+    assert lib.mt_rmsnorm_backward(A, B, C, E, F, G, 0, D, None) == INV
+    assert lib.mt_rmsnorm_backward(A, B, C, E, F, G, N, 20000, None) == UNS
+    assert lib.mt_rmsnorm_backward(A, B, C, E, C, G, N, D, None) == INV
+    assert lib.mt_rmsnorm_backward(A, B, C, E, F, B, N, D, None) == INV
+    # _ws: NULL / misaligned / overlapping workspace
+    assert lib.mt_rmsnorm_backward_ws(A, B, C, E, F, G, N, D, None, 1 << 20, None) == INV
+    assert lib.mt_rmsnorm_backward_ws(A, B, C, E, F, G, N, D, H + 4, 1 << 20, None) == INV
+    assert lib.mt_rmsnorm_backward_ws(A, B, C, E, F, G, N, D, A, 1 << 20, None) == INV
+    # LayerNorm
+    assert lib.mt_layernorm_backward(A, B, C, E, F, G, H, None, N, D, None) == INV
+    assert lib.mt_layernorm_backward(A, B, C, E, F, G, H, H, N, D, None) == INV  # dgamma == dbeta
+    assert lib.mt_layernorm_backward_ws(A, B, C, E, F, G, H, K, N, D, None, 0, None) == INV
+    # fused op: dS is nullable, others are not; dX may not alias dS
+    assert lib.mt_add_rmsnorm_backward(None, B, C, None, E, F, G, N, D, None) == INV
+    assert lib.mt_add_rmsnorm_backward(A, B, C, K, E, K, G, N, D, None) == INV
+    assert lib.mt_add_rmsnorm_backward_ws(A, B, C, None, E, F, G, N, D, None, 0, None) == INV
+
+
+def test_forward_validation_other_ops(lib):
+    N, D = 8, 64
+    assert lib.mt_layernorm_forward(A, B, None, C, E, F, N, D, 1e-5, None) == INV
+    assert lib.mt_layernorm_forward(A, B, C, E, F, F, N, D, 1e-5, None) == INV  # mean == rstd
+    assert lib.mt_layernorm_forward(A, B, C, E, F, G, N, D, 0.0, None) == INV
+    assert lib.mt_add_rmsnorm_forward(A, B, C, E, E, F, N, D, 1e-6, None) == INV  # S == Y
+    assert lib.mt_add_rmsnorm_forward(A, B, C, B, E, F, N, D, 1e-6, None) == INV  # S == R
+    assert lib.mt_add_rmsnorm_forward(A, B, C, E, F, G, N, 0, 1e-6, None) == INV
+
+
+def test_workspace_size_validation(lib):
+    out = ctypes.c_size_t(0)
+    assert lib.mt_norm_backward_workspace_size(0, 8, 64, 0, None) == INV
+    assert lib.mt_norm_backward_workspace_size(7, 8, 64, 0, ctypes.byref(out)) == INV
+    assert lib.mt_norm_backward_workspace_size(0, 0, 64, 0, ctypes.byref(out)) == INV
+    assert lib.mt_norm_backward_workspace_size(1, 8, 20000, 0, ctypes.byref(out)) == UNS
+    assert lib.mt_norm_backward_workspace_size(2, 8, 64, -1, ctypes.byref(out)) == INV
+    assert lib.mt_last_cuda_error() == 0  # nothing reached CUDA
+
+
+def test_product_path_does_not_import_oracle():
+    """The binding and the kernels never reach the oracle (test infrastructure)."""
+    pkg = os.path.join(ROOT, "row_wise_rmsnorm_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        if "_build" in dirpath:
+            continue
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "oracle" not in text.lower(), f"{f} mentions the oracle"

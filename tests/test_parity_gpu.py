@@ -1,0 +1,247 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Covers the five named workloads (the three large ones at full size, in the launch
+configuration the benchmark times, with Y/dX/stats compared on sampled rows and
+dgamma/dbeta on every column), a sweep of ragged and aligned widths, the scalar
+path on misaligned rows, the persistent backward over many rows, bitwise run-to-run
+determinism, NaN containment, out-of-bounds writes (canaries), the optional dS of
+the fused op, workspace handling and streams.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import row_wise_rmsnorm_gb300 as mt
+import workloads as W
+from parity import compare, f64, gpu_run, oracle_run
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.fail("a CUDA device is required for the -m gpu tests")
+    from row_wise_rmsnorm_gb300 import build
+    build.build()
+    mt.load()
+
+
+def to_dev(t):
+    return {k: v.to(DEV) for k, v in t.items()}
+
+
+# ------------------------------------------------------------- workloads ---
+
+@pytest.mark.parametrize("name", ["rmsnorm_17x257", "layernorm_128x1024"])
+def test_small_workloads_every_element(name):
+    w = W.WORKLOADS[name]
+    t = W.generate_workload(name)
+    got = gpu_run(w.op, to_dev(t), w.eps)
+    torch.cuda.synchronize()
+    ref = oracle_run(w.op, t, w.eps)
+    compare(w.op, got, ref, t["X"], tag=name)
+
+
+@pytest.mark.parametrize("name", ["rmsnorm_16384x4096", "add_rmsnorm_32768x4096",
+                                  "layernorm_2048x16384"])
+def test_full_size_workloads(name):
+    """Full-size inputs drawn on the device; stats/Y/dX on 96 sampled rows (first,
+    last and random), dgamma/dbeta over every column against the oracle on all rows."""
+    w = W.WORKLOADS[name]
+    t = W.generate_workload(name, device=DEV)
+    got = gpu_run(w.op, t, w.eps)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(5)
+    rows = np.unique(np.concatenate([[0, 1, w.N - 1], rng.integers(0, w.N, 93)]))
+    host = {k: v.cpu() for k, v in t.items()}
+    ref = oracle_run(w.op, host, w.eps, rows=rows)
+    compare(w.op, got, ref, host["X"], rows=rows, tag=name)
+
+
+def test_fused_without_residual_cotangent():
+    t = W.generate("add_rmsnorm", 333, 1000, with_ds=True)
+    got = gpu_run(W.ADD_RMSNORM, to_dev(t), 1e-6, use_ds=False)
+    ref = oracle_run(W.ADD_RMSNORM, t, 1e-6, use_ds=False)
+    compare(W.ADD_RMSNORM, got, ref, t["X"], tag="add, dS absent")
+
+
+# ----------------------------------------------------------- shape sweep ---
+
+SWEEP_D = [1, 2, 7, 8, 31, 32, 33, 127, 255, 257, 1023, 1024, 1025, 2048, 4095, 4096, 8191, 8192,
+           16384]
+
+
+@pytest.mark.parametrize("op", W.OPS)
+@pytest.mark.parametrize("D", SWEEP_D)
+def test_width_sweep(op, D):
+    for N in (1, 2, 17, 1000 if D <= 4096 else 200):
+        t = W.generate(op, N, D, seed=D + N, x_kind="normal", dy_std=1.0)
+        got = gpu_run(op, to_dev(t), 1e-5)
+        ref = oracle_run(op, t, 1e-5)
+        compare(op, got, ref, t["X"], tag=f"{op} N={N} D={D}")
+
+
+@pytest.mark.parametrize("op", W.OPS)
+@pytest.mark.parametrize("N,D", [(40000, 64), (20000, 1024), (3000, 4096), (700, 16384)])
+def test_persistent_backward_many_rows(op, N, D):
+    """Enough rows that each persistent backward CTA loops over many row slots."""
+    t = W.generate(op, N, D, seed=7, dy_std=1.0)
+    got = gpu_run(op, to_dev(t), 1e-5)
+    ref = oracle_run(op, t, 1e-5)
+    compare(op, got, ref, t["X"], tag=f"{op} N={N} D={D}")
+
+
+@pytest.mark.parametrize("op", W.OPS)
+@pytest.mark.parametrize("D", [64, 1024, 4096, 16384])
+def test_misaligned_rows_take_scalar_path(op, D):
+    """Every tensor starts 2 bytes past a 16-byte boundary: results stay within tolerance."""
+    N = 37
+    t = W.generate(op, N, D, seed=3, dy_std=1.0)
+    shifted = {}
+    for k, v in t.items():
+        buf = torch.empty(v.numel() + 8, dtype=v.dtype, device=DEV)
+        view = buf[1:1 + v.numel()].view(v.shape)
+        view.copy_(v.to(DEV))
+        assert view.data_ptr() % 16 == 2
+        shifted[k] = view
+    got = gpu_run(op, shifted, 1e-5)
+    ref = oracle_run(op, t, 1e-5)
+    compare(op, got, ref, t["X"], tag=f"{op} misaligned D={D}")
+
+
+# ------------------------------------------------- tolerance-free gates ---
+
+@pytest.mark.parametrize("op", W.OPS)
+@pytest.mark.parametrize("N,D", [(5000, 4096), (3000, 257), (600, 16384)])
+def test_bitwise_determinism(op, N, D):
+    t = to_dev(W.generate(op, N, D, seed=11, dy_std=0.5))
+    a = gpu_run(op, t, 1e-5)
+    b = gpu_run(op, t, 1e-5)
+    torch.cuda.synchronize()
+    for k in a:
+        assert torch.equal(a[k].view(torch.int16 if a[k].dtype == torch.float16 else torch.int32),
+                           b[k].view(torch.int16 if b[k].dtype == torch.float16 else torch.int32)), k
+
+
+@pytest.mark.parametrize("op", W.OPS)
+def test_nan_stays_in_its_row(op):
+    N, D, i, j = 64, 1024, 17, 300
+    t = W.generate(op, N, D, seed=13, dy_std=1.0)
+    t["dY"][i, j] = float("nan")
+    got = gpu_run(op, to_dev(t), 1e-5)
+    ref = oracle_run(op, t, 1e-5)
+    dX = f64(got["dX"])
+    assert np.isnan(dX[i]).all() and np.isfinite(np.delete(dX, i, axis=0)).all()
+    dg = f64(got["dgamma"])
+    assert np.isnan(dg[j]) and np.isfinite(np.delete(dg, j)).all()
+    # everything else still matches the oracle (NaN positions included)
+    got.pop("S", None)
+    ref.pop("S16", None)
+    compare(op, got, ref, t["X"], tag=f"{op} with a NaN cotangent")
+
+
+@pytest.mark.parametrize("op", W.OPS)
+@pytest.mark.parametrize("D", [257, 4096])
+def test_no_writes_outside_outputs(op, D):
+    """Outputs sit inside canary-filled buffers; the canaries must survive."""
+    N = 33
+    t = to_dev(W.generate(op, N, D, seed=17, dy_std=1.0))
+    pad = 64
+    canary16 = torch.tensor(-12345.0, dtype=torch.float16)
+    canary32 = -7.25e30
+
+    def padded(shape, dtype):
+        n = int(np.prod(shape))
+        buf = torch.full((n + 2 * pad,), canary32 if dtype == torch.float32 else canary16.item(),
+                         dtype=dtype, device=DEV)
+        return buf, buf[pad:pad + n].view(shape)
+
+    bufs = {}
+    X, g, dY = t["X"], t["gamma"], t["dY"]
+    for name, shape, dt in [("Y", (N, D), torch.float16), ("rstd", (N,), torch.float32),
+                            ("dX", (N, D), torch.float16), ("dg", (D,), torch.float32),
+                            ("mean", (N,), torch.float32), ("db", (D,), torch.float32),
+                            ("S", (N, D), torch.float16)]:
+        bufs[name] = padded(shape, dt)
+    o = {k: v[1] for k, v in bufs.items()}
+    if op == W.RMSNORM:
+        mt.mt_rmsnorm_forward(X, g, o["Y"], o["rstd"], N, D, 1e-5)
+        mt.mt_rmsnorm_backward(X, g, dY, o["rstd"], o["dX"], o["dg"], N, D)
+    elif op == W.LAYERNORM:
+        mt.mt_layernorm_forward(X, g, t["beta"], o["Y"], o["mean"], o["rstd"], N, D, 1e-5)
+        mt.mt_layernorm_backward(X, g, dY, o["mean"], o["rstd"], o["dX"], o["dg"], o["db"], N, D)
+    else:
+        mt.mt_add_rmsnorm_forward(X, t["R"], g, o["S"], o["Y"], o["rstd"], N, D, 1e-5)
+        mt.mt_add_rmsnorm_backward(o["S"], g, dY, t["dS"], o["rstd"], o["dX"], o["dg"], N, D)
+    torch.cuda.synchronize()
+    for name, (buf, _) in bufs.items():
+        head, tail = buf[:pad].cpu(), buf[-pad:].cpu()
+        want = canary32 if buf.dtype == torch.float32 else canary16.item()
+        assert (head == want).all() and (tail == want).all(), f"{op}: write outside {name}"
+
+
+# ------------------------------------------------------- API behaviour ---
+
+@pytest.mark.parametrize("op", W.OPS)
+def test_allocating_and_workspace_forms_agree_bitwise(op):
+    N, D = 2000, 2048
+    t = to_dev(W.generate(op, N, D, seed=19, dy_std=1.0))
+    a = gpu_run(op, t, 1e-5)
+    dX = torch.empty_like(a["dX"])
+    dg = torch.empty_like(a["dgamma"])
+    if op == W.RMSNORM:
+        mt.mt_rmsnorm_backward(t["X"], t["gamma"], t["dY"], a["rstd"], dX, dg, N, D)
+    elif op == W.LAYERNORM:
+        db = torch.empty_like(a["dbeta"])
+        mt.mt_layernorm_backward(t["X"], t["gamma"], t["dY"], a["mean"], a["rstd"], dX, dg, db,
+                                 N, D)
+        assert torch.equal(db, a["dbeta"])
+    else:
+        mt.mt_add_rmsnorm_backward(a["S"], t["gamma"], t["dY"], t["dS"], a["rstd"], dX, dg, N, D)
+    torch.cuda.synchronize()
+    assert torch.equal(dX, a["dX"]) and torch.equal(dg, a["dgamma"])
+
+
+def test_workspace_too_small_is_rejected():
+    N, D = 100, 512
+    t = to_dev(W.generate("rmsnorm", N, D))
+    y, rstd = mt.rmsnorm_forward(t["X"], t["gamma"])
+    need = mt.mt_norm_backward_workspace_size(mt.MT_OP_RMSNORM, N, D, 0)
+    ws = torch.empty(need, dtype=torch.uint8, device=DEV)
+    dX = torch.empty_like(t["X"])
+    dg = torch.empty(D, dtype=torch.float32, device=DEV)
+    with pytest.raises(mt.MtNormError) as e:
+        mt.mt_rmsnorm_backward_ws(t["X"], t["gamma"], t["dY"], rstd, dX, dg, N, D, ws, need - 256)
+    assert e.value.status == mt.MT_ERR_UNSUPPORTED
+
+
+def test_side_stream_and_convenience_wrappers():
+    N, D = 300, 768
+    t = W.generate("layernorm", N, D, seed=23, dy_std=1.0)
+    d = to_dev(t)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        y, mean, rstd = mt.layernorm_forward(d["X"], d["gamma"], d["beta"], eps=1e-5)
+        dx, dg, db = mt.layernorm_backward(d["X"], d["gamma"], d["dY"], mean, rstd)
+    s.synchronize()
+    got = dict(Y=y, mean=mean, rstd=rstd, dX=dx, dgamma=dg, dbeta=db)
+    compare(W.LAYERNORM, got, oracle_run(W.LAYERNORM, t, 1e-5), t["X"], tag="side stream")
+
+
+def test_invalid_arguments_raise_before_launch():
+    t = to_dev(W.generate("rmsnorm", 4, 64))
+    y = torch.empty_like(t["X"])
+    r = torch.empty(4, dtype=torch.float32, device=DEV)
+    with pytest.raises(mt.MtNormError) as e:
+        mt.mt_rmsnorm_forward(t["X"], t["gamma"], t["X"], r, 4, 64, 1e-5)  # in place
+    assert e.value.status == mt.MT_ERR_INVALID_ARG
+    with pytest.raises(mt.MtNormError) as e:
+        mt.mt_rmsnorm_forward(t["X"], t["gamma"], y, r, 4, 64, 0.0)
+    assert e.value.status == mt.MT_ERR_INVALID_ARG
+    with pytest.raises(mt.MtNormError) as e:
+        mt.mt_rmsnorm_forward(t["X"], t["gamma"], y, r, 4, mt.MT_MAX_COLS + 1, 1e-5)
+    assert e.value.status == mt.MT_ERR_UNSUPPORTED
