@@ -80,9 +80,14 @@ mt_status_t launch(const LaunchPlan &p, void *arg, cudaStream_t stream) {
 }
 
 mt_status_t run_forward(int op, const FwdArgs &a, bool vec8, mt_stream_t stream) {
-    LaunchPlan p = (op == kRms)     ? fwd_plan_rms(a.N, a.D, vec8)
-                   : (op == kLayer) ? fwd_plan_layer(a.N, a.D, vec8)
-                                    : fwd_plan_add(a.N, a.D, vec8);
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess) return cuda_fail(e);
+    LaunchPlan p;
+    e = (op == kRms)     ? fwd_plan_rms(a.N, a.D, vec8, device, &p)
+        : (op == kLayer) ? fwd_plan_layer(a.N, a.D, vec8, device, &p)
+                         : fwd_plan_add(a.N, a.D, vec8, device, &p);
+    if (e != cudaSuccess) return cuda_fail(e);
     FwdArgs copy = a;
     return launch(p, &copy, reinterpret_cast<cudaStream_t>(stream));
 }

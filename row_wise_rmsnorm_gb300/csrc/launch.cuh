@@ -14,6 +14,7 @@
 #include <algorithm>
 
 #include "kernels.cuh"
+#include "pipe.cuh"
 
 namespace mt {
 
@@ -38,15 +39,6 @@ namespace mt {
     X(8192, 512, 1, 16)       \
     X(16384, 1024, 1, 16)
 
-#define MT_BWD_SHAPES_VEC8(X) \
-    X(256, 32, 8, 1)          \
-    X(512, 32, 8, 2)          \
-    X(1024, 32, 8, 4)         \
-    X(2048, 128, 4, 2)        \
-    X(4096, 256, 2, 2)        \
-    X(8192, 512, 1, 2)        \
-    X(16384, 512, 1, 4)
-
 #define MT_BWD_SHAPES_VEC1(X) \
     X(64, 32, 8, 2)           \
     X(128, 32, 8, 4)          \
@@ -57,6 +49,33 @@ namespace mt {
     X(4096, 256, 2, 16)       \
     X(8192, 512, 1, 16)       \
     X(16384, 512, 1, 32)
+
+// Pipelined persistent shapes for 16-byte-aligned rows: X(max_D, TPR, RPC, CH, STAGES).
+// STAGES is the largest ring depth; pipe_stages() cuts it to fit shared memory.
+#define MT_FWD_PIPE_SHAPES(X)   \
+    X(2048, 256, 2, 1, 8)       \
+    X(4096, 512, 1, 1, 8)       \
+    X(8192, 512, 1, 2, 6)       \
+    X(16384, 512, 1, 4, 4)
+
+#define MT_BWD_PIPE_SHAPES(X)   \
+    X(256, 32, 16, 1, 6)        \
+    X(512, 64, 8, 1, 6)         \
+    X(1024, 128, 4, 1, 6)       \
+    X(2048, 256, 2, 1, 6)       \
+    X(4096, 512, 1, 1, 6)       \
+    X(8192, 512, 1, 2, 3)       \
+    X(16384, 512, 1, 4, 3)
+
+// Ring depth: the table's depth, cut so that ring + parameter slots fit the 227 KB of
+// dynamic shared memory a CTA may use, and never below 2.
+constexpr size_t kMaxDynSmem = 226 * 1024;
+constexpr int pipe_stages(int base, int narr, int npar, int ch, int threads) {
+    const size_t slot = (size_t)ch * threads * 16;
+    const int fit = (int)(((kMaxDynSmem / slot) - npar) / narr);
+    const int s = base < fit ? base : fit;
+    return s < 2 ? 2 : s;
+}
 
 struct LaunchPlan {
     const void *kernel = nullptr;
@@ -72,28 +91,60 @@ cudaError_t cached_occupancy(const void *kernel, int threads, size_t smem, int d
                              int *blocks_per_sm);
 
 template <int OP, int TPR, int RPC, int CH, int VEC>
-LaunchPlan fwd_plan_shape(int64_t N) {
-    LaunchPlan p;
-    p.kernel = reinterpret_cast<const void *>(&norm_fwd_kernel<OP, TPR, RPC, CH, VEC>);
-    p.threads = TPR * RPC;
-    p.grid = (int)((N + RPC - 1) / RPC);
-    p.rows_per_cta = RPC;
-    return p;
+cudaError_t fwd_plan_shape(int64_t N, LaunchPlan *p) {
+    p->kernel = reinterpret_cast<const void *>(&norm_fwd_kernel<OP, TPR, RPC, CH, VEC>);
+    p->threads = TPR * RPC;
+    p->grid = (int)((N + RPC - 1) / RPC);
+    p->smem = 0;
+    p->rows_per_cta = RPC;
+    return cudaSuccess;
+}
+
+// Persistent grid: as many CTAs as fit on the device at once, at most one per row slot.
+inline cudaError_t persistent_grid(LaunchPlan *p, int64_t N, int device) {
+    int per_sm = 0, sms = 0;
+    cudaError_t e = cached_occupancy(p->kernel, p->threads, p->smem, device, &per_sm);
+    if (e != cudaSuccess) return e;
+    e = device_sm_count(device, &sms);
+    if (e != cudaSuccess) return e;
+    const int64_t slots = (N + p->rows_per_cta - 1) / p->rows_per_cta;
+    const int64_t cap = (int64_t)sms * (int64_t)std::max(per_sm, 1);
+    p->grid = (int)std::min(slots, cap);
+    return cudaSuccess;
+}
+
+template <int OP, int TPR, int RPC, int CH, int STAGES>
+cudaError_t fwd_pipe_plan_shape(int64_t N, int device, LaunchPlan *p) {
+    constexpr int NARR = (OP == kAddRms) ? 2 : 1;
+    constexpr int NPAR = (OP == kLayer) ? 2 : 1;
+    constexpr int S = pipe_stages(STAGES, NARR, NPAR, CH, TPR * RPC);
+    static_assert(Ring<S, NARR, CH, TPR * RPC, NPAR>::kBytes <= kMaxDynSmem, "ring too large");
+    p->kernel = reinterpret_cast<const void *>(&norm_fwd_pipe_kernel<OP, TPR, RPC, CH, S>);
+    p->threads = TPR * RPC;
+    p->smem = Ring<S, NARR, CH, TPR * RPC, NPAR>::kBytes;
+    p->rows_per_cta = RPC;
+    return persistent_grid(p, N, device);
 }
 
 template <int OP>
-LaunchPlan fwd_plan(int64_t N, int D, bool vec8) {
+cudaError_t fwd_plan(int64_t N, int D, bool vec8, int device, LaunchPlan *p) {
 #define MT_TRY(maxd, tpr, rpc, ch) \
-    if (D <= maxd) return fwd_plan_shape<OP, tpr, rpc, ch, VEC>(N);
+    if (D <= maxd) return fwd_plan_shape<OP, tpr, rpc, ch, VEC>(N, p);
+#define MT_TRY_PIPE(maxd, tpr, rpc, ch, st) \
+    if (D <= maxd) return fwd_pipe_plan_shape<OP, tpr, rpc, ch, st>(N, device, p);
     if (vec8) {
         constexpr int VEC = 8;
-        MT_FWD_SHAPES_VEC8(MT_TRY)
+        if (D <= 1024) {
+            MT_FWD_SHAPES_VEC8(MT_TRY)
+        }
+        MT_FWD_PIPE_SHAPES(MT_TRY_PIPE)
     } else {
         constexpr int VEC = 1;
         MT_FWD_SHAPES_VEC1(MT_TRY)
     }
 #undef MT_TRY
-    return LaunchPlan{};
+#undef MT_TRY_PIPE
+    return cudaErrorInvalidValue;
 }
 
 template <int OP, int TPR, int RPC, int CH, int VEC, bool HAS_DS>
@@ -103,36 +154,42 @@ cudaError_t bwd_plan_shape(int64_t N, int D, int device, LaunchPlan *p) {
     p->threads = TPR * RPC;
     p->smem = (RPC > 1) ? (size_t)NV * (size_t)D * sizeof(float) : 0;
     p->rows_per_cta = RPC;
-    int per_sm = 0, sms = 0;
-    cudaError_t e = cached_occupancy(p->kernel, p->threads, p->smem, device, &per_sm);
-    if (e != cudaSuccess) return e;
-    e = device_sm_count(device, &sms);
-    if (e != cudaSuccess) return e;
-    const int64_t slots = (N + RPC - 1) / RPC;
-    const int64_t cap = (int64_t)sms * (int64_t)std::max(per_sm, 1);
-    p->grid = (int)std::min(slots, cap);
-    return cudaSuccess;
+    return persistent_grid(p, N, device);
+}
+
+template <int OP, int TPR, int RPC, int CH, int STAGES, bool HAS_DS>
+cudaError_t bwd_pipe_plan_shape(int64_t N, int device, LaunchPlan *p) {
+    constexpr int NARR = HAS_DS ? 3 : 2;
+    constexpr int S = pipe_stages(STAGES, NARR, 1, CH, TPR * RPC);
+    static_assert(Ring<S, NARR, CH, TPR * RPC, 1>::kBytes <= kMaxDynSmem, "ring too large");
+    p->kernel = reinterpret_cast<const void *>(&norm_bwd_pipe_kernel<OP, TPR, RPC, CH, S, HAS_DS>);
+    p->threads = TPR * RPC;
+    p->smem = Ring<S, NARR, CH, TPR * RPC, 1>::kBytes;
+    p->rows_per_cta = RPC;
+    return persistent_grid(p, N, device);
 }
 
 template <int OP, bool HAS_DS>
 cudaError_t bwd_plan(int64_t N, int D, bool vec8, int device, LaunchPlan *p) {
 #define MT_TRY(maxd, tpr, rpc, ch) \
     if (D <= maxd) return bwd_plan_shape<OP, tpr, rpc, ch, VEC, HAS_DS>(N, D, device, p);
+#define MT_TRY_PIPE(maxd, tpr, rpc, ch, st) \
+    if (D <= maxd) return bwd_pipe_plan_shape<OP, tpr, rpc, ch, st, HAS_DS>(N, device, p);
     if (vec8) {
-        constexpr int VEC = 8;
-        MT_BWD_SHAPES_VEC8(MT_TRY)
+        MT_BWD_PIPE_SHAPES(MT_TRY_PIPE)
     } else {
         constexpr int VEC = 1;
         MT_BWD_SHAPES_VEC1(MT_TRY)
     }
 #undef MT_TRY
+#undef MT_TRY_PIPE
     return cudaErrorInvalidValue;
 }
 
 // Per-op entry points, one translation unit each (compiled in parallel).
-LaunchPlan fwd_plan_rms(int64_t N, int D, bool vec8);
-LaunchPlan fwd_plan_layer(int64_t N, int D, bool vec8);
-LaunchPlan fwd_plan_add(int64_t N, int D, bool vec8);
+cudaError_t fwd_plan_rms(int64_t N, int D, bool vec8, int device, LaunchPlan *p);
+cudaError_t fwd_plan_layer(int64_t N, int D, bool vec8, int device, LaunchPlan *p);
+cudaError_t fwd_plan_add(int64_t N, int D, bool vec8, int device, LaunchPlan *p);
 cudaError_t bwd_plan_rms(int64_t N, int D, bool vec8, int device, LaunchPlan *p);
 cudaError_t bwd_plan_layer(int64_t N, int D, bool vec8, int device, LaunchPlan *p);
 cudaError_t bwd_plan_add(int64_t N, int D, bool vec8, bool has_ds, int device, LaunchPlan *p);

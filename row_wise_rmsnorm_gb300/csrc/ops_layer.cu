@@ -2,7 +2,9 @@
 #include "launch.cuh"
 
 namespace mt {
-LaunchPlan fwd_plan_layer(int64_t N, int D, bool vec8) { return fwd_plan<kLayer>(N, D, vec8); }
+cudaError_t fwd_plan_layer(int64_t N, int D, bool vec8, int device, LaunchPlan *p) {
+    return fwd_plan<kLayer>(N, D, vec8, device, p);
+}
 cudaError_t bwd_plan_layer(int64_t N, int D, bool vec8, int device, LaunchPlan *p) {
     return bwd_plan<kLayer, false>(N, D, vec8, device, p);
 }
