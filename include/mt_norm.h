@@ -162,6 +162,29 @@ mt_status_t mt_add_rmsnorm_backward_ws(const void *S, const void *gamma, const v
                                        void *workspace, size_t workspace_bytes,
                                        mt_stream_t stream);
 
+/* ----------------------------------------------- backward without allocation ---
+ * No counterpart on the pages: this entry point exists for callers that cannot
+ * allocate device memory. mt_rmsnorm_backward allocates its scratch and
+ * mt_rmsnorm_backward_ws needs the caller to provide it; a caller whose device memory
+ * is owned by a framework pool that must not be bypassed, or that runs in a loop where
+ * an allocator call is not allowed, can do neither.
+ *
+ * Same arguments, outputs and results as mt_rmsnorm_backward. The scratch comes from
+ * one fixed array of MT_NOALLOC_SCRATCH_BYTES compiled into the library, which every
+ * GPU that loads the library holds until the process exits; no allocation or free is
+ * made. The first call on each device looks up the array's device address (with that
+ * device current) and caches it, so make that first call before any stream capture.
+ * All calls share the array and leave their partials in it; nothing has to be cleared
+ * between calls, but calls that overlap on the GPU race on it and must not be made.
+ * A shape whose dgamma partials (one fp32 row of D per persistent CTA) exceed
+ * MT_NOALLOC_SCRATCH_BYTES returns MT_ERR_UNSUPPORTED and launches nothing; every
+ * shape up to MT_MAX_COLS columns fits on a 152-SM GB300.                            */
+#define MT_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+mt_status_t mt_rmsnorm_backward_noalloc(const void *X, const void *gamma, const void *dY,
+                                        const float *rstd, void *dX, float *dgamma,
+                                        int64_t N, int64_t D, mt_stream_t stream);
+
 /* ------------------------------------------------------------------ utilities --- */
 
 /* Scratch bytes a backward of `op` at [N, D] needs on CUDA device `device`: the

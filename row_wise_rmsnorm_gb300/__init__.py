@@ -11,6 +11,7 @@ from ._binding import (  # noqa: F401
     MT_ERR_INVALID_ARG,
     MT_ERR_UNSUPPORTED,
     MT_MAX_COLS,
+    MT_NOALLOC_SCRATCH_BYTES,
     MT_OK,
     MT_OP_ADD_RMSNORM,
     MT_OP_LAYERNORM,
@@ -32,6 +33,7 @@ from ._binding import (  # noqa: F401
     mt_norm_backward_workspace_size,
     mt_norm_version,
     mt_rmsnorm_backward,
+    mt_rmsnorm_backward_noalloc,
     mt_rmsnorm_backward_ws,
     mt_rmsnorm_forward,
     mt_status_string,

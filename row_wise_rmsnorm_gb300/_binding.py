@@ -31,9 +31,11 @@ EXPORTED = (
     "mt_rmsnorm_forward", "mt_rmsnorm_backward", "mt_rmsnorm_backward_ws",
     "mt_layernorm_forward", "mt_layernorm_backward", "mt_layernorm_backward_ws",
     "mt_add_rmsnorm_forward", "mt_add_rmsnorm_backward", "mt_add_rmsnorm_backward_ws",
+    "mt_rmsnorm_backward_noalloc",
     "mt_norm_backward_workspace_size", "mt_last_cuda_error", "mt_status_string",
     "mt_norm_version",
 )
+MT_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 class MtNormError(RuntimeError):
@@ -61,6 +63,7 @@ _SIGS = {
     "mt_add_rmsnorm_forward": [_P, _P, _P, _P, _P, _P, _I64, _I64, _F, _P],
     "mt_add_rmsnorm_backward": [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P],
     "mt_add_rmsnorm_backward_ws": [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P, _SZ, _P],
+    "mt_rmsnorm_backward_noalloc": [_P, _P, _P, _P, _P, _P, _I64, _I64, _P],
     "mt_norm_backward_workspace_size": [ctypes.c_int, _I64, _I64, ctypes.c_int,
                                         ctypes.POINTER(_SZ)],
     "mt_last_cuda_error": [],
@@ -171,6 +174,18 @@ def mt_add_rmsnorm_backward_ws(S, gamma, dY, dS, rstd, dX, dgamma, N, D, workspa
                                              _ptr(rstd), _ptr(dX), _ptr(dgamma), N, D,
                                              _ptr(workspace), workspace_bytes, _stream(stream)),
            "mt_add_rmsnorm_backward_ws")
+
+
+def mt_rmsnorm_backward_noalloc(X, gamma, dY, rstd, dX, dgamma, N, D, stream=None):
+    """RMSNorm backward with the library's fixed scratch array (no allocation).
+
+    For callers that may not allocate device memory; see include/mt_norm.h. The
+    first call on a device must come before any stream capture; calls must not
+    overlap on the GPU.
+    """
+    _check(load().mt_rmsnorm_backward_noalloc(_ptr(X), _ptr(gamma), _ptr(dY), _ptr(rstd),
+                                              _ptr(dX), _ptr(dgamma), N, D, _stream(stream)),
+           "mt_rmsnorm_backward_noalloc")
 
 
 def mt_norm_backward_workspace_size(op, N, D, device=0) -> int:

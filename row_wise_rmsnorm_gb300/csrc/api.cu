@@ -145,6 +145,8 @@ mt_status_t run_backward(int op, BwdArgs a, bool vec8, float *dgamma, float *dbe
 
 }  // namespace
 
+void record_cuda_error(cudaError_t e) { g_last_cuda_error = (int)e; }
+
 cudaError_t device_sm_count(int device, int *sms) {
     std::lock_guard<std::mutex> lock(g_cache_mu);
     auto it = g_sm_count.find(device);
