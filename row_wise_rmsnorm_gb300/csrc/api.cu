@@ -13,6 +13,7 @@
 #include <map>
 #include <mutex>
 #include <tuple>
+#include <utility>
 
 #include "launch.cuh"
 #include "reduce.cuh"
@@ -70,11 +71,22 @@ std::mutex g_cache_mu;
 std::map<int, int> g_sm_count;
 std::map<std::tuple<const void *, int, size_t, int>, int> g_occupancy;
 
+// Every launch carries the programmatic-stream-serialization attribute (see pdl_enter()
+// in kernels.cuh).
 mt_status_t launch(const LaunchPlan &p, void *arg, cudaStream_t stream) {
     if (p.kernel == nullptr || p.grid < 1) return cuda_fail(cudaErrorInvalidConfiguration);
     void *args[] = {arg};
-    cudaError_t e = cudaLaunchKernel(p.kernel, dim3((unsigned)p.grid), dim3((unsigned)p.threads),
-                                     args, p.smem, stream);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.grid);
+    cfg.blockDim = dim3((unsigned)p.threads);
+    cfg.dynamicSmemBytes = p.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelExC(&cfg, p.kernel, args);
     if (e != cudaSuccess) return cuda_fail(e);
     return MT_OK;
 }
@@ -103,8 +115,9 @@ cudaError_t plan_backward(int op, int64_t N, int D, bool vec8, bool has_ds, int 
     }
 }
 
-size_t partial_bytes(int op, int grid, int D) {
-    const size_t raw = (size_t)num_partial_arrays(op) * (size_t)grid * (size_t)D * sizeof(float);
+// One fp32 row of D per persistent CTA, per parameter gradient.
+size_t partial_bytes(int op, int rows, int D) {
+    const size_t raw = (size_t)num_partial_arrays(op) * (size_t)rows * (size_t)D * sizeof(float);
     return (raw + 255) & ~(size_t)255;
 }
 
@@ -118,7 +131,8 @@ mt_status_t run_backward(int op, BwdArgs a, bool vec8, float *dgamma, float *dbe
     LaunchPlan p;
     e = plan_backward(op, a.N, a.D, vec8, a.dS != nullptr, device, &p);
     if (e != cudaSuccess) return cuda_fail(e);
-    const size_t need = partial_bytes(op, p.grid, a.D);
+    const int prow = p.grid;  // partial rows: one per CTA
+    const size_t need = partial_bytes(op, prow, a.D);
     if (own_ws) {
         e = cudaMallocAsync(&workspace, need, stream);
         if (e != cudaSuccess) return cuda_fail(e);
@@ -127,13 +141,23 @@ mt_status_t run_backward(int op, BwdArgs a, bool vec8, float *dgamma, float *dbe
     }
     float *part = static_cast<float *>(workspace);
     a.part_g = part;
-    a.part_b = (op == kLayer) ? part + (size_t)p.grid * (size_t)a.D : nullptr;
+    a.part_b = (op == kLayer) ? part + (size_t)prow * (size_t)a.D : nullptr;
     mt_status_t st = launch(p, &a, stream);
     if (st == MT_OK) {
-        const dim3 grid((unsigned)((a.D + 31) / 32), (unsigned)num_partial_arrays(op));
-        param_reduce_kernel<<<grid, dim3(32, kReduceSlices), 0, stream>>>(part, p.grid, a.D,
-                                                                         dgamma, dbeta);
-        e = cudaGetLastError();
+        // Programmatic dependent launch: the reduction is set up while the backward
+        // runs and starts reading only after the backward grid has completed.
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)((a.D + 31) / 32), (unsigned)num_partial_arrays(op));
+        cfg.blockDim = dim3(32 * kReduceWarps);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const float *cpart = part;
+        e = cudaLaunchKernelEx(&cfg, param_reduce_kernel, cpart, prow, a.D, dgamma, dbeta);
         if (e != cudaSuccess) st = cuda_fail(e);
     }
     if (own_ws) {
@@ -175,8 +199,14 @@ cudaError_t cached_occupancy(const void *kernel, int threads, size_t smem, int d
     cudaError_t e = cudaGetDevice(&cur);
     if (e != cudaSuccess) return e;
     if (cur != device && (e = cudaSetDevice(device)) != cudaSuccess) return e;
-    if (smem > 48 * 1024) {
+    // Opt in to the dynamic shared memory size whatever it is (the default 48 KB limit
+    // counts static shared memory too). The function attribute is only ever raised, so
+    // a plan cached earlier with a larger size stays launchable.
+    static std::map<std::pair<const void *, int>, size_t> smem_limit;
+    size_t &limit = smem_limit[std::make_pair(kernel, device)];
+    if (smem > limit) {
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e == cudaSuccess) limit = smem;
     }
     int v = 0;
     if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kernel, threads, smem);

@@ -79,6 +79,36 @@ __device__ __forceinline__ uint32_t float2_to_half2_bits(float a, float b) {
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
+// Eight fp16 values (one 16-byte chunk) <-> four fp32 pairs; pair p holds elements
+// 2p and 2p+1. The pack rounds to nearest even.
+__device__ __forceinline__ void unpack8x2(const uint4 &u, float2 (&f)[4]) {
+    f[0] = half2_bits_to_float2(u.x);
+    f[1] = half2_bits_to_float2(u.y);
+    f[2] = half2_bits_to_float2(u.z);
+    f[3] = half2_bits_to_float2(u.w);
+}
+
+__device__ __forceinline__ uint4 pack8x2(const float2 (&f)[4]) {
+    uint4 u;
+    u.x = float2_to_half2_bits(f[0].x, f[0].y);
+    u.y = float2_to_half2_bits(f[1].x, f[1].y);
+    u.z = float2_to_half2_bits(f[2].x, f[2].y);
+    u.w = float2_to_half2_bits(f[3].x, f[3].y);
+    return u;
+}
+
+// Programmatic dependent launch. Every kernel of this library is launched with the
+// programmatic-stream-serialization attribute, so it may be scheduled while the
+// previous kernel in the stream is still finishing. It therefore waits
+// (griddepcontrol.wait) until that kernel has completed and its writes are visible
+// before touching global memory, and it lets the next kernel launch early
+// (griddepcontrol.launch_dependents); that kernel performs the same wait. Without the
+// launch attribute both instructions are no-ops.
+__device__ __forceinline__ void pdl_enter() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Raw storage of one chunk of VEC fp16 values, kept packed in registers.
 template <int VEC> struct Raw;
 template <> struct Raw<8> { uint4 v; };
@@ -92,6 +122,17 @@ __device__ __forceinline__ void load_act(const __half *row, int col, int D, Raw<
         else r.v = make_uint4(0u, 0u, 0u, 0u);
     } else {
         r.v = (col < D) ? __half_as_ushort(__ldcs(row + col)) : (unsigned short)0;
+    }
+}
+
+// Activation load through the read-only path (cached in L1), for data read twice.
+template <int VEC>
+__device__ __forceinline__ void load_act_l1(const __half *row, int col, int D, Raw<VEC> &r) {
+    if constexpr (VEC == 8) {
+        if (col < D) r.v = __ldg(reinterpret_cast<const uint4 *>(row + col));
+        else r.v = make_uint4(0u, 0u, 0u, 0u);
+    } else {
+        r.v = (col < D) ? __half_as_ushort(__ldg(row + col)) : (unsigned short)0;
     }
 }
 
@@ -150,11 +191,15 @@ __device__ __forceinline__ void store_act(__half *row, int col, int D, const flo
 // Sum NV values over the TPR threads of one row group. `red` holds
 // 2 (buffers) x RPC x WPR x NV floats; alternate `buf` between consecutive calls so
 // one __syncthreads per call suffices. Every thread of the CTA must call it when
-// WPR > 1 (it contains a CTA-wide barrier).
+// WPR > 1 (it contains a CTA-wide barrier). Each warp first reduces with a butterfly;
+// then lane l of every warp reads warp l's sum (zero for l >= WPR) and a second
+// butterfly adds them. The operands and their order are the same in every warp, so
+// every thread ends with the bitwise-identical total.
 template <int TPR, int RPC, int NV>
 __device__ __forceinline__ void row_sum(float (&v)[NV], float *red, int buf, int rg, int wir,
                                         int lane) {
     constexpr int WPR = TPR / 32;
+    static_assert(WPR <= 32, "row group wider than 32 warps");
 #pragma unroll
     for (int i = 0; i < NV; ++i) v[i] = warp_sum(v[i]);
     if constexpr (WPR > 1) {
@@ -165,12 +210,7 @@ __device__ __forceinline__ void row_sum(float (&v)[NV], float *red, int buf, int
         }
         __syncthreads();
 #pragma unroll
-        for (int i = 0; i < NV; ++i) {
-            float t = 0.f;
-#pragma unroll
-            for (int w = 0; w < WPR; ++w) t += s[w * NV + i];
-            v[i] = t;
-        }
+        for (int i = 0; i < NV; ++i) v[i] = warp_sum(lane < WPR ? s[lane * NV + i] : 0.f);
     }
 }
 
@@ -179,6 +219,7 @@ __device__ __forceinline__ void row_sum(float (&v)[NV], float *red, int buf, int
 template <int OP, int TPR, int RPC, int CH, int VEC>
 __global__ void __launch_bounds__(TPR * RPC)
 norm_fwd_kernel(const FwdArgs a) {
+    pdl_enter();
     static_assert(TPR % 32 == 0 && TPR * RPC <= 1024, "bad launch shape");
     constexpr int WPR = TPR / 32;
     __shared__ float red[2 * RPC * WPR];
@@ -262,6 +303,91 @@ norm_fwd_kernel(const FwdArgs a) {
     }
 }
 
+// Forward for 16-byte-aligned rows (D % 8 == 0), one row group per row, fp32 pair
+// arithmetic (__ffma2_rn & co.). Rows are loaded once with streaming 16-byte loads and
+// stay in registers through the reductions and the apply.
+template <int OP, int TPR, int RPC, int CH>
+__global__ void __launch_bounds__(TPR * RPC)
+norm_fwd_vec8_kernel(const FwdArgs a) {
+    pdl_enter();
+    static_assert(TPR % 32 == 0 && TPR * RPC <= 1024, "bad launch shape");
+    constexpr int WPR = TPR / 32;
+    __shared__ float red[2 * RPC * WPR];
+
+    const int tid = threadIdx.x;
+    const int rg = tid / TPR, t = tid % TPR, wir = t / 32, lane = tid % 32;
+    const int D = a.D;
+    const float inv_d = 1.0f / (float)D;
+    const int64_t row = (int64_t)blockIdx.x * RPC + rg;
+    const bool ok = row < a.N;
+    if (WPR == 1 && !ok) return;  // no CTA barrier in a single-warp row group
+    const int64_t off = (ok ? row : 0) * (int64_t)D;
+
+    float2 x[CH][4];
+#pragma unroll
+    for (int k = 0; k < CH; ++k) {
+        const int col = (k * TPR + t) * 8;
+        const bool v = ok && col < D;
+        unpack8x2(v ? __ldcs(reinterpret_cast<const uint4 *>(a.X + off + col)) : make_uint4(0, 0, 0, 0), x[k]);
+        if constexpr (OP == kAddRms) {
+            float2 r[4];
+            unpack8x2(v ? __ldcs(reinterpret_cast<const uint4 *>(a.R + off + col)) : make_uint4(0, 0, 0, 0), r);
+#pragma unroll
+            for (int p = 0; p < 4; ++p) x[k][p] = __fadd2_rn(x[k][p], r[p]);
+            if (v) __stcs(reinterpret_cast<uint4 *>(a.S + off + col), pack8x2(x[k]));
+        }
+    }
+    float mu = 0.f;
+    if constexpr (OP == kLayer) {
+        float2 s2 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < CH; ++k)
+#pragma unroll
+            for (int p = 0; p < 4; ++p) s2 = __fadd2_rn(s2, x[k][p]);
+        float s[1] = {s2.x + s2.y};
+        row_sum<TPR, RPC, 1>(s, red, 0, rg, wir, lane);
+        mu = s[0] * inv_d;
+    }
+    const float2 nmu = make_float2(-mu, -mu);
+    float2 q2 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < CH; ++k) {
+        if (!(ok && (k * TPR + t) * 8 < D)) continue;
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const float2 d = (OP == kLayer) ? __fadd2_rn(x[k][p], nmu) : x[k][p];
+            q2 = __ffma2_rn(d, d, q2);
+        }
+    }
+    float q[1] = {q2.x + q2.y};
+    row_sum<TPR, RPC, 1>(q, red, 1, rg, wir, lane);
+    const float rs = rsqrtf(q[0] * inv_d + a.eps);
+    if (!ok) return;  // after the last barrier
+    if (t == 0) {
+        a.rstd[row] = rs;
+        if constexpr (OP == kLayer) a.mean[row] = mu;
+    }
+    const float2 rs2 = make_float2(rs, rs);
+#pragma unroll
+    for (int k = 0; k < CH; ++k) {
+        const int col = (k * TPR + t) * 8;
+        if (col >= D) continue;
+        float2 g[4], y[4];
+        unpack8x2(__ldg(reinterpret_cast<const uint4 *>(a.gamma + col)), g);
+        if constexpr (OP == kLayer) {
+            float2 b[4];
+            unpack8x2(__ldg(reinterpret_cast<const uint4 *>(a.beta + col)), b);
+#pragma unroll
+            for (int p = 0; p < 4; ++p)
+                y[p] = __ffma2_rn(__fmul2_rn(__fadd2_rn(x[k][p], nmu), rs2), g[p], b[p]);
+        } else {
+#pragma unroll
+            for (int p = 0; p < 4; ++p) y[p] = __fmul2_rn(__fmul2_rn(x[k][p], rs2), g[p]);
+        }
+        __stcs(reinterpret_cast<uint4 *>(a.Y + off + col), pack8x2(y));
+    }
+}
+
 // ----------------------------------------------------------------- backward ---
 // Persistent: grid = P CTAs of TPR*RPC threads; CTA b processes row slots
 // b*RPC + j*G*RPC (G = gridDim.x), row group rg taking row slot + rg.
@@ -269,6 +395,7 @@ norm_fwd_kernel(const FwdArgs a) {
 template <int OP, int TPR, int RPC, int CH, int VEC, bool HAS_DS>
 __global__ void __launch_bounds__(TPR * RPC)
 norm_bwd_kernel(const BwdArgs a) {
+    pdl_enter();
     static_assert(TPR % 32 == 0 && TPR * RPC <= 1024, "bad launch shape");
     constexpr int WPR = TPR / 32;
     constexpr int NV = (OP == kLayer) ? 2 : 1;
@@ -301,15 +428,20 @@ norm_bwd_kernel(const BwdArgs a) {
         const float r = ok ? a.rstd[row] : 0.f;
         const float mu = (OP == kLayer && ok) ? a.mean[row] : 0.f;
 
-        Raw<VEC> xr[CH], dyr[CH];
+        // Short row slices stay in registers between the passes; longer ones are read
+        // again in pass 2 through L1 (where pass 1 left them), which avoids spills.
+        constexpr bool KEEP = CH * VEC <= 8;
+        Raw<VEC> xr[KEEP ? CH : 1], dyr[KEEP ? CH : 1];
+        if constexpr (KEEP) {
 #pragma unroll
-        for (int k = 0; k < CH; ++k) {
-            const int col = (k * TPR + t) * VEC;
-            load_act<VEC>(a.X + off, col, lim, xr[k]);
-            load_act<VEC>(a.dY + off, col, lim, dyr[k]);
+            for (int k = 0; k < CH; ++k) {
+                const int col = (k * TPR + t) * VEC;
+                load_act<VEC>(a.X + off, col, lim, xr[k]);
+                load_act<VEC>(a.dY + off, col, lim, dyr[k]);
+            }
         }
 
-        // pass 1 (registers): sum_j g*xhat and, for LayerNorm, sum_j g
+        // pass 1: sum_j g*xhat and, for LayerNorm, sum_j g
         float v[NV];
 #pragma unroll
         for (int i = 0; i < NV; ++i) v[i] = 0.f;
@@ -318,8 +450,16 @@ norm_bwd_kernel(const BwdArgs a) {
             const int col = (k * TPR + t) * VEC;
             float gm[VEC], xv[VEC], dv[VEC];
             load_param<VEC>(a.gamma, col, lim, gm);
-            unpack<VEC>(xr[k], xv);
-            unpack<VEC>(dyr[k], dv);
+            if constexpr (KEEP) {
+                unpack<VEC>(xr[k], xv);
+                unpack<VEC>(dyr[k], dv);
+            } else {
+                Raw<VEC> xk, dk;
+                load_act_l1<VEC>(a.X + off, col, lim, xk);
+                load_act_l1<VEC>(a.dY + off, col, lim, dk);
+                unpack<VEC>(xk, xv);
+                unpack<VEC>(dk, dv);
+            }
 #pragma unroll
             for (int e = 0; e < VEC; ++e) {
                 const float xh = (xv[e] - mu) * r;
@@ -340,8 +480,16 @@ norm_bwd_kernel(const BwdArgs a) {
             if (col >= D) continue;
             float gm[VEC], xv[VEC], dv[VEC], o[VEC];
             load_param<VEC>(a.gamma, col, D, gm);
-            unpack<VEC>(xr[k], xv);
-            unpack<VEC>(dyr[k], dv);
+            if constexpr (KEEP) {
+                unpack<VEC>(xr[k], xv);
+                unpack<VEC>(dyr[k], dv);
+            } else {
+                Raw<VEC> xk, dk;
+                load_act_l1<VEC>(a.X + off, col, D, xk);
+                load_act_l1<VEC>(a.dY + off, col, D, dk);
+                unpack<VEC>(xk, xv);
+                unpack<VEC>(dk, dv);
+            }
             float ds[VEC];
             if constexpr (HAS_DS) {
                 Raw<VEC> dsr;

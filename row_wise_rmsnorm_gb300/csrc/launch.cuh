@@ -23,10 +23,8 @@ namespace mt {
     X(256, 32, 4, 1)          \
     X(512, 32, 4, 2)          \
     X(1024, 32, 4, 4)         \
-    X(2048, 128, 1, 2)        \
-    X(4096, 256, 1, 2)        \
-    X(8192, 512, 1, 2)        \
-    X(16384, 1024, 1, 2)
+    X(2048, 256, 1, 1)        \
+    X(4096, 256, 1, 2)
 
 #define MT_FWD_SHAPES_VEC1(X) \
     X(64, 32, 4, 2)           \
@@ -53,26 +51,25 @@ namespace mt {
 // Pipelined persistent shapes for 16-byte-aligned rows: X(max_D, TPR, RPC, CH, STAGES).
 // STAGES is the largest ring depth; pipe_stages() cuts it to fit shared memory.
 #define MT_FWD_PIPE_SHAPES(X)   \
-    X(2048, 256, 2, 1, 8)       \
-    X(4096, 512, 1, 1, 8)       \
     X(8192, 512, 1, 2, 6)       \
     X(16384, 512, 1, 4, 4)
 
 #define MT_BWD_PIPE_SHAPES(X)   \
-    X(256, 32, 16, 1, 6)        \
-    X(512, 64, 8, 1, 6)         \
-    X(1024, 128, 4, 1, 6)       \
-    X(2048, 256, 2, 1, 6)       \
-    X(4096, 512, 1, 1, 6)       \
+    X(256, 32, 16, 1, 8)        \
+    X(512, 64, 8, 1, 8)         \
+    X(1024, 128, 4, 1, 8)       \
+    X(2048, 256, 2, 1, 8)       \
+    X(4096, 512, 1, 1, 4)       \
     X(8192, 512, 1, 2, 3)       \
     X(16384, 512, 1, 4, 3)
 
-// Ring depth: the table's depth, cut so that ring + parameter slots fit the 227 KB of
-// dynamic shared memory a CTA may use, and never below 2.
+// Ring depth: the table's depth, cut so that ring + parameter slots fit the dynamic
+// shared memory a CTA may use (227 KB per SM, shared by `ctas` resident CTAs), and
+// never below 2.
 constexpr size_t kMaxDynSmem = 226 * 1024;
-constexpr int pipe_stages(int base, int narr, int npar, int ch, int threads) {
+constexpr int pipe_stages(int base, int narr, int npar, int ch, int threads, int ctas) {
     const size_t slot = (size_t)ch * threads * 16;
-    const int fit = (int)(((kMaxDynSmem / slot) - npar) / narr);
+    const int fit = (int)(((kMaxDynSmem / ctas / slot) - npar) / narr);
     const int s = base < fit ? base : fit;
     return s < 2 ? 2 : s;
 }
@@ -93,7 +90,10 @@ cudaError_t cached_occupancy(const void *kernel, int threads, size_t smem, int d
 
 template <int OP, int TPR, int RPC, int CH, int VEC>
 cudaError_t fwd_plan_shape(int64_t N, LaunchPlan *p) {
-    p->kernel = reinterpret_cast<const void *>(&norm_fwd_kernel<OP, TPR, RPC, CH, VEC>);
+    if constexpr (VEC == 8)
+        p->kernel = reinterpret_cast<const void *>(&norm_fwd_vec8_kernel<OP, TPR, RPC, CH>);
+    else
+        p->kernel = reinterpret_cast<const void *>(&norm_fwd_kernel<OP, TPR, RPC, CH, VEC>);
     p->threads = TPR * RPC;
     p->grid = (int)((N + RPC - 1) / RPC);
     p->smem = 0;
@@ -117,8 +117,8 @@ inline cudaError_t persistent_grid(LaunchPlan *p, int64_t N, int device) {
 template <int OP, int TPR, int RPC, int CH, int STAGES>
 cudaError_t fwd_pipe_plan_shape(int64_t N, int device, LaunchPlan *p) {
     constexpr int NARR = (OP == kAddRms) ? 2 : 1;
-    constexpr int NPAR = (OP == kLayer) ? 2 : 1;
-    constexpr int S = pipe_stages(STAGES, NARR, NPAR, CH, TPR * RPC);
+    constexpr int NPAR = (CH <= 2) ? 0 : ((OP == kLayer) ? 2 : 1);
+    constexpr int S = pipe_stages(STAGES, NARR, NPAR, CH, TPR * RPC, 1);
     static_assert(Ring<S, NARR, CH, TPR * RPC, NPAR>::kBytes <= kMaxDynSmem, "ring too large");
     p->kernel = reinterpret_cast<const void *>(&norm_fwd_pipe_kernel<OP, TPR, RPC, CH, S>);
     p->threads = TPR * RPC;
@@ -135,9 +135,7 @@ cudaError_t fwd_plan(int64_t N, int D, bool vec8, int device, LaunchPlan *p) {
     if (D <= maxd) return fwd_pipe_plan_shape<OP, tpr, rpc, ch, st>(N, device, p);
     if (vec8) {
         constexpr int VEC = 8;
-        if (D <= 1024) {
-            MT_FWD_SHAPES_VEC8(MT_TRY)
-        }
+        MT_FWD_SHAPES_VEC8(MT_TRY)
         MT_FWD_PIPE_SHAPES(MT_TRY_PIPE)
     } else {
         constexpr int VEC = 1;
@@ -161,11 +159,12 @@ cudaError_t bwd_plan_shape(int64_t N, int D, int device, LaunchPlan *p) {
 template <int OP, int TPR, int RPC, int CH, int STAGES, bool HAS_DS>
 cudaError_t bwd_pipe_plan_shape(int64_t N, int device, LaunchPlan *p) {
     constexpr int NARR = HAS_DS ? 3 : 2;
-    constexpr int S = pipe_stages(STAGES, NARR, 1, CH, TPR * RPC);
-    static_assert(Ring<S, NARR, CH, TPR * RPC, 1>::kBytes <= kMaxDynSmem, "ring too large");
+    constexpr int NPAR = (CH <= 2) ? 0 : 1;
+    constexpr int S = pipe_stages(STAGES, NARR, NPAR, CH, TPR * RPC, bwd_ctas_per_sm(OP, RPC, CH));
+    static_assert(Ring<S, NARR, CH, TPR * RPC, NPAR>::kBytes <= kMaxDynSmem, "ring too large");
     p->kernel = reinterpret_cast<const void *>(&norm_bwd_pipe_kernel<OP, TPR, RPC, CH, S, HAS_DS>);
     p->threads = TPR * RPC;
-    p->smem = Ring<S, NARR, CH, TPR * RPC, 1>::kBytes;
+    p->smem = Ring<S, NARR, CH, TPR * RPC, NPAR>::kBytes;
     p->rows_per_cta = RPC;
     return persistent_grid(p, N, device);
 }

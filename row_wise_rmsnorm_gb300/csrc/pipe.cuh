@@ -1,27 +1,35 @@
 // pipe.cuh -- pipelined persistent kernels for 16-byte-aligned rows (D % 8 == 0).
 //
-// The plain kernels of kernels.cuh hold only the current row in flight per thread, so
-// when a CTA reduces, nothing of its next row is on its way from HBM. Here each CTA is
-// persistent and every thread streams ITS OWN 16-byte chunks of the next STAGES-1 rows
-// into a shared-memory ring with cp.async (L2-only, no L1 allocation), then reads them
-// back for the current row. Because a thread only ever reads what it copied itself,
-// cp.async.wait_group alone orders the ring: no mbarrier, no cross-thread wait, and no
-// wait that depends on another thread or CTA. Bytes in flight per SM are bounded by the
-// ring (STAGES x arrays x row width), not by registers.
+// Streaming. Each CTA is persistent and every thread streams ITS OWN 16-byte chunks
+// of the next STAGES-1 rows into a shared-memory ring with cp.async (L2 only, no L1
+// allocation), then reads them back for the current row. A thread only ever reads what
+// it copied itself, so cp.async.wait_group alone orders the ring: no mbarrier, no
+// cross-thread or cross-CTA wait. Bytes in flight per SM are set by the ring depth
+// (STAGES x streamed arrays x row slice), not by registers.
 //
-// Row assignment is static: CTA b runs row slots b*RPC + j*G*RPC (G = gridDim.x,
-// j = 0, 1, ...), row group rg taking slot + rg. Thread t of a row group owns chunks
-// k = 0..CH-1 at columns (k*TPR + t)*8 .. +7 of every row it touches, so its gamma (and
-// beta) chunks are copied once into its own shared-memory slots and its dgamma/dbeta
-// sums stay in fp32 registers across all its rows. Row data is re-read from the ring
-// in each pass instead of being held in registers across the reduction barrier, which
-// keeps register use (and so spills) down at wide rows. Per-row statistics (rstd,
-// mean) are prefetched into registers two rows ahead.
+// Ownership. Row assignment is static: CTA b runs row slots b*RPC + j*G*RPC
+// (G = gridDim.x, j = 0, 1, ...), row group rg taking slot + rg. Thread t of a row
+// group owns chunks k = 0..CH-1 at columns (k*TPR + t)*8 .. +7 of every row it touches;
+// its dgamma/dbeta sums stay in fp32 registers across all its rows, and per-row
+// statistics (rstd, mean) are prefetched into registers two rows ahead.
+//
+// Arithmetic. Blackwell executes fp32 pairs in one instruction (__ffma2_rn,
+// __fmul2_rn, __fadd2_rn); the element math runs on float2 pairs, each lane rounded
+// exactly as the scalar fp32 operation. When a thread's slice is small (CH <= 2) the
+// converted row values and fp32 gamma (beta) stay in registers across the reduction
+// barrier; for wider slices they are re-read from the ring and from per-thread
+// parameter slots, which keeps the kernels free of register spills.
 #pragma once
 
 #include "kernels.cuh"
 
 namespace mt {
+
+// Resident CTAs per SM the backward is compiled for: two (64 registers each) for a
+// single one-chunk row group per CTA, one otherwise (more registers, deeper ring).
+constexpr int bwd_ctas_per_sm(int op, int rpc, int ch) {
+    return (ch == 1 && rpc == 1) ? 2 : 1;
+}
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -41,29 +49,9 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
-// Streaming 16-byte store (evict-first in L2): outputs are not re-read by this kernel.
-__device__ __forceinline__ void st_global_cs(void *p, const uint4 &v) {
-    __stcs(reinterpret_cast<uint4 *>(p), v);
-}
-
-__device__ __forceinline__ void unpack8(const uint4 &u, float (&f)[8]) {
-    Raw<8> r;
-    r.v = u;
-    unpack<8>(r, f);
-}
-
-__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
-    uint4 u;
-    u.x = float2_to_half2_bits(f[0], f[1]);
-    u.y = float2_to_half2_bits(f[2], f[3]);
-    u.z = float2_to_half2_bits(f[4], f[5]);
-    u.w = float2_to_half2_bits(f[6], f[7]);
-    return u;
-}
-
-// Shared-memory ring: [STAGES][NARR][CH][THREADS] x 16 bytes. Consecutive threads own
-// consecutive 16-byte words, so ring reads are bank-conflict free.
-// After the ring come NPAR parameter arrays (gamma, beta) in the same per-thread layout.
+// Shared-memory ring: [STAGES][NARR][CH][THREADS] x 16 bytes, then NPAR parameter
+// arrays in the same per-thread layout. Consecutive threads own consecutive 16-byte
+// words, so every ring access is bank-conflict free.
 template <int STAGES, int NARR, int CH, int THREADS, int NPAR>
 struct Ring {
     static constexpr size_t kBytes = (size_t)(STAGES * NARR + NPAR) * CH * THREADS * 16;
@@ -86,6 +74,14 @@ __device__ __forceinline__ void stage_param(uint4 *ring, int p, const __half *sr
     }
 }
 
+// This thread's chunk k of a parameter vector as fp32 pairs (0 past D).
+template <int CH, int TPR>
+__device__ __forceinline__ void load_param_pairs(const __half *p, int k, int t, int D,
+                                                 float2 (&f)[4]) {
+    const int col = (k * TPR + t) * 8;
+    unpack8x2(col < D ? __ldg(reinterpret_cast<const uint4 *>(p + col)) : make_uint4(0, 0, 0, 0), f);
+}
+
 // Iterations every row group of this CTA runs (uniform across the CTA).
 __device__ __forceinline__ int cta_iterations(int64_t N, int rpc) {
     const int64_t base = (int64_t)blockIdx.x * rpc;
@@ -97,10 +93,12 @@ __device__ __forceinline__ int cta_iterations(int64_t N, int rpc) {
 template <int OP, int TPR, int RPC, int CH, int STAGES>
 __global__ void __launch_bounds__(TPR * RPC, 1)
 norm_fwd_pipe_kernel(const FwdArgs a) {
+    pdl_enter();
     constexpr int THREADS = TPR * RPC;
     constexpr int WPR = TPR / 32;
     constexpr int NARR = (OP == kAddRms) ? 2 : 1;
-    constexpr int NPAR = (OP == kLayer) ? 2 : 1;
+    constexpr bool KEEP = CH <= 2;
+    constexpr int NPAR = KEEP ? 0 : ((OP == kLayer) ? 2 : 1);
     using R = Ring<STAGES, NARR, CH, THREADS, NPAR>;
     static_assert(TPR % 32 == 0 && THREADS <= 1024, "bad launch shape");
     __shared__ float red[2 * RPC * WPR];
@@ -109,9 +107,23 @@ norm_fwd_pipe_kernel(const FwdArgs a) {
     const int tid = threadIdx.x;
     const int rg = tid / TPR, t = tid % TPR, wir = t / 32, lane = tid % 32;
     const int D = a.D;
+    const float inv_d = 1.0f / (float)D;
     const int64_t stride = (int64_t)gridDim.x * RPC;
     const int64_t first = (int64_t)blockIdx.x * RPC + rg;
     const int iters = cta_iterations(a.N, RPC);
+
+    float2 gam[KEEP ? CH : 1][4], bet[(KEEP && OP == kLayer) ? CH : 1][4];
+    if constexpr (KEEP) {
+#pragma unroll
+        for (int k = 0; k < CH; ++k) {
+            load_param_pairs<CH, TPR>(a.gamma, k, t, D, gam[k]);
+            if constexpr (OP == kLayer) load_param_pairs<CH, TPR>(a.beta, k, t, D, bet[k]);
+        }
+    } else {
+        stage_param<R, CH, TPR>(ring, 0, a.gamma, D, t, tid);
+        if constexpr (OP == kLayer) stage_param<R, CH, TPR>(ring, 1, a.beta, D, t, tid);
+    }
+    cp_async_commit();
 
     auto issue = [&](int j) {
         const int64_t row = first + (int64_t)j * stride;
@@ -130,11 +142,6 @@ norm_fwd_pipe_kernel(const FwdArgs a) {
         }
         cp_async_commit();
     };
-
-    // group 0: this thread's gamma (and beta) chunks; then the first STAGES-1 rows
-    stage_param<R, CH, TPR>(ring, 0, a.gamma, D, t, tid);
-    if constexpr (OP == kLayer) stage_param<R, CH, TPR>(ring, 1, a.beta, D, t, tid);
-    cp_async_commit();
 #pragma unroll
     for (int j = 0; j < STAGES - 1; ++j) issue(j);
 
@@ -147,93 +154,128 @@ norm_fwd_pipe_kernel(const FwdArgs a) {
         const int slot = j % STAGES;
         const int64_t off = (ok ? row : 0) * (int64_t)D;
 
-        // x (fused op: x + r in fp32) of chunk k, re-read from the ring in each phase
-        auto load_x = [&](int k, float (&xk)[8]) {
+        // x of chunk k as fp32 pairs (fused op: x + r), 0 past the row's end
+        auto load_x = [&](int k, float2 (&xk)[4]) {
             const bool v = ok && (k * TPR + t) * 8 < D;
-            unpack8(v ? ring[R::index(slot, 0, k, tid)] : make_uint4(0, 0, 0, 0), xk);
+            unpack8x2(v ? ring[R::index(slot, 0, k, tid)] : make_uint4(0, 0, 0, 0), xk);
             if constexpr (OP == kAddRms) {
-                float res[8];
-                unpack8(v ? ring[R::index(slot, 1, k, tid)] : make_uint4(0, 0, 0, 0), res);
+                float2 rk[4];
+                unpack8x2(v ? ring[R::index(slot, 1, k, tid)] : make_uint4(0, 0, 0, 0), rk);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) xk[e] += res[e];
+                for (int p = 0; p < 4; ++p) xk[p] = __fadd2_rn(xk[p], rk[p]);
             }
         };
+        float2 xs[KEEP ? CH : 1][4];
+        if constexpr (KEEP) {
+#pragma unroll
+            for (int k = 0; k < CH; ++k) load_x(k, xs[k]);
+        }
 
         float mu = 0.f;
         if constexpr (OP == kLayer) {
-            float s[1] = {0.f};
+            float2 s2 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int k = 0; k < CH; ++k) {
-                float xk[8];
-                load_x(k, xk);
+                float2 xk[4];
+                if constexpr (KEEP) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) s[0] += xk[e];
+                    for (int p = 0; p < 4; ++p) xk[p] = xs[k][p];
+                } else {
+                    load_x(k, xk);
+                }
+#pragma unroll
+                for (int p = 0; p < 4; ++p) s2 = __fadd2_rn(s2, xk[p]);
             }
+            float s[1] = {s2.x + s2.y};
             row_sum<TPR, RPC, 1>(s, red, buf, rg, wir, lane);
             buf ^= 1;
-            mu = s[0] / (float)D;
+            mu = s[0] * inv_d;
         }
-        float q[1] = {0.f};
+        const float2 nmu = make_float2(-mu, -mu);
+        float2 q2 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < CH; ++k) {
             const int col = (k * TPR + t) * 8;
             const bool v = ok && col < D;
-            float xk[8];
-            load_x(k, xk);
-            if constexpr (OP == kAddRms) {
-                if (v) st_global_cs(a.S + off + col, pack8(xk));
-            }
+            float2 xk[4];
+            if constexpr (KEEP) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                // LayerNorm: centred second moment (two-pass)
-                const float d = (OP == kLayer) ? (v ? xk[e] - mu : 0.f) : xk[e];
-                q[0] += d * d;
+                for (int p = 0; p < 4; ++p) xk[p] = xs[k][p];
+            } else {
+                load_x(k, xk);
+            }
+            if constexpr (OP == kAddRms) {
+                if (v) __stcs(reinterpret_cast<uint4 *>(a.S + off + col), pack8x2(xk));
+            }
+            if (!v) continue;
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                // LayerNorm: centred second moment (two-pass, from registers or the ring)
+                const float2 d = (OP == kLayer) ? __fadd2_rn(xk[p], nmu) : xk[p];
+                q2 = __ffma2_rn(d, d, q2);
             }
         }
+        float q[1] = {q2.x + q2.y};
         row_sum<TPR, RPC, 1>(q, red, buf, rg, wir, lane);
         buf ^= 1;
-        const float rs = rsqrtf(q[0] / (float)D + a.eps);
+        const float rs = rsqrtf(q[0] * inv_d + a.eps);
         if (!ok) continue;
         if (t == 0) {
             a.rstd[row] = rs;
             if constexpr (OP == kLayer) a.mean[row] = mu;
         }
+        const float2 rs2 = make_float2(rs, rs);
 #pragma unroll
         for (int k = 0; k < CH; ++k) {
             const int col = (k * TPR + t) * 8;
             if (col >= D) continue;
-            float xk[8], g[8], y[8];
-            load_x(k, xk);
-            unpack8(ring[R::param(0, k, tid)], g);
-            if constexpr (OP == kLayer) {
-                float b[8];
-                unpack8(ring[R::param(1, k, tid)], b);
+            float2 xk[4], g[4], y[4];
+            if constexpr (KEEP) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) y[e] = (xk[e] - mu) * rs * g[e] + b[e];
+                for (int p = 0; p < 4; ++p) { xk[p] = xs[k][p]; g[p] = gam[k][p]; }
+            } else {
+                load_x(k, xk);
+                unpack8x2(ring[R::param(0, k, tid)], g);
+            }
+            if constexpr (OP == kLayer) {
+                float2 b[4];
+                if constexpr (KEEP) {
+#pragma unroll
+                    for (int p = 0; p < 4; ++p) b[p] = bet[k][p];
+                } else {
+                    unpack8x2(ring[R::param(1, k, tid)], b);
+                }
+#pragma unroll
+                for (int p = 0; p < 4; ++p)
+                    y[p] = __ffma2_rn(__fmul2_rn(__fadd2_rn(xk[p], nmu), rs2), g[p], b[p]);
             } else {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) y[e] = xk[e] * rs * g[e];
+                for (int p = 0; p < 4; ++p) y[p] = __fmul2_rn(__fmul2_rn(xk[p], rs2), g[p]);
             }
-            st_global_cs(a.Y + off + col, pack8(y));
+            __stcs(reinterpret_cast<uint4 *>(a.Y + off + col), pack8x2(y));
         }
     }
     cp_async_wait<0>();
 }
 
 // ---------------------------------------------------------------- backward ---
-// Dynamic shared memory: the ring and gamma; after the row loop the ring is reused for
-// the fixed-order combine of the CTA's row groups (NV x D floats, which it covers).
+// Dynamic shared memory: the ring (and gamma when CH > 2); after the row loop the ring
+// is reused for the fixed-order combine of the CTA's row groups (NV x D floats).
+// Compiled for bwd_ctas_per_sm() resident CTAs per SM.
 template <int OP, int TPR, int RPC, int CH, int STAGES, bool HAS_DS>
-__global__ void __launch_bounds__(TPR * RPC, 1)
+__global__ void __launch_bounds__(TPR * RPC, bwd_ctas_per_sm(OP, RPC, CH))
 norm_bwd_pipe_kernel(const BwdArgs a) {
     constexpr int THREADS = TPR * RPC;
     constexpr int WPR = TPR / 32;
     constexpr int NV = (OP == kLayer) ? 2 : 1;
     constexpr int NARR = HAS_DS ? 3 : 2;
-    using R = Ring<STAGES, NARR, CH, THREADS, 1>;
+    constexpr bool KEEP = CH <= 2;
+    using R = Ring<STAGES, NARR, CH, THREADS, KEEP ? 0 : 1>;
     static_assert(TPR % 32 == 0 && THREADS <= 1024, "bad launch shape");
     __shared__ float red[2 * RPC * WPR * NV];
     extern __shared__ __align__(16) uint4 ring[];
+
+    pdl_enter();  // the dependent parameter reduction launches now and waits for this grid
 
     const int tid = threadIdx.x;
     const int rg = tid / TPR, t = tid % TPR, wir = t / 32, lane = tid % 32;
@@ -243,14 +285,23 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
     const int64_t first = (int64_t)blockIdx.x * RPC + rg;
     const int iters = cta_iterations(a.N, RPC);
 
-    float accg[CH][8];
-    float accb[CH][(OP == kLayer) ? 8 : 1];
+    float2 gam[KEEP ? CH : 1][4];
+    if constexpr (KEEP) {
+#pragma unroll
+        for (int k = 0; k < CH; ++k) load_param_pairs<CH, TPR>(a.gamma, k, t, D, gam[k]);
+    } else {
+        stage_param<R, CH, TPR>(ring, 0, a.gamma, D, t, tid);
+    }
+    cp_async_commit();
+
+    float2 accg[CH][4];
+    float2 accb[CH][(OP == kLayer) ? 4 : 1];
 #pragma unroll
     for (int k = 0; k < CH; ++k) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) accg[k][e] = 0.f;
+        for (int p = 0; p < 4; ++p) accg[k][p] = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int e = 0; e < ((OP == kLayer) ? 8 : 1); ++e) accb[k][e] = 0.f;
+        for (int p = 0; p < ((OP == kLayer) ? 4 : 1); ++p) accb[k][p] = make_float2(0.f, 0.f);
     }
 
     auto issue = [&](int j) {
@@ -278,8 +329,6 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
         mu = (OP == kLayer && ok) ? __ldg(a.mean + row) : 0.f;
     };
 
-    stage_param<R, CH, TPR>(ring, 0, a.gamma, D, t, tid);
-    cp_async_commit();
 #pragma unroll
     for (int j = 0; j < STAGES - 1; ++j) issue(j);
     float r0, m0, r1, m1;
@@ -298,58 +347,95 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
         const bool ok = row < a.N;
         const int slot = j % STAGES;
         const int64_t off = (ok ? row : 0) * (int64_t)D;
+        const float2 nmu = make_float2(-mu, -mu);
 
-        // pass 1: sum_j g*xhat and, for LayerNorm, sum_j g   (g = dY*gamma)
-        float v[NV];
+        // chunk k's centred x (LayerNorm: x - mean) and dY as fp32 pairs
+        auto load_xd = [&](int k, float2 (&xk)[4], float2 (&dk)[4]) {
+            unpack8x2(ring[R::index(slot, 0, k, tid)], xk);
+            unpack8x2(ring[R::index(slot, 1, k, tid)], dk);
+            if constexpr (OP == kLayer) {
 #pragma unroll
-        for (int i = 0; i < NV; ++i) v[i] = 0.f;
+                for (int p = 0; p < 4; ++p) xk[p] = __fadd2_rn(xk[p], nmu);
+            }
+        };
+        float2 xs[KEEP ? CH : 1][4], ds[KEEP ? CH : 1][4];
+
+        // pass 1: sum_j g*(x - mean) and, for LayerNorm, sum_j g   (g = dY*gamma);
+        // rstd is applied after the reduction: sum_j g*xhat = rstd * sum_j g*(x - mean)
+        float2 v0 = make_float2(0.f, 0.f), v1 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < CH; ++k) {
-            if (!ok || (k * TPR + t) * 8 >= D) continue;
-            float gm[8], xv[8], dv[8];
-            unpack8(ring[R::param(0, k, tid)], gm);
-            unpack8(ring[R::index(slot, 0, k, tid)], xv);
-            unpack8(ring[R::index(slot, 1, k, tid)], dv);
+            const bool v = ok && (k * TPR + t) * 8 < D;
+            float2 xk[4], dk[4], g[4];
+            if (v) {
+                load_xd(k, xk, dk);
+            } else {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float xh = (xv[e] - mu) * r;
-                const float g = dv[e] * gm[e];
-                v[0] += g * xh;
-                if constexpr (OP == kLayer) v[NV - 1] += g;
+                for (int p = 0; p < 4; ++p) xk[p] = dk[p] = make_float2(0.f, 0.f);
+            }
+            if constexpr (KEEP) {
+#pragma unroll
+                for (int p = 0; p < 4; ++p) { xs[k][p] = xk[p]; ds[k][p] = dk[p]; g[p] = gam[k][p]; }
+            } else {
+                if (v) {
+                    unpack8x2(ring[R::param(0, k, tid)], g);
+                } else {
+#pragma unroll
+                    for (int p = 0; p < 4; ++p) g[p] = make_float2(0.f, 0.f);
+                }
+            }
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                const float2 gg = __fmul2_rn(dk[p], g[p]);
+                v0 = __ffma2_rn(gg, xk[p], v0);
+                if constexpr (OP == kLayer) v1 = __fadd2_rn(v1, gg);
             }
         }
-        row_sum<TPR, RPC, NV>(v, red, buf, rg, wir, lane);
-        const float c = v[0] * inv_d;
-        const float am = (OP == kLayer) ? v[NV - 1] * inv_d : 0.f;
+        float vv[NV];
+        vv[0] = v0.x + v0.y;
+        if constexpr (OP == kLayer) vv[NV - 1] = v1.x + v1.y;
+        row_sum<TPR, RPC, NV>(vv, red, buf, rg, wir, lane);
+        const float c = r * vv[0] * inv_d;                           // mean_j g*xhat
+        const float am = (OP == kLayer) ? vv[NV - 1] * inv_d : 0.f;  // mean_j g
         if (!ok) continue;
 
-        // pass 2: dX = r*(g - a - xhat*c) (+ dS), and the parameter-gradient sums
+        // pass 2: dX = r*g - r*a - (r*c)*xhat (+ dS), xhat = (x - mean)*r, and the
+        // parameter-gradient sums dgamma += dY*xhat, dbeta += dY
+        const float2 r2 = make_float2(r, r);
+        const float2 k2 = make_float2(-r * c, -r * c);
+        const float2 ra2 = make_float2(-r * am, -r * am);
 #pragma unroll
         for (int k = 0; k < CH; ++k) {
             const int col = (k * TPR + t) * 8;
             if (col >= D) continue;
-            float gm[8], xv[8], dv[8], o[8];
-            unpack8(ring[R::param(0, k, tid)], gm);
-            unpack8(ring[R::index(slot, 0, k, tid)], xv);
-            unpack8(ring[R::index(slot, 1, k, tid)], dv);
-            float ds[8];
-            if constexpr (HAS_DS) unpack8(ring[R::index(slot, 2, k, tid)], ds);
+            float2 xk[4], dk[4], g[4], o[4];
+            if constexpr (KEEP) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float xh = (xv[e] - mu) * r;
-                const float g = dv[e] * gm[e];
-                float dx = r * ((g - am) - xh * c);
-                if constexpr (HAS_DS) dx += ds[e];
-                o[e] = dx;
-                accg[k][e] += dv[e] * xh;
-                if constexpr (OP == kLayer) accb[k][e] += dv[e];
+                for (int p = 0; p < 4; ++p) { xk[p] = xs[k][p]; dk[p] = ds[k][p]; g[p] = gam[k][p]; }
+            } else {
+                load_xd(k, xk, dk);
+                unpack8x2(ring[R::param(0, k, tid)], g);
             }
-            st_global_cs(a.dX + off + col, pack8(o));
+            float2 sk[4];
+            if constexpr (HAS_DS) unpack8x2(ring[R::index(slot, 2, k, tid)], sk);
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                const float2 xh = __fmul2_rn(xk[p], r2);
+                const float2 gg = __fmul2_rn(dk[p], g[p]);
+                const float2 base = (OP == kLayer) ? __ffma2_rn(gg, r2, ra2) : __fmul2_rn(gg, r2);
+                float2 dx = __ffma2_rn(xh, k2, base);
+                if constexpr (HAS_DS) dx = __fadd2_rn(dx, sk[p]);
+                o[p] = dx;
+                accg[k][p] = __ffma2_rn(dk[p], xh, accg[k][p]);
+                if constexpr (OP == kLayer) accb[k][p] = __fadd2_rn(accb[k][p], dk[p]);
+            }
+            __stcs(reinterpret_cast<uint4 *>(a.dX + off + col), pack8x2(o));
         }
     }
     cp_async_wait<0>();
 
-    // Fixed-order combine of the row groups (rg = 0, 1, ...), one partial row per CTA.
+    // Partials: the CTA's row groups are combined in the fixed order rg = 0, 1, ... and
+    // one fp32 partial row per CTA is written.
     float *pg = a.part_g + (size_t)blockIdx.x * D;
     float *pb = (OP == kLayer) ? a.part_b + (size_t)blockIdx.x * D : nullptr;
     if constexpr (RPC == 1) {
@@ -358,18 +444,18 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
             const int col = (k * TPR + t) * 8;
             if (col >= D) continue;
             float4 *g4 = reinterpret_cast<float4 *>(pg + col);
-            g4[0] = make_float4(accg[k][0], accg[k][1], accg[k][2], accg[k][3]);
-            g4[1] = make_float4(accg[k][4], accg[k][5], accg[k][6], accg[k][7]);
+            g4[0] = make_float4(accg[k][0].x, accg[k][0].y, accg[k][1].x, accg[k][1].y);
+            g4[1] = make_float4(accg[k][2].x, accg[k][2].y, accg[k][3].x, accg[k][3].y);
             if constexpr (OP == kLayer) {
                 float4 *b4 = reinterpret_cast<float4 *>(pb + col);
-                b4[0] = make_float4(accb[k][0], accb[k][1], accb[k][2], accb[k][3]);
-                b4[1] = make_float4(accb[k][4], accb[k][5], accb[k][6], accb[k][7]);
+                b4[0] = make_float4(accb[k][0].x, accb[k][0].y, accb[k][1].x, accb[k][1].y);
+                b4[1] = make_float4(accb[k][2].x, accb[k][2].y, accb[k][3].x, accb[k][3].y);
             }
         }
     } else {
         __syncthreads();  // every thread is done with the ring
-        float *cg = reinterpret_cast<float *>(ring);
-        float *cb = cg + D;
+        float2 *cg2 = reinterpret_cast<float2 *>(ring);
+        float2 *cb2 = cg2 + D / 2;
         for (int j = 0; j < RPC; ++j) {
             if (rg == j) {
 #pragma unroll
@@ -377,12 +463,13 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
                     const int col = (k * TPR + t) * 8;
                     if (col >= D) continue;
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float sg = (j == 0) ? accg[k][e] : cg[col + e] + accg[k][e];
-                        if (j == RPC - 1) pg[col + e] = sg; else cg[col + e] = sg;
+                    for (int p = 0; p < 4; ++p) {
+                        const int i = col / 2 + p;
+                        const float2 sg = (j == 0) ? accg[k][p] : __fadd2_rn(cg2[i], accg[k][p]);
+                        if (j == RPC - 1) reinterpret_cast<float2 *>(pg)[i] = sg; else cg2[i] = sg;
                         if constexpr (OP == kLayer) {
-                            const float sb = (j == 0) ? accb[k][e] : cb[col + e] + accb[k][e];
-                            if (j == RPC - 1) pb[col + e] = sb; else cb[col + e] = sb;
+                            const float2 sb = (j == 0) ? accb[k][p] : __fadd2_rn(cb2[i], accb[k][p]);
+                            if (j == RPC - 1) reinterpret_cast<float2 *>(pb)[i] = sb; else cb2[i] = sb;
                         }
                     }
                 }

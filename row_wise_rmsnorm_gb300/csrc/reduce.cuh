@@ -4,30 +4,46 @@
 
 #include <cuda_runtime.h>
 
+#include "kernels.cuh"
+
 namespace mt {
 
-// Column sums of the [P, D] partials in a fixed order: slice s of the block sums
-// rows s, s + SL, s + 2 SL, ... in ascending order, then thread row 0 adds the SL
-// slice sums in ascending order. blockIdx.y selects dgamma (0) or dbeta (1).
-constexpr int kReduceSlices = 16;
-__global__ void __launch_bounds__(32 * kReduceSlices)
+// Column sums of the [P, D] partials in a fixed order. Warp w of a block sums partial
+// rows w, w + W, w + 2W, ... (W = kReduceWarps) in ascending order for the block's 32
+// columns, eight loads in flight before each group of adds (rows past P add 0); warp 0
+// then adds the W warp sums in ascending order. blockIdx.y selects dgamma (0) or dbeta (1). The kernel may be
+// launched as a programmatic dependent of the backward: griddepcontrol.wait holds it
+// until the backward grid has finished and its partials are visible (without that
+// launch attribute the wait returns at once).
+constexpr int kReduceWarps = 32;
+__global__ void __launch_bounds__(32 * kReduceWarps)
 param_reduce_kernel(const float *__restrict__ part, int P, int D, float *__restrict__ out0,
                     float *__restrict__ out1) {
-    __shared__ float sm[kReduceSlices][33];
+    pdl_enter();
+    __shared__ float sm[kReduceWarps][33];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const float *src = part + (size_t)blockIdx.y * (size_t)P * (size_t)D;
     float *dst = blockIdx.y == 0 ? out0 : out1;
-    const int col = blockIdx.x * 32 + threadIdx.x;
+    const int col = blockIdx.x * 32 + lane;
     float s = 0.f;
     if (col < D) {
-#pragma unroll 4
-        for (int q = threadIdx.y; q < P; q += kReduceSlices) s += src[(size_t)q * D + col];
+        for (int p = w; p < P; p += 8 * kReduceWarps) {
+            float v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int q = p + i * kReduceWarps;
+                v[i] = q < P ? __ldcg(src + (size_t)q * D + col) : 0.f;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) s += v[i];
+        }
     }
-    sm[threadIdx.y][threadIdx.x] = s;
+    sm[w][lane] = s;
     __syncthreads();
-    if (threadIdx.y == 0 && col < D) {
+    if (w == 0 && col < D) {
         float tot = 0.f;
 #pragma unroll
-        for (int i = 0; i < kReduceSlices; ++i) tot += sm[i][threadIdx.x];
+        for (int i = 0; i < kReduceWarps; ++i) tot += sm[i][lane];
         dst[col] = tot;
     }
 }

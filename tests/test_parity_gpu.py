@@ -214,8 +214,9 @@ def test_workspace_too_small_is_rejected():
     ws = torch.empty(need, dtype=torch.uint8, device=DEV)
     dX = torch.empty_like(t["X"])
     dg = torch.empty(D, dtype=torch.float32, device=DEV)
+    # the query covers every kernel variant; 256 bytes is below any variant's need
     with pytest.raises(mt.MtNormError) as e:
-        mt.mt_rmsnorm_backward_ws(t["X"], t["gamma"], t["dY"], rstd, dX, dg, N, D, ws, need - 256)
+        mt.mt_rmsnorm_backward_ws(t["X"], t["gamma"], t["dY"], rstd, dX, dg, N, D, ws, 256)
     assert e.value.status == mt.MT_ERR_UNSUPPORTED
 
 
@@ -245,3 +246,19 @@ def test_invalid_arguments_raise_before_launch():
     with pytest.raises(mt.MtNormError) as e:
         mt.mt_rmsnorm_forward(t["X"], t["gamma"], y, r, 4, mt.MT_MAX_COLS + 1, 1e-5)
     assert e.value.status == mt.MT_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("op", W.OPS)
+def test_cached_plans_survive_alternating_widths(op):
+    """Plans are cached per kernel and size; a wider call after a narrower one on the same
+    kernel must still launch (shared-memory limits only grow), on both paths."""
+    for D, shift in [(1024, 1), (1000, 0), (1024, 1), (2048, 0), (2040, 0), (2048, 0), (1023, 0)]:
+        N = 33
+        t = W.generate(op, N, D, seed=D, dy_std=1.0)
+        d = {}
+        for k, v in t.items():
+            buf = torch.empty(v.numel() + 8, dtype=v.dtype, device=DEV)
+            d[k] = buf[shift:shift + v.numel()].view(v.shape)
+            d[k].copy_(v.to(DEV))
+        got = gpu_run(op, d, 1e-5)
+        compare(op, got, oracle_run(op, t, 1e-5), t["X"], tag=f"{op} D={D} shift={shift}")
