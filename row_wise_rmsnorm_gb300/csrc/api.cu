@@ -147,7 +147,8 @@ mt_status_t run_backward(int op, BwdArgs a, bool vec8, float *dgamma, float *dbe
         // Programmatic dependent launch: the reduction is set up while the backward
         // runs and starts reading only after the backward grid has completed.
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)((a.D + 31) / 32), (unsigned)num_partial_arrays(op));
+        cfg.gridDim = dim3((unsigned)((a.D + kReduceCols - 1) / kReduceCols),
+                           (unsigned)num_partial_arrays(op));
         cfg.blockDim = dim3(32 * kReduceWarps);
         cfg.dynamicSmemBytes = 0;
         cfg.stream = stream;
