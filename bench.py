@@ -336,6 +336,19 @@ def run_reference(args):
     return 0
 
 
+# ---------------------------------------------------------- multi-rank ---
+
+def max_over_ranks(value: float, device=None) -> float:
+    """The largest `value` over all ranks (the step time of the slowest replica)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # --------------------------------------------------------------- main ---
 
 def main(argv=None):
@@ -392,10 +405,7 @@ def main(argv=None):
     fwd_ms = statistics.mean(fwd)
     bwd_ms = statistics.mean(bwd)
     step_ms = total_ms / args.steps
-    if world > 1:
-        tt = torch.tensor([step_ms], device=device, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        step_ms = float(tt.item())
+    step_ms = max_over_ranks(step_ms, device)
 
     step_bytes = runner.fwd_bytes + runner.bwd_bytes
     value = world * step_bytes / (step_ms * 1e-3) / 1e9
@@ -436,9 +446,7 @@ def main(argv=None):
     if not args.no_e2e:
         e2e = e2e_run(args.workload, device, max(5, min(50, args.steps // 40)), 3, seed=rank)
         if world > 1:
-            tt = torch.tensor([e2e["ms_per_step"]], device=device, dtype=torch.float64)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e2e["ms_per_step"] = round(float(tt.item()), 4)
+            e2e["ms_per_step"] = round(max_over_ranks(e2e["ms_per_step"], device), 4)
             e2e["value"] = round(world * step_bytes / (e2e["ms_per_step"] * 1e-3) / 1e9, 2)
 
     cpu = None
