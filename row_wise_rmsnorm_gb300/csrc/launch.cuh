@@ -4,9 +4,10 @@
 // VEC fp16 elements per chunk). VEC = 8 (one 16-byte access per chunk) is legal when
 // D % 8 == 0 and every row base is 16-byte aligned; VEC = 1 covers everything else.
 // The first shape whose width covers D is taken. Forward rows up to 1024 wide get one
-// warp each (four rows per CTA); wider rows get one CTA each. The backward uses the
-// same split with more rows per CTA, so that few persistent CTAs cover the device
-// and the dgamma/dbeta partials stay small.
+// warp each (four rows per CTA); wider rows get one CTA each, one row per CTA (on
+// GB300 this beat a persistent pipelined forward at every width measured). The
+// aligned backward is persistent and pipelined (pipe.cuh), with few CTAs so that the
+// dgamma/dbeta partials stay small.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -24,7 +25,9 @@ namespace mt {
     X(512, 32, 4, 2)          \
     X(1024, 32, 4, 4)         \
     X(2048, 256, 1, 1)        \
-    X(4096, 256, 1, 2)
+    X(4096, 256, 1, 2)        \
+    X(8192, 512, 1, 2)        \
+    X(16384, 512, 1, 4)
 
 #define MT_FWD_SHAPES_VEC1(X) \
     X(64, 32, 4, 2)           \
@@ -48,12 +51,9 @@ namespace mt {
     X(8192, 512, 1, 16)       \
     X(16384, 512, 1, 32)
 
-// Pipelined persistent shapes for 16-byte-aligned rows: X(max_D, TPR, RPC, CH, STAGES).
-// STAGES is the largest ring depth; pipe_stages() cuts it to fit shared memory.
-#define MT_FWD_PIPE_SHAPES(X)   \
-    X(8192, 512, 1, 2, 6)       \
-    X(16384, 512, 1, 4, 4)
-
+// Pipelined persistent backward shapes for 16-byte-aligned rows:
+// X(max_D, TPR, RPC, CH, STAGES). STAGES is the largest ring depth; pipe_stages() cuts it
+// to fit shared memory.
 #define MT_BWD_PIPE_SHAPES(X)   \
     X(256, 32, 16, 1, 8)        \
     X(512, 64, 8, 1, 8)         \
@@ -114,35 +114,19 @@ inline cudaError_t persistent_grid(LaunchPlan *p, int64_t N, int device) {
     return cudaSuccess;
 }
 
-template <int OP, int TPR, int RPC, int CH, int STAGES>
-cudaError_t fwd_pipe_plan_shape(int64_t N, int device, LaunchPlan *p) {
-    constexpr int NARR = (OP == kAddRms) ? 2 : 1;
-    constexpr int NPAR = (CH <= 2) ? 0 : ((OP == kLayer) ? 2 : 1);
-    constexpr int S = pipe_stages(STAGES, NARR, NPAR, CH, TPR * RPC, 1);
-    static_assert(Ring<S, NARR, CH, TPR * RPC, NPAR>::kBytes <= kMaxDynSmem, "ring too large");
-    p->kernel = reinterpret_cast<const void *>(&norm_fwd_pipe_kernel<OP, TPR, RPC, CH, S>);
-    p->threads = TPR * RPC;
-    p->smem = Ring<S, NARR, CH, TPR * RPC, NPAR>::kBytes;
-    p->rows_per_cta = RPC;
-    return persistent_grid(p, N, device);
-}
-
 template <int OP>
 cudaError_t fwd_plan(int64_t N, int D, bool vec8, int device, LaunchPlan *p) {
+    (void)device;
 #define MT_TRY(maxd, tpr, rpc, ch) \
     if (D <= maxd) return fwd_plan_shape<OP, tpr, rpc, ch, VEC>(N, p);
-#define MT_TRY_PIPE(maxd, tpr, rpc, ch, st) \
-    if (D <= maxd) return fwd_pipe_plan_shape<OP, tpr, rpc, ch, st>(N, device, p);
     if (vec8) {
         constexpr int VEC = 8;
         MT_FWD_SHAPES_VEC8(MT_TRY)
-        MT_FWD_PIPE_SHAPES(MT_TRY_PIPE)
     } else {
         constexpr int VEC = 1;
         MT_FWD_SHAPES_VEC1(MT_TRY)
     }
 #undef MT_TRY
-#undef MT_TRY_PIPE
     return cudaErrorInvalidValue;
 }
 

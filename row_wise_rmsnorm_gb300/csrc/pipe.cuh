@@ -1,4 +1,4 @@
-// pipe.cuh -- pipelined persistent kernels for 16-byte-aligned rows (D % 8 == 0).
+// pipe.cuh -- pipelined persistent backward for 16-byte-aligned rows (D % 8 == 0).
 //
 // Streaming. Each CTA is persistent and every thread streams ITS OWN 16-byte chunks
 // of the next STAGES-1 rows into a shared-memory ring with cp.async (L2 only, no L1
@@ -18,7 +18,7 @@
 // exactly as the scalar fp32 operation. When a thread's slice is small (CH <= 2) the
 // converted row values and fp32 gamma (beta) stay in registers across the reduction
 // barrier; for wider slices they are re-read from the ring and from per-thread
-// parameter slots, which keeps the kernels free of register spills.
+// parameter slots, which keeps the kernel free of register spills.
 #pragma once
 
 #include "kernels.cuh"
@@ -87,175 +87,6 @@ __device__ __forceinline__ int cta_iterations(int64_t N, int rpc) {
     const int64_t base = (int64_t)blockIdx.x * rpc;
     const int64_t stride = (int64_t)gridDim.x * rpc;
     return base < N ? (int)((N - base + stride - 1) / stride) : 0;
-}
-
-// ----------------------------------------------------------------- forward ---
-template <int OP, int TPR, int RPC, int CH, int STAGES>
-__global__ void __launch_bounds__(TPR * RPC, 1)
-norm_fwd_pipe_kernel(const FwdArgs a) {
-    pdl_enter();
-    constexpr int THREADS = TPR * RPC;
-    constexpr int WPR = TPR / 32;
-    constexpr int NARR = (OP == kAddRms) ? 2 : 1;
-    constexpr bool KEEP = CH <= 2;
-    constexpr int NPAR = KEEP ? 0 : ((OP == kLayer) ? 2 : 1);
-    using R = Ring<STAGES, NARR, CH, THREADS, NPAR>;
-    static_assert(TPR % 32 == 0 && THREADS <= 1024, "bad launch shape");
-    __shared__ float red[2 * RPC * WPR];
-    extern __shared__ __align__(16) uint4 ring[];
-
-    const int tid = threadIdx.x;
-    const int rg = tid / TPR, t = tid % TPR, wir = t / 32, lane = tid % 32;
-    const int D = a.D;
-    const float inv_d = 1.0f / (float)D;
-    const int64_t stride = (int64_t)gridDim.x * RPC;
-    const int64_t first = (int64_t)blockIdx.x * RPC + rg;
-    const int iters = cta_iterations(a.N, RPC);
-
-    float2 gam[KEEP ? CH : 1][4], bet[(KEEP && OP == kLayer) ? CH : 1][4];
-    if constexpr (KEEP) {
-#pragma unroll
-        for (int k = 0; k < CH; ++k) {
-            load_param_pairs<CH, TPR>(a.gamma, k, t, D, gam[k]);
-            if constexpr (OP == kLayer) load_param_pairs<CH, TPR>(a.beta, k, t, D, bet[k]);
-        }
-    } else {
-        stage_param<R, CH, TPR>(ring, 0, a.gamma, D, t, tid);
-        if constexpr (OP == kLayer) stage_param<R, CH, TPR>(ring, 1, a.beta, D, t, tid);
-    }
-    cp_async_commit();
-
-    auto issue = [&](int j) {
-        const int64_t row = first + (int64_t)j * stride;
-        if (j < iters && row < a.N) {
-            const int slot = j % STAGES;
-            const int64_t off = row * (int64_t)D;
-#pragma unroll
-            for (int k = 0; k < CH; ++k) {
-                const int col = (k * TPR + t) * 8;
-                if (col < D) {
-                    cp_async16(smem_addr(&ring[R::index(slot, 0, k, tid)]), a.X + off + col);
-                    if constexpr (OP == kAddRms)
-                        cp_async16(smem_addr(&ring[R::index(slot, 1, k, tid)]), a.R + off + col);
-                }
-            }
-        }
-        cp_async_commit();
-    };
-#pragma unroll
-    for (int j = 0; j < STAGES - 1; ++j) issue(j);
-
-    int buf = 0;
-    for (int j = 0; j < iters; ++j) {
-        issue(j + STAGES - 1);
-        cp_async_wait<STAGES - 1>();
-        const int64_t row = first + (int64_t)j * stride;
-        const bool ok = row < a.N;
-        const int slot = j % STAGES;
-        const int64_t off = (ok ? row : 0) * (int64_t)D;
-
-        // x of chunk k as fp32 pairs (fused op: x + r), 0 past the row's end
-        auto load_x = [&](int k, float2 (&xk)[4]) {
-            const bool v = ok && (k * TPR + t) * 8 < D;
-            unpack8x2(v ? ring[R::index(slot, 0, k, tid)] : make_uint4(0, 0, 0, 0), xk);
-            if constexpr (OP == kAddRms) {
-                float2 rk[4];
-                unpack8x2(v ? ring[R::index(slot, 1, k, tid)] : make_uint4(0, 0, 0, 0), rk);
-#pragma unroll
-                for (int p = 0; p < 4; ++p) xk[p] = __fadd2_rn(xk[p], rk[p]);
-            }
-        };
-        float2 xs[KEEP ? CH : 1][4];
-        if constexpr (KEEP) {
-#pragma unroll
-            for (int k = 0; k < CH; ++k) load_x(k, xs[k]);
-        }
-
-        float mu = 0.f;
-        if constexpr (OP == kLayer) {
-            float2 s2 = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int k = 0; k < CH; ++k) {
-                float2 xk[4];
-                if constexpr (KEEP) {
-#pragma unroll
-                    for (int p = 0; p < 4; ++p) xk[p] = xs[k][p];
-                } else {
-                    load_x(k, xk);
-                }
-#pragma unroll
-                for (int p = 0; p < 4; ++p) s2 = __fadd2_rn(s2, xk[p]);
-            }
-            float s[1] = {s2.x + s2.y};
-            row_sum<TPR, RPC, 1>(s, red, buf, rg, wir, lane);
-            buf ^= 1;
-            mu = s[0] * inv_d;
-        }
-        const float2 nmu = make_float2(-mu, -mu);
-        float2 q2 = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int k = 0; k < CH; ++k) {
-            const int col = (k * TPR + t) * 8;
-            const bool v = ok && col < D;
-            float2 xk[4];
-            if constexpr (KEEP) {
-#pragma unroll
-                for (int p = 0; p < 4; ++p) xk[p] = xs[k][p];
-            } else {
-                load_x(k, xk);
-            }
-            if constexpr (OP == kAddRms) {
-                if (v) __stcs(reinterpret_cast<uint4 *>(a.S + off + col), pack8x2(xk));
-            }
-            if (!v) continue;
-#pragma unroll
-            for (int p = 0; p < 4; ++p) {
-                // LayerNorm: centred second moment (two-pass, from registers or the ring)
-                const float2 d = (OP == kLayer) ? __fadd2_rn(xk[p], nmu) : xk[p];
-                q2 = __ffma2_rn(d, d, q2);
-            }
-        }
-        float q[1] = {q2.x + q2.y};
-        row_sum<TPR, RPC, 1>(q, red, buf, rg, wir, lane);
-        buf ^= 1;
-        const float rs = rsqrtf(q[0] * inv_d + a.eps);
-        if (!ok) continue;
-        if (t == 0) {
-            a.rstd[row] = rs;
-            if constexpr (OP == kLayer) a.mean[row] = mu;
-        }
-        const float2 rs2 = make_float2(rs, rs);
-#pragma unroll
-        for (int k = 0; k < CH; ++k) {
-            const int col = (k * TPR + t) * 8;
-            if (col >= D) continue;
-            float2 xk[4], g[4], y[4];
-            if constexpr (KEEP) {
-#pragma unroll
-                for (int p = 0; p < 4; ++p) { xk[p] = xs[k][p]; g[p] = gam[k][p]; }
-            } else {
-                load_x(k, xk);
-                unpack8x2(ring[R::param(0, k, tid)], g);
-            }
-            if constexpr (OP == kLayer) {
-                float2 b[4];
-                if constexpr (KEEP) {
-#pragma unroll
-                    for (int p = 0; p < 4; ++p) b[p] = bet[k][p];
-                } else {
-                    unpack8x2(ring[R::param(1, k, tid)], b);
-                }
-#pragma unroll
-                for (int p = 0; p < 4; ++p)
-                    y[p] = __ffma2_rn(__fmul2_rn(__fadd2_rn(xk[p], nmu), rs2), g[p], b[p]);
-            } else {
-#pragma unroll
-                for (int p = 0; p < 4; ++p) y[p] = __fmul2_rn(__fmul2_rn(xk[p], rs2), g[p]);
-            }
-            __stcs(reinterpret_cast<uint4 *>(a.Y + off + col), pack8x2(y));
-        }
-    }
-    cp_async_wait<0>();
 }
 
 // ---------------------------------------------------------------- backward ---

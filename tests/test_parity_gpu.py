@@ -71,8 +71,9 @@ def test_fused_without_residual_cotangent():
 
 # ----------------------------------------------------------- shape sweep ---
 
-SWEEP_D = [1, 2, 7, 8, 31, 32, 33, 127, 255, 257, 1023, 1024, 1025, 2048, 4095, 4096, 8191, 8192,
-           16384]
+# 4104, 6144, 8192, 12288, 16384: wide aligned rows (no split, and cluster splits of 2, 3, 4)
+SWEEP_D = [1, 2, 7, 8, 31, 32, 33, 127, 255, 257, 1023, 1024, 1025, 2048, 4095, 4096, 4104, 6144,
+           8191, 8192, 12288, 16384]
 
 
 @pytest.mark.parametrize("op", W.OPS)
