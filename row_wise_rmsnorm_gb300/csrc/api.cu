@@ -145,11 +145,17 @@ mt_status_t run_backward(int op, BwdArgs a, bool vec8, float *dgamma, float *dbe
     mt_status_t st = launch(p, &a, stream);
     if (st == MT_OK) {
         // Programmatic dependent launch: the reduction is set up while the backward
-        // runs and starts reading only after the backward grid has completed.
+        // runs and starts reading only after the backward grid has completed. The wide
+        // form is used when its 128-column blocks still give one block per SM.
+        int sms = 0;
+        e = device_sm_count(device, &sms);
+        if (e != cudaSuccess) return cuda_fail(e);
+        const int arrays = num_partial_arrays(op);
+        const bool wide = (a.D % 4 == 0) && ((a.D + 127) / 128) * arrays >= sms;
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)((a.D + kReduceCols - 1) / kReduceCols),
-                           (unsigned)num_partial_arrays(op));
-        cfg.blockDim = dim3(32 * kReduceWarps);
+        cfg.gridDim = wide ? dim3((unsigned)((a.D + 127) / 128), (unsigned)arrays)
+                           : dim3((unsigned)((a.D + 31) / 32), (unsigned)arrays);
+        cfg.blockDim = dim3(32 * (wide ? kReduceWideWarps : kReduceNarrowWarps));
         cfg.dynamicSmemBytes = 0;
         cfg.stream = stream;
         cudaLaunchAttribute attr[1];
@@ -158,7 +164,10 @@ mt_status_t run_backward(int op, BwdArgs a, bool vec8, float *dgamma, float *dbe
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         const float *cpart = part;
-        e = cudaLaunchKernelEx(&cfg, param_reduce_kernel, cpart, prow, a.D, dgamma, dbeta);
+        e = wide ? cudaLaunchKernelEx(&cfg, param_reduce_kernel<4, kReduceWideWarps>, cpart, prow,
+                                      a.D, dgamma, dbeta)
+                 : cudaLaunchKernelEx(&cfg, param_reduce_kernel<1, kReduceNarrowWarps>, cpart,
+                                      prow, a.D, dgamma, dbeta);
         if (e != cudaSuccess) st = cuda_fail(e);
     }
     if (own_ws) {
