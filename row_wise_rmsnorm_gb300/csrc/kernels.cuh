@@ -188,14 +188,29 @@ __device__ __forceinline__ void store_act(__half *row, int col, int D, const flo
     }
 }
 
+// Barrier for one row group. NAMED: named barrier 1 + rg over the group's TPR threads,
+// so the row groups of a CTA do not wait for one another (the persistent backward, where
+// row groups run many rows; measured faster there). Otherwise, and for a CTA that is a
+// single row group, barrier 0 (__syncthreads; measured faster in the forward, where
+// every row group runs one row and exits).
+template <int TPR, int RPC, bool NAMED>
+__device__ __forceinline__ void row_group_sync(int rg) {
+    if constexpr (RPC == 1 || !NAMED) {
+        __syncthreads();
+    } else {
+        static_assert(RPC < 16, "one named barrier per row group");
+        asm volatile("bar.sync %0, %1;" ::"r"(1 + rg), "n"(TPR) : "memory");
+    }
+}
+
 // Sum NV values over the TPR threads of one row group. `red` holds
 // 2 (buffers) x RPC x WPR x NV floats; alternate `buf` between consecutive calls so
-// one __syncthreads per call suffices. Every thread of the CTA must call it when
-// WPR > 1 (it contains a CTA-wide barrier). Each warp first reduces with a butterfly;
-// then lane l of every warp reads warp l's sum (zero for l >= WPR) and a second
-// butterfly adds them. The operands and their order are the same in every warp, so
-// every thread ends with the bitwise-identical total.
-template <int TPR, int RPC, int NV>
+// one barrier per call suffices. When WPR > 1 it contains a barrier (see row_group_sync):
+// every thread of the row group (of the CTA, unless NAMED) must call it. Each warp first reduces with a
+// butterfly; then lane l of every warp reads warp l's sum (zero for l >= WPR) and a
+// second butterfly adds them. The operands and their order are the same in every
+// warp, so every thread ends with the bitwise-identical total.
+template <int TPR, int RPC, int NV, bool NAMED = false>
 __device__ __forceinline__ void row_sum(float (&v)[NV], float *red, int buf, int rg, int wir,
                                         int lane) {
     constexpr int WPR = TPR / 32;
@@ -208,7 +223,7 @@ __device__ __forceinline__ void row_sum(float (&v)[NV], float *red, int buf, int
 #pragma unroll
             for (int i = 0; i < NV; ++i) s[wir * NV + i] = v[i];
         }
-        __syncthreads();
+        row_group_sync<TPR, RPC, NAMED>(rg);
 #pragma unroll
         for (int i = 0; i < NV; ++i) v[i] = warp_sum(lane < WPR ? s[lane * NV + i] : 0.f);
     }
@@ -305,9 +320,10 @@ norm_fwd_kernel(const FwdArgs a) {
 
 // Forward for 16-byte-aligned rows (D % 8 == 0), one row group per row, fp32 pair
 // arithmetic (__ffma2_rn & co.). Rows are loaded once with streaming 16-byte loads and
-// stay in registers through the reductions and the apply.
-template <int OP, int TPR, int RPC, int CH>
-__global__ void __launch_bounds__(TPR * RPC)
+// stay in registers through the reductions and the apply. MINB is the minimum number of
+// resident CTAs per SM asked of the compiler (it bounds the registers per thread).
+template <int OP, int TPR, int RPC, int CH, int MINB>
+__global__ void __launch_bounds__(TPR * RPC, MINB)
 norm_fwd_vec8_kernel(const FwdArgs a) {
     pdl_enter();
     static_assert(TPR % 32 == 0 && TPR * RPC <= 1024, "bad launch shape");
@@ -384,6 +400,113 @@ norm_fwd_vec8_kernel(const FwdArgs a) {
 #pragma unroll
             for (int p = 0; p < 4; ++p) y[p] = __fmul2_rn(__fmul2_rn(x[k][p], rs2), g[p]);
         }
+        __stcs(reinterpret_cast<uint4 *>(a.Y + off + col), pack8x2(y));
+    }
+}
+
+// The same forward for RMSNorm and LayerNorm with the row kept as the loaded fp16 chunks
+// and widened to fp32 pairs at each use: half the registers of norm_fwd_vec8_kernel, so
+// more CTAs (and more bytes in flight) fit per SM, for one more conversion per pass.
+// (The fused op normalises the unrounded fp32 x + r, so it cannot keep fp16 chunks.)
+template <int OP, int TPR, int RPC, int CH, int MINB>
+__global__ void __launch_bounds__(TPR * RPC, MINB)
+norm_fwd_packed_kernel(const FwdArgs a) {
+    pdl_enter();
+    static_assert(TPR % 32 == 0 && TPR * RPC <= 1024, "bad launch shape");
+    static_assert(OP == kRms || OP == kLayer, "the fused op keeps its fp32 sum");
+    constexpr int WPR = TPR / 32;
+    __shared__ float red[2 * RPC * WPR];
+
+    const int tid = threadIdx.x;
+    const int rg = tid / TPR, t = tid % TPR, wir = t / 32, lane = tid % 32;
+    const int D = a.D;
+    const float inv_d = 1.0f / (float)D;
+    const int64_t row = (int64_t)blockIdx.x * RPC + rg;
+    const bool ok = row < a.N;
+    if (WPR == 1 && !ok) return;  // no CTA barrier in a single-warp row group
+    const int64_t off = (ok ? row : 0) * (int64_t)D;
+
+    uint4 raw[CH];
+#pragma unroll
+    for (int k = 0; k < CH; ++k) {
+        const int col = (k * TPR + t) * 8;
+        raw[k] = (ok && col < D) ? __ldcs(reinterpret_cast<const uint4 *>(a.X + off + col))
+                                 : make_uint4(0, 0, 0, 0);
+    }
+    // Chunk k as fp32 pairs. Each pass widens the chunks again rather than keep fp32
+    // copies of the row alive across the reductions. So that the compiler does not merge
+    // those conversions, a pass XORs the words with `zero & bits(after)`, where `after`
+    // is a value of that pass (the mean, rstd) and `zero` is a runtime zero (D < 2^30):
+    // the words are unchanged, but each pass's conversions have their own inputs, which
+    // exist only once the pass's reduction is done.
+    const uint32_t zero = (uint32_t)D >> 30;
+    auto pairs = [&](int k, float2 (&f)[4], float after) {
+        const uint32_t key = zero & __float_as_uint(after);
+        unpack8x2(make_uint4(raw[k].x ^ key, raw[k].y ^ key, raw[k].z ^ key, raw[k].w ^ key), f);
+    };
+
+    float mu = 0.f;
+    if constexpr (OP == kLayer) {
+        float2 s2 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < CH; ++k) {
+            float2 f[4];
+            unpack8x2(raw[k], f);
+#pragma unroll
+            for (int p = 0; p < 4; ++p) s2 = __fadd2_rn(s2, f[p]);
+        }
+        float s[1] = {s2.x + s2.y};
+        row_sum<TPR, RPC, 1>(s, red, 0, rg, wir, lane);
+        mu = s[0] * inv_d;
+    }
+    const float2 nmu = make_float2(-mu, -mu);
+    float2 q2 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < CH; ++k) {
+        if (!(ok && (k * TPR + t) * 8 < D)) continue;
+        float2 f[4];
+        if constexpr (OP == kLayer) pairs(k, f, mu);
+        else unpack8x2(raw[k], f);
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const float2 d = (OP == kLayer) ? __fadd2_rn(f[p], nmu) : f[p];
+            q2 = __ffma2_rn(d, d, q2);
+        }
+    }
+    float q[1] = {q2.x + q2.y};
+    row_sum<TPR, RPC, 1>(q, red, 1, rg, wir, lane);
+    const float rs = rsqrtf(q[0] * inv_d + a.eps);
+    if (!ok) return;  // after the last barrier
+    if (t == 0) {
+        a.rstd[row] = rs;
+        if constexpr (OP == kLayer) a.mean[row] = mu;
+    }
+    const float2 rs2 = make_float2(rs, rs);
+    // gamma (beta) are read chunk by chunk at the point of use: `chain` (always zero)
+    // makes each chunk's parameter address depend on rs and on the previous chunk's
+    // result, so the compiler neither hoists the loads above the reductions nor issues
+    // all chunks' loads at once, either of which would hold CH x 16 (32) bytes of
+    // registers per thread.
+    uint32_t chain = zero & __float_as_uint(rs);
+#pragma unroll
+    for (int k = 0; k < CH; ++k) {
+        const int col = (k * TPR + t) * 8;
+        if (col >= D) continue;
+        float2 f[4], g[4], y[4];
+        pairs(k, f, rs);
+        const int pc = col + (int)chain;
+        unpack8x2(__ldg(reinterpret_cast<const uint4 *>(a.gamma + pc)), g);
+        if constexpr (OP == kLayer) {
+            float2 b[4];
+            unpack8x2(__ldg(reinterpret_cast<const uint4 *>(a.beta + pc)), b);
+#pragma unroll
+            for (int p = 0; p < 4; ++p)
+                y[p] = __ffma2_rn(__fmul2_rn(__fadd2_rn(f[p], nmu), rs2), g[p], b[p]);
+        } else {
+#pragma unroll
+            for (int p = 0; p < 4; ++p) y[p] = __fmul2_rn(__fmul2_rn(f[p], rs2), g[p]);
+        }
+        chain = zero & __float_as_uint(y[0].x);
         __stcs(reinterpret_cast<uint4 *>(a.Y + off + col), pack8x2(y));
     }
 }

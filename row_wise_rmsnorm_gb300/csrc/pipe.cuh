@@ -25,12 +25,6 @@
 
 namespace mt {
 
-// Resident CTAs per SM the backward is compiled for: two (64 registers each) for a
-// single one-chunk row group per CTA, one otherwise (more registers, deeper ring).
-constexpr int bwd_ctas_per_sm(int op, int rpc, int ch) {
-    return (ch == 1 && rpc == 1) ? 2 : 1;
-}
-
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return (uint32_t)__cvta_generic_to_shared(p);
 }
@@ -92,9 +86,9 @@ __device__ __forceinline__ int cta_iterations(int64_t N, int rpc) {
 // ---------------------------------------------------------------- backward ---
 // Dynamic shared memory: the ring (and gamma when CH > 2); after the row loop the ring
 // is reused for the fixed-order combine of the CTA's row groups (NV x D floats).
-// Compiled for bwd_ctas_per_sm() resident CTAs per SM.
-template <int OP, int TPR, int RPC, int CH, int STAGES, bool HAS_DS>
-__global__ void __launch_bounds__(TPR * RPC, bwd_ctas_per_sm(OP, RPC, CH))
+// Compiled for CTAS resident CTAs per SM (it caps the registers per thread).
+template <int OP, int TPR, int RPC, int CH, int STAGES, bool HAS_DS, int CTAS>
+__global__ void __launch_bounds__(TPR * RPC, CTAS)
 norm_bwd_pipe_kernel(const BwdArgs a) {
     constexpr int THREADS = TPR * RPC;
     constexpr int WPR = TPR / 32;
@@ -225,7 +219,7 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
         float vv[NV];
         vv[0] = v0.x + v0.y;
         if constexpr (OP == kLayer) vv[NV - 1] = v1.x + v1.y;
-        row_sum<TPR, RPC, NV>(vv, red, buf, rg, wir, lane);
+        row_sum<TPR, RPC, NV, true>(vv, red, buf, rg, wir, lane);
         const float c = r * vv[0] * inv_d;                           // mean_j g*xhat
         const float am = (OP == kLayer) ? vv[NV - 1] * inv_d : 0.f;  // mean_j g
         if (!ok) continue;
