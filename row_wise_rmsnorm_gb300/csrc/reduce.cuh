@@ -18,7 +18,7 @@ namespace mt {
 // SM, so small D keeps its loads spread over many SMs. The kernel is launched as a
 // programmatic dependent of the backward: pdl_enter() holds it until the backward grid
 // has finished and its partials are visible.
-constexpr int kReduceBatch = 8;
+constexpr int kReduceBatch = 12;
 
 template <int V> struct VecF;
 template <> struct VecF<1> {
