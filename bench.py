@@ -137,18 +137,25 @@ class ClockSampler:
 # ------------------------------------------------------------ GPU arm ---
 
 class OpRunner:
-    """Holds one workload's device buffers and issues its forward/backward C-ABI calls."""
+    """Holds one workload's device buffers and issues its forward/backward C-ABI calls.
 
-    def __init__(self, name: str, device, seed: int):
+    ``dtype`` (a torch dtype) stores every activation, parameter and cotangent in that
+    type and goes through the explicit-dtype entry points; None keeps the fp16 ones."""
+
+    def __init__(self, name: str, device, seed: int, dtype=None):
         import torch
         import row_wise_rmsnorm_gb300 as mt
         self.mt = mt
         self.w = W.WORKLOADS[name]
         self.dev = device
         w = self.w
-        self.t = W.generate_workload(name, device=device, seed=seed)
+        self.dtype = dtype
+        dt = torch.float16 if dtype is None else dtype
+        self.t = W.generate(w.op, w.N, w.D, device=device, seed=seed, x_kind=w.x_kind,
+                            dy_std=w.dy_std, beta_std=w.beta_std, x_dtype=dt, w_dtype=dt,
+                            g_dtype=dt)
         N, D = w.N, w.D
-        h = dict(dtype=torch.float16, device=device)
+        h = dict(dtype=dt, device=device)
         f = dict(dtype=torch.float32, device=device)
         self.Y = torch.empty((N, D), **h)
         self.rstd = torch.empty(N, **f)
@@ -161,11 +168,19 @@ class OpRunner:
                   W.ADD_RMSNORM: mt.MT_OP_ADD_RMSNORM}[w.op]
         self.ws_bytes = mt.mt_norm_backward_workspace_size(opcode, N, D, device.index or 0)
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
-        self.fwd_bytes = W.compulsory_bytes(w.op, "forward", N, D)
-        self.bwd_bytes = W.compulsory_bytes(w.op, "backward", N, D)
+        eb = torch.empty(0, dtype=dt).element_size()
+        self.fwd_bytes = W.compulsory_bytes(w.op, "forward", N, D, xb=eb, wb=eb, gb=eb)
+        self.bwd_bytes = W.compulsory_bytes(w.op, "backward", N, D, xb=eb, wb=eb, gb=eb)
+        self.opcode = opcode
 
     def forward(self, stream):
         w, t, mt = self.w, self.t, self.mt
+        if self.dtype is not None:
+            c = mt.dtype_code(self.dtype)
+            mt.mt_norm_forward_ex(self.opcode, c, c, t["X"], t.get("R"), t["gamma"],
+                                  t.get("beta"), self.S, self.Y, self.mean, self.rstd, w.N, w.D,
+                                  w.eps, stream)
+            return
         if w.op == W.RMSNORM:
             mt.mt_rmsnorm_forward(t["X"], t["gamma"], self.Y, self.rstd, w.N, w.D, w.eps, stream)
         elif w.op == W.LAYERNORM:
@@ -177,6 +192,13 @@ class OpRunner:
 
     def backward(self, stream):
         w, t, mt = self.w, self.t, self.mt
+        if self.dtype is not None:
+            c = mt.dtype_code(self.dtype)
+            x = self.S if w.op == W.ADD_RMSNORM else t["X"]
+            mt.mt_norm_backward_ex(self.opcode, c, c, c, x, t["gamma"], t["dY"], t.get("dS"),
+                                   self.mean, self.rstd, self.dX, self.dg, self.db, w.N, w.D,
+                                   self.ws, self.ws_bytes, stream)
+            return
         if w.op == W.RMSNORM:
             mt.mt_rmsnorm_backward_ws(t["X"], t["gamma"], t["dY"], self.rstd, self.dX, self.dg,
                                       w.N, w.D, self.ws, self.ws_bytes, stream)
@@ -442,6 +464,25 @@ def main(argv=None):
             del r2
             torch.cuda.empty_cache()
 
+    # Storage types other than fp16 on the headline workload (bf16, fp32), per op time.
+    dtypes = {}
+    if not args.no_others and rank == 0:
+        for dname, tdt in (("bf16", torch.bfloat16), ("f32", torch.float32)):
+            r2 = [OpRunner(args.workload, device, seed=i, dtype=tdt) for i in range(2)]
+            f2, b2, _ = time_ops(r2, max(50, args.steps // 10), args.warmup, stream)
+            r2 = r2[0]
+            fg = r2.fwd_bytes / (statistics.mean(f2) * 1e-3) / 1e9
+            bg = r2.bwd_bytes / (statistics.mean(b2) * 1e-3) / 1e9
+            dtypes[dname] = {
+                "forward_gbs": round(fg, 2), "backward_gbs": round(bg, 2),
+                "forward_frac_of_measured": round(fg / peak, 4),
+                "backward_frac_of_measured": round(bg / peak, 4),
+                "forward_us": round(1e3 * statistics.mean(f2), 3),
+                "backward_us": round(1e3 * statistics.mean(b2), 3),
+                "compulsory_bytes": {"forward": r2.fwd_bytes, "backward": r2.bwd_bytes}}
+            del r2
+            torch.cuda.empty_cache()
+
     e2e = None
     if not args.no_e2e:
         e2e = e2e_run(args.workload, device, max(5, min(50, args.steps // 40)), 3, seed=rank)
@@ -490,6 +531,7 @@ def main(argv=None):
         "clocks": clocks.summary(),
         "timed_region_wall_s": round(wall, 3),
         "other_workloads": others,
+        "storage_types": {"workload": args.workload, **dtypes},
     }
     if rank == 0:
         print(json.dumps(line))

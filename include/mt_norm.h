@@ -59,7 +59,7 @@ typedef enum mt_status {
     MT_ERR_CUDA = 3
 } mt_status_t;
 
-/* Operation selector for the workspace-size query. */
+/* Operation selector for the workspace-size query and the explicit-dtype entry points. */
 typedef enum mt_norm_op {
     MT_OP_RMSNORM = 0,
     MT_OP_LAYERNORM = 1,
@@ -162,6 +162,49 @@ mt_status_t mt_add_rmsnorm_backward_ws(const void *S, const void *gamma, const v
                                        void *workspace, size_t workspace_bytes,
                                        mt_stream_t stream);
 
+/* -------------------------------------------------------- explicit storage types ---
+ * [meTile] contract: storage is FP16 or FP32, with weight, bias and cotangents each in
+ * either type independently; statistics, accumulation and parameter gradients are FP32.
+ * This library adds bf16 as a third storage type. The entry points above are the fp16
+ * case of these two.
+ *
+ * x_dtype  X, R, S, Y (forward) and X or S, dX (backward): the activations. The
+ *          forward output and the residual sum use the source type, as [meTile]
+ *          states; dX also uses it, as the fp16 entry points do.
+ * w_dtype  gamma, beta.
+ * g_dtype  dY, dS: the cotangents.
+ * mean, rstd, dgamma, dbeta are fp32 in every combination. Any combination of the three
+ * types is accepted; fp16/bf16 activations with parameters and cotangents of the same
+ * type or fp32, and all-fp32, take the vectorised kernels (D % 8 == 0 and 16-byte-aligned
+ * bases), everything else the scalar kernels. Results are rounded to nearest even.
+ *
+ * op selects which pointers are used: MT_OP_RMSNORM uses X, gamma, Y, rstd (forward)
+ * and X, gamma, dY, rstd, dX, dgamma (backward); MT_OP_LAYERNORM adds beta and mean
+ * (forward) and mean and dbeta (backward); MT_OP_ADD_RMSNORM adds R and S (forward)
+ * and takes the saved S as X and the optional dS (backward). Pointers an op does not
+ * use are ignored. Errors as for the fp16 entry points, plus MT_ERR_INVALID_ARG for an
+ * unknown op or dtype code.
+ * Backward workspace: NULL allocates stream-ordered scratch as mt_rmsnorm_backward
+ * does; otherwise it is a caller buffer of workspace_bytes >=
+ * mt_norm_backward_workspace_size(op, N, D, device), which covers every dtype.       */
+typedef enum mt_dtype {
+    MT_DTYPE_F16 = 0,
+    MT_DTYPE_BF16 = 1,
+    MT_DTYPE_F32 = 2
+} mt_dtype_t;
+
+mt_status_t mt_norm_forward_ex(mt_norm_op_t op, mt_dtype_t x_dtype, mt_dtype_t w_dtype,
+                               const void *X, const void *R, const void *gamma,
+                               const void *beta, void *S, void *Y, float *mean, float *rstd,
+                               int64_t N, int64_t D, float eps, mt_stream_t stream);
+
+mt_status_t mt_norm_backward_ex(mt_norm_op_t op, mt_dtype_t x_dtype, mt_dtype_t w_dtype,
+                                mt_dtype_t g_dtype, const void *X, const void *gamma,
+                                const void *dY, const void *dS, const float *mean,
+                                const float *rstd, void *dX, float *dgamma, float *dbeta,
+                                int64_t N, int64_t D, void *workspace, size_t workspace_bytes,
+                                mt_stream_t stream);
+
 /* ----------------------------------------------- backward without allocation ---
  * No counterpart on the pages: this entry point exists for callers that cannot
  * allocate device memory. mt_rmsnorm_backward allocates its scratch and
@@ -187,8 +230,9 @@ mt_status_t mt_rmsnorm_backward_noalloc(const void *X, const void *gamma, const 
 
 /* ------------------------------------------------------------------ utilities --- */
 
-/* Scratch bytes a backward of `op` at [N, D] needs on CUDA device `device`: the
- * fixed-order dgamma (and dbeta) partials, one fp32 row of D per persistent CTA.
+/* Scratch bytes a backward of `op` at [N, D] needs on CUDA device `device`, whatever
+ * its storage types: the fixed-order dgamma (and dbeta) partials, one fp32 row of D per
+ * persistent CTA.
  * Writes the size to *bytes. Errors: MT_ERR_INVALID_ARG / MT_ERR_UNSUPPORTED as the
  * backward would return them, MT_ERR_INVALID_ARG for a NULL `bytes` or an unknown
  * op, MT_ERR_CUDA if the device cannot be queried.                                */

@@ -175,6 +175,45 @@ def add_rmsnorm_backward(S, gamma, dY, dS, rstd, lib=None):
     return dX, dg, dga
 
 
+BF16_MAX = (2.0 - 2.0 ** -7) * 2.0 ** 127  # largest finite bfloat16
+
+
 def round_fp16(a) -> np.ndarray:
     """Round fp64 values to IEEE binary16, round-to-nearest-even (numpy's conversion)."""
     return np.asarray(a, dtype=np.float64).astype(np.float16)
+
+
+def round_bf16(a) -> np.ndarray:
+    """Round fp64 values to bfloat16 (7 fraction bits, the fp32 exponent range), round to
+    nearest even, returned as fp64.
+
+    Direct rounding from fp64 (not through fp32, which would round twice): with
+    e = max(floor(log2|x|), -126) the bf16 grid step near x is 2^(e-7); |x| / step is
+    exact (a power-of-two scaling), numpy's rint rounds it to the nearest integer with
+    ties to even, and the product with the step is exact. Past the largest finite bf16
+    the result is infinity; NaN stays NaN.
+    """
+    x = np.asarray(a, dtype=np.float64)
+    ax = np.abs(x)
+    with np.errstate(invalid="ignore"):
+        _, E = np.frexp(ax)
+        step = np.ldexp(1.0, np.maximum(E - 1, -126) - 7)
+        r = np.rint(ax / step) * step
+    r = np.where(r > BF16_MAX, np.inf, r)
+    return np.copysign(r, x)
+
+
+def round_f32(a) -> np.ndarray:
+    """Round fp64 values to IEEE binary32, round-to-nearest-even, returned as fp64."""
+    return np.asarray(a, dtype=np.float64).astype(np.float32).astype(np.float64)
+
+
+def round_storage(a, dtype: str) -> np.ndarray:
+    """Round to a storage type named "f16", "bf16" or "f32" (returned as fp64)."""
+    if dtype == "f16":
+        return round_fp16(a).astype(np.float64)
+    if dtype == "bf16":
+        return round_bf16(a)
+    if dtype == "f32":
+        return round_f32(a)
+    raise ValueError(dtype)

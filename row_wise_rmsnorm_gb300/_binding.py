@@ -24,6 +24,7 @@ LIB_PATH = _build.LIB
 
 MT_OK, MT_ERR_INVALID_ARG, MT_ERR_UNSUPPORTED, MT_ERR_CUDA = 0, 1, 2, 3
 MT_OP_RMSNORM, MT_OP_LAYERNORM, MT_OP_ADD_RMSNORM = 0, 1, 2
+MT_DTYPE_F16, MT_DTYPE_BF16, MT_DTYPE_F32 = 0, 1, 2
 MT_MAX_COLS = 16384
 
 # Every exported symbol of include/mt_norm.h.
@@ -31,6 +32,7 @@ EXPORTED = (
     "mt_rmsnorm_forward", "mt_rmsnorm_backward", "mt_rmsnorm_backward_ws",
     "mt_layernorm_forward", "mt_layernorm_backward", "mt_layernorm_backward_ws",
     "mt_add_rmsnorm_forward", "mt_add_rmsnorm_backward", "mt_add_rmsnorm_backward_ws",
+    "mt_norm_forward_ex", "mt_norm_backward_ex",
     "mt_rmsnorm_backward_noalloc",
     "mt_norm_backward_workspace_size", "mt_last_cuda_error", "mt_status_string",
     "mt_norm_version",
@@ -63,6 +65,10 @@ _SIGS = {
     "mt_add_rmsnorm_forward": [_P, _P, _P, _P, _P, _P, _I64, _I64, _F, _P],
     "mt_add_rmsnorm_backward": [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P],
     "mt_add_rmsnorm_backward_ws": [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P, _SZ, _P],
+    "mt_norm_forward_ex": [ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P, _P, _P, _P, _P, _P,
+                           _P, _I64, _I64, _F, _P],
+    "mt_norm_backward_ex": [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P, _P,
+                            _P, _P, _P, _P, _P, _P, _I64, _I64, _P, _SZ, _P],
     "mt_rmsnorm_backward_noalloc": [_P, _P, _P, _P, _P, _P, _I64, _I64, _P],
     "mt_norm_backward_workspace_size": [ctypes.c_int, _I64, _I64, ctypes.c_int,
                                         ctypes.POINTER(_SZ)],
@@ -176,6 +182,21 @@ def mt_add_rmsnorm_backward_ws(S, gamma, dY, dS, rstd, dX, dgamma, N, D, workspa
            "mt_add_rmsnorm_backward_ws")
 
 
+def mt_norm_forward_ex(op, x_dtype, w_dtype, X, R, gamma, beta, S, Y, mean, rstd, N, D, eps,
+                       stream=None):
+    _check(load().mt_norm_forward_ex(op, x_dtype, w_dtype, _ptr(X), _ptr(R), _ptr(gamma),
+                                     _ptr(beta), _ptr(S), _ptr(Y), _ptr(mean), _ptr(rstd), N, D,
+                                     eps, _stream(stream)), "mt_norm_forward_ex")
+
+
+def mt_norm_backward_ex(op, x_dtype, w_dtype, g_dtype, X, gamma, dY, dS, mean, rstd, dX, dgamma,
+                        dbeta, N, D, workspace=None, workspace_bytes=0, stream=None):
+    _check(load().mt_norm_backward_ex(op, x_dtype, w_dtype, g_dtype, _ptr(X), _ptr(gamma),
+                                      _ptr(dY), _ptr(dS), _ptr(mean), _ptr(rstd), _ptr(dX),
+                                      _ptr(dgamma), _ptr(dbeta), N, D, _ptr(workspace),
+                                      workspace_bytes, _stream(stream)), "mt_norm_backward_ex")
+
+
 def mt_rmsnorm_backward_noalloc(X, gamma, dY, rstd, dX, dgamma, N, D, stream=None):
     """RMSNorm backward with the library's fixed scratch array (no allocation).
 
@@ -285,3 +306,53 @@ def add_rmsnorm_backward(s, gamma, dy, ds, rstd):
     ws, nbytes = _workspace(MT_OP_ADD_RMSNORM, s)
     mt_add_rmsnorm_backward_ws(s, gamma, dy, ds, rstd, dx, dgamma, n, d, ws, nbytes)
     return dx, dgamma
+
+
+# ------------------------------------------------ wrappers for any storage type ---
+
+def dtype_code(torch_dtype) -> int:
+    """mt_dtype_t of a torch dtype (float16, bfloat16 or float32)."""
+    import torch
+    codes = {torch.float16: MT_DTYPE_F16, torch.bfloat16: MT_DTYPE_BF16,
+             torch.float32: MT_DTYPE_F32}
+    if torch_dtype not in codes:
+        raise TypeError(f"unsupported storage type {torch_dtype}")
+    return codes[torch_dtype]
+
+
+def norm_forward(op, x, gamma, beta=None, residual=None, eps=1e-5):
+    """Forward of `op` for any storage types; the output (and residual sum) take x's type.
+
+    Returns (y, rstd) for RMSNorm, (y, mean, rstd) for LayerNorm and (y, s, rstd) for the
+    fused residual-add + RMSNorm.
+    """
+    import torch
+    n, d = x.shape
+    y = _new(x, (n, d), x.dtype)
+    rstd = _new(x, (n,), torch.float32)
+    mean = _new(x, (n,), torch.float32) if op == MT_OP_LAYERNORM else None
+    s = _new(x, (n, d), x.dtype) if op == MT_OP_ADD_RMSNORM else None
+    mt_norm_forward_ex(op, dtype_code(x.dtype), dtype_code(gamma.dtype), x, residual, gamma,
+                       beta, s, y, mean, rstd, n, d, eps)
+    if op == MT_OP_LAYERNORM:
+        return y, mean, rstd
+    if op == MT_OP_ADD_RMSNORM:
+        return y, s, rstd
+    return y, rstd
+
+
+def norm_backward(op, x, gamma, dy, rstd, mean=None, ds=None):
+    """Backward of `op` for any storage types (x is the saved S for the fused op).
+
+    dx takes x's type; dgamma (and dbeta) are fp32. Returns (dx, dgamma) or, for
+    LayerNorm, (dx, dgamma, dbeta).
+    """
+    import torch
+    n, d = x.shape
+    dx = _new(x, (n, d), x.dtype)
+    dgamma = _new(x, (d,), torch.float32)
+    dbeta = _new(x, (d,), torch.float32) if op == MT_OP_LAYERNORM else None
+    ws, nbytes = _workspace(op, x)
+    mt_norm_backward_ex(op, dtype_code(x.dtype), dtype_code(gamma.dtype), dtype_code(dy.dtype),
+                        x, gamma, dy, ds, mean, rstd, dx, dgamma, dbeta, n, d, ws, nbytes)
+    return (dx, dgamma, dbeta) if op == MT_OP_LAYERNORM else (dx, dgamma)

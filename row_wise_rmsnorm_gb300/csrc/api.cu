@@ -91,29 +91,52 @@ mt_status_t launch(const LaunchPlan &p, void *arg, cudaStream_t stream) {
     return MT_OK;
 }
 
+// The vector plan for (op, activation type), or kNoVectorPlan.
+cudaError_t plan_forward_vec(int op, int xdt, int64_t N, int D, int wdt, LaunchPlan *p) {
+#define MT_CASE(OP, XT) \
+    if (op == OP && xdt == XT) return fwd_plan_for<OP, XT>(N, D, wdt, p);
+    MT_ALL_PLANS(MT_CASE)
+#undef MT_CASE
+    return kNoVectorPlan;
+}
+
+cudaError_t plan_backward_vec(int op, int xdt, int64_t N, int D, int wdt, int gdt, bool has_ds,
+                              int device, LaunchPlan *p) {
+#define MT_CASE(OP, XT) \
+    if (op == OP && xdt == XT) return bwd_plan_for<OP, XT>(N, D, wdt, gdt, has_ds, device, p);
+    MT_ALL_PLANS(MT_CASE)
+#undef MT_CASE
+    return kNoVectorPlan;
+}
+
+// The vector kernel when the row layout allows it and the dtype combination has one,
+// else the scalar kernel.
+cudaError_t plan_forward(int op, int64_t N, int D, bool vec8, int xdt, int wdt, LaunchPlan *p) {
+    if (vec8) {
+        const cudaError_t e = plan_forward_vec(op, xdt, N, D, wdt, p);
+        if (e != kNoVectorPlan) return e;
+    }
+    return fwd_plan_scalar_op(op, N, D, p);
+}
+
+cudaError_t plan_backward(int op, int64_t N, int D, bool vec8, int xdt, int wdt, int gdt,
+                          bool has_ds, int device, LaunchPlan *p) {
+    if (vec8) {
+        const cudaError_t e = plan_backward_vec(op, xdt, N, D, wdt, gdt, has_ds, device, p);
+        if (e != kNoVectorPlan) return e;
+    }
+    return bwd_plan_scalar_op(op, N, D, has_ds, device, p);
+}
+
 mt_status_t run_forward(int op, const FwdArgs &a, bool vec8, mt_stream_t stream) {
-    int device = 0;
-    cudaError_t e = cudaGetDevice(&device);
-    if (e != cudaSuccess) return cuda_fail(e);
     LaunchPlan p;
-    e = (op == kRms)     ? fwd_plan_rms(a.N, a.D, vec8, device, &p)
-        : (op == kLayer) ? fwd_plan_layer(a.N, a.D, vec8, device, &p)
-                         : fwd_plan_add(a.N, a.D, vec8, device, &p);
+    const cudaError_t e = plan_forward(op, a.N, a.D, vec8, a.xdt, a.wdt, &p);
     if (e != cudaSuccess) return cuda_fail(e);
     FwdArgs copy = a;
     return launch(p, &copy, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int num_partial_arrays(int op) { return op == kLayer ? 2 : 1; }
-
-cudaError_t plan_backward(int op, int64_t N, int D, bool vec8, bool has_ds, int device,
-                          LaunchPlan *p) {
-    switch (op) {
-        case kRms: return bwd_plan_rms(N, D, vec8, device, p);
-        case kLayer: return bwd_plan_layer(N, D, vec8, device, p);
-        default: return bwd_plan_add(N, D, vec8, has_ds, device, p);
-    }
-}
 
 // One fp32 row of D per persistent CTA, per parameter gradient.
 size_t partial_bytes(int op, int rows, int D) {
@@ -129,7 +152,7 @@ mt_status_t run_backward(int op, BwdArgs a, bool vec8, float *dgamma, float *dbe
     cudaError_t e = cudaGetDevice(&device);
     if (e != cudaSuccess) return cuda_fail(e);
     LaunchPlan p;
-    e = plan_backward(op, a.N, a.D, vec8, a.dS != nullptr, device, &p);
+    e = plan_backward(op, a.N, a.D, vec8, a.xdt, a.wdt, a.gdt, a.dS != nullptr, device, &p);
     if (e != cudaSuccess) return cuda_fail(e);
     const int prow = p.grid;  // partial rows: one per CTA
     const size_t need = partial_bytes(op, prow, a.D);
@@ -231,65 +254,113 @@ cudaError_t cached_occupancy(const void *kernel, int threads, size_t smem, int d
 
 using namespace mt;
 
+// ====================================================== generic forward/backward ===
+
+namespace {
+
+bool valid_dtype(int dt) { return dt == kF16 || dt == kBF16 || dt == kF32; }
+size_t dtype_bytes(int dt) { return dt == kF32 ? 4 : 2; }
+
+// Forward of `op` with activations of type xdt and gamma/beta of type wdt. Pointers the
+// op does not use are ignored.
+mt_status_t forward_impl(int op, int xdt, int wdt, const void *X, const void *R,
+                         const void *gamma, const void *beta, void *S, void *Y, float *mean,
+                         float *rstd, int64_t N, int64_t D, float eps, mt_stream_t stream) {
+    const bool ln = op == kLayer, add = op == kAddRms;
+    if (!ln) { beta = nullptr; mean = nullptr; }
+    if (!add) { R = nullptr; S = nullptr; }
+    if (!X || !gamma || !Y || !rstd || (ln && (!beta || !mean)) || (add && (!R || !S)))
+        return MT_ERR_INVALID_ARG;
+    if (!valid_dtype(xdt) || !valid_dtype(wdt)) return MT_ERR_INVALID_ARG;
+    mt_status_t s = check_shape(N, D);
+    if (s != MT_OK) return s;
+    if ((s = check_eps(eps)) != MT_OK) return s;
+    const size_t act = (size_t)N * (size_t)D * dtype_bytes(xdt);
+    const size_t par = (size_t)D * dtype_bytes(wdt), st = (size_t)N * 4;
+    if (any_overlap({{S, act}, {Y, act}, {mean, st}, {rstd, st}},
+                    {{X, act}, {R, act}, {gamma, par}, {beta, par}}))
+        return MT_ERR_INVALID_ARG;
+    FwdArgs a{};
+    a.X = X;
+    a.R = R;
+    a.gamma = gamma;
+    a.beta = beta;
+    a.S = S;
+    a.Y = Y;
+    a.mean = mean;
+    a.rstd = rstd;
+    a.N = N;
+    a.D = (int)D;
+    a.eps = eps;
+    a.xdt = xdt;
+    a.wdt = wdt;
+    const bool vec8 = (D % 8 == 0) && aligned16({X, R, gamma, beta, S, Y});
+    return run_forward(op, a, vec8, stream);
+}
+
+// Backward of `op`: X (or the saved S) and dX of type xdt, gamma of type wdt, dY/dS of
+// type gdt. dS may be NULL (fused op only; ignored otherwise). workspace NULL with
+// own_ws: stream-ordered scratch is allocated here.
+mt_status_t backward_impl(int op, int xdt, int wdt, int gdt, const void *X, const void *gamma,
+                          const void *dY, const void *dS, const float *mean, const float *rstd,
+                          void *dX, float *dgamma, float *dbeta, int64_t N, int64_t D,
+                          void *ws, size_t ws_bytes, bool own_ws, mt_stream_t stream) {
+    const bool ln = op == kLayer, add = op == kAddRms;
+    if (!ln) { mean = nullptr; dbeta = nullptr; }
+    if (!add) dS = nullptr;
+    if (!X || !gamma || !dY || !rstd || !dX || !dgamma || (ln && (!mean || !dbeta)))
+        return MT_ERR_INVALID_ARG;
+    if (!valid_dtype(xdt) || !valid_dtype(wdt) || !valid_dtype(gdt)) return MT_ERR_INVALID_ARG;
+    mt_status_t s = check_shape(N, D);
+    if (s != MT_OK) return s;
+    const size_t act = (size_t)N * (size_t)D * dtype_bytes(xdt);
+    const size_t cot = (size_t)N * (size_t)D * dtype_bytes(gdt);
+    const size_t par = (size_t)D * dtype_bytes(wdt), st = (size_t)N * 4, grad = (size_t)D * 4;
+    if (!own_ws && (ws == nullptr || ((uintptr_t)ws & 15u) != 0)) return MT_ERR_INVALID_ARG;
+    if (any_overlap({{dX, act}, {dgamma, grad}, {dbeta, grad}, {own_ws ? nullptr : ws, ws_bytes}},
+                    {{X, act}, {gamma, par}, {dY, cot}, {dS, cot}, {mean, st}, {rstd, st}}))
+        return MT_ERR_INVALID_ARG;
+    BwdArgs a{};
+    a.X = X;
+    a.gamma = gamma;
+    a.dY = dY;
+    a.dS = dS;
+    a.mean = mean;
+    a.rstd = rstd;
+    a.dX = dX;
+    a.N = N;
+    a.D = (int)D;
+    a.xdt = xdt;
+    a.wdt = wdt;
+    a.gdt = gdt;
+    const bool vec8 = (D % 8 == 0) && aligned16({X, gamma, dY, dS, dX});
+    return run_backward(op, a, vec8, dgamma, dbeta, ws, ws_bytes, own_ws, stream);
+}
+
+}  // namespace
+
 // ================================================================= RMSNorm ===
 
 extern "C" mt_status_t mt_rmsnorm_forward(const void *X, const void *gamma, void *Y,
                                           float *rstd, int64_t N, int64_t D, float eps,
                                           mt_stream_t stream) {
-    if (!X || !gamma || !Y || !rstd) return MT_ERR_INVALID_ARG;
-    mt_status_t s = check_shape(N, D);
-    if (s != MT_OK) return s;
-    if ((s = check_eps(eps)) != MT_OK) return s;
-    const size_t act = (size_t)N * (size_t)D * 2, par = (size_t)D * 2, st = (size_t)N * 4;
-    if (any_overlap({{Y, act}, {rstd, st}}, {{X, act}, {gamma, par}})) return MT_ERR_INVALID_ARG;
-    FwdArgs a{};
-    a.X = static_cast<const __half *>(X);
-    a.gamma = static_cast<const __half *>(gamma);
-    a.Y = static_cast<__half *>(Y);
-    a.rstd = rstd;
-    a.N = N;
-    a.D = (int)D;
-    a.eps = eps;
-    const bool vec8 = (D % 8 == 0) && aligned16({X, gamma, Y});
-    return run_forward(kRms, a, vec8, stream);
-}
-
-static mt_status_t rms_backward_impl(const void *X, const void *gamma, const void *dY,
-                                     const float *rstd, void *dX, float *dgamma, int64_t N,
-                                     int64_t D, void *ws, size_t ws_bytes, bool own_ws,
-                                     mt_stream_t stream) {
-    if (!X || !gamma || !dY || !rstd || !dX || !dgamma) return MT_ERR_INVALID_ARG;
-    mt_status_t s = check_shape(N, D);
-    if (s != MT_OK) return s;
-    const size_t act = (size_t)N * (size_t)D * 2, par = (size_t)D * 2, st = (size_t)N * 4;
-    if (!own_ws && (ws == nullptr || ((uintptr_t)ws & 15u) != 0)) return MT_ERR_INVALID_ARG;
-    if (any_overlap({{dX, act}, {dgamma, (size_t)D * 4}, {own_ws ? nullptr : ws, ws_bytes}},
-                    {{X, act}, {gamma, par}, {dY, act}, {rstd, st}}))
-        return MT_ERR_INVALID_ARG;
-    BwdArgs a{};
-    a.X = static_cast<const __half *>(X);
-    a.gamma = static_cast<const __half *>(gamma);
-    a.dY = static_cast<const __half *>(dY);
-    a.rstd = rstd;
-    a.dX = static_cast<__half *>(dX);
-    a.N = N;
-    a.D = (int)D;
-    const bool vec8 = (D % 8 == 0) && aligned16({X, gamma, dY, dX});
-    return run_backward(kRms, a, vec8, dgamma, nullptr, ws, ws_bytes, own_ws, stream);
+    return forward_impl(kRms, kF16, kF16, X, nullptr, gamma, nullptr, nullptr, Y, nullptr, rstd,
+                        N, D, eps, stream);
 }
 
 extern "C" mt_status_t mt_rmsnorm_backward(const void *X, const void *gamma, const void *dY,
                                            const float *rstd, void *dX, float *dgamma,
                                            int64_t N, int64_t D, mt_stream_t stream) {
-    return rms_backward_impl(X, gamma, dY, rstd, dX, dgamma, N, D, nullptr, 0, true, stream);
+    return backward_impl(kRms, kF16, kF16, kF16, X, gamma, dY, nullptr, nullptr, rstd, dX, dgamma,
+                         nullptr, N, D, nullptr, 0, true, stream);
 }
 
 extern "C" mt_status_t mt_rmsnorm_backward_ws(const void *X, const void *gamma, const void *dY,
                                               const float *rstd, void *dX, float *dgamma,
                                               int64_t N, int64_t D, void *workspace,
                                               size_t workspace_bytes, mt_stream_t stream) {
-    return rms_backward_impl(X, gamma, dY, rstd, dX, dgamma, N, D, workspace, workspace_bytes,
-                             false, stream);
+    return backward_impl(kRms, kF16, kF16, kF16, X, gamma, dY, nullptr, nullptr, rstd, dX, dgamma,
+                         nullptr, N, D, workspace, workspace_bytes, false, stream);
 }
 
 // =============================================================== LayerNorm ===
@@ -297,60 +368,16 @@ extern "C" mt_status_t mt_rmsnorm_backward_ws(const void *X, const void *gamma, 
 extern "C" mt_status_t mt_layernorm_forward(const void *X, const void *gamma, const void *beta,
                                             void *Y, float *mean, float *rstd, int64_t N,
                                             int64_t D, float eps, mt_stream_t stream) {
-    if (!X || !gamma || !beta || !Y || !mean || !rstd) return MT_ERR_INVALID_ARG;
-    mt_status_t s = check_shape(N, D);
-    if (s != MT_OK) return s;
-    if ((s = check_eps(eps)) != MT_OK) return s;
-    const size_t act = (size_t)N * (size_t)D * 2, par = (size_t)D * 2, st = (size_t)N * 4;
-    if (any_overlap({{Y, act}, {mean, st}, {rstd, st}}, {{X, act}, {gamma, par}, {beta, par}}))
-        return MT_ERR_INVALID_ARG;
-    FwdArgs a{};
-    a.X = static_cast<const __half *>(X);
-    a.gamma = static_cast<const __half *>(gamma);
-    a.beta = static_cast<const __half *>(beta);
-    a.Y = static_cast<__half *>(Y);
-    a.mean = mean;
-    a.rstd = rstd;
-    a.N = N;
-    a.D = (int)D;
-    a.eps = eps;
-    const bool vec8 = (D % 8 == 0) && aligned16({X, gamma, beta, Y});
-    return run_forward(kLayer, a, vec8, stream);
-}
-
-static mt_status_t ln_backward_impl(const void *X, const void *gamma, const void *dY,
-                                    const float *mean, const float *rstd, void *dX,
-                                    float *dgamma, float *dbeta, int64_t N, int64_t D, void *ws,
-                                    size_t ws_bytes, bool own_ws, mt_stream_t stream) {
-    if (!X || !gamma || !dY || !mean || !rstd || !dX || !dgamma || !dbeta)
-        return MT_ERR_INVALID_ARG;
-    mt_status_t s = check_shape(N, D);
-    if (s != MT_OK) return s;
-    const size_t act = (size_t)N * (size_t)D * 2, par = (size_t)D * 2, st = (size_t)N * 4;
-    if (!own_ws && (ws == nullptr || ((uintptr_t)ws & 15u) != 0)) return MT_ERR_INVALID_ARG;
-    if (any_overlap({{dX, act}, {dgamma, (size_t)D * 4}, {dbeta, (size_t)D * 4},
-                     {own_ws ? nullptr : ws, ws_bytes}},
-                    {{X, act}, {gamma, par}, {dY, act}, {mean, st}, {rstd, st}}))
-        return MT_ERR_INVALID_ARG;
-    BwdArgs a{};
-    a.X = static_cast<const __half *>(X);
-    a.gamma = static_cast<const __half *>(gamma);
-    a.dY = static_cast<const __half *>(dY);
-    a.mean = mean;
-    a.rstd = rstd;
-    a.dX = static_cast<__half *>(dX);
-    a.N = N;
-    a.D = (int)D;
-    const bool vec8 = (D % 8 == 0) && aligned16({X, gamma, dY, dX});
-    return run_backward(kLayer, a, vec8, dgamma, dbeta, ws, ws_bytes, own_ws, stream);
+    return forward_impl(kLayer, kF16, kF16, X, nullptr, gamma, beta, nullptr, Y, mean, rstd, N,
+                        D, eps, stream);
 }
 
 extern "C" mt_status_t mt_layernorm_backward(const void *X, const void *gamma, const void *dY,
                                              const float *mean, const float *rstd, void *dX,
                                              float *dgamma, float *dbeta, int64_t N, int64_t D,
                                              mt_stream_t stream) {
-    return ln_backward_impl(X, gamma, dY, mean, rstd, dX, dgamma, dbeta, N, D, nullptr, 0, true,
-                            stream);
+    return backward_impl(kLayer, kF16, kF16, kF16, X, gamma, dY, nullptr, mean, rstd, dX, dgamma,
+                         dbeta, N, D, nullptr, 0, true, stream);
 }
 
 extern "C" mt_status_t mt_layernorm_backward_ws(const void *X, const void *gamma, const void *dY,
@@ -358,8 +385,8 @@ extern "C" mt_status_t mt_layernorm_backward_ws(const void *X, const void *gamma
                                                 float *dgamma, float *dbeta, int64_t N,
                                                 int64_t D, void *workspace,
                                                 size_t workspace_bytes, mt_stream_t stream) {
-    return ln_backward_impl(X, gamma, dY, mean, rstd, dX, dgamma, dbeta, N, D, workspace,
-                            workspace_bytes, false, stream);
+    return backward_impl(kLayer, kF16, kF16, kF16, X, gamma, dY, nullptr, mean, rstd, dX, dgamma,
+                         dbeta, N, D, workspace, workspace_bytes, false, stream);
 }
 
 // ============================================== fused residual add + RMSNorm ===
@@ -367,57 +394,16 @@ extern "C" mt_status_t mt_layernorm_backward_ws(const void *X, const void *gamma
 extern "C" mt_status_t mt_add_rmsnorm_forward(const void *X, const void *R, const void *gamma,
                                               void *S, void *Y, float *rstd, int64_t N,
                                               int64_t D, float eps, mt_stream_t stream) {
-    if (!X || !R || !gamma || !S || !Y || !rstd) return MT_ERR_INVALID_ARG;
-    mt_status_t s = check_shape(N, D);
-    if (s != MT_OK) return s;
-    if ((s = check_eps(eps)) != MT_OK) return s;
-    const size_t act = (size_t)N * (size_t)D * 2, par = (size_t)D * 2, st = (size_t)N * 4;
-    if (any_overlap({{S, act}, {Y, act}, {rstd, st}}, {{X, act}, {R, act}, {gamma, par}}))
-        return MT_ERR_INVALID_ARG;
-    FwdArgs a{};
-    a.X = static_cast<const __half *>(X);
-    a.R = static_cast<const __half *>(R);
-    a.gamma = static_cast<const __half *>(gamma);
-    a.S = static_cast<__half *>(S);
-    a.Y = static_cast<__half *>(Y);
-    a.rstd = rstd;
-    a.N = N;
-    a.D = (int)D;
-    a.eps = eps;
-    const bool vec8 = (D % 8 == 0) && aligned16({X, R, gamma, S, Y});
-    return run_forward(kAddRms, a, vec8, stream);
-}
-
-static mt_status_t add_backward_impl(const void *S, const void *gamma, const void *dY,
-                                     const void *dS, const float *rstd, void *dX, float *dgamma,
-                                     int64_t N, int64_t D, void *ws, size_t ws_bytes,
-                                     bool own_ws, mt_stream_t stream) {
-    if (!S || !gamma || !dY || !rstd || !dX || !dgamma) return MT_ERR_INVALID_ARG;
-    mt_status_t s = check_shape(N, D);
-    if (s != MT_OK) return s;
-    const size_t act = (size_t)N * (size_t)D * 2, par = (size_t)D * 2, st = (size_t)N * 4;
-    if (!own_ws && (ws == nullptr || ((uintptr_t)ws & 15u) != 0)) return MT_ERR_INVALID_ARG;
-    if (any_overlap({{dX, act}, {dgamma, (size_t)D * 4}, {own_ws ? nullptr : ws, ws_bytes}},
-                    {{S, act}, {gamma, par}, {dY, act}, {dS, dS ? act : 0}, {rstd, st}}))
-        return MT_ERR_INVALID_ARG;
-    BwdArgs a{};
-    a.X = static_cast<const __half *>(S);
-    a.gamma = static_cast<const __half *>(gamma);
-    a.dY = static_cast<const __half *>(dY);
-    a.dS = static_cast<const __half *>(dS);
-    a.rstd = rstd;
-    a.dX = static_cast<__half *>(dX);
-    a.N = N;
-    a.D = (int)D;
-    const bool vec8 = (D % 8 == 0) && aligned16({S, gamma, dY, dS, dX});
-    return run_backward(kAddRms, a, vec8, dgamma, nullptr, ws, ws_bytes, own_ws, stream);
+    return forward_impl(kAddRms, kF16, kF16, X, R, gamma, nullptr, S, Y, nullptr, rstd, N, D, eps,
+                        stream);
 }
 
 extern "C" mt_status_t mt_add_rmsnorm_backward(const void *S, const void *gamma, const void *dY,
                                                const void *dS, const float *rstd, void *dX,
                                                float *dgamma, int64_t N, int64_t D,
                                                mt_stream_t stream) {
-    return add_backward_impl(S, gamma, dY, dS, rstd, dX, dgamma, N, D, nullptr, 0, true, stream);
+    return backward_impl(kAddRms, kF16, kF16, kF16, S, gamma, dY, dS, nullptr, rstd, dX, dgamma,
+                         nullptr, N, D, nullptr, 0, true, stream);
 }
 
 extern "C" mt_status_t mt_add_rmsnorm_backward_ws(const void *S, const void *gamma,
@@ -425,8 +411,40 @@ extern "C" mt_status_t mt_add_rmsnorm_backward_ws(const void *S, const void *gam
                                                   const float *rstd, void *dX, float *dgamma,
                                                   int64_t N, int64_t D, void *workspace,
                                                   size_t workspace_bytes, mt_stream_t stream) {
-    return add_backward_impl(S, gamma, dY, dS, rstd, dX, dgamma, N, D, workspace,
-                             workspace_bytes, false, stream);
+    return backward_impl(kAddRms, kF16, kF16, kF16, S, gamma, dY, dS, nullptr, rstd, dX, dgamma,
+                         nullptr, N, D, workspace, workspace_bytes, false, stream);
+}
+
+// ========================================================= explicit dtypes ===
+
+static int op_code(mt_norm_op_t op) {
+    return (op == MT_OP_RMSNORM) ? kRms : (op == MT_OP_LAYERNORM) ? kLayer
+                                        : (op == MT_OP_ADD_RMSNORM) ? kAddRms : -1;
+}
+
+extern "C" mt_status_t mt_norm_forward_ex(mt_norm_op_t op, mt_dtype_t x_dtype, mt_dtype_t w_dtype,
+                                          const void *X, const void *R, const void *gamma,
+                                          const void *beta, void *S, void *Y, float *mean,
+                                          float *rstd, int64_t N, int64_t D, float eps,
+                                          mt_stream_t stream) {
+    const int kop = op_code(op);
+    if (kop < 0) return MT_ERR_INVALID_ARG;
+    return forward_impl(kop, (int)x_dtype, (int)w_dtype, X, R, gamma, beta, S, Y, mean, rstd, N,
+                        D, eps, stream);
+}
+
+extern "C" mt_status_t mt_norm_backward_ex(mt_norm_op_t op, mt_dtype_t x_dtype,
+                                           mt_dtype_t w_dtype, mt_dtype_t g_dtype, const void *X,
+                                           const void *gamma, const void *dY, const void *dS,
+                                           const float *mean, const float *rstd, void *dX,
+                                           float *dgamma, float *dbeta, int64_t N, int64_t D,
+                                           void *workspace, size_t workspace_bytes,
+                                           mt_stream_t stream) {
+    const int kop = op_code(op);
+    if (kop < 0) return MT_ERR_INVALID_ARG;
+    return backward_impl(kop, (int)x_dtype, (int)w_dtype, (int)g_dtype, X, gamma, dY, dS, mean,
+                         rstd, dX, dgamma, dbeta, N, D, workspace, workspace_bytes,
+                         workspace == nullptr, stream);
 }
 
 // =============================================================== utilities ===
@@ -440,17 +458,24 @@ extern "C" mt_status_t mt_norm_backward_workspace_size(mt_norm_op_t op, int64_t 
     if (s != MT_OK) return s;
     if (device < 0) return MT_ERR_INVALID_ARG;
     const int kop = (op == MT_OP_RMSNORM) ? kRms : (op == MT_OP_LAYERNORM) ? kLayer : kAddRms;
-    // The largest of the variants a call may take (vectorised or not, with or
-    // without dS), so one size fits every call with this op and shape.
+    // The largest of the variants a call may take (vectorised or not, with or without
+    // dS, any storage types), so one size fits every call with this op and shape.
     size_t best = 0;
     for (int v = 0; v < 2; ++v) {
+        if (v == 1 && D % 8 != 0) continue;
         for (int ds = 0; ds < (kop == kAddRms ? 2 : 1); ++ds) {
-            if (v == 1 && D % 8 != 0) continue;
-            LaunchPlan p;
-            cudaError_t e = plan_backward(kop, N, (int)D, v == 1, ds == 1, device, &p);
-            if (e != cudaSuccess) return cuda_fail(e);
-            const size_t b = partial_bytes(kop, p.grid, (int)D);
-            if (b > best) best = b;
+            for (int xdt = 0; xdt < 3; ++xdt) {
+                for (int wdt = 0; wdt < 3; ++wdt) {
+                    for (int gdt = 0; gdt < 3; ++gdt) {
+                        LaunchPlan p;
+                        cudaError_t e = plan_backward(kop, N, (int)D, v == 1, xdt, wdt, gdt,
+                                                      ds == 1, device, &p);
+                        if (e != cudaSuccess) return cuda_fail(e);
+                        const size_t b = partial_bytes(kop, p.grid, (int)D);
+                        if (b > best) best = b;
+                    }
+                }
+            }
         }
     }
     *bytes = best;
@@ -469,4 +494,4 @@ extern "C" const char *mt_status_string(mt_status_t status) {
     return "unknown mt_status_t";
 }
 
-extern "C" int mt_norm_version(void) { return 100; }
+extern "C" int mt_norm_version(void) { return 200; }

@@ -25,40 +25,46 @@
 // "RMSnorm -- Llama-style" and "LayerNorm -- standard".
 #pragma once
 
-#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include "dtype.cuh"
 
 namespace mt {
 
 enum NormOp : int { kRms = 0, kLayer = 1, kAddRms = 2 };
 
+// Activations X, R, S, Y are stored as xdt, gamma/beta as wdt (DType codes). The vector
+// kernels take the types as template parameters; the scalar fallback reads these fields.
 struct FwdArgs {
-    const __half *X;      // [N, D]
-    const __half *R;      // [N, D] residual (fused op only)
-    const __half *gamma;  // [D]
-    const __half *beta;   // [D] (LayerNorm only)
-    __half *S;            // [N, D] residual sum out (fused op only)
-    __half *Y;            // [N, D]
+    const void *X;        // [N, D]
+    const void *R;        // [N, D] residual (fused op only)
+    const void *gamma;    // [D]
+    const void *beta;     // [D] (LayerNorm only)
+    void *S;              // [N, D] residual sum out (fused op only)
+    void *Y;              // [N, D]
     float *mean;          // [N] (LayerNorm only)
     float *rstd;          // [N]
     int64_t N;
     int D;
     float eps;
+    int xdt, wdt;
 };
 
+// X (or the saved S) and dX are stored as xdt, gamma as wdt, dY/dS as gdt.
 struct BwdArgs {
-    const __half *X;      // [N, D]: X (RMSNorm, LayerNorm) or the saved S (fused op)
-    const __half *gamma;  // [D]
-    const __half *dY;     // [N, D]
-    const __half *dS;     // [N, D] or nullptr (fused op only)
+    const void *X;        // [N, D]: X (RMSNorm, LayerNorm) or the saved S (fused op)
+    const void *gamma;    // [D]
+    const void *dY;       // [N, D]
+    const void *dS;       // [N, D] or nullptr (fused op only)
     const float *mean;    // [N] (LayerNorm only)
     const float *rstd;    // [N]
-    __half *dX;           // [N, D]
+    void *dX;             // [N, D]
     float *part_g;        // [P, D] dgamma partials, one row per CTA
     float *part_b;        // [P, D] dbeta partials (LayerNorm only)
     int64_t N;
     int D;
+    int xdt, wdt, gdt;
 };
 
 // ------------------------------------------------------------------ helpers ---
@@ -69,33 +75,10 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-__device__ __forceinline__ float2 half2_bits_to_float2(uint32_t w) {
-    __half2 h = *reinterpret_cast<const __half2 *>(&w);
-    return __half22float2(h);
-}
-
-__device__ __forceinline__ uint32_t float2_to_half2_bits(float a, float b) {
-    __half2 h = __floats2half2_rn(a, b);
-    return *reinterpret_cast<const uint32_t *>(&h);
-}
-
-// Eight fp16 values (one 16-byte chunk) <-> four fp32 pairs; pair p holds elements
-// 2p and 2p+1. The pack rounds to nearest even.
-__device__ __forceinline__ void unpack8x2(const uint4 &u, float2 (&f)[4]) {
-    f[0] = half2_bits_to_float2(u.x);
-    f[1] = half2_bits_to_float2(u.y);
-    f[2] = half2_bits_to_float2(u.z);
-    f[3] = half2_bits_to_float2(u.w);
-}
-
-__device__ __forceinline__ uint4 pack8x2(const float2 (&f)[4]) {
-    uint4 u;
-    u.x = float2_to_half2_bits(f[0].x, f[0].y);
-    u.y = float2_to_half2_bits(f[1].x, f[1].y);
-    u.z = float2_to_half2_bits(f[2].x, f[2].y);
-    u.w = float2_to_half2_bits(f[3].x, f[3].y);
-    return u;
-}
+// Eight fp16 values (one 16-byte chunk) <-> four fp32 pairs (the fp16 case of
+// unpack_unit / pack_unit).
+__device__ __forceinline__ void unpack8x2(const uint4 &u, float2 (&f)[4]) { unpack_unit<kF16>(u, f); }
+__device__ __forceinline__ uint4 pack8x2(const float2 (&f)[4]) { return pack_unit<kF16>(f); }
 
 // Programmatic dependent launch. Every kernel of this library is launched with the
 // programmatic-stream-serialization attribute, so it may be scheduled while the
@@ -107,85 +90,6 @@ __device__ __forceinline__ uint4 pack8x2(const float2 (&f)[4]) {
 __device__ __forceinline__ void pdl_enter() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-// Raw storage of one chunk of VEC fp16 values, kept packed in registers.
-template <int VEC> struct Raw;
-template <> struct Raw<8> { uint4 v; };
-template <> struct Raw<1> { unsigned short v; };
-
-// Streaming (evict-first) load of one activation chunk; columns at or past D read 0.
-template <int VEC>
-__device__ __forceinline__ void load_act(const __half *row, int col, int D, Raw<VEC> &r) {
-    if constexpr (VEC == 8) {
-        if (col < D) r.v = __ldcs(reinterpret_cast<const uint4 *>(row + col));
-        else r.v = make_uint4(0u, 0u, 0u, 0u);
-    } else {
-        r.v = (col < D) ? __half_as_ushort(__ldcs(row + col)) : (unsigned short)0;
-    }
-}
-
-// Activation load through the read-only path (cached in L1), for data read twice.
-template <int VEC>
-__device__ __forceinline__ void load_act_l1(const __half *row, int col, int D, Raw<VEC> &r) {
-    if constexpr (VEC == 8) {
-        if (col < D) r.v = __ldg(reinterpret_cast<const uint4 *>(row + col));
-        else r.v = make_uint4(0u, 0u, 0u, 0u);
-    } else {
-        r.v = (col < D) ? __half_as_ushort(__ldg(row + col)) : (unsigned short)0;
-    }
-}
-
-template <int VEC>
-__device__ __forceinline__ float elem(const Raw<VEC> &r, int e) {
-    if constexpr (VEC == 8) {
-        const uint32_t w = (e < 2) ? r.v.x : (e < 4) ? r.v.y : (e < 6) ? r.v.z : r.v.w;
-        const float2 f = half2_bits_to_float2(w);
-        return (e & 1) ? f.y : f.x;
-    } else {
-        return __half2float(__ushort_as_half(r.v));
-    }
-}
-
-template <int VEC>
-__device__ __forceinline__ void unpack(const Raw<VEC> &r, float (&f)[VEC]) {
-    if constexpr (VEC == 8) {
-        float2 a = half2_bits_to_float2(r.v.x), b = half2_bits_to_float2(r.v.y);
-        float2 c = half2_bits_to_float2(r.v.z), d = half2_bits_to_float2(r.v.w);
-        f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
-        f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
-    } else {
-        f[0] = __half2float(__ushort_as_half(r.v));
-    }
-}
-
-// Read-only cached load of a parameter chunk (gamma/beta); past D reads 0.
-template <int VEC>
-__device__ __forceinline__ void load_param(const __half *p, int col, int D, float (&f)[VEC]) {
-    Raw<VEC> r;
-    if constexpr (VEC == 8) {
-        if (col < D) r.v = __ldg(reinterpret_cast<const uint4 *>(p + col));
-        else r.v = make_uint4(0u, 0u, 0u, 0u);
-    } else {
-        r.v = (col < D) ? __half_as_ushort(__ldg(p + col)) : (unsigned short)0;
-    }
-    unpack<VEC>(r, f);
-}
-
-// Round VEC fp32 values to fp16 (nearest even) and store; nothing is stored past D.
-template <int VEC>
-__device__ __forceinline__ void store_act(__half *row, int col, int D, const float (&f)[VEC]) {
-    if (col >= D) return;
-    if constexpr (VEC == 8) {
-        uint4 u;
-        u.x = float2_to_half2_bits(f[0], f[1]);
-        u.y = float2_to_half2_bits(f[2], f[3]);
-        u.z = float2_to_half2_bits(f[4], f[5]);
-        u.w = float2_to_half2_bits(f[6], f[7]);
-        *reinterpret_cast<uint4 *>(row + col) = u;
-    } else {
-        row[col] = __float2half_rn(f[0]);
-    }
 }
 
 // Barrier for one row group. NAMED: named barrier 1 + rg over the group's TPR threads,
@@ -230,8 +134,10 @@ __device__ __forceinline__ void row_sum(float (&v)[NV], float *red, int buf, int
 }
 
 // ------------------------------------------------------------------ forward ---
-// One row group per row; grid = ceil(N / RPC) CTAs of TPR*RPC threads.
-template <int OP, int TPR, int RPC, int CH, int VEC>
+// Scalar fallback for any alignment and any width: one row group per row, thread t
+// owning the CH columns k*TPR + t; types chosen at run time (a.xdt, a.wdt).
+// grid = ceil(N / RPC) CTAs of TPR*RPC threads.
+template <int OP, int TPR, int RPC, int CH>
 __global__ void __launch_bounds__(TPR * RPC)
 norm_fwd_kernel(const FwdArgs a) {
     pdl_enter();
@@ -250,22 +156,16 @@ norm_fwd_kernel(const FwdArgs a) {
     const int64_t off = (ok ? row : 0) * (int64_t)D;
     const int lim = ok ? D : 0;  // masked row: every column counts as past the end
 
-    float x[CH][VEC];
+    float x[CH];
 #pragma unroll
     for (int k = 0; k < CH; ++k) {
-        const int col = (k * TPR + t) * VEC;
-        Raw<VEC> r;
-        load_act<VEC>(a.X + off, col, lim, r);
-        unpack<VEC>(r, x[k]);
+        const int col = k * TPR + t;
+        const bool v = col < lim;
+        x[k] = v ? ld_elem_stream(a.X, off + col, a.xdt) : 0.f;
         if constexpr (OP == kAddRms) {
-            // fused op: s = x + r in fp32, normalise the unrounded s, store fp16(s)
-            Raw<VEC> rr;
-            float res[VEC];
-            load_act<VEC>(a.R + off, col, lim, rr);
-            unpack<VEC>(rr, res);
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) x[k][e] += res[e];
-            store_act<VEC>(a.S + off, col, lim, x[k]);
+            // fused op: s = x + r in fp32, normalise the unrounded s, store s rounded
+            x[k] += v ? ld_elem_stream(a.R, off + col, a.xdt) : 0.f;
+            if (v) st_elem(a.S, off + col, x[k], a.xdt);
         }
     }
 
@@ -273,23 +173,16 @@ norm_fwd_kernel(const FwdArgs a) {
     if constexpr (OP == kLayer) {
         float s[1] = {0.f};
 #pragma unroll
-        for (int k = 0; k < CH; ++k)
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) s[0] += x[k][e];
+        for (int k = 0; k < CH; ++k) s[0] += x[k];
         row_sum<TPR, RPC, 1>(s, red, 0, rg, wir, lane);
         mu = s[0] / (float)D;
     }
     float q[1] = {0.f};
 #pragma unroll
     for (int k = 0; k < CH; ++k) {
-        const int col = (k * TPR + t) * VEC;
-        const bool valid = col < lim;
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-            // LayerNorm: centred second moment (two-pass, from registers)
-            const float d = (OP == kLayer) ? (valid ? x[k][e] - mu : 0.f) : x[k][e];
-            q[0] += d * d;
-        }
+        // LayerNorm: centred second moment (two-pass, from registers)
+        const float d = (OP == kLayer) ? ((k * TPR + t) < lim ? x[k] - mu : 0.f) : x[k];
+        q[0] += d * d;
     }
     row_sum<TPR, RPC, 1>(q, red, 1, rg, wir, lane);
     const float rs = rsqrtf(q[0] / (float)D + a.eps);
@@ -301,28 +194,22 @@ norm_fwd_kernel(const FwdArgs a) {
 
 #pragma unroll
     for (int k = 0; k < CH; ++k) {
-        const int col = (k * TPR + t) * VEC;
+        const int col = k * TPR + t;
         if (col >= D) continue;
-        float g[VEC], y[VEC];
-        load_param<VEC>(a.gamma, col, D, g);
-        if constexpr (OP == kLayer) {
-            float b[VEC];
-            load_param<VEC>(a.beta, col, D, b);
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) y[e] = (x[k][e] - mu) * rs * g[e] + b[e];
-        } else {
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) y[e] = x[k][e] * rs * g[e];
-        }
-        store_act<VEC>(a.Y + off, col, D, y);
+        const float g = ld_elem(a.gamma, col, a.wdt);
+        float y;
+        if constexpr (OP == kLayer) y = (x[k] - mu) * rs * g + ld_elem(a.beta, col, a.wdt);
+        else y = x[k] * rs * g;
+        st_elem(a.Y, off + col, y, a.xdt);
     }
 }
 
 // Forward for 16-byte-aligned rows (D % 8 == 0), one row group per row, fp32 pair
-// arithmetic (__ffma2_rn & co.). Rows are loaded once with streaming 16-byte loads and
-// stay in registers through the reductions and the apply. MINB is the minimum number of
-// resident CTAs per SM asked of the compiler (it bounds the registers per thread).
-template <int OP, int TPR, int RPC, int CH, int MINB>
+// arithmetic (__ffma2_rn & co.). Rows are loaded once with streaming loads and stay in
+// registers (as fp32 pairs) through the reductions and the apply. Activations are of
+// type XT, gamma/beta of type WT. MINB is the minimum number of resident CTAs per SM
+// asked of the compiler (it bounds the registers per thread; 0: the compiler's choice).
+template <int OP, int TPR, int RPC, int CH, int MINB, int XT, int WT>
 __global__ void __launch_bounds__(TPR * RPC, MINB)
 norm_fwd_vec8_kernel(const FwdArgs a) {
     pdl_enter();
@@ -344,13 +231,13 @@ norm_fwd_vec8_kernel(const FwdArgs a) {
     for (int k = 0; k < CH; ++k) {
         const int col = (k * TPR + t) * 8;
         const bool v = ok && col < D;
-        unpack8x2(v ? __ldcs(reinterpret_cast<const uint4 *>(a.X + off + col)) : make_uint4(0, 0, 0, 0), x[k]);
+        ld_chunk<XT, kStream>(as<XT>(a.X) + off + col, v, x[k]);
         if constexpr (OP == kAddRms) {
             float2 r[4];
-            unpack8x2(v ? __ldcs(reinterpret_cast<const uint4 *>(a.R + off + col)) : make_uint4(0, 0, 0, 0), r);
+            ld_chunk<XT, kStream>(as<XT>(a.R) + off + col, v, r);
 #pragma unroll
             for (int p = 0; p < 4; ++p) x[k][p] = __fadd2_rn(x[k][p], r[p]);
-            if (v) __stcs(reinterpret_cast<uint4 *>(a.S + off + col), pack8x2(x[k]));
+            if (v) st_chunk<XT>(as<XT>(a.S) + off + col, x[k]);
         }
     }
     float mu = 0.f;
@@ -389,10 +276,10 @@ norm_fwd_vec8_kernel(const FwdArgs a) {
         const int col = (k * TPR + t) * 8;
         if (col >= D) continue;
         float2 g[4], y[4];
-        unpack8x2(__ldg(reinterpret_cast<const uint4 *>(a.gamma + col)), g);
+        ld_param<WT>(as<WT>(a.gamma) + col, g);
         if constexpr (OP == kLayer) {
             float2 b[4];
-            unpack8x2(__ldg(reinterpret_cast<const uint4 *>(a.beta + col)), b);
+            ld_param<WT>(as<WT>(a.beta) + col, b);
 #pragma unroll
             for (int p = 0; p < 4; ++p)
                 y[p] = __ffma2_rn(__fmul2_rn(__fadd2_rn(x[k][p], nmu), rs2), g[p], b[p]);
@@ -400,22 +287,25 @@ norm_fwd_vec8_kernel(const FwdArgs a) {
 #pragma unroll
             for (int p = 0; p < 4; ++p) y[p] = __fmul2_rn(__fmul2_rn(x[k][p], rs2), g[p]);
         }
-        __stcs(reinterpret_cast<uint4 *>(a.Y + off + col), pack8x2(y));
+        st_chunk<XT>(as<XT>(a.Y) + off + col, y);
     }
 }
 
-// The same forward for RMSNorm and LayerNorm with the row kept as the loaded fp16 chunks
-// and widened to fp32 pairs at each use: half the registers of norm_fwd_vec8_kernel, so
-// more CTAs (and more bytes in flight) fit per SM, for one more conversion per pass.
-// (The fused op normalises the unrounded fp32 x + r, so it cannot keep fp16 chunks.)
-template <int OP, int TPR, int RPC, int CH, int MINB>
+// The same forward for RMSNorm and LayerNorm with 2-byte activations (XT = fp16 or
+// bf16), the row kept as the loaded 16-byte chunks and widened to fp32 pairs at each use:
+// half the registers of norm_fwd_vec8_kernel, so more CTAs (and more bytes in flight)
+// fit per SM, for one more conversion per pass. (The fused op normalises the unrounded
+// fp32 x + r, so it cannot keep 2-byte chunks.)
+template <int OP, int TPR, int RPC, int CH, int MINB, int XT, int WT>
 __global__ void __launch_bounds__(TPR * RPC, MINB)
 norm_fwd_packed_kernel(const FwdArgs a) {
     pdl_enter();
     static_assert(TPR % 32 == 0 && TPR * RPC <= 1024, "bad launch shape");
     static_assert(OP == kRms || OP == kLayer, "the fused op keeps its fp32 sum");
+    static_assert(XT == kF16 || XT == kBF16, "2-byte activations only");
     constexpr int WPR = TPR / 32;
     __shared__ float red[2 * RPC * WPR];
+    const auto *X = as<XT>(a.X);
 
     const int tid = threadIdx.x;
     const int rg = tid / TPR, t = tid % TPR, wir = t / 32, lane = tid % 32;
@@ -430,8 +320,7 @@ norm_fwd_packed_kernel(const FwdArgs a) {
 #pragma unroll
     for (int k = 0; k < CH; ++k) {
         const int col = (k * TPR + t) * 8;
-        raw[k] = (ok && col < D) ? __ldcs(reinterpret_cast<const uint4 *>(a.X + off + col))
-                                 : make_uint4(0, 0, 0, 0);
+        raw[k] = (ok && col < D) ? ld_unit<kStream>(X + off + col) : make_uint4(0, 0, 0, 0);
     }
     // Chunk k as fp32 pairs. Each pass widens the chunks again rather than keep fp32
     // copies of the row alive across the reductions. So that the compiler does not merge
@@ -442,7 +331,7 @@ norm_fwd_packed_kernel(const FwdArgs a) {
     const uint32_t zero = (uint32_t)D >> 30;
     auto pairs = [&](int k, float2 (&f)[4], float after) {
         const uint32_t key = zero & __float_as_uint(after);
-        unpack8x2(make_uint4(raw[k].x ^ key, raw[k].y ^ key, raw[k].z ^ key, raw[k].w ^ key), f);
+        unpack_unit<XT>(make_uint4(raw[k].x ^ key, raw[k].y ^ key, raw[k].z ^ key, raw[k].w ^ key), f);
     };
 
     float mu = 0.f;
@@ -451,7 +340,7 @@ norm_fwd_packed_kernel(const FwdArgs a) {
 #pragma unroll
         for (int k = 0; k < CH; ++k) {
             float2 f[4];
-            unpack8x2(raw[k], f);
+            unpack_unit<XT>(raw[k], f);
 #pragma unroll
             for (int p = 0; p < 4; ++p) s2 = __fadd2_rn(s2, f[p]);
         }
@@ -466,7 +355,7 @@ norm_fwd_packed_kernel(const FwdArgs a) {
         if (!(ok && (k * TPR + t) * 8 < D)) continue;
         float2 f[4];
         if constexpr (OP == kLayer) pairs(k, f, mu);
-        else unpack8x2(raw[k], f);
+        else unpack_unit<XT>(raw[k], f);
 #pragma unroll
         for (int p = 0; p < 4; ++p) {
             const float2 d = (OP == kLayer) ? __fadd2_rn(f[p], nmu) : f[p];
@@ -495,10 +384,10 @@ norm_fwd_packed_kernel(const FwdArgs a) {
         float2 f[4], g[4], y[4];
         pairs(k, f, rs);
         const int pc = col + (int)chain;
-        unpack8x2(__ldg(reinterpret_cast<const uint4 *>(a.gamma + pc)), g);
+        ld_param<WT>(as<WT>(a.gamma) + pc, g);
         if constexpr (OP == kLayer) {
             float2 b[4];
-            unpack8x2(__ldg(reinterpret_cast<const uint4 *>(a.beta + pc)), b);
+            ld_param<WT>(as<WT>(a.beta) + pc, b);
 #pragma unroll
             for (int p = 0; p < 4; ++p)
                 y[p] = __ffma2_rn(__fmul2_rn(__fadd2_rn(f[p], nmu), rs2), g[p], b[p]);
@@ -507,16 +396,18 @@ norm_fwd_packed_kernel(const FwdArgs a) {
             for (int p = 0; p < 4; ++p) y[p] = __fmul2_rn(__fmul2_rn(f[p], rs2), g[p]);
         }
         chain = zero & __float_as_uint(y[0].x);
-        __stcs(reinterpret_cast<uint4 *>(a.Y + off + col), pack8x2(y));
+        st_chunk<XT>(as<XT>(a.Y) + off + col, y);
     }
 }
 
 // ----------------------------------------------------------------- backward ---
-// Persistent: grid = P CTAs of TPR*RPC threads; CTA b processes row slots
-// b*RPC + j*G*RPC (G = gridDim.x), row group rg taking row slot + rg.
-// Dynamic shared memory (RPC > 1): NV x D floats for the fixed-order combine.
-template <int OP, int TPR, int RPC, int CH, int VEC, bool HAS_DS>
-__global__ void __launch_bounds__(TPR * RPC)
+// Scalar fallback for any alignment and any width; types chosen at run time (a.xdt,
+// a.wdt, a.gdt). Persistent: grid = P CTAs of TPR*RPC threads; CTA b processes row
+// slots b*RPC + j*G*RPC (G = gridDim.x), row group rg taking row slot + rg.
+// Dynamic shared memory (RPC > 1): NV x D floats for the fixed-order combine. Compiled
+// for one resident CTA per SM, so the run-time type selection costs registers, not spills.
+template <int OP, int TPR, int RPC, int CH, bool HAS_DS>
+__global__ void __launch_bounds__(TPR * RPC, 1)
 norm_bwd_kernel(const BwdArgs a) {
     pdl_enter();
     static_assert(TPR % 32 == 0 && TPR * RPC <= 1024, "bad launch shape");
@@ -530,15 +421,12 @@ norm_bwd_kernel(const BwdArgs a) {
     const int D = a.D;
     const float inv_d = 1.0f / (float)D;
 
-    float accg[CH][VEC];
-    float accb[CH][(OP == kLayer) ? VEC : 1];
+    float accg[CH];
+    float accb[(OP == kLayer) ? CH : 1];
 #pragma unroll
-    for (int k = 0; k < CH; ++k) {
+    for (int k = 0; k < CH; ++k) accg[k] = 0.f;
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) accg[k][e] = 0.f;
-#pragma unroll
-        for (int e = 0; e < ((OP == kLayer) ? VEC : 1); ++e) accb[k][e] = 0.f;
-    }
+    for (int k = 0; k < ((OP == kLayer) ? CH : 1); ++k) accb[k] = 0.f;
 
     int buf = 0;
     for (int64_t base = (int64_t)blockIdx.x * RPC; base < a.N;
@@ -553,14 +441,14 @@ norm_bwd_kernel(const BwdArgs a) {
 
         // Short row slices stay in registers between the passes; longer ones are read
         // again in pass 2 through L1 (where pass 1 left them), which avoids spills.
-        constexpr bool KEEP = CH * VEC <= 8;
-        Raw<VEC> xr[KEEP ? CH : 1], dyr[KEEP ? CH : 1];
+        constexpr bool KEEP = CH <= 8;
+        float xs[KEEP ? CH : 1], dys[KEEP ? CH : 1];
         if constexpr (KEEP) {
 #pragma unroll
             for (int k = 0; k < CH; ++k) {
-                const int col = (k * TPR + t) * VEC;
-                load_act<VEC>(a.X + off, col, lim, xr[k]);
-                load_act<VEC>(a.dY + off, col, lim, dyr[k]);
+                const int col = k * TPR + t;
+                xs[k] = col < lim ? ld_elem_stream(a.X, off + col, a.xdt) : 0.f;
+                dys[k] = col < lim ? ld_elem_stream(a.dY, off + col, a.gdt) : 0.f;
             }
         }
 
@@ -570,26 +458,21 @@ norm_bwd_kernel(const BwdArgs a) {
         for (int i = 0; i < NV; ++i) v[i] = 0.f;
 #pragma unroll
         for (int k = 0; k < CH; ++k) {
-            const int col = (k * TPR + t) * VEC;
-            float gm[VEC], xv[VEC], dv[VEC];
-            load_param<VEC>(a.gamma, col, lim, gm);
+            const int col = k * TPR + t;
+            const bool in = col < lim;
+            const float gm = in ? ld_elem(a.gamma, col, a.wdt) : 0.f;
+            float xv, dv;
             if constexpr (KEEP) {
-                unpack<VEC>(xr[k], xv);
-                unpack<VEC>(dyr[k], dv);
+                xv = xs[k];
+                dv = dys[k];
             } else {
-                Raw<VEC> xk, dk;
-                load_act_l1<VEC>(a.X + off, col, lim, xk);
-                load_act_l1<VEC>(a.dY + off, col, lim, dk);
-                unpack<VEC>(xk, xv);
-                unpack<VEC>(dk, dv);
+                xv = in ? ld_elem(a.X, off + col, a.xdt) : 0.f;
+                dv = in ? ld_elem(a.dY, off + col, a.gdt) : 0.f;
             }
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                const float xh = (xv[e] - mu) * r;
-                const float g = dv[e] * gm[e];
-                v[0] += g * xh;
-                if constexpr (OP == kLayer) v[NV - 1] += g;
-            }
+            const float xh = (xv - mu) * r;
+            const float g = dv * gm;
+            v[0] += g * xh;
+            if constexpr (OP == kLayer) v[NV - 1] += g;
         }
         row_sum<TPR, RPC, NV>(v, red, buf, rg, wir, lane);
         const float c = v[0] * inv_d;
@@ -599,37 +482,24 @@ norm_bwd_kernel(const BwdArgs a) {
         // pass 2: dX and the parameter-gradient sums
 #pragma unroll
         for (int k = 0; k < CH; ++k) {
-            const int col = (k * TPR + t) * VEC;
+            const int col = k * TPR + t;
             if (col >= D) continue;
-            float gm[VEC], xv[VEC], dv[VEC], o[VEC];
-            load_param<VEC>(a.gamma, col, D, gm);
+            const float gm = ld_elem(a.gamma, col, a.wdt);
+            float xv, dv;
             if constexpr (KEEP) {
-                unpack<VEC>(xr[k], xv);
-                unpack<VEC>(dyr[k], dv);
+                xv = xs[k];
+                dv = dys[k];
             } else {
-                Raw<VEC> xk, dk;
-                load_act_l1<VEC>(a.X + off, col, D, xk);
-                load_act_l1<VEC>(a.dY + off, col, D, dk);
-                unpack<VEC>(xk, xv);
-                unpack<VEC>(dk, dv);
+                xv = ld_elem(a.X, off + col, a.xdt);
+                dv = ld_elem(a.dY, off + col, a.gdt);
             }
-            float ds[VEC];
-            if constexpr (HAS_DS) {
-                Raw<VEC> dsr;
-                load_act<VEC>(a.dS + off, col, D, dsr);
-                unpack<VEC>(dsr, ds);
-            }
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                const float xh = (xv[e] - mu) * r;
-                const float g = dv[e] * gm[e];
-                float dx = r * ((g - am) - xh * c);
-                if constexpr (HAS_DS) dx += ds[e];
-                o[e] = dx;
-                accg[k][e] += dv[e] * xh;
-                if constexpr (OP == kLayer) accb[k][e] += dv[e];
-            }
-            store_act<VEC>(a.dX + off, col, D, o);
+            const float xh = (xv - mu) * r;
+            const float g = dv * gm;
+            float dx = r * ((g - am) - xh * c);
+            if constexpr (HAS_DS) dx += ld_elem_stream(a.dS, off + col, a.gdt);
+            accg[k] += dv * xh;
+            if constexpr (OP == kLayer) accb[k] += dv;
+            st_elem(a.dX, off + col, dx, a.xdt);
         }
     }
 
@@ -640,13 +510,10 @@ norm_bwd_kernel(const BwdArgs a) {
     if constexpr (RPC == 1) {
 #pragma unroll
         for (int k = 0; k < CH; ++k) {
-            const int col = (k * TPR + t) * VEC;
+            const int col = k * TPR + t;
             if (col >= D) continue;
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                pg[col + e] = accg[k][e];
-                if constexpr (OP == kLayer) pb[col + e] = accb[k][e];
-            }
+            pg[col] = accg[k];
+            if constexpr (OP == kLayer) pb[col] = accb[k];
         }
     } else {
         float *cg = comb;
@@ -655,16 +522,13 @@ norm_bwd_kernel(const BwdArgs a) {
             if (rg == j) {
 #pragma unroll
                 for (int k = 0; k < CH; ++k) {
-                    const int col = (k * TPR + t) * VEC;
+                    const int col = k * TPR + t;
                     if (col >= D) continue;
-#pragma unroll
-                    for (int e = 0; e < VEC; ++e) {
-                        const float sg = (j == 0) ? accg[k][e] : cg[col + e] + accg[k][e];
-                        if (j == RPC - 1) pg[col + e] = sg; else cg[col + e] = sg;
-                        if constexpr (OP == kLayer) {
-                            const float sb = (j == 0) ? accb[k][e] : cb[col + e] + accb[k][e];
-                            if (j == RPC - 1) pb[col + e] = sb; else cb[col + e] = sb;
-                        }
+                    const float sg = (j == 0) ? accg[k] : cg[col] + accg[k];
+                    if (j == RPC - 1) pg[col] = sg; else cg[col] = sg;
+                    if constexpr (OP == kLayer) {
+                        const float sb = (j == 0) ? accb[k] : cb[col] + accb[k];
+                        if (j == RPC - 1) pb[col] = sb; else cb[col] = sb;
                     }
                 }
             }

@@ -1,14 +1,20 @@
-// launch.cuh -- launch shapes and per-op planning for the normalization kernels.
+// launch.cuh -- launch shapes and per-op, per-dtype planning for the normalization kernels.
 //
-// A launch shape is (TPR threads per row, RPC rows per CTA, CH chunks per thread,
-// VEC fp16 elements per chunk). VEC = 8 (one 16-byte access per chunk) is legal when
-// D % 8 == 0 and every row base is 16-byte aligned; VEC = 1 covers everything else.
-// The first shape whose width covers D is taken. Forward rows up to 1024 wide get one
-// warp each (four rows per CTA, two for the fused op at 1024); wider rows get a row
+// A vector launch shape is (TPR threads per row, RPC rows per CTA, CH chunks of 8
+// elements per thread). The vector kernels are legal when D % 8 == 0 and every row base
+// is 16-byte aligned; the scalar kernels (one element per access, types chosen at run
+// time) cover everything else, and every dtype combination the vector tables do not
+// list. The first shape whose width covers D is taken. Forward rows up to 1024 wide get
+// one warp each (four rows per CTA, two for the fused op at 1024); wider rows get a row
 // group of 64-512 threads, one row per CTA (on GB300 this beat a persistent pipelined
-// forward at every width measured). The
-// aligned backward is persistent and pipelined (pipe.cuh), with few CTAs so that the
-// dgamma/dbeta partials stay small.
+// forward at every width measured). The aligned backward is persistent and pipelined
+// (pipe.cuh), with few CTAs so that the dgamma/dbeta partials stay small.
+//
+// Storage types: activations XT, parameters WT, cotangents GT (dtype.cuh). The full
+// tables were tuned for fp16 and serve every combination whose three types match; the
+// others (fp32 parameters or cotangents with 2-byte activations, and all-fp32 in the
+// backward) use short tables. A backward ring that cannot hold two stages, and any
+// combination not listed, take the scalar kernel.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -21,11 +27,11 @@
 namespace mt {
 
 // Forward shapes for 16-byte-aligned rows, per op: X(max_D, TPR, RPC, CH, PACK, MINB).
-// PACK runs norm_fwd_packed_kernel (the row kept as fp16 chunks; RMSNorm and LayerNorm
-// only), otherwise norm_fwd_vec8_kernel (the row kept as fp32 pairs). MINB is the
-// resident-CTA floor per SM the kernel is compiled for, which caps its registers per
-// thread (0: the compiler's choice). Every entry was timed on GB300 against its
-// neighbours and compiles without spills.
+// PACK runs norm_fwd_packed_kernel (the row kept as the loaded 2-byte chunks; RMSNorm and
+// LayerNorm with fp16/bf16 activations only), otherwise norm_fwd_vec8_kernel (the row
+// kept as fp32 pairs). MINB is the resident-CTA floor per SM the kernel is compiled for,
+// which caps its registers per thread (0: the compiler's choice). Every entry was timed
+// on GB300 against its neighbours and compiles without spills.
 #ifndef MT_FWD_SHAPES_RMS
 #define MT_FWD_SHAPES_RMS(X)           \
     X(256, 32, 4, 1, false, 0)         \
@@ -51,32 +57,38 @@ namespace mt {
     X(256, 32, 4, 1, false, 16)        \
     X(512, 32, 4, 2, false, 16)        \
     X(1024, 64, 2, 2, false, 16)       \
-    X(2048, 128, 1, 2, false, 16)      \
+    X(2048, 128, 1, 2, false, 12)      \
     X(4096, 512, 1, 1, false, 4)       \
-    X(8192, 512, 1, 2, false, 4)       \
+    X(8192, 512, 1, 2, false, 3)       \
     X(16384, 512, 1, 4, false, 0)
 #endif
+// Short forward table (fp32 parameters with 2-byte activations), every op.
+#define MT_FWD_SHAPES_SHORT(X)         \
+    X(1024, 32, 4, 4, false, 0)        \
+    X(4096, 512, 1, 1, false, 4)       \
+    X(16384, 512, 1, 4, false, 0)
 
-#define MT_FWD_SHAPES_VEC1(X) \
-    X(64, 32, 4, 2)           \
-    X(128, 32, 4, 4)          \
-    X(256, 32, 4, 8)          \
-    X(512, 32, 4, 16)         \
-    X(1024, 32, 4, 32)        \
-    X(2048, 128, 1, 16)       \
-    X(4096, 256, 1, 16)       \
-    X(8192, 512, 1, 16)       \
+// Scalar fallback shapes: X(max_D, TPR, RPC, CH), CH elements per thread.
+#define MT_FWD_SHAPES_SCALAR(X) \
+    X(64, 32, 4, 2)             \
+    X(128, 32, 4, 4)            \
+    X(256, 32, 4, 8)            \
+    X(512, 32, 4, 16)           \
+    X(1024, 32, 4, 32)          \
+    X(2048, 128, 1, 16)         \
+    X(4096, 256, 1, 16)         \
+    X(8192, 512, 1, 16)         \
     X(16384, 1024, 1, 16)
 
-#define MT_BWD_SHAPES_VEC1(X) \
-    X(64, 32, 8, 2)           \
-    X(128, 32, 8, 4)          \
-    X(256, 32, 8, 8)          \
-    X(512, 32, 8, 16)         \
-    X(1024, 64, 4, 16)        \
-    X(2048, 128, 4, 16)       \
-    X(4096, 256, 2, 16)       \
-    X(8192, 512, 1, 16)       \
+#define MT_BWD_SHAPES_SCALAR(X) \
+    X(64, 32, 8, 2)             \
+    X(128, 32, 8, 4)            \
+    X(256, 32, 8, 8)            \
+    X(512, 32, 8, 16)           \
+    X(1024, 64, 4, 16)          \
+    X(2048, 128, 4, 16)         \
+    X(4096, 256, 2, 16)         \
+    X(8192, 512, 1, 16)         \
     X(16384, 512, 1, 32)
 
 // Pipelined persistent backward shapes for 16-byte-aligned rows, RMSNorm and the fused
@@ -105,16 +117,38 @@ namespace mt {
     X(8192, 512, 1, 2, 3, 1)        \
     X(16384, 512, 1, 4, 3, 1)
 #endif
+// All-fp32 backward: an fp32 chunk takes two ring units per array, so these shapes keep
+// 2-3 ring stages; 16384-wide fp32 rows (128 KB per stage) take the scalar kernel.
+#define MT_BWD_PIPE_SHAPES_F32(X)   \
+    X(1024, 128, 4, 1, 8, 2)        \
+    X(2048, 256, 2, 1, 8, 2)        \
+    X(4096, 512, 1, 1, 4, 1)        \
+    X(8192, 512, 1, 2, 3, 1)
+#define MT_BWD_PIPE_SHAPES_F32_LAYER(X) \
+    X(1024, 128, 1, 1, 6, 6)            \
+    X(2048, 256, 1, 1, 6, 3)            \
+    X(4096, 512, 1, 1, 4, 1)            \
+    X(8192, 512, 1, 2, 3, 1)
+// Short backward tables: one shape per width class.
+#define MT_BWD_PIPE_SHAPES_RMS_SHORT(X) \
+    X(1024, 128, 4, 1, 8, 2)            \
+    X(4096, 512, 1, 1, 4, 2)            \
+    X(16384, 512, 1, 4, 3, 1)
+#define MT_BWD_PIPE_SHAPES_LAYER_SHORT(X) \
+    X(1024, 128, 1, 1, 6, 6)              \
+    X(4096, 512, 1, 1, 4, 2)              \
+    X(16384, 512, 1, 4, 3, 1)
 
-// Ring depth: the table's depth, cut so that ring + parameter slots fit the dynamic
-// shared memory a CTA may use (227 KB per SM, shared by `ctas` resident CTAs), and
-// never below 2.
+// Ring depth: the table's depth, cut so that the ring plus the parameter slots fit the
+// dynamic shared memory a CTA may use (227 KB per SM, shared by `ctas` resident CTAs);
+// 0 when not even two stages fit.
 constexpr size_t kMaxDynSmem = 226 * 1024;
-constexpr int pipe_stages(int base, int narr, int npar, int ch, int threads, int ctas) {
-    const size_t slot = (size_t)ch * threads * 16;
-    const int fit = (int)(((kMaxDynSmem / ctas / slot) - npar) / narr);
-    const int s = base < fit ? base : fit;
-    return s < 2 ? 2 : s;
+constexpr int pipe_stages(int base, size_t stage_bytes, size_t param_bytes, int ctas) {
+    return (param_bytes + 2 * stage_bytes > kMaxDynSmem / ctas)
+               ? 0
+               : ((int)((kMaxDynSmem / ctas - param_bytes) / stage_bytes) < base
+                      ? (int)((kMaxDynSmem / ctas - param_bytes) / stage_bytes)
+                      : base);
 }
 
 struct LaunchPlan {
@@ -131,22 +165,6 @@ cudaError_t device_sm_count(int device, int *sms);
 cudaError_t cached_occupancy(const void *kernel, int threads, size_t smem, int device,
                              int *blocks_per_sm);
 
-template <int OP, int TPR, int RPC, int CH, int VEC, bool PACK = false, int MINB = 1>
-cudaError_t fwd_plan_shape(int64_t N, LaunchPlan *p) {
-    static_assert(!(PACK && OP == kAddRms), "the fused op keeps its fp32 sum");
-    if constexpr (VEC == 8 && PACK)
-        p->kernel = reinterpret_cast<const void *>(&norm_fwd_packed_kernel<OP, TPR, RPC, CH, MINB>);
-    else if constexpr (VEC == 8)
-        p->kernel = reinterpret_cast<const void *>(&norm_fwd_vec8_kernel<OP, TPR, RPC, CH, MINB>);
-    else
-        p->kernel = reinterpret_cast<const void *>(&norm_fwd_kernel<OP, TPR, RPC, CH, VEC>);
-    p->threads = TPR * RPC;
-    p->grid = (int)((N + RPC - 1) / RPC);
-    p->smem = 0;
-    p->rows_per_cta = RPC;
-    return cudaSuccess;
-}
-
 // Persistent grid: as many CTAs as fit on the device at once, at most one per row slot.
 inline cudaError_t persistent_grid(LaunchPlan *p, int64_t N, int device) {
     int per_sm = 0, sms = 0;
@@ -160,81 +178,197 @@ inline cudaError_t persistent_grid(LaunchPlan *p, int64_t N, int device) {
     return cudaSuccess;
 }
 
+// Returned by a vector plan for a dtype combination or shape it does not cover: the
+// caller takes the scalar kernel.
+constexpr cudaError_t kNoVectorPlan = cudaErrorNotSupported;
+
+// ------------------------------------------------------------------ forward ---
+
+template <int OP, int TPR, int RPC, int CH>
+cudaError_t fwd_scalar_shape(int64_t N, LaunchPlan *p) {
+    p->kernel = reinterpret_cast<const void *>(&norm_fwd_kernel<OP, TPR, RPC, CH>);
+    p->threads = TPR * RPC;
+    p->grid = (int)((N + RPC - 1) / RPC);
+    p->smem = 0;
+    p->rows_per_cta = RPC;
+    return cudaSuccess;
+}
+
 template <int OP>
-cudaError_t fwd_plan(int64_t N, int D, bool vec8, int device, LaunchPlan *p) {
-    (void)device;
-#define MT_TRY8(maxd, tpr, rpc, ch, pack, minb) \
-    if (D <= maxd) return fwd_plan_shape<OP, tpr, rpc, ch, 8, pack, minb>(N, p);
+cudaError_t fwd_plan_scalar(int64_t N, int D, LaunchPlan *p) {
 #define MT_TRY(maxd, tpr, rpc, ch) \
-    if (D <= maxd) return fwd_plan_shape<OP, tpr, rpc, ch, VEC>(N, p);
-    if (vec8) {
-        if constexpr (OP == kRms) {
-            MT_FWD_SHAPES_RMS(MT_TRY8)
-        } else if constexpr (OP == kLayer) {
-            MT_FWD_SHAPES_LAYER(MT_TRY8)
-        } else {
-            MT_FWD_SHAPES_FUSED(MT_TRY8)
-        }
-    } else {
-        constexpr int VEC = 1;
-        MT_FWD_SHAPES_VEC1(MT_TRY)
-    }
+    if (D <= maxd) return fwd_scalar_shape<OP, tpr, rpc, ch>(N, p);
+    MT_FWD_SHAPES_SCALAR(MT_TRY)
 #undef MT_TRY
-#undef MT_TRY8
     return cudaErrorInvalidValue;
 }
 
-template <int OP, int TPR, int RPC, int CH, int VEC, bool HAS_DS>
-cudaError_t bwd_plan_shape(int64_t N, int D, int device, LaunchPlan *p) {
+// The register floors (MINB) were set for 2-byte types; with fp32 activations or
+// parameters the compiler chooses (MINB 0), since the floors would force spills there.
+template <int OP, int XT, int WT, int TPR, int RPC, int CH, bool PACK, int MINB>
+cudaError_t fwd_vec_shape(int64_t N, LaunchPlan *p) {
+    constexpr int minb = (XT == kF32 || WT == kF32) ? 0 : MINB;
+    if constexpr (PACK && OP != kAddRms && XT != kF32)
+        p->kernel = reinterpret_cast<const void *>(
+            &norm_fwd_packed_kernel<OP, TPR, RPC, CH, minb, XT, WT>);
+    else
+        p->kernel = reinterpret_cast<const void *>(
+            &norm_fwd_vec8_kernel<OP, TPR, RPC, CH, minb, XT, WT>);
+    p->threads = TPR * RPC;
+    p->grid = (int)((N + RPC - 1) / RPC);
+    p->smem = 0;
+    p->rows_per_cta = RPC;
+    return cudaSuccess;
+}
+
+// Vector forward for activations XT and parameters WT; SHORT selects the short table.
+template <int OP, int XT, int WT, bool SHORT>
+cudaError_t fwd_plan_vec(int64_t N, int D, LaunchPlan *p) {
+#define MT_TRY(maxd, tpr, rpc, ch, pack, minb) \
+    if (D <= maxd) return fwd_vec_shape<OP, XT, WT, tpr, rpc, ch, pack, minb>(N, p);
+    if constexpr (SHORT) {
+        MT_FWD_SHAPES_SHORT(MT_TRY)
+    } else if constexpr (OP == kRms) {
+        MT_FWD_SHAPES_RMS(MT_TRY)
+    } else if constexpr (OP == kLayer) {
+        MT_FWD_SHAPES_LAYER(MT_TRY)
+    } else {
+        MT_FWD_SHAPES_FUSED(MT_TRY)
+    }
+#undef MT_TRY
+    return kNoVectorPlan;
+}
+
+// ----------------------------------------------------------------- backward ---
+
+template <int OP, int TPR, int RPC, int CH, bool HAS_DS>
+cudaError_t bwd_scalar_shape(int64_t N, int D, int device, LaunchPlan *p) {
     constexpr int NV = (OP == kLayer) ? 2 : 1;
-    p->kernel = reinterpret_cast<const void *>(&norm_bwd_kernel<OP, TPR, RPC, CH, VEC, HAS_DS>);
+    p->kernel = reinterpret_cast<const void *>(&norm_bwd_kernel<OP, TPR, RPC, CH, HAS_DS>);
     p->threads = TPR * RPC;
     p->smem = (RPC > 1) ? (size_t)NV * (size_t)D * sizeof(float) : 0;
     p->rows_per_cta = RPC;
     return persistent_grid(p, N, device);
 }
 
-template <int OP, int TPR, int RPC, int CH, int STAGES, bool HAS_DS, int CTAS>
-cudaError_t bwd_pipe_plan_shape(int64_t N, int device, LaunchPlan *p) {
-    constexpr int NARR = HAS_DS ? 3 : 2;
-    constexpr int NPAR = (CH <= 2) ? 0 : 1;
-    constexpr int S = pipe_stages(STAGES, NARR, NPAR, CH, TPR * RPC, CTAS);
-    static_assert(Ring<S, NARR, CH, TPR * RPC, NPAR>::kBytes <= kMaxDynSmem, "ring too large");
-    p->kernel = reinterpret_cast<const void *>(
-        &norm_bwd_pipe_kernel<OP, TPR, RPC, CH, S, HAS_DS, CTAS>);
-    p->threads = TPR * RPC;
-    p->smem = Ring<S, NARR, CH, TPR * RPC, NPAR>::kBytes;
-    p->rows_per_cta = RPC;
-    return persistent_grid(p, N, device);
-}
-
 template <int OP, bool HAS_DS>
-cudaError_t bwd_plan(int64_t N, int D, bool vec8, int device, LaunchPlan *p) {
+cudaError_t bwd_plan_scalar(int64_t N, int D, int device, LaunchPlan *p) {
 #define MT_TRY(maxd, tpr, rpc, ch) \
-    if (D <= maxd) return bwd_plan_shape<OP, tpr, rpc, ch, VEC, HAS_DS>(N, D, device, p);
-#define MT_TRY_PIPE(maxd, tpr, rpc, ch, st, ctas) \
-    if (D <= maxd) return bwd_pipe_plan_shape<OP, tpr, rpc, ch, st, HAS_DS, ctas>(N, device, p);
-    if (vec8) {
-        if constexpr (OP == kLayer) {
-            MT_BWD_PIPE_SHAPES_LAYER(MT_TRY_PIPE)
-        } else {
-            MT_BWD_PIPE_SHAPES_RMS(MT_TRY_PIPE)
-        }
-    } else {
-        constexpr int VEC = 1;
-        MT_BWD_SHAPES_VEC1(MT_TRY)
-    }
+    if (D <= maxd) return bwd_scalar_shape<OP, tpr, rpc, ch, HAS_DS>(N, D, device, p);
+    MT_BWD_SHAPES_SCALAR(MT_TRY)
 #undef MT_TRY
-#undef MT_TRY_PIPE
     return cudaErrorInvalidValue;
 }
 
-// Per-op entry points, one translation unit each (compiled in parallel).
-cudaError_t fwd_plan_rms(int64_t N, int D, bool vec8, int device, LaunchPlan *p);
-cudaError_t fwd_plan_layer(int64_t N, int D, bool vec8, int device, LaunchPlan *p);
-cudaError_t fwd_plan_add(int64_t N, int D, bool vec8, int device, LaunchPlan *p);
-cudaError_t bwd_plan_rms(int64_t N, int D, bool vec8, int device, LaunchPlan *p);
-cudaError_t bwd_plan_layer(int64_t N, int D, bool vec8, int device, LaunchPlan *p);
-cudaError_t bwd_plan_add(int64_t N, int D, bool vec8, bool has_ds, int device, LaunchPlan *p);
+template <int OP, int XT, int WT, int GT, int TPR, int RPC, int CH, int STAGES, bool HAS_DS,
+          int CTAS>
+cudaError_t bwd_pipe_shape(int64_t N, int device, LaunchPlan *p) {
+    constexpr int NPAR = (CH <= 2) ? 0 : 1;
+    using R1 = Ring<1, CH, TPR * RPC, chunk_units<XT>(), chunk_units<GT>(), HAS_DS,
+                    chunk_units<WT>(), NPAR>;
+    constexpr int S = pipe_stages(STAGES, R1::kStageBytes, R1::kParamBytes, CTAS);
+    if constexpr (S < 2) {
+        (void)N; (void)device; (void)p;
+        return kNoVectorPlan;
+    } else {
+        using R = Ring<S, CH, TPR * RPC, chunk_units<XT>(), chunk_units<GT>(), HAS_DS,
+                       chunk_units<WT>(), NPAR>;
+        static_assert(R::kBytes <= kMaxDynSmem, "ring too large");
+        p->kernel = reinterpret_cast<const void *>(
+            &norm_bwd_pipe_kernel<OP, TPR, RPC, CH, S, HAS_DS, CTAS, XT, WT, GT>);
+        p->threads = TPR * RPC;
+        p->smem = R::kBytes;
+        p->rows_per_cta = RPC;
+        return persistent_grid(p, N, device);
+    }
+}
+
+// Vector backward for activations XT, parameters WT and cotangents GT; SHORT selects the
+// short tables.
+template <int OP, int XT, int WT, int GT, bool HAS_DS, bool SHORT>
+cudaError_t bwd_plan_vec(int64_t N, int D, int device, LaunchPlan *p) {
+#define MT_TRY(maxd, tpr, rpc, ch, st, ctas) \
+    if (D <= maxd) return bwd_pipe_shape<OP, XT, WT, GT, tpr, rpc, ch, st, HAS_DS, ctas>(N, device, p);
+    if constexpr (XT == kF32 && WT == kF32 && GT == kF32 && OP == kLayer) {
+        MT_BWD_PIPE_SHAPES_F32_LAYER(MT_TRY)
+    } else if constexpr (XT == kF32 && WT == kF32 && GT == kF32) {
+        MT_BWD_PIPE_SHAPES_F32(MT_TRY)
+    } else if constexpr (SHORT && OP == kLayer) {
+        MT_BWD_PIPE_SHAPES_LAYER_SHORT(MT_TRY)
+    } else if constexpr (SHORT) {
+        MT_BWD_PIPE_SHAPES_RMS_SHORT(MT_TRY)
+    } else if constexpr (OP == kLayer) {
+        MT_BWD_PIPE_SHAPES_LAYER(MT_TRY)
+    } else {
+        MT_BWD_PIPE_SHAPES_RMS(MT_TRY)
+    }
+#undef MT_TRY
+    return kNoVectorPlan;
+}
+
+// ------------------------------------------------------------ entry points ---
+// The dtype combinations the vector kernels cover for activations XT: parameters and
+// cotangents each of the activation type or fp32 (all three matching: the full tables;
+// otherwise the short ones). All-fp32 uses the full forward tables and its own backward
+// table (an fp32 row takes twice the ring). Anything else returns kNoVectorPlan.
+// Each (op, XT) pair is instantiated in its own translation unit (ops_<op>_<type>.cu),
+// so the kernels compile in parallel.
+
+template <int OP, int XT>
+cudaError_t fwd_plan_for(int64_t N, int D, int wdt, LaunchPlan *p) {
+    if constexpr (XT == kF32) {
+        return (wdt == kF32) ? fwd_plan_vec<OP, kF32, kF32, false>(N, D, p) : kNoVectorPlan;
+    } else {
+        if (wdt == XT) return fwd_plan_vec<OP, XT, XT, false>(N, D, p);
+        if (wdt == kF32) return fwd_plan_vec<OP, XT, kF32, true>(N, D, p);
+        return kNoVectorPlan;
+    }
+}
+
+template <int OP, int XT, int WT, int GT>
+cudaError_t bwd_plan_ds(int64_t N, int D, bool has_ds, int device, LaunchPlan *p) {
+    constexpr bool SHORT = !(WT == XT && GT == XT) || XT == kF32;
+    if constexpr (OP == kAddRms) {
+        if (has_ds) return bwd_plan_vec<OP, XT, WT, GT, true, SHORT>(N, D, device, p);
+    }
+    return bwd_plan_vec<OP, XT, WT, GT, false, SHORT>(N, D, device, p);
+}
+
+template <int OP, int XT>
+cudaError_t bwd_plan_for(int64_t N, int D, int wdt, int gdt, bool has_ds, int device,
+                         LaunchPlan *p) {
+    if constexpr (XT == kF32) {
+        if (wdt != kF32 || gdt != kF32) return kNoVectorPlan;
+        return bwd_plan_ds<OP, kF32, kF32, kF32>(N, D, has_ds, device, p);
+    } else {
+        const bool w32 = (wdt == kF32), g32 = (gdt == kF32);
+        if ((!w32 && wdt != XT) || (!g32 && gdt != XT)) return kNoVectorPlan;
+        if (!w32 && !g32) return bwd_plan_ds<OP, XT, XT, XT>(N, D, has_ds, device, p);
+        if (!w32 && g32) return bwd_plan_ds<OP, XT, XT, kF32>(N, D, has_ds, device, p);
+        if (w32 && !g32) return bwd_plan_ds<OP, XT, kF32, XT>(N, D, has_ds, device, p);
+        return bwd_plan_ds<OP, XT, kF32, kF32>(N, D, has_ds, device, p);
+    }
+}
+
+#define MT_EXTERN_PLANS(OP, XT)                                                            \
+    extern template cudaError_t fwd_plan_for<OP, XT>(int64_t, int, int, LaunchPlan *);     \
+    extern template cudaError_t bwd_plan_for<OP, XT>(int64_t, int, int, int, bool, int,    \
+                                                     LaunchPlan *);
+#define MT_INSTANTIATE_PLANS(OP, XT)                                               \
+    template cudaError_t fwd_plan_for<OP, XT>(int64_t, int, int, LaunchPlan *);    \
+    template cudaError_t bwd_plan_for<OP, XT>(int64_t, int, int, int, bool, int,   \
+                                              LaunchPlan *);
+
+#define MT_ALL_PLANS(M) \
+    M(kRms, kF16) M(kRms, kBF16) M(kRms, kF32) \
+    M(kLayer, kF16) M(kLayer, kBF16) M(kLayer, kF32) \
+    M(kAddRms, kF16) M(kAddRms, kBF16) M(kAddRms, kF32)
+#ifndef MT_PLANS_TU
+MT_ALL_PLANS(MT_EXTERN_PLANS)
+#endif
+
+// Scalar plans (ops_scalar.cu).
+cudaError_t fwd_plan_scalar_op(int op, int64_t N, int D, LaunchPlan *p);
+cudaError_t bwd_plan_scalar_op(int op, int64_t N, int D, bool has_ds, int device, LaunchPlan *p);
 
 }  // namespace mt

@@ -1,0 +1,8 @@
+// ops_rms_bf16.cu -- RMSNorm vector kernels with bf16 activations (every parameter
+// and cotangent type the plans cover), one translation unit so they compile in parallel.
+#define MT_PLANS_TU
+#include "launch.cuh"
+
+namespace mt {
+MT_INSTANTIATE_PLANS(kRms, kBF16)
+}  // namespace mt

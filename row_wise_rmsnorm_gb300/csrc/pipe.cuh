@@ -43,37 +43,43 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
-// Shared-memory ring: [STAGES][NARR][CH][THREADS] x 16 bytes, then NPAR parameter
-// arrays in the same per-thread layout. Consecutive threads own consecutive 16-byte
-// words, so every ring access is bank-conflict free.
-template <int STAGES, int NARR, int CH, int THREADS, int NPAR>
+// Shared-memory ring. Per stage and thread: CH chunks of X (UX 16-byte units each), of
+// dY (UG units) and, with HAS_DS, of dS (UG units); after the STAGES stages, NPAR
+// parameter slots of CH chunks of gamma (UW units). Unit u of a thread's chunk sits
+// THREADS units after unit u-1, and consecutive threads own consecutive 16-byte words,
+// so every ring access is bank-conflict free. Array ids: 0 = X, 1 = dY, 2 = dS.
+template <int STAGES, int CH, int THREADS, int UX, int UG, bool HAS_DS, int UW, int NPAR>
 struct Ring {
-    static constexpr size_t kBytes = (size_t)(STAGES * NARR + NPAR) * CH * THREADS * 16;
+    static constexpr int kStageUnits = CH * (UX + UG * (HAS_DS ? 2 : 1));
+    static constexpr size_t kStageBytes = (size_t)kStageUnits * THREADS * 16;
+    static constexpr size_t kParamBytes = (size_t)NPAR * CH * UW * THREADS * 16;
+    static constexpr size_t kBytes = STAGES * kStageBytes + kParamBytes;
     __device__ static __forceinline__ int index(int slot, int arr, int k, int tid) {
-        return ((slot * NARR + arr) * CH + k) * THREADS + tid;
+        const int base = (arr == 0) ? k * UX : (arr == 1) ? CH * UX + k * UG : CH * (UX + UG) + k * UG;
+        return (slot * kStageUnits + base) * THREADS + tid;
     }
-    __device__ static __forceinline__ int param(int p, int k, int tid) {
-        return ((STAGES * NARR + p) * CH + k) * THREADS + tid;
+    __device__ static __forceinline__ int param(int k, int tid) {
+        return (STAGES * kStageUnits + k * UW) * THREADS + tid;
     }
 };
 
-// Copy this thread's chunks of a parameter vector into its ring parameter slots.
-template <class R, int CH, int TPR>
-__device__ __forceinline__ void stage_param(uint4 *ring, int p, const __half *src, int D, int t,
-                                            int tid) {
+// Copy one 8-element chunk of type DT (chunk_units<DT>() 16-byte units) from global
+// memory into ring units dst, dst + THREADS, ...
+template <int DT, int THREADS>
+__device__ __forceinline__ void cp_chunk(uint4 *dst, const void *src) {
+#pragma unroll
+    for (int u = 0; u < chunk_units<DT>(); ++u)
+        cp_async16(smem_addr(dst + u * THREADS), static_cast<const char *>(src) + 16 * u);
+}
+
+// Copy this thread's chunks of the parameter vector into its ring parameter slots.
+template <class R, int WT, int CH, int TPR, int THREADS>
+__device__ __forceinline__ void stage_param(uint4 *ring, const void *src, int D, int t, int tid) {
 #pragma unroll
     for (int k = 0; k < CH; ++k) {
         const int col = (k * TPR + t) * 8;
-        if (col < D) cp_async16(smem_addr(&ring[R::param(p, k, tid)]), src + col);
+        if (col < D) cp_chunk<WT, THREADS>(&ring[R::param(k, tid)], as<WT>(src) + col);
     }
-}
-
-// This thread's chunk k of a parameter vector as fp32 pairs (0 past D).
-template <int CH, int TPR>
-__device__ __forceinline__ void load_param_pairs(const __half *p, int k, int t, int D,
-                                                 float2 (&f)[4]) {
-    const int col = (k * TPR + t) * 8;
-    unpack8x2(col < D ? __ldg(reinterpret_cast<const uint4 *>(p + col)) : make_uint4(0, 0, 0, 0), f);
 }
 
 // Iterations every row group of this CTA runs (uniform across the CTA).
@@ -86,16 +92,18 @@ __device__ __forceinline__ int cta_iterations(int64_t N, int rpc) {
 // ---------------------------------------------------------------- backward ---
 // Dynamic shared memory: the ring (and gamma when CH > 2); after the row loop the ring
 // is reused for the fixed-order combine of the CTA's row groups (NV x D floats).
-// Compiled for CTAS resident CTAs per SM (it caps the registers per thread).
-template <int OP, int TPR, int RPC, int CH, int STAGES, bool HAS_DS, int CTAS>
+// Compiled for CTAS resident CTAs per SM (it caps the registers per thread). X (or S) and
+// dX are of type XT, gamma of type WT, dY and dS of type GT.
+template <int OP, int TPR, int RPC, int CH, int STAGES, bool HAS_DS, int CTAS, int XT, int WT,
+          int GT>
 __global__ void __launch_bounds__(TPR * RPC, CTAS)
 norm_bwd_pipe_kernel(const BwdArgs a) {
     constexpr int THREADS = TPR * RPC;
     constexpr int WPR = TPR / 32;
     constexpr int NV = (OP == kLayer) ? 2 : 1;
-    constexpr int NARR = HAS_DS ? 3 : 2;
     constexpr bool KEEP = CH <= 2;
-    using R = Ring<STAGES, NARR, CH, THREADS, KEEP ? 0 : 1>;
+    using R = Ring<STAGES, CH, THREADS, chunk_units<XT>(), chunk_units<GT>(), HAS_DS,
+                   chunk_units<WT>(), KEEP ? 0 : 1>;
     static_assert(TPR % 32 == 0 && THREADS <= 1024, "bad launch shape");
     __shared__ float red[2 * RPC * WPR * NV];
     extern __shared__ __align__(16) uint4 ring[];
@@ -113,9 +121,12 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
     float2 gam[KEEP ? CH : 1][4];
     if constexpr (KEEP) {
 #pragma unroll
-        for (int k = 0; k < CH; ++k) load_param_pairs<CH, TPR>(a.gamma, k, t, D, gam[k]);
+        for (int k = 0; k < CH; ++k) {
+            const int col = (k * TPR + t) * 8;
+            ld_chunk<WT, kReadOnly>(as<WT>(a.gamma) + col, col < D, gam[k]);
+        }
     } else {
-        stage_param<R, CH, TPR>(ring, 0, a.gamma, D, t, tid);
+        stage_param<R, WT, CH, TPR, THREADS>(ring, a.gamma, D, t, tid);
     }
     cp_async_commit();
 
@@ -138,10 +149,10 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
             for (int k = 0; k < CH; ++k) {
                 const int col = (k * TPR + t) * 8;
                 if (col < D) {
-                    cp_async16(smem_addr(&ring[R::index(slot, 0, k, tid)]), a.X + off + col);
-                    cp_async16(smem_addr(&ring[R::index(slot, 1, k, tid)]), a.dY + off + col);
+                    cp_chunk<XT, THREADS>(&ring[R::index(slot, 0, k, tid)], as<XT>(a.X) + off + col);
+                    cp_chunk<GT, THREADS>(&ring[R::index(slot, 1, k, tid)], as<GT>(a.dY) + off + col);
                     if constexpr (HAS_DS)
-                        cp_async16(smem_addr(&ring[R::index(slot, 2, k, tid)]), a.dS + off + col);
+                        cp_chunk<GT, THREADS>(&ring[R::index(slot, 2, k, tid)], as<GT>(a.dS) + off + col);
                 }
             }
         }
@@ -176,8 +187,8 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
 
         // chunk k's centred x (LayerNorm: x - mean) and dY as fp32 pairs
         auto load_xd = [&](int k, float2 (&xk)[4], float2 (&dk)[4]) {
-            unpack8x2(ring[R::index(slot, 0, k, tid)], xk);
-            unpack8x2(ring[R::index(slot, 1, k, tid)], dk);
+            unpack_chunk<XT>(&ring[R::index(slot, 0, k, tid)], THREADS, xk);
+            unpack_chunk<GT>(&ring[R::index(slot, 1, k, tid)], THREADS, dk);
             if constexpr (OP == kLayer) {
 #pragma unroll
                 for (int p = 0; p < 4; ++p) xk[p] = __fadd2_rn(xk[p], nmu);
@@ -203,7 +214,7 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
                 for (int p = 0; p < 4; ++p) { xs[k][p] = xk[p]; ds[k][p] = dk[p]; g[p] = gam[k][p]; }
             } else {
                 if (v) {
-                    unpack8x2(ring[R::param(0, k, tid)], g);
+                    unpack_chunk<WT>(&ring[R::param(k, tid)], THREADS, g);
                 } else {
 #pragma unroll
                     for (int p = 0; p < 4; ++p) g[p] = make_float2(0.f, 0.f);
@@ -239,10 +250,10 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
                 for (int p = 0; p < 4; ++p) { xk[p] = xs[k][p]; dk[p] = ds[k][p]; g[p] = gam[k][p]; }
             } else {
                 load_xd(k, xk, dk);
-                unpack8x2(ring[R::param(0, k, tid)], g);
+                unpack_chunk<WT>(&ring[R::param(k, tid)], THREADS, g);
             }
             float2 sk[4];
-            if constexpr (HAS_DS) unpack8x2(ring[R::index(slot, 2, k, tid)], sk);
+            if constexpr (HAS_DS) unpack_chunk<GT>(&ring[R::index(slot, 2, k, tid)], THREADS, sk);
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
                 const float2 xh = __fmul2_rn(xk[p], r2);
@@ -254,7 +265,7 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
                 accg[k][p] = __ffma2_rn(dk[p], xh, accg[k][p]);
                 if constexpr (OP == kLayer) accb[k][p] = __fadd2_rn(accb[k][p], dk[p]);
             }
-            __stcs(reinterpret_cast<uint4 *>(a.dX + off + col), pack8x2(o));
+            st_chunk<XT>(as<XT>(a.dX) + off + col, o);
         }
     }
     cp_async_wait<0>();

@@ -42,7 +42,7 @@ def test_header_is_plain_c():
 
 def test_exports_every_declared_symbol(lib):
     decl = declared_functions()
-    assert len(decl) == 14
+    assert len(decl) == 16
     assert sorted(mt.EXPORTED) == decl
     out = subprocess.run(["nm", "-D", "--defined-only", mt.library_path()], capture_output=True,
                          text=True, check=True).stdout
@@ -116,6 +116,35 @@ def test_forward_validation_other_ops(lib):
     assert lib.mt_add_rmsnorm_forward(A, B, C, E, E, F, N, D, 1e-6, None) == INV  # S == Y
     assert lib.mt_add_rmsnorm_forward(A, B, C, B, E, F, N, D, 1e-6, None) == INV  # S == R
     assert lib.mt_add_rmsnorm_forward(A, B, C, E, F, G, N, 0, 1e-6, None) == INV
+
+
+def test_explicit_dtype_validation(lib):
+    """mt_norm_forward_ex / mt_norm_backward_ex: codes, required pointers by op, and
+    overlap checks sized by the storage type."""
+    N, D = 8, 64
+    F16, BF16, F32 = mt.MT_DTYPE_F16, mt.MT_DTYPE_BF16, mt.MT_DTYPE_F32
+    RMS, LN, ADD = mt.MT_OP_RMSNORM, mt.MT_OP_LAYERNORM, mt.MT_OP_ADD_RMSNORM
+    fwd, bwd = lib.mt_norm_forward_ex, lib.mt_norm_backward_ex
+    # unknown op or dtype code
+    assert fwd(5, F16, F16, A, None, B, None, None, C, None, E, N, D, 1e-5, None) == INV
+    assert fwd(RMS, 3, F16, A, None, B, None, None, C, None, E, N, D, 1e-5, None) == INV
+    assert fwd(RMS, F16, -1, A, None, B, None, None, C, None, E, N, D, 1e-5, None) == INV
+    assert bwd(RMS, F16, F16, 9, A, B, C, None, None, E, F, G, None, N, D, None, 0, None) == INV
+    # required pointers depend on the op; unused ones are ignored
+    assert fwd(LN, F32, F32, A, None, B, None, None, C, E, F, N, D, 1e-5, None) == INV  # beta
+    assert fwd(ADD, BF16, F32, A, None, B, None, E, C, None, F, N, D, 1e-5, None) == INV  # R
+    assert bwd(LN, BF16, BF16, F32, A, B, C, None, E, F, G, H, None, N, D, None, 0, None) == INV
+    # an fp32 activation spans 4 bytes per element: Y placed 2*N*D bytes after X overlaps
+    # X for fp32 (invalid) but not for fp16 (then only eps decides: 0 is invalid too,
+    # so use a valid eps and an invalid shape to stay away from CUDA)
+    half = 2 * N * D
+    assert fwd(RMS, F32, F32, A, None, B, None, None, A + half, None, E, N, D, 1e-5, None) == INV
+    assert fwd(RMS, F16, F16, A, None, B, None, None, A + half, None, E, N, 20000, 1e-5,
+               None) == UNS
+    # dY in fp32 overlapping dX placed right after an fp16-sized dY
+    assert bwd(RMS, F16, F16, F32, A, B, C, None, None, E, C + half, G, None, N, D, None, 0,
+               None) == INV
+    assert lib.mt_last_cuda_error() == 0  # nothing reached CUDA
 
 
 def test_workspace_size_validation(lib):

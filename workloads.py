@@ -6,8 +6,9 @@ seed and the draw order, plus the byte accounting used to express throughput.
 
 Every tensor is drawn from ONE seeded torch generator in the fixed order
 X, R, s_row, gamma, beta, dY, dS (absent entries are skipped), as fp32, then
-rounded to fp16 (round-to-nearest-even) before either side sees it. ``N(m, s)``
-means mean m and standard deviation s.
+rounded to its storage type (round-to-nearest-even; fp16 unless a call asks for
+bf16 or fp32 per role) before either side sees it. ``N(m, s)`` means mean m and
+standard deviation s.
 
 The five workloads (name: op, N x D, recipe):
   rmsnorm_17x257        RMSNorm, ragged width. X, dY ~ N(0,1); gamma = 1 + 0.1 N(0,1); eps 1e-6.
@@ -72,8 +73,11 @@ def make_generator(device, seed: int = 0) -> torch.Generator:
 
 def generate(op: str, N: int, D: int, *, device="cpu", seed: int = 0,
              x_kind: str = "normal", dy_std: float = 1.0, beta_std: float = 0.1,
-             with_ds: bool = True) -> dict[str, torch.Tensor]:
-    """Draw one op's inputs as fp16 tensors on ``device``.
+             with_ds: bool = True, x_dtype=torch.float16, w_dtype=torch.float16,
+             g_dtype=torch.float16) -> dict[str, torch.Tensor]:
+    """Draw one op's inputs on ``device``: X and R stored as ``x_dtype``, gamma and beta as
+    ``w_dtype``, dY and dS as ``g_dtype`` (fp16, bf16 or fp32; the draws do not depend on
+    the types).
 
     Returns a dict with X, gamma, dY and, by op: R and dS (fused add), beta (LayerNorm).
     ``with_ds=False`` leaves out dS for the fused op (the absent-cotangent case).
@@ -103,15 +107,15 @@ def generate(op: str, N: int, D: int, *, device="cpu", seed: int = 0,
     dY = normal((N, D), std=dy_std)
     dS = normal((N, D), std=dy_std) if (op == ADD_RMSNORM and with_ds) else None
 
-    out["X"] = X.half()
+    out["X"] = X.to(x_dtype)
     if R is not None:
-        out["R"] = R.half()
-    out["gamma"] = gamma.half()
+        out["R"] = R.to(x_dtype)
+    out["gamma"] = gamma.to(w_dtype)
     if beta is not None:
-        out["beta"] = beta.half()
-    out["dY"] = dY.half()
+        out["beta"] = beta.to(w_dtype)
+    out["dY"] = dY.to(g_dtype)
     if dS is not None:
-        out["dS"] = dS.half()
+        out["dS"] = dS.to(g_dtype)
     return out
 
 
@@ -123,22 +127,25 @@ def generate_workload(name: str, *, device="cpu", seed: int = 0, rows: int | Non
                     x_kind=w.x_kind, dy_std=w.dy_std, beta_std=w.beta_std, with_ds=with_ds)
 
 
-def compulsory_bytes(op: str, direction: str, N: int, D: int, with_ds: bool = True) -> int:
-    """Bytes that any implementation must move (fp16 activations, fp32 stats/grads).
+def compulsory_bytes(op: str, direction: str, N: int, D: int, with_ds: bool = True,
+                     xb: int = 2, wb: int = 2, gb: int = 2) -> int:
+    """Bytes that any implementation must move: activations of xb bytes per element,
+    parameters of wb, cotangents of gb (2 for fp16/bf16, 4 for fp32), fp32 statistics and
+    parameter gradients. With the defaults (fp16 everywhere):
 
     forward:  RMSNorm 4ND + 4N + 2D; LayerNorm 4ND + 8N + 4D; fused add 8ND + 4N + 2D.
     backward: RMSNorm 6ND + 4N + 6D; LayerNorm 6ND + 8N + 10D; fused add 8ND + 4N + 6D
               (6ND + 4N + 6D when the residual-output cotangent is absent).
     Workspace traffic (dgamma/dbeta partials) is not compulsory.
     """
+    nd = N * D
     if direction == "forward":
-        return {RMSNORM: 4 * N * D + 4 * N + 2 * D,
-                LAYERNORM: 4 * N * D + 8 * N + 4 * D,
-                ADD_RMSNORM: 8 * N * D + 4 * N + 2 * D}[op]
+        return {RMSNORM: 2 * xb * nd + 4 * N + wb * D,
+                LAYERNORM: 2 * xb * nd + 8 * N + 2 * wb * D,
+                ADD_RMSNORM: 4 * xb * nd + 4 * N + wb * D}[op]
     if direction == "backward":
-        if op == ADD_RMSNORM and not with_ds:
-            return 6 * N * D + 4 * N + 6 * D
-        return {RMSNORM: 6 * N * D + 4 * N + 6 * D,
-                LAYERNORM: 6 * N * D + 8 * N + 10 * D,
-                ADD_RMSNORM: 8 * N * D + 4 * N + 6 * D}[op]
+        if op == ADD_RMSNORM:
+            return (2 * xb + (2 if with_ds else 1) * gb) * nd + 4 * N + (wb + 4) * D
+        return {RMSNORM: (2 * xb + gb) * nd + 4 * N + (wb + 4) * D,
+                LAYERNORM: (2 * xb + gb) * nd + 8 * N + (wb + 8) * D}[op]
     raise ValueError(direction)
