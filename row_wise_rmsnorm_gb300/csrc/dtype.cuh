@@ -21,12 +21,17 @@ namespace mt {
 enum DType : int { kF16 = 0, kBF16 = 1, kF32 = 2 };
 
 template <int DT> struct Store;
-template <> struct Store<kF16> { using T = __half; static constexpr int kUnits = 1; };
-template <> struct Store<kBF16> { using T = __nv_bfloat16; static constexpr int kUnits = 1; };
-template <> struct Store<kF32> { using T = float; static constexpr int kUnits = 2; };
+template <> struct Store<kF16> { using T = __half; };
+template <> struct Store<kBF16> { using T = __nv_bfloat16; };
+template <> struct Store<kF32> { using T = float; };
 
-// 16-byte units in one 8-element chunk of type DT.
-template <int DT> __host__ __device__ constexpr int chunk_units() { return Store<DT>::kUnits; }
+// A chunk is PPC fp32 pairs (2*PPC consecutive elements): PPC = 4 (8 elements) in
+// general, PPC = 2 (4 elements, one 16-byte unit) for kernels whose arrays are all fp32.
+// 16-byte units in one chunk of type DT:
+template <int DT, int PPC = 4>
+__host__ __device__ constexpr int chunk_units() {
+    return (int)sizeof(typename Store<DT>::T) * 2 * PPC / 16;
+}
 
 // ------------------------------------------------------------- conversions ---
 
@@ -67,17 +72,19 @@ __device__ __forceinline__ uint4 pack_unit(const float2 (&f)[4]) {
     return u;
 }
 
-// The chunk's 16-byte units (U = chunk_units<DT>(), read from `units`, `stride` apart)
-// as four fp32 pairs.
-template <int DT>
-__device__ __forceinline__ void unpack_chunk(const uint4 *units, int stride, float2 (&f)[4]) {
+// The chunk's 16-byte units (chunk_units<DT, PPC>() of them, read from `units`, `stride`
+// apart) as PPC fp32 pairs.
+template <int DT, int PPC = 4>
+__device__ __forceinline__ void unpack_chunk(const uint4 *units, int stride, float2 (&f)[PPC]) {
     if constexpr (DT == kF32) {
-        const uint4 a = units[0], b = units[stride];
-        f[0] = make_float2(__uint_as_float(a.x), __uint_as_float(a.y));
-        f[1] = make_float2(__uint_as_float(a.z), __uint_as_float(a.w));
-        f[2] = make_float2(__uint_as_float(b.x), __uint_as_float(b.y));
-        f[3] = make_float2(__uint_as_float(b.z), __uint_as_float(b.w));
+#pragma unroll
+        for (int u = 0; u < PPC / 2; ++u) {
+            const uint4 a = units[u * stride];
+            f[2 * u] = make_float2(__uint_as_float(a.x), __uint_as_float(a.y));
+            f[2 * u + 1] = make_float2(__uint_as_float(a.z), __uint_as_float(a.w));
+        }
     } else {
+        static_assert(PPC == 4, "a 2-byte chunk is one 16-byte unit of 8 elements");
         unpack_unit<DT>(units[0], f);
     }
 }
@@ -94,16 +101,18 @@ __device__ __forceinline__ uint4 ld_unit(const void *p) {
 }
 
 // Load a chunk as fp32 pairs; all zeros when !valid (nothing is read).
-template <int DT, int H>
-__device__ __forceinline__ void ld_chunk(const void *p, bool valid, float2 (&f)[4]) {
+template <int DT, int H, int PPC = 4>
+__device__ __forceinline__ void ld_chunk(const void *p, bool valid, float2 (&f)[PPC]) {
     if constexpr (DT == kF32) {
-        const uint4 a = valid ? ld_unit<H>(p) : make_uint4(0, 0, 0, 0);
-        const uint4 b = valid ? ld_unit<H>(static_cast<const float *>(p) + 4) : make_uint4(0, 0, 0, 0);
-        f[0] = make_float2(__uint_as_float(a.x), __uint_as_float(a.y));
-        f[1] = make_float2(__uint_as_float(a.z), __uint_as_float(a.w));
-        f[2] = make_float2(__uint_as_float(b.x), __uint_as_float(b.y));
-        f[3] = make_float2(__uint_as_float(b.z), __uint_as_float(b.w));
+#pragma unroll
+        for (int u = 0; u < PPC / 2; ++u) {
+            const uint4 a = valid ? ld_unit<H>(static_cast<const float *>(p) + 4 * u)
+                                  : make_uint4(0, 0, 0, 0);
+            f[2 * u] = make_float2(__uint_as_float(a.x), __uint_as_float(a.y));
+            f[2 * u + 1] = make_float2(__uint_as_float(a.z), __uint_as_float(a.w));
+        }
     } else {
+        static_assert(PPC == 4, "a 2-byte chunk is one 16-byte unit of 8 elements");
         unpack_unit<DT>(valid ? ld_unit<H>(p) : make_uint4(0, 0, 0, 0), f);
     }
 }
@@ -124,12 +133,15 @@ __device__ __forceinline__ void ld_param(const typename Store<DT>::T *p, float2 
 }
 
 // Round a chunk to DT (nearest even) and store it with streaming (evict-first) stores.
-template <int DT>
-__device__ __forceinline__ void st_chunk(void *p, const float2 (&f)[4]) {
+template <int DT, int PPC = 4>
+__device__ __forceinline__ void st_chunk(void *p, const float2 (&f)[PPC]) {
     if constexpr (DT == kF32) {
-        __stcs(reinterpret_cast<float4 *>(p), make_float4(f[0].x, f[0].y, f[1].x, f[1].y));
-        __stcs(reinterpret_cast<float4 *>(p) + 1, make_float4(f[2].x, f[2].y, f[3].x, f[3].y));
+#pragma unroll
+        for (int u = 0; u < PPC / 2; ++u)
+            __stcs(reinterpret_cast<float4 *>(p) + u,
+                   make_float4(f[2 * u].x, f[2 * u].y, f[2 * u + 1].x, f[2 * u + 1].y));
     } else {
+        static_assert(PPC == 4, "a 2-byte chunk is one 16-byte unit of 8 elements");
         __stcs(reinterpret_cast<uint4 *>(p), pack_unit<DT>(f));
     }
 }

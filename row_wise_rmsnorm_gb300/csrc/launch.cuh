@@ -119,11 +119,13 @@ namespace mt {
 #endif
 // All-fp32 backward: an fp32 chunk takes two ring units per array, so these shapes keep
 // 2-3 ring stages; 16384-wide fp32 rows (128 KB per stage) take the scalar kernel.
+#ifndef MT_BWD_PIPE_SHAPES_F32
 #define MT_BWD_PIPE_SHAPES_F32(X)   \
     X(1024, 128, 4, 1, 8, 2)        \
     X(2048, 256, 2, 1, 8, 2)        \
     X(4096, 512, 1, 1, 4, 1)        \
     X(8192, 512, 1, 2, 3, 1)
+#endif
 #define MT_BWD_PIPE_SHAPES_F32_LAYER(X) \
     X(1024, 128, 1, 1, 6, 6)            \
     X(2048, 256, 1, 1, 6, 3)            \
@@ -264,15 +266,14 @@ template <int OP, int XT, int WT, int GT, int TPR, int RPC, int CH, int STAGES, 
           int CTAS>
 cudaError_t bwd_pipe_shape(int64_t N, int device, LaunchPlan *p) {
     constexpr int NPAR = (CH <= 2) ? 0 : 1;
-    using R1 = Ring<1, CH, TPR * RPC, chunk_units<XT>(), chunk_units<GT>(), HAS_DS,
-                    chunk_units<WT>(), NPAR>;
+    using G = PipeGeom<CH, XT, WT, GT>;
+    using R1 = Ring<1, G::CK, TPR * RPC, G::UX, G::UG, HAS_DS, G::UW, NPAR>;
     constexpr int S = pipe_stages(STAGES, R1::kStageBytes, R1::kParamBytes, CTAS);
     if constexpr (S < 2) {
         (void)N; (void)device; (void)p;
         return kNoVectorPlan;
     } else {
-        using R = Ring<S, CH, TPR * RPC, chunk_units<XT>(), chunk_units<GT>(), HAS_DS,
-                       chunk_units<WT>(), NPAR>;
+        using R = Ring<S, G::CK, TPR * RPC, G::UX, G::UG, HAS_DS, G::UW, NPAR>;
         static_assert(R::kBytes <= kMaxDynSmem, "ring too large");
         p->kernel = reinterpret_cast<const void *>(
             &norm_bwd_pipe_kernel<OP, TPR, RPC, CH, S, HAS_DS, CTAS, XT, WT, GT>);

@@ -8,10 +8,11 @@
 // (STAGES x streamed arrays x row slice), not by registers.
 //
 // Ownership. Row assignment is static: CTA b runs row slots b*RPC + j*G*RPC
-// (G = gridDim.x, j = 0, 1, ...), row group rg taking slot + rg. Thread t of a row
-// group owns chunks k = 0..CH-1 at columns (k*TPR + t)*8 .. +7 of every row it touches;
-// its dgamma/dbeta sums stay in fp32 registers across all its rows, and per-row
-// statistics (rstd, mean) are prefetched into registers two rows ahead.
+// (G = gridDim.x, j = 0, 1, ...), row group rg taking slot + rg. Thread t of a row group
+// owns chunks k of EPC consecutive elements at columns (k*TPR + t)*EPC of every row it
+// touches (EPC = 8, or 4 when every array is fp32; see PipeGeom); its dgamma/dbeta sums
+// stay in fp32 registers across all its rows, and per-row statistics (rstd, mean) are
+// prefetched into registers two rows ahead.
 //
 // Arithmetic. Blackwell executes fp32 pairs in one instruction (__ffma2_rn,
 // __fmul2_rn, __fadd2_rn); the element math runs on float2 pairs, each lane rounded
@@ -63,22 +64,36 @@ struct Ring {
     }
 };
 
-// Copy one 8-element chunk of type DT (chunk_units<DT>() 16-byte units) from global
-// memory into ring units dst, dst + THREADS, ...
-template <int DT, int THREADS>
+// Copy one chunk of type DT (chunk_units<DT, PPC>() 16-byte units) from global memory
+// into ring units dst, dst + THREADS, ...
+template <int DT, int PPC, int THREADS>
 __device__ __forceinline__ void cp_chunk(uint4 *dst, const void *src) {
 #pragma unroll
-    for (int u = 0; u < chunk_units<DT>(); ++u)
+    for (int u = 0; u < chunk_units<DT, PPC>(); ++u)
         cp_async16(smem_addr(dst + u * THREADS), static_cast<const char *>(src) + 16 * u);
 }
 
+// Chunk geometry of a backward kernel. CH in the shape tables counts 8-element chunks.
+// When every array is fp32 the kernel works in 4-element chunks (PPC = 2 pairs, CK = 2 CH
+// of them), so each copy instruction of a warp covers 512 contiguous bytes; otherwise a
+// chunk is 8 elements (PPC = 4, CK = CH) and an fp32 array's chunk takes two units.
+template <int CH, int XT, int WT, int GT>
+struct PipeGeom {
+    static constexpr int PPC = (XT == kF32 && WT == kF32 && GT == kF32) ? 2 : 4;
+    static constexpr int EPC = 2 * PPC;      // elements per chunk
+    static constexpr int CK = CH * 4 / PPC;  // chunks per thread
+    static constexpr int UX = chunk_units<XT, PPC>();
+    static constexpr int UG = chunk_units<GT, PPC>();
+    static constexpr int UW = chunk_units<WT, PPC>();
+};
+
 // Copy this thread's chunks of the parameter vector into its ring parameter slots.
-template <class R, int WT, int CH, int TPR, int THREADS>
+template <class R, int WT, int PPC, int CK, int TPR, int THREADS>
 __device__ __forceinline__ void stage_param(uint4 *ring, const void *src, int D, int t, int tid) {
 #pragma unroll
-    for (int k = 0; k < CH; ++k) {
-        const int col = (k * TPR + t) * 8;
-        if (col < D) cp_chunk<WT, THREADS>(&ring[R::param(k, tid)], as<WT>(src) + col);
+    for (int k = 0; k < CK; ++k) {
+        const int col = (k * TPR + t) * 2 * PPC;
+        if (col < D) cp_chunk<WT, PPC, THREADS>(&ring[R::param(k, tid)], as<WT>(src) + col);
     }
 }
 
@@ -102,8 +117,9 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
     constexpr int WPR = TPR / 32;
     constexpr int NV = (OP == kLayer) ? 2 : 1;
     constexpr bool KEEP = CH <= 2;
-    using R = Ring<STAGES, CH, THREADS, chunk_units<XT>(), chunk_units<GT>(), HAS_DS,
-                   chunk_units<WT>(), KEEP ? 0 : 1>;
+    using G = PipeGeom<CH, XT, WT, GT>;
+    constexpr int PPC = G::PPC, EPC = G::EPC, CK = G::CK;
+    using R = Ring<STAGES, CK, THREADS, G::UX, G::UG, HAS_DS, G::UW, KEEP ? 0 : 1>;
     static_assert(TPR % 32 == 0 && THREADS <= 1024, "bad launch shape");
     __shared__ float red[2 * RPC * WPR * NV];
     extern __shared__ __align__(16) uint4 ring[];
@@ -118,26 +134,26 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
     const int64_t first = (int64_t)blockIdx.x * RPC + rg;
     const int iters = cta_iterations(a.N, RPC);
 
-    float2 gam[KEEP ? CH : 1][4];
+    float2 gam[KEEP ? CK : 1][PPC];
     if constexpr (KEEP) {
 #pragma unroll
-        for (int k = 0; k < CH; ++k) {
-            const int col = (k * TPR + t) * 8;
-            ld_chunk<WT, kReadOnly>(as<WT>(a.gamma) + col, col < D, gam[k]);
+        for (int k = 0; k < CK; ++k) {
+            const int col = (k * TPR + t) * EPC;
+            ld_chunk<WT, kReadOnly, PPC>(as<WT>(a.gamma) + col, col < D, gam[k]);
         }
     } else {
-        stage_param<R, WT, CH, TPR, THREADS>(ring, a.gamma, D, t, tid);
+        stage_param<R, WT, PPC, CK, TPR, THREADS>(ring, a.gamma, D, t, tid);
     }
     cp_async_commit();
 
-    float2 accg[CH][4];
-    float2 accb[CH][(OP == kLayer) ? 4 : 1];
+    float2 accg[CK][PPC];
+    float2 accb[CK][(OP == kLayer) ? PPC : 1];
 #pragma unroll
-    for (int k = 0; k < CH; ++k) {
+    for (int k = 0; k < CK; ++k) {
 #pragma unroll
-        for (int p = 0; p < 4; ++p) accg[k][p] = make_float2(0.f, 0.f);
+        for (int p = 0; p < PPC; ++p) accg[k][p] = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int p = 0; p < ((OP == kLayer) ? 4 : 1); ++p) accb[k][p] = make_float2(0.f, 0.f);
+        for (int p = 0; p < ((OP == kLayer) ? PPC : 1); ++p) accb[k][p] = make_float2(0.f, 0.f);
     }
 
     auto issue = [&](int j) {
@@ -146,13 +162,13 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
             const int slot = j % STAGES;
             const int64_t off = row * (int64_t)D;
 #pragma unroll
-            for (int k = 0; k < CH; ++k) {
-                const int col = (k * TPR + t) * 8;
+            for (int k = 0; k < CK; ++k) {
+                const int col = (k * TPR + t) * EPC;
                 if (col < D) {
-                    cp_chunk<XT, THREADS>(&ring[R::index(slot, 0, k, tid)], as<XT>(a.X) + off + col);
-                    cp_chunk<GT, THREADS>(&ring[R::index(slot, 1, k, tid)], as<GT>(a.dY) + off + col);
+                    cp_chunk<XT, PPC, THREADS>(&ring[R::index(slot, 0, k, tid)], as<XT>(a.X) + off + col);
+                    cp_chunk<GT, PPC, THREADS>(&ring[R::index(slot, 1, k, tid)], as<GT>(a.dY) + off + col);
                     if constexpr (HAS_DS)
-                        cp_chunk<GT, THREADS>(&ring[R::index(slot, 2, k, tid)], as<GT>(a.dS) + off + col);
+                        cp_chunk<GT, PPC, THREADS>(&ring[R::index(slot, 2, k, tid)], as<GT>(a.dS) + off + col);
                 }
             }
         }
@@ -186,42 +202,42 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
         const float2 nmu = make_float2(-mu, -mu);
 
         // chunk k's centred x (LayerNorm: x - mean) and dY as fp32 pairs
-        auto load_xd = [&](int k, float2 (&xk)[4], float2 (&dk)[4]) {
-            unpack_chunk<XT>(&ring[R::index(slot, 0, k, tid)], THREADS, xk);
-            unpack_chunk<GT>(&ring[R::index(slot, 1, k, tid)], THREADS, dk);
+        auto load_xd = [&](int k, float2 (&xk)[PPC], float2 (&dk)[PPC]) {
+            unpack_chunk<XT, PPC>(&ring[R::index(slot, 0, k, tid)], THREADS, xk);
+            unpack_chunk<GT, PPC>(&ring[R::index(slot, 1, k, tid)], THREADS, dk);
             if constexpr (OP == kLayer) {
 #pragma unroll
-                for (int p = 0; p < 4; ++p) xk[p] = __fadd2_rn(xk[p], nmu);
+                for (int p = 0; p < PPC; ++p) xk[p] = __fadd2_rn(xk[p], nmu);
             }
         };
-        float2 xs[KEEP ? CH : 1][4], ds[KEEP ? CH : 1][4];
+        float2 xs[KEEP ? CK : 1][PPC], ds[KEEP ? CK : 1][PPC];
 
         // pass 1: sum_j g*(x - mean) and, for LayerNorm, sum_j g   (g = dY*gamma);
         // rstd is applied after the reduction: sum_j g*xhat = rstd * sum_j g*(x - mean)
         float2 v0 = make_float2(0.f, 0.f), v1 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int k = 0; k < CH; ++k) {
-            const bool v = ok && (k * TPR + t) * 8 < D;
-            float2 xk[4], dk[4], g[4];
+        for (int k = 0; k < CK; ++k) {
+            const bool v = ok && (k * TPR + t) * EPC < D;
+            float2 xk[PPC], dk[PPC], g[PPC];
             if (v) {
                 load_xd(k, xk, dk);
             } else {
 #pragma unroll
-                for (int p = 0; p < 4; ++p) xk[p] = dk[p] = make_float2(0.f, 0.f);
+                for (int p = 0; p < PPC; ++p) xk[p] = dk[p] = make_float2(0.f, 0.f);
             }
             if constexpr (KEEP) {
 #pragma unroll
-                for (int p = 0; p < 4; ++p) { xs[k][p] = xk[p]; ds[k][p] = dk[p]; g[p] = gam[k][p]; }
+                for (int p = 0; p < PPC; ++p) { xs[k][p] = xk[p]; ds[k][p] = dk[p]; g[p] = gam[k][p]; }
             } else {
                 if (v) {
-                    unpack_chunk<WT>(&ring[R::param(k, tid)], THREADS, g);
+                    unpack_chunk<WT, PPC>(&ring[R::param(k, tid)], THREADS, g);
                 } else {
 #pragma unroll
-                    for (int p = 0; p < 4; ++p) g[p] = make_float2(0.f, 0.f);
+                    for (int p = 0; p < PPC; ++p) g[p] = make_float2(0.f, 0.f);
                 }
             }
 #pragma unroll
-            for (int p = 0; p < 4; ++p) {
+            for (int p = 0; p < PPC; ++p) {
                 const float2 gg = __fmul2_rn(dk[p], g[p]);
                 v0 = __ffma2_rn(gg, xk[p], v0);
                 if constexpr (OP == kLayer) v1 = __fadd2_rn(v1, gg);
@@ -241,21 +257,21 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
         const float2 k2 = make_float2(-r * c, -r * c);
         const float2 ra2 = make_float2(-r * am, -r * am);
 #pragma unroll
-        for (int k = 0; k < CH; ++k) {
-            const int col = (k * TPR + t) * 8;
+        for (int k = 0; k < CK; ++k) {
+            const int col = (k * TPR + t) * EPC;
             if (col >= D) continue;
-            float2 xk[4], dk[4], g[4], o[4];
+            float2 xk[PPC], dk[PPC], g[PPC], o[PPC];
             if constexpr (KEEP) {
 #pragma unroll
-                for (int p = 0; p < 4; ++p) { xk[p] = xs[k][p]; dk[p] = ds[k][p]; g[p] = gam[k][p]; }
+                for (int p = 0; p < PPC; ++p) { xk[p] = xs[k][p]; dk[p] = ds[k][p]; g[p] = gam[k][p]; }
             } else {
                 load_xd(k, xk, dk);
-                unpack_chunk<WT>(&ring[R::param(k, tid)], THREADS, g);
+                unpack_chunk<WT, PPC>(&ring[R::param(k, tid)], THREADS, g);
             }
-            float2 sk[4];
-            if constexpr (HAS_DS) unpack_chunk<GT>(&ring[R::index(slot, 2, k, tid)], THREADS, sk);
+            float2 sk[PPC];
+            if constexpr (HAS_DS) unpack_chunk<GT, PPC>(&ring[R::index(slot, 2, k, tid)], THREADS, sk);
 #pragma unroll
-            for (int p = 0; p < 4; ++p) {
+            for (int p = 0; p < PPC; ++p) {
                 const float2 xh = __fmul2_rn(xk[p], r2);
                 const float2 gg = __fmul2_rn(dk[p], g[p]);
                 const float2 base = (OP == kLayer) ? __ffma2_rn(gg, r2, ra2) : __fmul2_rn(gg, r2);
@@ -265,7 +281,7 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
                 accg[k][p] = __ffma2_rn(dk[p], xh, accg[k][p]);
                 if constexpr (OP == kLayer) accb[k][p] = __fadd2_rn(accb[k][p], dk[p]);
             }
-            st_chunk<XT>(as<XT>(a.dX) + off + col, o);
+            st_chunk<XT, PPC>(as<XT>(a.dX) + off + col, o);
         }
     }
     cp_async_wait<0>();
@@ -276,16 +292,20 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
     float *pb = (OP == kLayer) ? a.part_b + (size_t)blockIdx.x * D : nullptr;
     if constexpr (RPC == 1) {
 #pragma unroll
-        for (int k = 0; k < CH; ++k) {
-            const int col = (k * TPR + t) * 8;
+        for (int k = 0; k < CK; ++k) {
+            const int col = (k * TPR + t) * EPC;
             if (col >= D) continue;
             float4 *g4 = reinterpret_cast<float4 *>(pg + col);
-            g4[0] = make_float4(accg[k][0].x, accg[k][0].y, accg[k][1].x, accg[k][1].y);
-            g4[1] = make_float4(accg[k][2].x, accg[k][2].y, accg[k][3].x, accg[k][3].y);
+#pragma unroll
+            for (int q = 0; q < PPC / 2; ++q)
+                g4[q] = make_float4(accg[k][2 * q].x, accg[k][2 * q].y, accg[k][2 * q + 1].x,
+                                    accg[k][2 * q + 1].y);
             if constexpr (OP == kLayer) {
                 float4 *b4 = reinterpret_cast<float4 *>(pb + col);
-                b4[0] = make_float4(accb[k][0].x, accb[k][0].y, accb[k][1].x, accb[k][1].y);
-                b4[1] = make_float4(accb[k][2].x, accb[k][2].y, accb[k][3].x, accb[k][3].y);
+#pragma unroll
+                for (int q = 0; q < PPC / 2; ++q)
+                    b4[q] = make_float4(accb[k][2 * q].x, accb[k][2 * q].y, accb[k][2 * q + 1].x,
+                                        accb[k][2 * q + 1].y);
             }
         }
     } else {
@@ -295,11 +315,11 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
         for (int j = 0; j < RPC; ++j) {
             if (rg == j) {
 #pragma unroll
-                for (int k = 0; k < CH; ++k) {
-                    const int col = (k * TPR + t) * 8;
+                for (int k = 0; k < CK; ++k) {
+                    const int col = (k * TPR + t) * EPC;
                     if (col >= D) continue;
 #pragma unroll
-                    for (int p = 0; p < 4; ++p) {
+                    for (int p = 0; p < PPC; ++p) {
                         const int i = col / 2 + p;
                         const float2 sg = (j == 0) ? accg[k][p] : __fadd2_rn(cg2[i], accg[k][p]);
                         if (j == RPC - 1) reinterpret_cast<float2 *>(pg)[i] = sg; else cg2[i] = sg;
