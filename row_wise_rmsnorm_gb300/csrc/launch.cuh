@@ -91,14 +91,26 @@ namespace mt {
     X(8192, 512, 1, 16)         \
     X(16384, 512, 1, 32)
 
-// Pipelined persistent backward shapes for 16-byte-aligned rows, RMSNorm and the fused
-// op (the first table) and LayerNorm: X(max_D, TPR, RPC, CH, STAGES, CTAS). STAGES is the
+// Pipelined persistent backward shapes for 16-byte-aligned rows, per op (RMSNorm, the fused
+// op, LayerNorm): X(max_D, TPR, RPC, CH, STAGES, CTAS). STAGES is the
 // largest ring depth (pipe_stages() cuts it to fit shared memory); CTAS the resident CTAs
 // per SM the kernel is compiled for, which caps its registers per thread. The persistent
-// grid is the resident CTA count, one dgamma/dbeta partial row per CTA. LayerNorm keeps
-// two sums per thread and column, so its narrow shapes use single-row-group CTAs.
+// grid is the resident CTA count, one dgamma/dbeta partial row per CTA. From 1024 to
+// 4096 columns RMSNorm and LayerNorm run one 512-thread CTA per SM holding several row
+// groups of 16 elements per thread with a 3-deep ring (measured faster than two CTAs of
+// 8 elements per thread: fewer per-row instructions per byte).
 #ifndef MT_BWD_PIPE_SHAPES_RMS
 #define MT_BWD_PIPE_SHAPES_RMS(X)   \
+    X(256, 32, 16, 1, 8, 2)         \
+    X(512, 64, 8, 1, 8, 2)          \
+    X(1024, 64, 8, 2, 3, 1)         \
+    X(2048, 128, 4, 2, 3, 1)        \
+    X(4096, 256, 2, 2, 3, 1)        \
+    X(8192, 512, 1, 2, 3, 1)        \
+    X(16384, 512, 1, 4, 3, 1)
+#endif
+#ifndef MT_BWD_PIPE_SHAPES_FUSED
+#define MT_BWD_PIPE_SHAPES_FUSED(X) \
     X(256, 32, 16, 1, 8, 2)         \
     X(512, 64, 8, 1, 8, 2)          \
     X(1024, 128, 4, 1, 8, 2)        \
@@ -111,9 +123,9 @@ namespace mt {
 #define MT_BWD_PIPE_SHAPES_LAYER(X) \
     X(256, 32, 16, 1, 8, 1)         \
     X(512, 64, 1, 1, 8, 16)         \
-    X(1024, 128, 1, 1, 6, 6)        \
-    X(2048, 256, 1, 1, 6, 3)        \
-    X(4096, 512, 1, 1, 4, 2)        \
+    X(1024, 64, 8, 2, 3, 1)         \
+    X(2048, 128, 4, 2, 3, 1)        \
+    X(4096, 256, 2, 2, 3, 1)        \
     X(8192, 512, 1, 2, 3, 1)        \
     X(16384, 512, 1, 4, 3, 1)
 #endif
@@ -300,6 +312,8 @@ cudaError_t bwd_plan_vec(int64_t N, int D, int device, LaunchPlan *p) {
         MT_BWD_PIPE_SHAPES_RMS_SHORT(MT_TRY)
     } else if constexpr (OP == kLayer) {
         MT_BWD_PIPE_SHAPES_LAYER(MT_TRY)
+    } else if constexpr (OP == kAddRms) {
+        MT_BWD_PIPE_SHAPES_FUSED(MT_TRY)
     } else {
         MT_BWD_PIPE_SHAPES_RMS(MT_TRY)
     }
