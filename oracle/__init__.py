@@ -1,4 +1,5 @@
-"""fp64 CPU oracle for row-wise normalization -- TEST INFRASTRUCTURE ONLY.
+"""fp64 CPU oracle for row-wise normalization, row softmax and per-row cross-entropy --
+TEST INFRASTRUCTURE ONLY.
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg
 (``cpu_baseline`` and ``--impl reference``) may import this package. The CUDA
@@ -16,7 +17,11 @@ Sources for the formulas (page title, section):
     residual-add + RMSNorm (unrounded sum normalised; residual-output cotangent
     added to both input gradients), backward at the saved statistics.
   * tensorcore, "Training kernels", "RMSnorm -- Llama-style" (Math) and
-    "LayerNorm -- standard".
+    "LayerNorm -- standard"; "Softmax -- standalone, row-wise".
+  * meTile reduction and loss checklists: softmax / log-softmax with input
+    gradients; cross-entropy with ignore-index, none/sum/mean, label smoothing,
+    z-loss. "Metal subgroup LayerNorm and cross-entropy report", "Structural
+    repair exercised by cross-entropy": the per-row loss formula.
 
 Parity pins: tests/test_oracle_pins.py pins every function here against finite
 differences, closed forms, invariants, the worked LayerNorm example of the
@@ -60,9 +65,18 @@ def _declare(lib):
     lib.oracle_layernorm_backward.argtypes = [_dp] * 10 + [_i64, _i64]
     lib.oracle_add_rmsnorm_forward.argtypes = [_dp] * 6 + [_i64, _i64, ctypes.c_double]
     lib.oracle_add_rmsnorm_backward.argtypes = [_dp] * 8 + [_i64, _i64]
+    _lp = ctypes.POINTER(ctypes.c_int64)
+    lib.oracle_softmax_forward.argtypes = [_dp, _dp, _i64, _i64, ctypes.c_int]
+    lib.oracle_softmax_backward.argtypes = [_dp, _dp, _dp, _i64, _i64, ctypes.c_int]
+    lib.oracle_cross_entropy_forward.argtypes = [_dp, _lp, _i64, _i64, _i64, ctypes.c_double,
+                                                 ctypes.c_double, _dp, _dp]
+    lib.oracle_cross_entropy_backward.argtypes = [_dp, _lp, _dp, _dp, _i64, _i64, _i64,
+                                                  ctypes.c_double, ctypes.c_double, _dp]
     for name in ("oracle_rmsnorm_forward", "oracle_rmsnorm_backward",
                  "oracle_layernorm_forward", "oracle_layernorm_backward",
-                 "oracle_add_rmsnorm_forward", "oracle_add_rmsnorm_backward"):
+                 "oracle_add_rmsnorm_forward", "oracle_add_rmsnorm_backward",
+                 "oracle_softmax_forward", "oracle_softmax_backward",
+                 "oracle_cross_entropy_forward", "oracle_cross_entropy_backward"):
         getattr(lib, name).restype = None
     return lib
 
@@ -173,6 +187,86 @@ def add_rmsnorm_backward(S, gamma, dY, dS, rstd, lib=None):
                                     None if dS_arr is None else _p(dS_arr),
                                     _p(rstd), _p(dX), _p(dg), _p(dga), N, D)
     return dX, dg, dga
+
+
+# ------------------------------------------------ row softmax, cross-entropy ---
+
+def softmax_forward(X, log_softmax=False, lib=None):
+    """Row softmax (or log-softmax) of X [N, D] -> Y fp64. tensorcore "Training kernels",
+    "Softmax -- standalone, row-wise"; meTile softmax / log-softmax."""
+    lib = lib or load_library()
+    X = _f64(X)
+    N, D = _shape(X)
+    Y = np.empty((N, D))
+    lib.oracle_softmax_forward(_p(X), _p(Y), N, D, int(bool(log_softmax)))
+    return Y
+
+
+def softmax_backward(Y, dY, log_softmax=False, lib=None):
+    """Input gradient of the row softmax (log-softmax) from its output Y and dY."""
+    lib = lib or load_library()
+    Y, dY = _f64(Y), _f64(dY)
+    N, D = _shape(Y)
+    dX = np.empty((N, D))
+    lib.oracle_softmax_backward(_p(Y), _p(dY), _p(dX), N, D, int(bool(log_softmax)))
+    return dX
+
+
+def _targets(T) -> np.ndarray:
+    if hasattr(T, "detach"):
+        T = T.detach().cpu().numpy()
+    return np.ascontiguousarray(np.asarray(T, dtype=np.int64))
+
+
+def cross_entropy_forward(X, T, ignore_index=-100, label_smoothing=0.0, z_loss=0.0, lib=None):
+    """Per-row cross-entropy of logits X [N, D] with integer targets T [N] (meTile losses;
+    LuisaCompute report formula) -> (loss [N], lse [N]) fp64; ignored rows have loss 0."""
+    lib = lib or load_library()
+    X = _f64(X)
+    N, D = _shape(X)
+    T = _targets(T)
+    loss, lse = np.empty(N), np.empty(N)
+    lib.oracle_cross_entropy_forward(_p(X), T.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+                                     N, D, int(ignore_index), float(label_smoothing),
+                                     float(z_loss), _p(loss), _p(lse))
+    return loss, lse
+
+
+def cross_entropy_reduce(loss, T, ignore_index, reduction):
+    """The plain reductions: "none" -> loss [N]; "sum" -> sum; "mean" -> sum / number of
+    rows whose target is not ignore_index (0 if there is none). Returns (value, n_valid)."""
+    n_valid = float(np.sum(_targets(T) != ignore_index))
+    if reduction == "none":
+        return np.asarray(loss, dtype=np.float64), n_valid
+    total = float(np.sum(loss))
+    if reduction == "sum":
+        return total, n_valid
+    return (total / n_valid if n_valid > 0 else 0.0), n_valid
+
+
+def cross_entropy_row_grad(dloss, N, n_valid, reduction):
+    """Upstream gradient per row g_i: none -> dloss_i; sum -> dloss; mean -> dloss / n_valid
+    (0 if no row is valid)."""
+    if reduction == "none":
+        return _f64(dloss).reshape(N)
+    d = float(np.asarray(dloss, dtype=np.float64).reshape(-1)[0])
+    if reduction == "sum":
+        return np.full(N, d)
+    return np.full(N, d / n_valid if n_valid > 0 else 0.0)
+
+
+def cross_entropy_backward(X, T, lse, g, ignore_index=-100, label_smoothing=0.0, z_loss=0.0,
+                           lib=None):
+    """Gradient of sum_i g_i * loss_i with respect to the logits, at the saved lse."""
+    lib = lib or load_library()
+    X, lse, g = _f64(X), _f64(lse), _f64(g)
+    N, D = _shape(X)
+    T = _targets(T)
+    dX = np.empty((N, D))
+    lib.oracle_cross_entropy_backward(_p(X), T.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+                                      _p(lse), _p(g), N, D, int(ignore_index),
+                                      float(label_smoothing), float(z_loss), _p(dX))
+    return dX
 
 
 BF16_MAX = (2.0 - 2.0 ** -7) * 2.0 ** 127  # largest finite bfloat16

@@ -212,3 +212,120 @@ void oracle_add_rmsnorm_backward(const double *S, const double *gamma,
             dX[i] += dS[i];
     }
 }
+
+/* ========================================================================= */
+/* Row softmax and per-row cross-entropy (the next row-reduction family).
+ *
+ * Sources (page title, section):
+ *   [tc]      "Training kernels", section "Softmax -- standalone, row-wise":
+ *             numerically stable row softmax, subtract the row maximum,
+ *             exponentiate, sum, divide; backward from the output Y and dY.
+ *   [meTile]  "Kernel coverage and training scope", "Reduction and attention
+ *             parity checklist" (softmax and log-softmax with input gradients)
+ *             and "Loss parity checklist" / the native training_losses notes
+ *             (cross-entropy row loss and logit gradients with ignore-index,
+ *             none/sum/mean reduction, uniform label smoothing, squared
+ *             log-sum-exp z-loss; mean over valid rows; maxima and
+ *             log-denominators saved for the backward).
+ *   [report]  "Metal subgroup LayerNorm and cross-entropy report", section
+ *             "Structural repair exercised by cross-entropy": peak = max,
+ *             total = sum exp(logit - peak), loss = log(total) + peak - selected.
+ * The reductions over rows (sum, mean) are left to the caller.              */
+
+/* Softmax forward. [tc] Softmax; [meTile] softmax / log-softmax:
+ *   m_i = max_j x_ij,   s_i = sum_j exp(x_ij - m_i)
+ *   softmax:      y_ij = exp(x_ij - m_i) / s_i
+ *   log-softmax:  y_ij = x_ij - m_i - log(s_i)                                 */
+void oracle_softmax_forward(const double *X, double *Y, int64_t N, int64_t D,
+                            int log_softmax)
+{
+    for (int64_t i = 0; i < N; ++i) {
+        const double *x = X + i * D;
+        double m = x[0];
+        for (int64_t j = 1; j < D; ++j)
+            if (x[j] > m) m = x[j];
+        double s = 0.0;
+        for (int64_t j = 0; j < D; ++j)
+            s += exp(x[j] - m);
+        for (int64_t j = 0; j < D; ++j)
+            Y[i * D + j] = log_softmax ? (x[j] - m - log(s)) : (exp(x[j] - m) / s);
+    }
+}
+
+/* Softmax backward from the forward output, for L = sum_ij dY_ij * y_ij:
+ *   softmax:      dX_ij = y_ij * (dY_ij - sum_k dY_ik * y_ik)
+ *   log-softmax:  dX_ij = dY_ij - exp(y_ij) * sum_k dY_ik                       */
+void oracle_softmax_backward(const double *Y, const double *dY, double *dX,
+                             int64_t N, int64_t D, int log_softmax)
+{
+    for (int64_t i = 0; i < N; ++i) {
+        const double *y = Y + i * D;
+        const double *dy = dY + i * D;
+        double dot = 0.0;
+        for (int64_t j = 0; j < D; ++j)
+            dot += log_softmax ? dy[j] : dy[j] * y[j];
+        for (int64_t j = 0; j < D; ++j)
+            dX[i * D + j] = log_softmax ? (dy[j] - exp(y[j]) * dot) : (y[j] * (dy[j] - dot));
+    }
+}
+
+/* Cross-entropy forward per row. [meTile] losses; [report] formula. Target
+ * distribution with uniform label smoothing eps over the D classes:
+ *   q_ij = (1 - eps) * [j == t_i] + eps / D
+ *   lse_i  = m_i + log(sum_j exp(x_ij - m_i))            (saved for backward)
+ *   loss_i = sum_j q_ij * (lse_i - x_ij) + z * lse_i^2
+ *          = lse_i - (1 - eps) * x_i,t_i - (eps / D) * sum_j x_ij + z * lse_i^2
+ * A row whose target equals ignore_index has loss 0 (lse still written). A
+ * target outside [0, D) that is not ignore_index gives a NaN loss.            */
+void oracle_cross_entropy_forward(const double *X, const int64_t *T, int64_t N,
+                                  int64_t D, int64_t ignore_index, double eps,
+                                  double z, double *loss, double *lse)
+{
+    for (int64_t i = 0; i < N; ++i) {
+        const double *x = X + i * D;
+        double m = x[0];
+        for (int64_t j = 1; j < D; ++j)
+            if (x[j] > m) m = x[j];
+        double s = 0.0, sum_x = 0.0;
+        for (int64_t j = 0; j < D; ++j) {
+            s += exp(x[j] - m);
+            sum_x += x[j];
+        }
+        double l = m + log(s);
+        lse[i] = l;
+        int64_t t = T[i];
+        if (t == ignore_index) {
+            loss[i] = 0.0;
+        } else if (t < 0 || t >= D) {
+            loss[i] = NAN;
+        } else {
+            loss[i] = l - (1.0 - eps) * x[t] - (eps / (double)D) * sum_x + z * l * l;
+        }
+    }
+}
+
+/* Cross-entropy backward: derivative of loss_i above, times the row's upstream
+ * gradient g_i (the caller forms g from the reduction: none -> dloss_i,
+ * sum -> dloss, mean -> dloss / number of valid rows), at the saved lse:
+ *   p_ij   = exp(x_ij - lse_i)
+ *   dX_ij  = g_i * ((1 + 2 z lse_i) * p_ij - q_ij)
+ * Ignored rows get 0.                                                          */
+void oracle_cross_entropy_backward(const double *X, const int64_t *T,
+                                   const double *lse, const double *g,
+                                   int64_t N, int64_t D, int64_t ignore_index,
+                                   double eps, double z, double *dX)
+{
+    for (int64_t i = 0; i < N; ++i) {
+        const double *x = X + i * D;
+        int64_t t = T[i];
+        for (int64_t j = 0; j < D; ++j) {
+            if (t == ignore_index) {
+                dX[i * D + j] = 0.0;
+                continue;
+            }
+            double p = exp(x[j] - lse[i]);
+            double q = (1.0 - eps) * (j == t ? 1.0 : 0.0) + eps / (double)D;
+            dX[i * D + j] = g[i] * ((1.0 + 2.0 * z * lse[i]) * p - q);
+        }
+    }
+}

@@ -322,6 +322,124 @@ def pin_special_cases(lib):
     _close(rstd, np.full(3, 1e3), 0, 1e-12, "rms zero row rstd")
 
 
+# --------------------------------------------------------------------------- #
+# Row softmax and per-row cross-entropy.
+# --------------------------------------------------------------------------- #
+def pin_fd_softmax(lib):
+    """Finite differences of L = sum dY * Y for softmax and log-softmax (4 x 8)."""
+    rng = np.random.default_rng(21)
+    X = 3.0 * rng.standard_normal((4, 8))
+    dY = rng.standard_normal((4, 8))
+    for log in (False, True):
+        def loss():
+            return float(np.sum(dY * oracle.softmax_forward(X, log, lib=lib)))
+        Y = oracle.softmax_forward(X, log, lib=lib)
+        dX = oracle.softmax_backward(Y, dY, log, lib=lib)
+        _close(dX, _fd(loss, X), 1e-7, 1e-6, f"softmax(log={log}) dX vs finite differences")
+
+
+def pin_fd_cross_entropy(lib):
+    """Finite differences of L = sum_i g_i loss_i w.r.t. the logits, with label smoothing,
+    z-loss and an ignored row (5 x 8)."""
+    rng = np.random.default_rng(22)
+    X = 2.0 * rng.standard_normal((5, 8))
+    T = np.array([3, 0, -100, 7, 5])
+    g = rng.standard_normal(5)
+    for eps, z in ((0.0, 0.0), (0.1, 0.0), (0.0, 1e-2), (0.2, 3e-2)):
+        def loss():
+            l, _ = oracle.cross_entropy_forward(X, T, -100, eps, z, lib=lib)
+            return float(np.sum(g * l))
+        _, lse = oracle.cross_entropy_forward(X, T, -100, eps, z, lib=lib)
+        dX = oracle.cross_entropy_backward(X, T, lse, g, -100, eps, z, lib=lib)
+        _close(dX, _fd(loss, X), 1e-7, 1e-6, f"ce(eps={eps}, z={z}) dX vs finite differences")
+
+
+def pin_torch_softmax_ce(lib):
+    """torch's fp64 CPU softmax / log_softmax / cross_entropy (label smoothing, ignore
+    index, none/sum/mean) with autograd; the z-loss term z * logsumexp^2 added in torch."""
+    import torch
+    import torch.nn.functional as F
+
+    rng = np.random.default_rng(23)
+    N, D = 17, 257
+    X = 4.0 * rng.standard_normal((N, D))
+    dY = rng.standard_normal((N, D))
+    tight = dict(atol=1e-12, rtol=1e-10)
+    for log in (False, True):
+        x = torch.tensor(X, requires_grad=True)
+        y = F.log_softmax(x, dim=1) if log else F.softmax(x, dim=1)
+        (y * torch.tensor(dY)).sum().backward()
+        Y = oracle.softmax_forward(X, log, lib=lib)
+        _close(Y, y.detach().numpy(), what=f"softmax(log={log}) vs torch", **tight)
+        _close(oracle.softmax_backward(Y, dY, log, lib=lib), x.grad.numpy(),
+               what=f"softmax(log={log}) dX vs torch autograd", **tight)
+    T = rng.integers(0, D, N)
+    T[[2, 9]] = -100
+    for eps, z, red in ((0.0, 0.0, "none"), (0.1, 0.0, "sum"), (0.05, 1e-3, "mean"),
+                        (0.0, 1e-2, "mean")):
+        x = torch.tensor(X, requires_grad=True)
+        t = torch.tensor(T)
+        ce = F.cross_entropy(x, t, reduction="none", ignore_index=-100, label_smoothing=eps)
+        lse_t = torch.logsumexp(x, dim=1)
+        rows = ce + z * lse_t ** 2 * (t != -100)
+        valid = float((t != -100).sum())
+        tot = rows if red == "none" else (rows.sum() if red == "sum" else rows.sum() / valid)
+        up = rng.standard_normal(N) if red == "none" else np.array([1.7])
+        (tot * torch.tensor(up if red == "none" else up[0])).sum().backward()
+        loss, lse = oracle.cross_entropy_forward(X, T, -100, eps, z, lib=lib)
+        val, nv = oracle.cross_entropy_reduce(loss, T, -100, red)
+        _close(lse, lse_t.detach().numpy(), what="ce lse vs torch logsumexp", **tight)
+        _close(val, tot.detach().numpy(), what=f"ce {red} loss vs torch", **tight)
+        g = oracle.cross_entropy_row_grad(up, N, nv, red)
+        dX = oracle.cross_entropy_backward(X, T, lse, g, -100, eps, z, lib=lib)
+        _close(dX, x.grad.numpy(), what=f"ce {red} dX vs torch autograd", **tight)
+
+
+def pin_softmax_ce_closed_forms(lib):
+    """Uniform logits: softmax = 1/D, log-softmax = -log D, loss = log D + z log^2 D (any
+    smoothing), gradient = (1 + 2 z log D)/D - q. Rows sum to one; a shifted row gives the
+    same softmax; the gradient rows sum to 2 z lse g; the report's peak/total/selected
+    formula on a row; an out-of-range target gives NaN and an ignored row 0."""
+    D = 10
+    X = np.full((2, D), 0.37)
+    Y = oracle.softmax_forward(X, False, lib=lib)
+    _close(Y, np.full((2, D), 1.0 / D), 0, 1e-15, "softmax of a constant row")
+    _close(oracle.softmax_forward(X, True, lib=lib), np.full((2, D), -np.log(D)), 1e-15, 1e-15,
+           "log-softmax of a constant row")
+    z, eps = 0.02, 0.3
+    loss, lse = oracle.cross_entropy_forward(X, [4, 0], -100, eps, z, lib=lib)
+    ld = np.log(D) + 0.37
+    _close(loss, np.full(2, np.log(D) + z * ld * ld), 1e-14, 1e-14, "ce of a constant row")
+    g = np.array([1.0, -2.0])
+    dX = oracle.cross_entropy_backward(X, [4, 0], lse, g, -100, eps, z, lib=lib)
+    q = np.full((2, D), eps / D)
+    q[0, 4] += 1 - eps
+    q[1, 0] += 1 - eps
+    want = g[:, None] * ((1 + 2 * z * ld) / D - q)
+    _close(dX, want, 1e-14, 1e-13, "ce gradient of a constant row")
+    rng = np.random.default_rng(24)
+    X = 5.0 * rng.standard_normal((6, 33))
+    Y = oracle.softmax_forward(X, False, lib=lib)
+    _close(Y.sum(axis=1), np.ones(6), 1e-14, 0, "softmax rows sum to one")
+    _close(oracle.softmax_forward(X + 11.5, False, lib=lib), Y, 1e-15, 1e-12, "softmax shift")
+    _close(oracle.softmax_backward(Y, rng.standard_normal((6, 33)), False, lib=lib).sum(axis=1),
+           np.zeros(6), 1e-14, 0, "softmax dX rows sum to zero")
+    T = rng.integers(0, 33, 6)
+    loss, lse = oracle.cross_entropy_forward(X, T, -100, 0.0, 0.0, lib=lib)
+    peak = X.max(axis=1)
+    total = np.exp(X - peak[:, None]).sum(axis=1)
+    _close(loss, np.log(total) + peak - X[np.arange(6), T], 1e-13, 1e-13,
+           "report formula log(total) + peak - selected")
+    g = rng.standard_normal(6)
+    dX = oracle.cross_entropy_backward(X, T, lse, g, -100, 0.1, 0.05, lib=lib)
+    _, lse2 = oracle.cross_entropy_forward(X, T, -100, 0.1, 0.05, lib=lib)
+    _close(dX.sum(axis=1), 2 * 0.05 * lse2 * g, 1e-12, 1e-12, "ce gradient rows sum")
+    loss, _ = oracle.cross_entropy_forward(X[:2], [-100, 40], -100, 0.0, 0.0, lib=lib)
+    assert loss[0] == 0.0 and np.isnan(loss[1]), "ignored row 0, out-of-range target NaN"
+    val, nv = oracle.cross_entropy_reduce(np.zeros(3), [-100, -100, -100], -100, "mean")
+    assert val == 0.0 and nv == 0.0, "mean over no valid row is 0"
+
+
 ALL_PINS = [
     pin_fd_rmsnorm,
     pin_fd_layernorm,
@@ -332,4 +450,8 @@ ALL_PINS = [
     pin_worked_example,
     pin_shift_and_scale,
     pin_special_cases,
+    pin_fd_softmax,
+    pin_fd_cross_entropy,
+    pin_torch_softmax_ce,
+    pin_softmax_ce_closed_forms,
 ]

@@ -28,6 +28,17 @@ MUTATIONS = {
     "add_residual_dropped": ("S[i] = X[i] + R[i];", "S[i] = X[i];"),
     "add_ds_subtracted": ("dX[i] += dS[i];", "dX[i] -= dS[i];"),
     "add_ds_ignored": ("dX[i] += dS[i];", "dX[i] += 0.0 * dS[i];"),
+    "softmax_sum_without_max": ("        for (int64_t j = 0; j < D; ++j)\n            s += exp(x[j] - m);",
+                                "        for (int64_t j = 0; j < D; ++j)\n            s += exp(x[j]);"),
+    "softmax_bwd_sign": ("(y[j] * (dy[j] - dot))", "(y[j] * (dy[j] + dot))"),
+    "logsoftmax_bwd_missing_exp": ("(dy[j] - exp(y[j]) * dot)", "(dy[j] - y[j] * dot)"),
+    "logsoftmax_missing_log": ("(x[j] - m - log(s))", "(x[j] - m - s)"),
+    "ce_smoothing_dropped": ("- (eps / (double)D) * sum_x", "- 0.0 * sum_x"),
+    "ce_target_index": ("l - (1.0 - eps) * x[t]", "l - (1.0 - eps) * x[(t + 1) % D]"),
+    "ce_zloss_factor": ("(1.0 + 2.0 * z * lse[i])", "(1.0 + z * lse[i])"),
+    "ce_grad_sign": ("* p - q);", "* p + q);"),
+    "ce_ignored_row_not_zeroed": ("                dX[i * D + j] = 0.0;\n                continue;",
+                                  "                ;"),
 }
 
 
