@@ -212,6 +212,63 @@ class OpRunner:
                                           stream)
 
 
+class SoftmaxRunner:
+    """Row softmax forward + backward on synthetic N(0, 3^2) rows (same timing protocol)."""
+
+    def __init__(self, N, D, device, seed, dtype):
+        import torch
+        import row_wise_rmsnorm_gb300 as mt
+        self.mt, self.N, self.D = mt, N, D
+        g = torch.Generator(device=device)
+        g.manual_seed(seed)
+        self.x = (torch.randn((N, D), generator=g, device=device) * 3).to(dtype)
+        self.dy = torch.randn((N, D), generator=g, device=device).to(dtype)
+        self.y = torch.empty_like(self.x)
+        self.dx = torch.empty_like(self.x)
+        self.code = mt.dtype_code(dtype)
+        eb = self.x.element_size()
+        self.fwd_bytes = 2 * eb * N * D
+        self.bwd_bytes = 3 * eb * N * D
+
+    def forward(self, stream):
+        self.mt.mt_softmax_forward(self.code, self.x, self.y, self.N, self.D, 0, stream)
+
+    def backward(self, stream):
+        self.mt.mt_softmax_backward(self.code, self.y, self.dy, self.dx, self.N, self.D, 0, stream)
+
+
+class CrossEntropyRunner:
+    """Per-row cross-entropy (mean reduction, label smoothing 0.1, z-loss 1e-4) forward +
+    backward on synthetic N(0, 2^2) logits with uniform random targets."""
+
+    def __init__(self, N, D, device, seed, dtype):
+        import torch
+        import row_wise_rmsnorm_gb300 as mt
+        self.mt, self.N, self.D = mt, N, D
+        g = torch.Generator(device=device)
+        g.manual_seed(seed)
+        self.x = (torch.randn((N, D), generator=g, device=device) * 2).to(dtype)
+        self.t = torch.randint(0, D, (N,), generator=g, device=device, dtype=torch.int64)
+        f = dict(dtype=torch.float32, device=device)
+        self.rows, self.lse = torch.empty(N, **f), torch.empty(N, **f)
+        self.out, self.nv, self.dl = torch.empty(1, **f), torch.empty(1, **f), torch.ones(1, **f)
+        self.dx = torch.empty_like(self.x)
+        self.code = mt.dtype_code(dtype)
+        eb = self.x.element_size()
+        self.fwd_bytes = eb * N * D + 16 * N + 8     # logits, targets, loss and lse rows
+        self.bwd_bytes = 2 * eb * N * D + 12 * N     # logits, dlogits, targets, lse
+
+    def forward(self, stream):
+        self.mt.mt_cross_entropy_forward(self.code, self.x, self.t, self.N, self.D, -100, 0.1,
+                                         1e-4, self.mt.MT_REDUCTION_MEAN, self.rows, self.lse,
+                                         self.out, self.nv, stream)
+
+    def backward(self, stream):
+        self.mt.mt_cross_entropy_backward(self.code, self.x, self.t, self.lse, self.N, self.D, -100,
+                                          0.1, 1e-4, self.mt.MT_REDUCTION_MEAN, self.dl, self.nv,
+                                          self.dx, stream)
+
+
 def time_ops(sets, steps: int, warmup: int, stream):
     """CUDA-event times (ms) of `steps` back-to-back steps, each a forward on buffer set
     s % n and a backward on set (s + 1) % n: a backward never finds in L2 the rows its
@@ -483,6 +540,27 @@ def main(argv=None):
             del r2
             torch.cuda.empty_cache()
 
+    # The row softmax and the per-row cross-entropy (the next row-reduction family).
+    row_ops = {}
+    if not args.no_others and rank == 0:
+        for name, cls, N, D, tdt in (("softmax_16384x4096_f16", SoftmaxRunner, 16384, 4096,
+                                      torch.float16),
+                                     ("cross_entropy_4096x32768_bf16", CrossEntropyRunner, 4096,
+                                      32768, torch.bfloat16)):
+            r2 = [cls(N, D, device, i, tdt) for i in range(2)]
+            f2, b2, _ = time_ops(r2, max(50, args.steps // 10), args.warmup, stream)
+            fg = r2[0].fwd_bytes / (statistics.mean(f2) * 1e-3) / 1e9
+            bg = r2[0].bwd_bytes / (statistics.mean(b2) * 1e-3) / 1e9
+            row_ops[name] = {"forward_gbs": round(fg, 2), "backward_gbs": round(bg, 2),
+                             "forward_frac_of_measured": round(fg / peak, 4),
+                             "backward_frac_of_measured": round(bg / peak, 4),
+                             "forward_us": round(1e3 * statistics.mean(f2), 3),
+                             "backward_us": round(1e3 * statistics.mean(b2), 3),
+                             "compulsory_bytes": {"forward": r2[0].fwd_bytes,
+                                                  "backward": r2[0].bwd_bytes}}
+            del r2
+            torch.cuda.empty_cache()
+
     e2e = None
     if not args.no_e2e:
         e2e = e2e_run(args.workload, device, max(5, min(50, args.steps // 40)), 3, seed=rank)
@@ -532,6 +610,7 @@ def main(argv=None):
         "timed_region_wall_s": round(wall, 3),
         "other_workloads": others,
         "storage_types": {"workload": args.workload, **dtypes},
+        "row_ops": row_ops,
     }
     if rank == 0:
         print(json.dumps(line))

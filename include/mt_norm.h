@@ -5,6 +5,9 @@
  *   RMSNorm                       mt_rmsnorm_forward / mt_rmsnorm_backward
  *   LayerNorm                     mt_layernorm_forward / mt_layernorm_backward
  *   fused residual-add + RMSNorm  mt_add_rmsnorm_forward / mt_add_rmsnorm_backward
+ * with explicit storage types (mt_norm_forward_ex / mt_norm_backward_ex), and on the same
+ * row skeleton a row softmax / log-softmax (mt_softmax_*) and a per-row cross-entropy
+ * (mt_cross_entropy_*).
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -204,6 +207,65 @@ mt_status_t mt_norm_backward_ex(mt_norm_op_t op, mt_dtype_t x_dtype, mt_dtype_t 
                                 const float *rstd, void *dX, float *dgamma, float *dbeta,
                                 int64_t N, int64_t D, void *workspace, size_t workspace_bytes,
                                 mt_stream_t stream);
+
+/* ------------------------------------------------------------ row softmax ---
+ * [tc] "Softmax -- standalone, row-wise": numerically stable softmax of each row
+ * (subtract the row maximum, exponentiate, sum, divide); [meTile] reduction checklist:
+ * softmax and log-softmax with input gradients.
+ *   softmax:      Y_ij = exp(X_ij - m_i) / sum_k exp(X_ik - m_i),  m_i = max_k X_ik
+ *   log-softmax:  Y_ij = X_ij - m_i - log(sum_k exp(X_ik - m_i))
+ *   backward from the forward output Y and dY:
+ *     softmax:      dX_ij = Y_ij * (dY_ij - sum_k dY_ik * Y_ik)
+ *     log-softmax:  dX_ij = dY_ij - exp(Y_ij) * sum_k dY_ik
+ * X, Y, dY, dX are [N, D] of type `dtype`; log_softmax != 0 selects log-softmax.
+ * Bounds as for the normalizations (1 <= D <= MT_MAX_COLS). Errors: MT_ERR_INVALID_ARG
+ * for a NULL pointer, N or D < 1, an unknown dtype or an output overlapping an input.
+ * Arithmetic fp32; results rounded to `dtype`, nearest even.                       */
+mt_status_t mt_softmax_forward(mt_dtype_t dtype, const void *X, void *Y, int64_t N, int64_t D,
+                               int log_softmax, mt_stream_t stream);
+mt_status_t mt_softmax_backward(mt_dtype_t dtype, const void *Y, const void *dY, void *dX,
+                                int64_t N, int64_t D, int log_softmax, mt_stream_t stream);
+
+/* ---------------------------------------------------------- cross-entropy ---
+ * [meTile] loss checklist and training_losses notes: per-row cross-entropy of logits
+ * with integer class targets, ignore-index, none/sum/mean reduction (mean over the
+ * rows whose target is not ignore_index; 0 when there is none), uniform label
+ * smoothing and the squared log-sum-exp z-loss; maxima and log-denominators saved for
+ * the backward. ["Metal subgroup LayerNorm and cross-entropy report", "Structural
+ * repair exercised by cross-entropy"]: loss = log(total) + peak - selected.
+ *   lse_i  = log(sum_j exp(X_ij))                 (computed from the row maximum)
+ *   q_ij   = (1 - label_smoothing) [j == t_i] + label_smoothing / D
+ *   loss_i = lse_i - (1 - label_smoothing) X_i,t_i - (label_smoothing / D) sum_j X_ij
+ *            + z_loss * lse_i^2,      0 when t_i == ignore_index
+ *   backward: dX_ij = g_i * ((1 + 2 z_loss lse_i) exp(X_ij - lse_i) - q_ij),
+ *            g_i = dloss_i (NONE), dloss (SUM), dloss / n_valid (MEAN), 0 if ignored.
+ * logits X / dX: [N, D] of type `dtype`; targets: [N] int64 (device); loss_rows, lse:
+ * [N] fp32 (lse is saved for the backward and written for every row); loss_out and
+ * n_valid: one fp32 each, written for SUM/MEAN (may be NULL for NONE); the backward's
+ * dloss is [N] for NONE and one value otherwise, and n_valid (MEAN) is the forward's.
+ * A target outside [0, D) that is not ignore_index gives a NaN loss for its row.
+ * Bounds: 1 <= D <= MT_MAX_CE_COLS, 1 <= N <= 2^31 - 1; 0 <= label_smoothing <= 1,
+ * z_loss >= 0 (both finite), else MT_ERR_INVALID_ARG. The sum over rows runs in a
+ * fixed order, so every result is bitwise identical run to run.                     */
+#define MT_MAX_CE_COLS 262144
+
+typedef enum mt_reduction {
+    MT_REDUCTION_NONE = 0,
+    MT_REDUCTION_SUM = 1,
+    MT_REDUCTION_MEAN = 2
+} mt_reduction_t;
+
+mt_status_t mt_cross_entropy_forward(mt_dtype_t dtype, const void *logits,
+                                     const int64_t *targets, int64_t N, int64_t D,
+                                     int64_t ignore_index, float label_smoothing, float z_loss,
+                                     mt_reduction_t reduction, float *loss_rows, float *lse,
+                                     float *loss_out, float *n_valid, mt_stream_t stream);
+mt_status_t mt_cross_entropy_backward(mt_dtype_t dtype, const void *logits,
+                                      const int64_t *targets, const float *lse, int64_t N,
+                                      int64_t D, int64_t ignore_index, float label_smoothing,
+                                      float z_loss, mt_reduction_t reduction,
+                                      const float *dloss, const float *n_valid, void *dlogits,
+                                      mt_stream_t stream);
 
 /* ----------------------------------------------- backward without allocation ---
  * No counterpart on the pages: this entry point exists for callers that cannot

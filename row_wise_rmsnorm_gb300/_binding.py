@@ -25,6 +25,8 @@ LIB_PATH = _build.LIB
 MT_OK, MT_ERR_INVALID_ARG, MT_ERR_UNSUPPORTED, MT_ERR_CUDA = 0, 1, 2, 3
 MT_OP_RMSNORM, MT_OP_LAYERNORM, MT_OP_ADD_RMSNORM = 0, 1, 2
 MT_DTYPE_F16, MT_DTYPE_BF16, MT_DTYPE_F32 = 0, 1, 2
+MT_REDUCTION_NONE, MT_REDUCTION_SUM, MT_REDUCTION_MEAN = 0, 1, 2
+MT_MAX_CE_COLS = 262144
 MT_MAX_COLS = 16384
 
 # Every exported symbol of include/mt_norm.h.
@@ -33,6 +35,8 @@ EXPORTED = (
     "mt_layernorm_forward", "mt_layernorm_backward", "mt_layernorm_backward_ws",
     "mt_add_rmsnorm_forward", "mt_add_rmsnorm_backward", "mt_add_rmsnorm_backward_ws",
     "mt_norm_forward_ex", "mt_norm_backward_ex",
+    "mt_softmax_forward", "mt_softmax_backward",
+    "mt_cross_entropy_forward", "mt_cross_entropy_backward",
     "mt_rmsnorm_backward_noalloc",
     "mt_norm_backward_workspace_size", "mt_last_cuda_error", "mt_status_string",
     "mt_norm_version",
@@ -69,6 +73,12 @@ _SIGS = {
                            _P, _I64, _I64, _F, _P],
     "mt_norm_backward_ex": [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P, _P,
                             _P, _P, _P, _P, _P, _P, _I64, _I64, _P, _SZ, _P],
+    "mt_softmax_forward": [ctypes.c_int, _P, _P, _I64, _I64, ctypes.c_int, _P],
+    "mt_softmax_backward": [ctypes.c_int, _P, _P, _P, _I64, _I64, ctypes.c_int, _P],
+    "mt_cross_entropy_forward": [ctypes.c_int, _P, _P, _I64, _I64, _I64, _F, _F, ctypes.c_int,
+                                 _P, _P, _P, _P, _P],
+    "mt_cross_entropy_backward": [ctypes.c_int, _P, _P, _P, _I64, _I64, _I64, _F, _F,
+                                  ctypes.c_int, _P, _P, _P, _P],
     "mt_rmsnorm_backward_noalloc": [_P, _P, _P, _P, _P, _P, _I64, _I64, _P],
     "mt_norm_backward_workspace_size": [ctypes.c_int, _I64, _I64, ctypes.c_int,
                                         ctypes.POINTER(_SZ)],
@@ -195,6 +205,32 @@ def mt_norm_backward_ex(op, x_dtype, w_dtype, g_dtype, X, gamma, dY, dS, mean, r
                                       _ptr(dY), _ptr(dS), _ptr(mean), _ptr(rstd), _ptr(dX),
                                       _ptr(dgamma), _ptr(dbeta), N, D, _ptr(workspace),
                                       workspace_bytes, _stream(stream)), "mt_norm_backward_ex")
+
+
+def mt_softmax_forward(dtype, X, Y, N, D, log_softmax=0, stream=None):
+    _check(load().mt_softmax_forward(dtype, _ptr(X), _ptr(Y), N, D, int(log_softmax),
+                                     _stream(stream)), "mt_softmax_forward")
+
+
+def mt_softmax_backward(dtype, Y, dY, dX, N, D, log_softmax=0, stream=None):
+    _check(load().mt_softmax_backward(dtype, _ptr(Y), _ptr(dY), _ptr(dX), N, D, int(log_softmax),
+                                      _stream(stream)), "mt_softmax_backward")
+
+
+def mt_cross_entropy_forward(dtype, logits, targets, N, D, ignore_index, label_smoothing, z_loss,
+                             reduction, loss_rows, lse, loss_out, n_valid, stream=None):
+    _check(load().mt_cross_entropy_forward(dtype, _ptr(logits), _ptr(targets), N, D, ignore_index,
+                                           label_smoothing, z_loss, reduction, _ptr(loss_rows),
+                                           _ptr(lse), _ptr(loss_out), _ptr(n_valid),
+                                           _stream(stream)), "mt_cross_entropy_forward")
+
+
+def mt_cross_entropy_backward(dtype, logits, targets, lse, N, D, ignore_index, label_smoothing,
+                              z_loss, reduction, dloss, n_valid, dlogits, stream=None):
+    _check(load().mt_cross_entropy_backward(dtype, _ptr(logits), _ptr(targets), _ptr(lse), N, D,
+                                            ignore_index, label_smoothing, z_loss, reduction,
+                                            _ptr(dloss), _ptr(n_valid), _ptr(dlogits),
+                                            _stream(stream)), "mt_cross_entropy_backward")
 
 
 def mt_rmsnorm_backward_noalloc(X, gamma, dY, rstd, dX, dgamma, N, D, stream=None):
@@ -356,3 +392,51 @@ def norm_backward(op, x, gamma, dy, rstd, mean=None, ds=None):
     mt_norm_backward_ex(op, dtype_code(x.dtype), dtype_code(gamma.dtype), dtype_code(dy.dtype),
                         x, gamma, dy, ds, mean, rstd, dx, dgamma, dbeta, n, d, ws, nbytes)
     return (dx, dgamma, dbeta) if op == MT_OP_LAYERNORM else (dx, dgamma)
+
+
+# ------------------------------------------------ row softmax, cross-entropy ---
+
+_REDUCTIONS = {"none": MT_REDUCTION_NONE, "sum": MT_REDUCTION_SUM, "mean": MT_REDUCTION_MEAN}
+
+
+def softmax_forward(x, log_softmax=False):
+    """Row softmax (or log-softmax) of x [N, D]; the output takes x's type."""
+    n, d = x.shape
+    y = _new(x, (n, d), x.dtype)
+    mt_softmax_forward(dtype_code(x.dtype), x, y, n, d, log_softmax)
+    return y
+
+
+def softmax_backward(y, dy, log_softmax=False):
+    """Input gradient of the row softmax (log-softmax) from its output y and dy (same type)."""
+    n, d = y.shape
+    dx = _new(y, (n, d), y.dtype)
+    mt_softmax_backward(dtype_code(y.dtype), y, dy, dx, n, d, log_softmax)
+    return dx
+
+
+def cross_entropy_forward(logits, targets, ignore_index=-100, label_smoothing=0.0, z_loss=0.0,
+                          reduction="mean"):
+    """-> (loss, lse, n_valid): loss [N] fp32 for "none", else a 1-element fp32 tensor;
+    lse [N] fp32 (saved for the backward); n_valid a 1-element fp32 tensor (or None for
+    "none"). targets: int64 [N] on the device."""
+    import torch
+    n, d = logits.shape
+    rows = _new(logits, (n,), torch.float32)
+    lse = _new(logits, (n,), torch.float32)
+    red = _REDUCTIONS[reduction]
+    out = _new(logits, (1,), torch.float32) if red else None
+    nv = _new(logits, (1,), torch.float32) if red else None
+    mt_cross_entropy_forward(dtype_code(logits.dtype), logits, targets, n, d, ignore_index,
+                             label_smoothing, z_loss, red, rows, lse, out, nv)
+    return (rows if red == MT_REDUCTION_NONE else out), lse, nv
+
+
+def cross_entropy_backward(logits, targets, lse, dloss, n_valid=None, ignore_index=-100,
+                           label_smoothing=0.0, z_loss=0.0, reduction="mean"):
+    """Gradient of the reduced loss with respect to the logits (logits' type)."""
+    n, d = logits.shape
+    dx = _new(logits, (n, d), logits.dtype)
+    mt_cross_entropy_backward(dtype_code(logits.dtype), logits, targets, lse, n, d, ignore_index,
+                              label_smoothing, z_loss, _REDUCTIONS[reduction], dloss, n_valid, dx)
+    return dx

@@ -71,10 +71,12 @@ std::mutex g_cache_mu;
 std::map<int, int> g_sm_count;
 std::map<std::tuple<const void *, int, size_t, int>, int> g_occupancy;
 
+}  // namespace
+
 // Every launch carries the programmatic-stream-serialization attribute (see pdl_enter()
 // in kernels.cuh).
-mt_status_t launch(const LaunchPlan &p, void *arg, cudaStream_t stream) {
-    if (p.kernel == nullptr || p.grid < 1) return cuda_fail(cudaErrorInvalidConfiguration);
+cudaError_t launch_pdl(const LaunchPlan &p, void *arg, cudaStream_t stream) {
+    if (p.kernel == nullptr || p.grid < 1) return cudaErrorInvalidConfiguration;
     void *args[] = {arg};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.grid);
@@ -86,10 +88,17 @@ mt_status_t launch(const LaunchPlan &p, void *arg, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelExC(&cfg, p.kernel, args);
+    return cudaLaunchKernelExC(&cfg, p.kernel, args);
+}
+
+namespace {
+
+mt_status_t launch(const LaunchPlan &p, void *arg, cudaStream_t stream) {
+    const cudaError_t e = launch_pdl(p, arg, stream);
     if (e != cudaSuccess) return cuda_fail(e);
     return MT_OK;
 }
+
 
 // The vector plan for (op, activation type), or kNoVectorPlan.
 cudaError_t plan_forward_vec(int op, int xdt, int64_t N, int D, int wdt, LaunchPlan *p) {

@@ -175,6 +175,8 @@ struct LaunchPlan {
 
 // Host helpers defined in api.cu (cached per device; thread-safe).
 void record_cuda_error(cudaError_t e);  // what mt_last_cuda_error() reports on this thread
+// Launch p.kernel(*arg) on `stream` with the programmatic-stream-serialization attribute.
+cudaError_t launch_pdl(const LaunchPlan &p, void *arg, cudaStream_t stream);
 cudaError_t device_sm_count(int device, int *sms);
 cudaError_t cached_occupancy(const void *kernel, int threads, size_t smem, int device,
                              int *blocks_per_sm);

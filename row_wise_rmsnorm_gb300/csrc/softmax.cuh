@@ -1,0 +1,412 @@
+// softmax.cuh -- row softmax / log-softmax (forward, backward) and per-row cross-entropy
+// (forward, backward) on the row skeleton of the normalization kernels.
+//
+// Sources (page title, section): tensorcore "Training kernels", "Softmax -- standalone,
+// row-wise" (subtract the row maximum, exponentiate, sum, divide; backward from Y and
+// dY); meTile "Kernel coverage and training scope", the reduction and loss checklists
+// (softmax / log-softmax with input gradients; cross-entropy with integer targets,
+// ignore-index, none/sum/mean reduction, uniform label smoothing, squared log-sum-exp
+// z-loss, maxima and log-denominators saved for the backward); "Metal subgroup
+// LayerNorm and cross-entropy report", "Structural repair exercised by cross-entropy"
+// (loss = log(total) + peak - selected).
+//
+//  * Softmax keeps the row in registers like the normalization forward (two row
+//    reductions: the maximum, then the sum of exp(x - max)); its backward keeps Y and dY
+//    (one reduction: sum dY*Y, or sum dY for log-softmax). Neither has parameters, so
+//    neither has partials: one row group per row, non-persistent.
+//  * Cross-entropy rows may be far wider than registers hold (vocabularies), so the
+//    forward streams each row once, keeping a running maximum and a running sum of
+//    exp(x - running max) (rescaled when the maximum grows), the sum of x (for label
+//    smoothing), and reads the target logit directly; the per-thread states combine
+//    with the same rescaling in a fixed order. The backward streams the row again and
+//    needs no reduction: dX = g * ((1 + 2 z lse) exp(x - lse) - q). A last small kernel
+//    sums the per-row losses in a fixed order for the sum/mean reductions.
+//  * exp is __expf (the hardware exp2 path): relative error about 2^-21 for the ranges
+//    met here, well inside every output tolerance; log is logf, once per row.
+#pragma once
+
+#include "kernels.cuh"
+
+namespace mt {
+
+struct SoftmaxArgs {
+    const void *X;   // forward: X; backward: the forward output Y
+    const void *dY;  // backward only
+    void *Y;         // forward: Y; backward: dX
+    int64_t N;
+    int D;
+    int xdt, gdt;    // storage types (scalar fallback): X/Y/dX, and dY
+};
+
+struct CeArgs {
+    const void *X;             // logits [N, D]
+    const int64_t *T;          // targets [N]
+    float *loss;               // forward: per-row loss [N]
+    float *lse;                // forward: written; backward: read [N]
+    const float *dloss;        // backward: [N] (none) or [1] (sum, mean)
+    const float *n_valid;      // backward, mean: the forward's count of valid rows
+    void *dX;                  // backward: [N, D]
+    int64_t N;
+    int D;
+    int64_t ignore_index;
+    float eps;                 // label smoothing
+    float z;                   // z-loss coefficient
+    int reduction;             // 0 none, 1 sum, 2 mean
+    int xdt;                   // storage type of X and dX (scalar fallback)
+};
+
+// Maximum over the TPR threads of one row group (same pattern as row_sum, fmaxf).
+template <int TPR, int RPC>
+__device__ __forceinline__ float row_max(float v, float *red, int buf, int rg, int wir, int lane) {
+    constexpr int WPR = TPR / 32;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if constexpr (WPR > 1) {
+        float *s = red + (buf * RPC + rg) * WPR;
+        if (lane == 0) s[wir] = v;
+        row_group_sync<TPR, RPC, false>(rg);
+        v = lane < WPR ? s[lane] : -INFINITY;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    }
+    return v;
+}
+
+// ------------------------------------------------------------------ softmax ---
+
+// Forward for aligned rows (D % 8 == 0): one row group of TPR threads per row, thread t
+// owning CH chunks of 8 at columns (k*TPR + t)*8; the row stays in fp32 pairs.
+template <int TPR, int RPC, int CH, bool LOG, int XT>
+__global__ void __launch_bounds__(TPR * RPC)
+softmax_fwd_vec8_kernel(const SoftmaxArgs a) {
+    pdl_enter();
+    constexpr int WPR = TPR / 32;
+    __shared__ float red[2 * RPC * WPR];
+    const int tid = threadIdx.x;
+    const int rg = tid / TPR, t = tid % TPR, wir = t / 32, lane = tid % 32;
+    const int D = a.D;
+    const int64_t row = (int64_t)blockIdx.x * RPC + rg;
+    const bool ok = row < a.N;
+    if (WPR == 1 && !ok) return;
+    const int64_t off = (ok ? row : 0) * (int64_t)D;
+
+    float2 x[CH][4];
+    float m = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < CH; ++k) {
+        const int col = (k * TPR + t) * 8;
+        const bool v = ok && col < D;
+        ld_chunk<XT, kStream>(as<XT>(a.X) + off + col, v, x[k]);
+        if (v) {
+#pragma unroll
+            for (int p = 0; p < 4; ++p) m = fmaxf(m, fmaxf(x[k][p].x, x[k][p].y));
+        }
+    }
+    m = row_max<TPR, RPC>(m, red, 0, rg, wir, lane);
+    float s[1] = {0.f};
+#pragma unroll
+    for (int k = 0; k < CH; ++k) {
+        if (!(ok && (k * TPR + t) * 8 < D)) continue;
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            x[k][p] = make_float2(x[k][p].x - m, x[k][p].y - m);
+            if constexpr (!LOG) x[k][p] = make_float2(__expf(x[k][p].x), __expf(x[k][p].y));
+            s[0] += LOG ? (__expf(x[k][p].x) + __expf(x[k][p].y)) : (x[k][p].x + x[k][p].y);
+        }
+    }
+    row_sum<TPR, RPC, 1>(s, red, 1, rg, wir, lane);
+    if (!ok) return;
+    const float inv = 1.0f / s[0], ls = logf(s[0]);
+#pragma unroll
+    for (int k = 0; k < CH; ++k) {
+        const int col = (k * TPR + t) * 8;
+        if (col >= D) continue;
+        float2 y[4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p)
+            y[p] = LOG ? make_float2(x[k][p].x - ls, x[k][p].y - ls)
+                       : make_float2(x[k][p].x * inv, x[k][p].y * inv);
+        st_chunk<XT>(as<XT>(a.Y) + off + col, y);
+    }
+}
+
+// Backward for aligned rows from the forward output Y (type XT) and dY (type XT):
+//   softmax: dX = Y * (dY - sum dY*Y);  log-softmax: dX = dY - exp(Y) * sum dY.
+template <int TPR, int RPC, int CH, bool LOG, int XT>
+__global__ void __launch_bounds__(TPR * RPC)
+softmax_bwd_vec8_kernel(const SoftmaxArgs a) {
+    pdl_enter();
+    constexpr int WPR = TPR / 32;
+    __shared__ float red[2 * RPC * WPR];
+    const int tid = threadIdx.x;
+    const int rg = tid / TPR, t = tid % TPR, wir = t / 32, lane = tid % 32;
+    const int D = a.D;
+    const int64_t row = (int64_t)blockIdx.x * RPC + rg;
+    const bool ok = row < a.N;
+    if (WPR == 1 && !ok) return;
+    const int64_t off = (ok ? row : 0) * (int64_t)D;
+
+    float2 y[CH][4], dy[CH][4];
+    float dot[1] = {0.f};
+#pragma unroll
+    for (int k = 0; k < CH; ++k) {
+        const int col = (k * TPR + t) * 8;
+        const bool v = ok && col < D;
+        ld_chunk<XT, kStream>(as<XT>(a.X) + off + col, v, y[k]);
+        ld_chunk<XT, kStream>(as<XT>(a.dY) + off + col, v, dy[k]);
+#pragma unroll
+        for (int p = 0; p < 4; ++p)
+            dot[0] += LOG ? (dy[k][p].x + dy[k][p].y) : (dy[k][p].x * y[k][p].x + dy[k][p].y * y[k][p].y);
+    }
+    row_sum<TPR, RPC, 1>(dot, red, 0, rg, wir, lane);
+    if (!ok) return;
+    const float c = dot[0];
+#pragma unroll
+    for (int k = 0; k < CH; ++k) {
+        const int col = (k * TPR + t) * 8;
+        if (col >= D) continue;
+        float2 o[4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p)
+            o[p] = LOG ? make_float2(dy[k][p].x - __expf(y[k][p].x) * c, dy[k][p].y - __expf(y[k][p].y) * c)
+                       : make_float2(y[k][p].x * (dy[k][p].x - c), y[k][p].y * (dy[k][p].y - c));
+        st_chunk<XT>(as<XT>(a.Y) + off + col, o);
+    }
+}
+
+// Scalar forward/backward for any alignment and width (types at run time): thread t of a
+// row group owns columns k*TPR + t, k < CH.
+template <int TPR, int RPC, int CH, bool LOG, bool BWD>
+__global__ void __launch_bounds__(TPR * RPC, 1)
+softmax_scalar_kernel(const SoftmaxArgs a) {
+    pdl_enter();
+    constexpr int WPR = TPR / 32;
+    __shared__ float red[2 * RPC * WPR];
+    const int tid = threadIdx.x;
+    const int rg = tid / TPR, t = tid % TPR, wir = t / 32, lane = tid % 32;
+    const int D = a.D;
+    const int64_t row = (int64_t)blockIdx.x * RPC + rg;
+    const bool ok = row < a.N;
+    if (WPR == 1 && !ok) return;
+    const int64_t off = (ok ? row : 0) * (int64_t)D;
+    const int lim = ok ? D : 0;
+
+    float x[CH], dy[BWD ? CH : 1];
+    if constexpr (!BWD) {
+        float m = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < CH; ++k) {
+            const int col = k * TPR + t;
+            x[k] = col < lim ? ld_elem_stream(a.X, off + col, a.xdt) : -INFINITY;
+            m = fmaxf(m, x[k]);
+        }
+        m = row_max<TPR, RPC>(m, red, 0, rg, wir, lane);
+        float s[1] = {0.f};
+#pragma unroll
+        for (int k = 0; k < CH; ++k) {
+            if (k * TPR + t >= lim) continue;
+            x[k] -= m;
+            s[0] += __expf(x[k]);
+        }
+        row_sum<TPR, RPC, 1>(s, red, 1, rg, wir, lane);
+        if (!ok) return;
+        const float inv = 1.0f / s[0], ls = logf(s[0]);
+#pragma unroll
+        for (int k = 0; k < CH; ++k) {
+            const int col = k * TPR + t;
+            if (col >= D) continue;
+            st_elem(a.Y, off + col, LOG ? x[k] - ls : __expf(x[k]) * inv, a.xdt);
+        }
+    } else {
+        float dot[1] = {0.f};
+#pragma unroll
+        for (int k = 0; k < CH; ++k) {
+            const int col = k * TPR + t;
+            const bool v = col < lim;
+            x[k] = v ? ld_elem_stream(a.X, off + col, a.xdt) : 0.f;
+            dy[k] = v ? ld_elem_stream(a.dY, off + col, a.gdt) : 0.f;
+            dot[0] += LOG ? dy[k] : dy[k] * x[k];
+        }
+        row_sum<TPR, RPC, 1>(dot, red, 0, rg, wir, lane);
+        if (!ok) return;
+        const float c = dot[0];
+#pragma unroll
+        for (int k = 0; k < CH; ++k) {
+            const int col = k * TPR + t;
+            if (col >= D) continue;
+            st_elem(a.Y, off + col, LOG ? dy[k] - __expf(x[k]) * c : x[k] * (dy[k] - c), a.xdt);
+        }
+    }
+}
+
+// ------------------------------------------------------------- cross-entropy ---
+
+// Running (maximum, sum of exp(x - maximum)) state and its order-fixed combination.
+struct MaxSum {
+    float m, s;
+};
+__device__ __forceinline__ MaxSum combine(MaxSum a, MaxSum b) {
+    const float m = fmaxf(a.m, b.m);
+    if (m == -INFINITY) return {m, 0.f};
+    return {m, a.s * __expf(a.m - m) + b.s * __expf(b.m - m)};
+}
+__device__ __forceinline__ void add_value(MaxSum &st, float x) {
+    if (x > st.m) {
+        st.s = st.s * __expf(st.m - x) + 1.f;
+        st.m = x;
+    } else {
+        st.s += __expf(x - st.m);
+    }
+}
+
+// One CTA of TPR threads per row. VEC8: 8-element chunks (D % 8 == 0, aligned rows),
+// thread t taking chunks t, t + TPR, ...; otherwise single elements, same striding.
+template <int TPR, bool VEC8, int XT>
+__global__ void __launch_bounds__(TPR)
+ce_fwd_kernel(const CeArgs a) {
+    pdl_enter();
+    constexpr int W = TPR / 32;
+    __shared__ float sm_m[W], sm_s[W], sm_x[W];
+    const int t = threadIdx.x, lane = t % 32, w = t / 32;
+    const int64_t row = blockIdx.x;
+    const int D = a.D;
+    const int64_t off = row * (int64_t)D;
+
+    MaxSum st{-INFINITY, 0.f};
+    float sx = 0.f;
+    if constexpr (VEC8) {
+        for (int c = t; c * 8 < D; c += TPR) {
+            float2 f[4];
+            ld_chunk<XT, kStream>(as<XT>(a.X) + off + c * 8, true, f);
+            float cm = -INFINITY;
+#pragma unroll
+            for (int p = 0; p < 4; ++p) cm = fmaxf(cm, fmaxf(f[p].x, f[p].y));
+            const float m = fmaxf(st.m, cm);
+            float cs = 0.f;
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                cs += __expf(f[p].x - m) + __expf(f[p].y - m);
+                sx += f[p].x + f[p].y;
+            }
+            st.s = (st.m == -INFINITY ? 0.f : st.s * __expf(st.m - m)) + cs;
+            st.m = m;
+        }
+    } else {
+        for (int j = t; j < D; j += TPR) {
+            const float v = ld_elem_stream(a.X, off + j, a.xdt);
+            add_value(st, v);
+            sx += v;
+        }
+    }
+    // fixed-order combination: butterfly within the warp, then warps 0..W-1
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        MaxSum other{__shfl_xor_sync(0xffffffffu, st.m, o), __shfl_xor_sync(0xffffffffu, st.s, o)};
+        st = (lane & o) ? combine(other, st) : combine(st, other);
+        sx += __shfl_xor_sync(0xffffffffu, sx, o);
+    }
+    if (lane == 0) {
+        sm_m[w] = st.m;
+        sm_s[w] = st.s;
+        sm_x[w] = sx;
+    }
+    __syncthreads();
+    if (t == 0) {
+        MaxSum tot{sm_m[0], sm_s[0]};
+        float tx = sm_x[0];
+        for (int i = 1; i < W; ++i) {
+            tot = combine(tot, MaxSum{sm_m[i], sm_s[i]});
+            tx += sm_x[i];
+        }
+        const float l = tot.m + logf(tot.s);
+        a.lse[row] = l;
+        const int64_t tg = a.T[row];
+        float loss;
+        if (tg == a.ignore_index) {
+            loss = 0.f;
+        } else if (tg < 0 || tg >= D) {
+            loss = __int_as_float(0x7fc00000);
+        } else {
+            const float xt = ld_elem(a.X, off + tg, a.xdt);
+            loss = l - (1.f - a.eps) * xt - (a.eps / (float)D) * tx + a.z * l * l;
+        }
+        a.loss[row] = loss;
+    }
+}
+
+// The upstream gradient of row `row` (0 for an ignored row).
+__device__ __forceinline__ float ce_row_grad(const CeArgs &a, int64_t row, int64_t tg) {
+    if (tg == a.ignore_index) return 0.f;
+    if (a.reduction == 0) return a.dloss[row];
+    if (a.reduction == 1) return a.dloss[0];
+    const float n = a.n_valid[0];
+    return n > 0.f ? a.dloss[0] / n : 0.f;
+}
+
+template <int TPR, bool VEC8, int XT>
+__global__ void __launch_bounds__(TPR)
+ce_bwd_kernel(const CeArgs a) {
+    pdl_enter();
+    const int t = threadIdx.x;
+    const int64_t row = blockIdx.x;
+    const int D = a.D;
+    const int64_t off = row * (int64_t)D;
+    const int64_t tg = a.T[row];
+    const float g = ce_row_grad(a, row, tg);
+    const float l = a.lse[row];
+    const float scale = g * (1.f + 2.f * a.z * l);   // multiplies p = exp(x - lse)
+    const float gq = g * a.eps / (float)D;            // g * (uniform part of q)
+    const float gt = g * (1.f - a.eps);               // g * (target part of q)
+    if constexpr (VEC8) {
+        for (int c = t; c * 8 < D; c += TPR) {
+            float2 f[4], o[4];
+            ld_chunk<XT, kStream>(as<XT>(a.X) + off + c * 8, true, f);
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                const int j = c * 8 + 2 * p;
+                o[p].x = scale * __expf(f[p].x - l) - gq - (j == tg ? gt : 0.f);
+                o[p].y = scale * __expf(f[p].y - l) - gq - (j + 1 == tg ? gt : 0.f);
+            }
+            st_chunk<XT>(as<XT>(a.dX) + off + c * 8, o);
+        }
+    } else {
+        for (int j = t; j < D; j += TPR) {
+            const float v = ld_elem_stream(a.X, off + j, a.xdt);
+            st_elem(a.dX, off + j, scale * __expf(v - l) - gq - (j == tg ? gt : 0.f), a.xdt);
+        }
+    }
+}
+
+// Fixed-order reduction of the per-row losses for sum/mean: one block; thread i sums rows
+// i, i + B, ... in order and counts the rows whose target is not ignore_index; then a
+// fixed tree. out[0] = sum (reduction 1) or sum / count (2; 0 when no row is valid),
+// n_valid[0] = count.
+template <int B>
+__global__ void __launch_bounds__(B)
+ce_loss_reduce_kernel(const float *loss, const int64_t *T, int64_t N, int64_t ignore_index,
+                      int reduction, float *out, float *n_valid) {
+    pdl_enter();
+    __shared__ float ss[B], sc[B];
+    float s = 0.f, c = 0.f;
+    for (int64_t i = threadIdx.x; i < N; i += B) {
+        s += loss[i];
+        c += (T[i] != ignore_index) ? 1.f : 0.f;
+    }
+    ss[threadIdx.x] = s;
+    sc[threadIdx.x] = c;
+    __syncthreads();
+    for (int h = B / 2; h > 0; h >>= 1) {
+        if ((int)threadIdx.x < h) {
+            ss[threadIdx.x] += ss[threadIdx.x + h];
+            sc[threadIdx.x] += sc[threadIdx.x + h];
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        const float tot = ss[0], cnt = sc[0];
+        out[0] = (reduction == 2) ? (cnt > 0.f ? tot / cnt : 0.f) : tot;
+        n_valid[0] = cnt;
+    }
+}
+
+}  // namespace mt

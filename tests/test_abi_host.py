@@ -42,7 +42,7 @@ def test_header_is_plain_c():
 
 def test_exports_every_declared_symbol(lib):
     decl = declared_functions()
-    assert len(decl) == 16
+    assert len(decl) == 20
     assert sorted(mt.EXPORTED) == decl
     out = subprocess.run(["nm", "-D", "--defined-only", mt.library_path()], capture_output=True,
                          text=True, check=True).stdout
@@ -144,6 +144,30 @@ def test_explicit_dtype_validation(lib):
     # dY in fp32 overlapping dX placed right after an fp16-sized dY
     assert bwd(RMS, F16, F16, F32, A, B, C, None, None, E, C + half, G, None, N, D, None, 0,
                None) == INV
+    assert lib.mt_last_cuda_error() == 0  # nothing reached CUDA
+
+
+def test_softmax_and_cross_entropy_validation(lib):
+    N, D = 8, 64
+    F16, F32 = mt.MT_DTYPE_F16, mt.MT_DTYPE_F32
+    NONE, SUM, MEAN = mt.MT_REDUCTION_NONE, mt.MT_REDUCTION_SUM, mt.MT_REDUCTION_MEAN
+    assert lib.mt_softmax_forward(F16, None, B, N, D, 0, None) == INV
+    assert lib.mt_softmax_forward(5, A, B, N, D, 0, None) == INV
+    assert lib.mt_softmax_forward(F16, A, A, N, D, 1, None) == INV          # in place
+    assert lib.mt_softmax_forward(F16, A, B, N, mt.MT_MAX_COLS + 1, 0, None) == UNS
+    assert lib.mt_softmax_backward(F32, A, None, C, N, D, 0, None) == INV
+    assert lib.mt_softmax_backward(F32, A, B, B, N, D, 0, None) == INV      # dX aliases dY
+    ce_f, ce_b = lib.mt_cross_entropy_forward, lib.mt_cross_entropy_backward
+    assert ce_f(F16, A, B, N, D, -100, 0.0, 0.0, SUM, C, E, None, G, None) == INV  # loss_out
+    assert ce_f(F16, A, B, N, D, -100, 1.5, 0.0, NONE, C, E, None, None, None) == INV
+    assert ce_f(F16, A, B, N, D, -100, 0.0, -1.0, NONE, C, E, None, None, None) == INV
+    assert ce_f(F16, A, B, N, D, -100, 0.0, float("nan"), NONE, C, E, None, None, None) == INV
+    assert ce_f(F16, A, B, N, D, -100, 0.0, 0.0, 3, C, E, F, G, None) == INV         # reduction
+    assert ce_f(F16, A, B, N, mt.MT_MAX_CE_COLS + 1, -100, 0.0, 0.0, NONE, C, E, None, None,
+                None) == UNS
+    assert ce_f(F16, A, B, N, D, -100, 0.0, 0.0, NONE, C, C, None, None, None) == INV  # lse==rows
+    assert ce_b(F16, A, B, C, N, D, -100, 0.0, 0.0, MEAN, E, None, G, None) == INV    # n_valid
+    assert ce_b(F16, A, B, C, N, D, -100, 0.0, 0.0, NONE, E, None, A, None) == INV    # dX == X
     assert lib.mt_last_cuda_error() == 0  # nothing reached CUDA
 
 

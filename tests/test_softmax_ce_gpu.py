@@ -1,0 +1,157 @@
+"""Row softmax / log-softmax and per-row cross-entropy on the GPU against the fp64 oracle
+(tensorcore "Training kernels", "Softmax -- standalone, row-wise"; meTile reduction and
+loss checklists; "Metal subgroup LayerNorm and cross-entropy report", cross-entropy).
+
+Inputs are seeded and synthetic: softmax rows N(0, 3^2) (peaked rows), cotangents N(0, 1);
+logits N(0, 2^2) with uniform random targets and a few ignored rows. Shapes: the report's
+cross-entropy shapes (1x127, 17x257, 128x1024, 64x4096), ragged widths for the scalar
+paths, and vocabulary-wide rows up to the 262144-column bound.
+
+Tolerances: softmax outputs and gradients use the storage type's output tolerance
+(parity.OUT_TOL); cross-entropy losses and lse (fp32, computed from the stored logits)
+|err| <= 1e-5 (1 + |ref|): the fp32 running sums of exp carry about
+(elements per thread + log2 threads) * 2^-24 relative error and __expf about 2^-21, so
+the log of the sum is good to a few 1e-6; reduced losses 1e-5 of sum_i |loss_i|; logit
+gradients rtol * |ref| + atol * max_j |ref_ij| per row with the storage type's (atol,
+rtol), since most entries are tiny probabilities next to the target's O(1) entry.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import row_wise_rmsnorm_gb300 as mt
+from parity import OUT_TOL, check_out, f64
+
+pytestmark = pytest.mark.gpu
+
+F16, BF16, F32 = torch.float16, torch.bfloat16, torch.float32
+DTYPES = [F16, BF16, F32]
+NAMES = {F16: "f16", BF16: "bf16", F32: "f32"}
+
+
+def _gen(shape, std, dtype, seed):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    return (torch.randn(shape, generator=g, device="cuda") * std).to(dtype)
+
+
+# -------------------------------------------------------------------- softmax ---
+
+SM_SHAPES = [(1, 127), (17, 257), (96, 1024), (40, 4104), (9, 16384), (300, 64)]
+
+
+@pytest.mark.parametrize("log", [False, True], ids=["softmax", "log_softmax"])
+@pytest.mark.parametrize("shape", SM_SHAPES, ids=lambda s: f"{s[0]}x{s[1]}")
+@pytest.mark.parametrize("dtype", DTYPES, ids=lambda d: NAMES[d])
+def test_softmax_parity(dtype, shape, log):
+    N, D = shape
+    x = _gen((N, D), 3.0, dtype, 1)
+    dy = _gen((N, D), 1.0, dtype, 2)
+    y = mt.softmax_forward(x, log)
+    dx = mt.softmax_backward(y, dy, log)
+    torch.cuda.synchronize()
+    Y = oracle.softmax_forward(f64(x), log)
+    check_out(y, Y, dtype, f"softmax(log={log}) Y {NAMES[dtype]} {N}x{D}")
+    # the backward is checked from the GPU's own stored Y (its input)
+    dX = oracle.softmax_backward(f64(y), f64(dy), log)
+    check_out(dx, dX, dtype, f"softmax(log={log}) dX {NAMES[dtype]} {N}x{D}")
+    if not log:
+        s = f64(y).sum(axis=1)
+        assert np.all(np.abs(s - 1.0) <= D * OUT_TOL[dtype][0] + 1e-6), "rows sum to one"
+
+
+def test_softmax_misaligned_and_deterministic():
+    N, D = 33, 1024
+    x = _gen((N, D), 3.0, F16, 4)
+    buf = torch.empty(N * D + 1, dtype=F16, device="cuda")
+    xs = buf[1:].view(N, D)
+    xs.copy_(x)
+    a = mt.softmax_forward(xs)
+    b = mt.softmax_forward(x)
+    check_out(a, oracle.softmax_forward(f64(x)), F16, "misaligned softmax")
+    assert torch.equal(mt.softmax_forward(x), b), "softmax not deterministic"
+
+
+# -------------------------------------------------------------- cross-entropy ---
+
+CE_SHAPES = [(1, 127), (17, 257), (128, 1024), (64, 4096), (8, 32768), (5, 50001),
+             (3, 131072), (2, 262144)]
+
+
+def _targets(N, D, seed, ignore=(-100,)):
+    rng = np.random.default_rng(seed)
+    t = rng.integers(0, D, N)
+    if N >= 4:
+        t[1] = ignore[0]
+    return torch.tensor(t, dtype=torch.int64, device="cuda")
+
+
+def _check_rows(got, ref, what):
+    """Per-row fp32 values (losses, lse): |err| <= 1e-5 (1 + |ref|); NaN where ref is NaN."""
+    g = f64(got)
+    assert np.array_equal(np.isnan(g), np.isnan(ref)), f"{what}: NaN positions"
+    m = ~np.isnan(ref)
+    assert np.all(np.abs(g[m] - ref[m]) <= 1e-5 * (1 + np.abs(ref[m]))), (
+        f"{what}: max err {np.max(np.abs(g[m] - ref[m])):.3e}")
+
+
+def _check_grad(got, ref, dtype, what):
+    atol, rtol = OUT_TOL[dtype]
+    g, r = f64(got), f64(ref)
+    scale = np.max(np.abs(r), axis=1, keepdims=True)
+    bad = ~(np.abs(g - r) <= rtol * np.abs(r) + atol * scale + 1e-30)
+    assert not bad.any(), (f"{what}: {bad.sum()} of {bad.size} out of tolerance, max err "
+                           f"{np.max(np.abs(g - r)):.3e}")
+
+
+@pytest.mark.parametrize("opts", [(0.0, 0.0, "none"), (0.1, 0.0, "mean"), (0.0, 1e-4, "sum"),
+                                  (0.05, 1e-3, "mean")], ids=lambda o: f"ls{o[0]}-z{o[1]}-{o[2]}")
+@pytest.mark.parametrize("shape", CE_SHAPES, ids=lambda s: f"{s[0]}x{s[1]}")
+@pytest.mark.parametrize("dtype", DTYPES, ids=lambda d: NAMES[d])
+def test_cross_entropy_parity(dtype, shape, opts):
+    eps, z, red = opts
+    N, D = shape
+    x = _gen((N, D), 2.0, dtype, 3)
+    t = _targets(N, D, 5)
+    loss, lse, nv = mt.cross_entropy_forward(x, t, -100, eps, z, red)
+    rng = np.random.default_rng(6)
+    up = rng.standard_normal(N) if red == "none" else np.array([1.3])
+    dloss = torch.tensor(up, dtype=torch.float32, device="cuda")
+    dx = mt.cross_entropy_backward(x, t, lse, dloss, nv, -100, eps, z, red)
+    torch.cuda.synchronize()
+    X = f64(x)
+    T = t.cpu().numpy()
+    rows, ref_lse = oracle.cross_entropy_forward(X, T, -100, eps, z)
+    val, n_valid = oracle.cross_entropy_reduce(rows, T, -100, red)
+    tag = f"ce {NAMES[dtype]} {N}x{D} {opts}"
+    _check_rows(lse, ref_lse, tag + " lse")
+    if red == "none":
+        _check_rows(loss, rows, tag + " loss rows")
+    else:
+        tol = 1e-5 * np.sum(np.abs(rows)) + 1e-6
+        assert abs(float(loss.item()) - val) <= tol, f"{tag}: reduced loss {loss.item()} vs {val}"
+        assert float(nv.item()) == n_valid, f"{tag}: n_valid"
+    g = oracle.cross_entropy_row_grad(up, N, n_valid, red)
+    ref_dx = oracle.cross_entropy_backward(X, T, f64(lse), g, -100, eps, z)
+    _check_grad(dx, ref_dx, dtype, tag + " dlogits")
+
+
+def test_cross_entropy_edge_cases():
+    """All rows ignored (mean = 0, gradient 0), an out-of-range target (NaN in its row
+    only), a custom ignore index, and bitwise determinism of the reduced loss."""
+    N, D = 6, 1000
+    x = _gen((N, D), 2.0, F32, 7)
+    t = torch.full((N,), 7, dtype=torch.int64, device="cuda")
+    loss, lse, nv = mt.cross_entropy_forward(x, t, 7, 0.0, 0.0, "mean")
+    dx = mt.cross_entropy_backward(x, t, lse, torch.ones(1, device="cuda"), nv, 7, 0.0, 0.0, "mean")
+    assert loss.item() == 0.0 and nv.item() == 0.0 and torch.count_nonzero(dx).item() == 0
+    t = torch.tensor([3, D + 5, 2, -1, 9, 0], dtype=torch.int64, device="cuda")
+    rows, _, _ = mt.cross_entropy_forward(x, t, -1, 0.0, 0.0, "none")
+    r = rows.cpu().numpy()
+    assert np.isnan(r[1]) and r[3] == 0.0 and np.all(np.isfinite(r[[0, 2, 4, 5]]))
+    x = _gen((4096, 4096), 2.0, BF16, 8)
+    t = _targets(4096, 4096, 9)
+    a = mt.cross_entropy_forward(x, t, -100, 0.1, 1e-4, "mean")
+    b = mt.cross_entropy_forward(x, t, -100, 0.1, 1e-4, "mean")
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
