@@ -241,7 +241,14 @@ softmax_scalar_kernel(const SoftmaxArgs a) {
 
 // ------------------------------------------------------------- cross-entropy ---
 
-// Running (maximum, sum of exp(x - maximum)) state and its order-fixed combination.
+// Chunks each cross-entropy thread loads before using the first (bytes in flight).
+#ifndef MT_CE_UNROLL
+#define MT_CE_UNROLL 4
+#endif
+constexpr int kCeUnroll = MT_CE_UNROLL;
+
+// Running (maximum, sum of exp(x - maximum)) state and its order-fixed combination. A
+// state whose maximum is -inf has seen only -inf logits (masked columns) and sums to 0.
 struct MaxSum {
     float m, s;
 };
@@ -254,19 +261,44 @@ __device__ __forceinline__ void add_value(MaxSum &st, float x) {
     if (x > st.m) {
         st.s = st.s * __expf(st.m - x) + 1.f;
         st.m = x;
-    } else {
+    } else if (st.m != -INFINITY) {
         st.s += __expf(x - st.m);
     }
 }
 
+// Loads the kCeUnroll chunks c0, c0 + TPR, ... of one row (zeros past the end).
+template <int TPR, int XT>
+__device__ __forceinline__ void ce_load(const void *X, int64_t off, int c0, int D,
+                                        float2 (&f)[kCeUnroll][4]) {
+#pragma unroll
+    for (int u = 0; u < kCeUnroll; ++u) {
+        const int c = c0 + u * TPR;
+        ld_chunk<XT, kStream>(as<XT>(X) + off + c * 8, c * 8 < D, f[u]);
+    }
+}
+
+// Element e (0..7) of an 8-element chunk held as four fp32 pairs.
+__device__ __forceinline__ float chunk_elem(const float2 (&f)[4], int e) {
+    float v = f[0].x;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        v = (e == 2 * p) ? f[p].x : v;
+        v = (e == 2 * p + 1) ? f[p].y : v;
+    }
+    return v;
+}
+
 // One CTA of TPR threads per row. VEC8: 8-element chunks (D % 8 == 0, aligned rows),
 // thread t taking chunks t, t + TPR, ...; otherwise single elements, same striding.
-template <int TPR, bool VEC8, int XT>
-__global__ void __launch_bounds__(TPR)
+// Every thread reads the row's target with its first logits; the thread that meets the
+// target column keeps its logit, so no load waits on another at the end of the row.
+template <int TPR, bool VEC8, int XT, int MINB>
+__global__ void __launch_bounds__(TPR, MINB)
 ce_fwd_kernel(const CeArgs a) {
     pdl_enter();
     constexpr int W = TPR / 32;
-    __shared__ float sm_m[W], sm_s[W], sm_x[W];
+    static_assert(W <= 32 && (W & (W - 1)) == 0, "warps per row: a power of two up to 32");
+    __shared__ float sm_m[W], sm_s[W], sm_x[W], sm_t;
     const int t = threadIdx.x, lane = t % 32, w = t / 32;
     const int64_t row = blockIdx.x;
     const int D = a.D;
@@ -275,30 +307,45 @@ ce_fwd_kernel(const CeArgs a) {
     MaxSum st{-INFINITY, 0.f};
     float sx = 0.f;
     if constexpr (VEC8) {
-        for (int c = t; c * 8 < D; c += TPR) {
-            float2 f[4];
-            ld_chunk<XT, kStream>(as<XT>(a.X) + off + c * 8, true, f);
-            float cm = -INFINITY;
+        float2 f[kCeUnroll][4];
+        ce_load<TPR, XT>(a.X, off, t, D, f);
+        const int64_t tg = a.T[row];
+        const int tc = (tg >= 0 && tg < D) ? (int)(tg >> 3) : -1;   // chunk holding the target
+        for (int c0 = t;;) {
 #pragma unroll
-            for (int p = 0; p < 4; ++p) cm = fmaxf(cm, fmaxf(f[p].x, f[p].y));
-            const float m = fmaxf(st.m, cm);
-            float cs = 0.f;
+            for (int u = 0; u < kCeUnroll; ++u) {
+                const int c = c0 + u * TPR;
+                if (c * 8 >= D) continue;
+                float cm = -INFINITY;
 #pragma unroll
-            for (int p = 0; p < 4; ++p) {
-                cs += __expf(f[p].x - m) + __expf(f[p].y - m);
-                sx += f[p].x + f[p].y;
+                for (int p = 0; p < 4; ++p) cm = fmaxf(cm, fmaxf(f[u][p].x, f[u][p].y));
+                const float m = fmaxf(st.m, cm);
+                const float ms = (m == -INFINITY) ? 0.f : m;   // all -inf so far: exps are 0
+                float cs = 0.f;
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    cs += __expf(f[u][p].x - ms) + __expf(f[u][p].y - ms);
+                    sx += f[u][p].x + f[u][p].y;
+                }
+                st.s = st.s * __expf(st.m - ms) + cs;
+                st.m = m;
+                if (c == tc) sm_t = chunk_elem(f[u], (int)(tg & 7));
             }
-            st.s = (st.m == -INFINITY ? 0.f : st.s * __expf(st.m - m)) + cs;
-            st.m = m;
+            c0 += kCeUnroll * TPR;
+            if (c0 * 8 >= D) break;
+            ce_load<TPR, XT>(a.X, off, c0, D, f);
         }
     } else {
+        const int64_t tg = a.T[row];
         for (int j = t; j < D; j += TPR) {
             const float v = ld_elem_stream(a.X, off + j, a.xdt);
             add_value(st, v);
             sx += v;
+            if (j == tg) sm_t = v;
         }
     }
-    // fixed-order combination: butterfly within the warp, then warps 0..W-1
+    // fixed-order combination: butterfly within each warp, then across the W warp results
+    // (lower-indexed partial first in every pair)
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         MaxSum other{__shfl_xor_sync(0xffffffffu, st.m, o), __shfl_xor_sync(0xffffffffu, st.s, o)};
@@ -311,13 +358,16 @@ ce_fwd_kernel(const CeArgs a) {
         sm_x[w] = sx;
     }
     __syncthreads();
-    if (t == 0) {
-        MaxSum tot{sm_m[0], sm_s[0]};
-        float tx = sm_x[0];
-        for (int i = 1; i < W; ++i) {
-            tot = combine(tot, MaxSum{sm_m[i], sm_s[i]});
-            tx += sm_x[i];
-        }
+    if (w != 0) return;
+    MaxSum tot{lane < W ? sm_m[lane] : -INFINITY, lane < W ? sm_s[lane] : 0.f};
+    float tx = lane < W ? sm_x[lane] : 0.f;
+#pragma unroll
+    for (int o = W / 2; o > 0; o >>= 1) {
+        MaxSum other{__shfl_xor_sync(0xffffffffu, tot.m, o), __shfl_xor_sync(0xffffffffu, tot.s, o)};
+        tot = (lane & o) ? combine(other, tot) : combine(tot, other);
+        tx += __shfl_xor_sync(0xffffffffu, tx, o);
+    }
+    if (lane == 0) {
         const float l = tot.m + logf(tot.s);
         a.lse[row] = l;
         const int64_t tg = a.T[row];
@@ -327,49 +377,72 @@ ce_fwd_kernel(const CeArgs a) {
         } else if (tg < 0 || tg >= D) {
             loss = __int_as_float(0x7fc00000);
         } else {
-            const float xt = ld_elem(a.X, off + tg, a.xdt);
-            loss = l - (1.f - a.eps) * xt - (a.eps / (float)D) * tx + a.z * l * l;
+            loss = l - (1.f - a.eps) * sm_t - (a.eps / (float)D) * tx + a.z * l * l;
         }
         a.loss[row] = loss;
     }
 }
 
-// The upstream gradient of row `row` (0 for an ignored row).
+// The upstream gradient of a row whose target is tg (0 for an ignored row). The loads
+// do not wait on tg, so they are issued together.
 __device__ __forceinline__ float ce_row_grad(const CeArgs &a, int64_t row, int64_t tg) {
-    if (tg == a.ignore_index) return 0.f;
-    if (a.reduction == 0) return a.dloss[row];
-    if (a.reduction == 1) return a.dloss[0];
-    const float n = a.n_valid[0];
-    return n > 0.f ? a.dloss[0] / n : 0.f;
+    const float d = a.dloss[a.reduction == 0 ? row : 0];
+    const float n = (a.reduction == 2) ? a.n_valid[0] : 1.f;
+    float g = (a.reduction == 2) ? (n > 0.f ? d / n : 0.f) : d;
+    return tg == a.ignore_index ? 0.f : g;
 }
 
-template <int TPR, bool VEC8, int XT>
-__global__ void __launch_bounds__(TPR)
+template <int TPR, bool VEC8, int XT, int MINB>
+__global__ void __launch_bounds__(TPR, MINB)
 ce_bwd_kernel(const CeArgs a) {
     pdl_enter();
     const int t = threadIdx.x;
     const int64_t row = blockIdx.x;
     const int D = a.D;
     const int64_t off = row * (int64_t)D;
-    const int64_t tg = a.T[row];
-    const float g = ce_row_grad(a, row, tg);
-    const float l = a.lse[row];
-    const float scale = g * (1.f + 2.f * a.z * l);   // multiplies p = exp(x - lse)
-    const float gq = g * a.eps / (float)D;            // g * (uniform part of q)
-    const float gt = g * (1.f - a.eps);               // g * (target part of q)
     if constexpr (VEC8) {
-        for (int c = t; c * 8 < D; c += TPR) {
-            float2 f[4], o[4];
-            ld_chunk<XT, kStream>(as<XT>(a.X) + off + c * 8, true, f);
+        // the first logits are requested before the per-row scalars are waited on
+        float2 f[kCeUnroll][4];
+        ce_load<TPR, XT>(a.X, off, t, D, f);
+        const int64_t tg = a.T[row];
+        const float g = ce_row_grad(a, row, tg);
+        const float l = a.lse[row];
+        const float scale = g * (1.f + 2.f * a.z * l);   // multiplies p = exp(x - lse)
+        const float gq = g * a.eps / (float)D;            // g * (uniform part of q)
+        const float gt = g * (1.f - a.eps);               // g * (target part of q)
+        const int tc = (tg >= 0 && tg < D) ? (int)(tg >> 3) : -1;
+        for (int c0 = t;;) {
 #pragma unroll
-            for (int p = 0; p < 4; ++p) {
-                const int j = c * 8 + 2 * p;
-                o[p].x = scale * __expf(f[p].x - l) - gq - (j == tg ? gt : 0.f);
-                o[p].y = scale * __expf(f[p].y - l) - gq - (j + 1 == tg ? gt : 0.f);
+            for (int u = 0; u < kCeUnroll; ++u) {
+                const int c = c0 + u * TPR;
+                if (c * 8 >= D) continue;
+                float2 o[4];
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    o[p].x = scale * __expf(f[u][p].x - l) - gq;
+                    o[p].y = scale * __expf(f[u][p].y - l) - gq;
+                }
+                if (c == tc) {
+                    const int e = (int)(tg & 7);
+#pragma unroll
+                    for (int p = 0; p < 4; ++p) {
+                        o[p].x -= (e == 2 * p) ? gt : 0.f;
+                        o[p].y -= (e == 2 * p + 1) ? gt : 0.f;
+                    }
+                }
+                st_chunk<XT>(as<XT>(a.dX) + off + c * 8, o);
             }
-            st_chunk<XT>(as<XT>(a.dX) + off + c * 8, o);
+            c0 += kCeUnroll * TPR;
+            if (c0 * 8 >= D) break;
+            ce_load<TPR, XT>(a.X, off, c0, D, f);
         }
     } else {
+        const int64_t tg = a.T[row];
+        const float g = ce_row_grad(a, row, tg);
+        const float l = a.lse[row];
+        const float scale = g * (1.f + 2.f * a.z * l);
+        const float gq = g * a.eps / (float)D;
+        const float gt = g * (1.f - a.eps);
         for (int j = t; j < D; j += TPR) {
             const float v = ld_elem_stream(a.X, off + j, a.xdt);
             st_elem(a.dX, off + j, scale * __expf(v - l) - gq - (j == tg ? gt : 0.f), a.xdt);

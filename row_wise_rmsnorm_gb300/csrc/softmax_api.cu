@@ -15,22 +15,27 @@ namespace {
 
 // Softmax shapes, X(max_D, TPR, RPC, CH): 8-element chunks for aligned rows (a warp per
 // row up to 1024 columns, one CTA per row above), single elements otherwise.
+#ifndef MT_SOFTMAX_SHAPES_VEC8
 #define MT_SOFTMAX_SHAPES_VEC8(X) \
     X(256, 32, 4, 1)              \
     X(1024, 32, 4, 4)             \
-    X(4096, 256, 1, 2)            \
+    X(4096, 128, 1, 4)            \
     X(16384, 512, 1, 4)
+#endif
 #define MT_SOFTMAX_SHAPES_SCALAR(X) \
     X(256, 32, 4, 8)                \
     X(1024, 32, 4, 32)              \
     X(4096, 256, 1, 16)             \
     X(16384, 1024, 1, 16)
 
-// Cross-entropy: one CTA per row, X(max_D, TPR).
+// Cross-entropy: one CTA per row, X(max_D, TPR, MINB), MINB a floor on resident CTAs per
+// SM for the register allocator (0: the compiler's choice).
+#ifndef MT_CE_SHAPES
 #define MT_CE_SHAPES(X) \
-    X(2048, 128)        \
-    X(16384, 256)       \
-    X(MT_MAX_CE_COLS, 512)
+    X(2048, 128, 0)     \
+    X(16384, 256, 0)    \
+    X(MT_MAX_CE_COLS, 512, 0)
+#endif
 
 mt_status_t fail(cudaError_t e) {
     record_cuda_error(e);
@@ -108,14 +113,14 @@ cudaError_t softmax_plan(int64_t N, int D, bool vec8, int xdt, LaunchPlan *p) {
 
 template <bool BWD, bool VEC8, int XT>
 cudaError_t ce_plan_t(int64_t N, int D, LaunchPlan *p) {
-#define MT_TRY(maxd, tpr)                                                                  \
-    if (D <= maxd) {                                                                       \
-        p->kernel = BWD ? reinterpret_cast<const void *>(&ce_bwd_kernel<tpr, VEC8, XT>)    \
-                        : reinterpret_cast<const void *>(&ce_fwd_kernel<tpr, VEC8, XT>);   \
-        p->threads = tpr;                                                                  \
-        p->grid = (int)N;                                                                  \
-        p->rows_per_cta = 1;                                                               \
-        return cudaSuccess;                                                                \
+#define MT_TRY(maxd, tpr, minb)                                                                \
+    if (D <= maxd) {                                                                           \
+        p->kernel = BWD ? reinterpret_cast<const void *>(&ce_bwd_kernel<tpr, VEC8, XT, minb>)  \
+                        : reinterpret_cast<const void *>(&ce_fwd_kernel<tpr, VEC8, XT, minb>); \
+        p->threads = tpr;                                                                      \
+        p->grid = (int)N;                                                                      \
+        p->rows_per_cta = 1;                                                                   \
+        return cudaSuccess;                                                                    \
     }
     MT_CE_SHAPES(MT_TRY)
 #undef MT_TRY

@@ -155,3 +155,33 @@ def test_cross_entropy_edge_cases():
     a = mt.cross_entropy_forward(x, t, -100, 0.1, 1e-4, "mean")
     b = mt.cross_entropy_forward(x, t, -100, 0.1, 1e-4, "mean")
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("shape", [(64, 4096), (17, 1001), (4, 50000)],
+                         ids=lambda s: f"{s[0]}x{s[1]}")
+@pytest.mark.parametrize("dtype", [BF16, F32], ids=lambda d: NAMES[d])
+def test_cross_entropy_masked_columns(dtype, shape):
+    """Logits of -inf (a masked vocabulary: a leading and a trailing block of columns) add
+    nothing to the row's sum of exponentials, also where a thread's first logits are all
+    masked; with label smoothing the loss is +inf (mass placed on impossible classes)."""
+    N, D = shape
+    x = _gen((N, D), 2.0, dtype, 11)
+    lead, tail = D // 4, D // 8
+    x[:, :lead] = float("-inf")
+    x[:, D - tail:] = float("-inf")
+    rng = np.random.default_rng(12)
+    t = torch.tensor(rng.integers(lead, D - tail, N), dtype=torch.int64, device="cuda")
+    loss, lse, nv = mt.cross_entropy_forward(x, t, -100, 0.0, 1e-4, "none")
+    up = rng.standard_normal(N)
+    dloss = torch.tensor(up, dtype=torch.float32, device="cuda")
+    dx = mt.cross_entropy_backward(x, t, lse, dloss, nv, -100, 0.0, 1e-4, "none")
+    torch.cuda.synchronize()
+    X, T = f64(x), t.cpu().numpy()
+    rows, ref_lse = oracle.cross_entropy_forward(X, T, -100, 0.0, 1e-4)
+    _check_rows(lse, ref_lse, "masked lse")
+    _check_rows(loss, rows, "masked loss")
+    ref_dx = oracle.cross_entropy_backward(X, T, f64(lse), up, -100, 0.0, 1e-4)
+    _check_grad(dx, ref_dx, dtype, "masked dlogits")
+    assert torch.count_nonzero(dx[:, :lead]).item() == 0
+    smooth, _, _ = mt.cross_entropy_forward(x, t, -100, 0.1, 0.0, "none")
+    assert torch.all(torch.isposinf(smooth)).item()
