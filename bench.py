@@ -41,7 +41,8 @@ METRIC = ("achieved HBM GB/s (% of ~8 TB/s) and rows/s, norm fwd+bwd at N×D fp1
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 DEFAULT_WORKLOAD = "rmsnorm_16384x4096"
-LARGE_WORKLOADS = ["rmsnorm_16384x4096", "add_rmsnorm_32768x4096", "layernorm_2048x16384"]
+LARGE_WORKLOADS = ["rmsnorm_16384x4096", "add_rmsnorm_32768x4096", "layernorm_2048x16384",
+                   "rmsnorm_4096x32768", "layernorm_1024x131072"]
 CSRC = os.path.join(ROOT, "row_wise_rmsnorm_gb300", "csrc")
 
 

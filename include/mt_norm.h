@@ -27,9 +27,12 @@
  * Arithmetic. All arithmetic is fp32; fp16 results are rounded to nearest even.
  *           dgamma/dbeta are reduced in a fixed order without atomics, so every output
  *           is bitwise identical from run to run on the same device and shape.
- * Bounds.   1 <= N <= 2^31 - 1 and 1 <= D <= MT_MAX_COLS. eps must be finite and > 0.
+ * Bounds.   0 <= N <= 2^31 - 1 and 1 <= D <= MT_MAX_COLS. eps must be finite and > 0.
+ * Empty batch. N = 0 is a no-op that returns MT_OK: nothing is read, the activation
+ *           and per-row pointers may be NULL, and a backward only sets dgamma (and
+ *           dbeta) to 0, the empty sum over rows, with no workspace.
  * Errors.   Arguments are validated before any CUDA call is made:
- *             MT_ERR_INVALID_ARG  a required pointer is NULL, N < 1, D < 1, eps not
+ *             MT_ERR_INVALID_ARG  a required pointer is NULL, N < 0, D < 1, eps not
  *                                 finite or not > 0, or an output overlaps an input or
  *                                 another output;
  *             MT_ERR_UNSUPPORTED  D > MT_MAX_COLS, N > 2^31 - 1, or a caller-supplied
@@ -73,9 +76,15 @@ typedef enum mt_norm_op {
 struct CUstream_st;
 typedef struct CUstream_st *mt_stream_t;
 
-/* Widest supported row. [meTile] bounds rows to 1..8192 columns; this library
- * extends the bound to 16384 so that 16384-wide LayerNorm rows are covered. */
-#define MT_MAX_COLS 16384
+/* Widest supported row of the normalizations. [meTile] bounds rows to 1..8192 columns;
+ * this library extends the bound to 131072. Rows up to 16384 columns run on one CTA;
+ * wider rows are split across a thread-block cluster of 2, 4 or 8 CTAs (one slice of
+ * at most 16384 columns each) that add their row sums through distributed shared
+ * memory in a fixed order, so results stay bitwise reproducible. */
+#define MT_MAX_COLS 131072
+
+/* Widest row of the softmax / log-softmax (register-resident rows). */
+#define MT_MAX_SOFTMAX_COLS 16384
 
 /* ---------------------------------------------------------------- RMSNorm ---
  * [tc] "RMSnorm -- Llama-style", Math; [meTile] contract (zero-offset weight):
@@ -218,8 +227,9 @@ mt_status_t mt_norm_backward_ex(mt_norm_op_t op, mt_dtype_t x_dtype, mt_dtype_t 
  *     softmax:      dX_ij = Y_ij * (dY_ij - sum_k dY_ik * Y_ik)
  *     log-softmax:  dX_ij = dY_ij - exp(Y_ij) * sum_k dY_ik
  * X, Y, dY, dX are [N, D] of type `dtype`; log_softmax != 0 selects log-softmax.
- * Bounds as for the normalizations (1 <= D <= MT_MAX_COLS). Errors: MT_ERR_INVALID_ARG
- * for a NULL pointer, N or D < 1, an unknown dtype or an output overlapping an input.
+ * Bounds: 1 <= D <= MT_MAX_SOFTMAX_COLS, 0 <= N <= 2^31 - 1 (N = 0: a no-op, pointers
+ * may be NULL). Errors: MT_ERR_INVALID_ARG for a NULL pointer, N < 0, D < 1, an unknown
+ * dtype or an output overlapping an input; MT_ERR_UNSUPPORTED for D or N past the bound.
  * Arithmetic fp32; results rounded to `dtype`, nearest even.                       */
 mt_status_t mt_softmax_forward(mt_dtype_t dtype, const void *X, void *Y, int64_t N, int64_t D,
                                int log_softmax, mt_stream_t stream);
@@ -244,9 +254,11 @@ mt_status_t mt_softmax_backward(mt_dtype_t dtype, const void *Y, const void *dY,
  * n_valid: one fp32 each, written for SUM/MEAN (may be NULL for NONE); the backward's
  * dloss is [N] for NONE and one value otherwise, and n_valid (MEAN) is the forward's.
  * A target outside [0, D) that is not ignore_index gives a NaN loss for its row.
- * Bounds: 1 <= D <= MT_MAX_CE_COLS, 1 <= N <= 2^31 - 1; 0 <= label_smoothing <= 1,
- * z_loss >= 0 (both finite), else MT_ERR_INVALID_ARG. The sum over rows runs in a
- * fixed order, so every result is bitwise identical run to run.                     */
+ * Bounds: 1 <= D <= MT_MAX_CE_COLS, 0 <= N <= 2^31 - 1; 0 <= label_smoothing <= 1,
+ * z_loss >= 0 (both finite), else MT_ERR_INVALID_ARG. N = 0: the forward writes only
+ * loss_out = 0 and n_valid = 0 (SUM/MEAN), the backward nothing; the [N] pointers may
+ * be NULL. The sum over rows runs in a fixed order, so every result is bitwise
+ * identical run to run.                                                             */
 #define MT_MAX_CE_COLS 262144
 
 typedef enum mt_reduction {
@@ -281,9 +293,9 @@ mt_status_t mt_cross_entropy_backward(mt_dtype_t dtype, const void *logits,
  * device current) and caches it, so make that first call before any stream capture.
  * All calls share the array and leave their partials in it; nothing has to be cleared
  * between calls, but calls that overlap on the GPU race on it and must not be made.
- * A shape whose dgamma partials (one fp32 row of D per persistent CTA) exceed
- * MT_NOALLOC_SCRATCH_BYTES returns MT_ERR_UNSUPPORTED and launches nothing; every
- * shape up to MT_MAX_COLS columns fits on a 152-SM GB300.                            */
+ * A shape whose dgamma partials (one fp32 row of D per persistent CTA, or per cluster
+ * of a split row) exceed MT_NOALLOC_SCRATCH_BYTES returns MT_ERR_UNSUPPORTED and
+ * launches nothing; every shape up to MT_MAX_COLS columns fits on a 152-SM GB300.    */
 #define MT_NOALLOC_SCRATCH_BYTES (16u << 20)
 
 mt_status_t mt_rmsnorm_backward_noalloc(const void *X, const void *gamma, const void *dY,
@@ -294,7 +306,7 @@ mt_status_t mt_rmsnorm_backward_noalloc(const void *X, const void *gamma, const 
 
 /* Scratch bytes a backward of `op` at [N, D] needs on CUDA device `device`, whatever
  * its storage types: the fixed-order dgamma (and dbeta) partials, one fp32 row of D per
- * persistent CTA.
+ * persistent CTA (per cluster of a split row); 0 for N = 0.
  * Writes the size to *bytes. Errors: MT_ERR_INVALID_ARG / MT_ERR_UNSUPPORTED as the
  * backward would return them, MT_ERR_INVALID_ARG for a NULL `bytes` or an unknown
  * op, MT_ERR_CUDA if the device cannot be queried.                                */

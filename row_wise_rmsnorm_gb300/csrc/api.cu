@@ -51,8 +51,9 @@ bool any_overlap(std::initializer_list<Buf> outs, std::initializer_list<Buf> ins
     return false;
 }
 
+// N = 0 is a valid, empty batch (see forward_impl / backward_impl).
 mt_status_t check_shape(int64_t N, int64_t D) {
-    if (N < 1 || D < 1) return MT_ERR_INVALID_ARG;
+    if (N < 0 || D < 1) return MT_ERR_INVALID_ARG;
     if (D > MT_MAX_COLS || N > (int64_t)INT32_MAX) return MT_ERR_UNSUPPORTED;
     return MT_OK;
 }
@@ -70,6 +71,7 @@ bool aligned16(std::initializer_list<const void *> ptrs) {
 std::mutex g_cache_mu;
 std::map<int, int> g_sm_count;
 std::map<std::tuple<const void *, int, size_t, int>, int> g_occupancy;
+std::map<std::tuple<const void *, int, size_t, int, int>, int> g_cluster_occupancy;
 
 }  // namespace
 
@@ -83,11 +85,19 @@ cudaError_t launch_pdl(const LaunchPlan &p, void *arg, cudaStream_t stream) {
     cfg.blockDim = dim3((unsigned)p.threads);
     cfg.dynamicSmemBytes = p.smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (p.cluster > 1) {
+        if (p.grid % p.cluster != 0) return cudaErrorInvalidConfiguration;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = (unsigned)p.cluster;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
+    }
     return cudaLaunchKernelExC(&cfg, p.kernel, args);
 }
 
@@ -125,6 +135,7 @@ cudaError_t plan_forward(int op, int64_t N, int D, bool vec8, int xdt, int wdt, 
         const cudaError_t e = plan_forward_vec(op, xdt, N, D, wdt, p);
         if (e != kNoVectorPlan) return e;
     }
+    *p = LaunchPlan{};
     return fwd_plan_scalar_op(op, N, D, p);
 }
 
@@ -134,6 +145,7 @@ cudaError_t plan_backward(int op, int64_t N, int D, bool vec8, int xdt, int wdt,
         const cudaError_t e = plan_backward_vec(op, xdt, N, D, wdt, gdt, has_ds, device, p);
         if (e != kNoVectorPlan) return e;
     }
+    *p = LaunchPlan{};
     return bwd_plan_scalar_op(op, N, D, has_ds, device, p);
 }
 
@@ -142,6 +154,7 @@ mt_status_t run_forward(int op, const FwdArgs &a, bool vec8, mt_stream_t stream)
     const cudaError_t e = plan_forward(op, a.N, a.D, vec8, a.xdt, a.wdt, &p);
     if (e != cudaSuccess) return cuda_fail(e);
     FwdArgs copy = a;
+    copy.slice = p.slice;
     return launch(p, &copy, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -163,7 +176,8 @@ mt_status_t run_backward(int op, BwdArgs a, bool vec8, float *dgamma, float *dbe
     LaunchPlan p;
     e = plan_backward(op, a.N, a.D, vec8, a.xdt, a.wdt, a.gdt, a.dS != nullptr, device, &p);
     if (e != cudaSuccess) return cuda_fail(e);
-    const int prow = p.grid;  // partial rows: one per CTA
+    const int prow = p.owners();  // partial rows: one per CTA, or per cluster of a split row
+    a.slice = p.slice;
     const size_t need = partial_bytes(op, prow, a.D);
     if (own_ws) {
         e = cudaMallocAsync(&workspace, need, stream);
@@ -259,6 +273,41 @@ cudaError_t cached_occupancy(const void *kernel, int threads, size_t smem, int d
     return cudaSuccess;
 }
 
+// Called after cached_occupancy for the same kernel and shape, which has raised the
+// kernel's dynamic shared memory limit.
+cudaError_t cached_cluster_occupancy(const void *kernel, int threads, size_t smem, int cluster,
+                                     int device, int *clusters) {
+    std::lock_guard<std::mutex> lock(g_cache_mu);
+    auto key = std::make_tuple(kernel, threads, smem, cluster, device);
+    auto it = g_cluster_occupancy.find(key);
+    if (it != g_cluster_occupancy.end()) {
+        *clusters = it->second;
+        return cudaSuccess;
+    }
+    int cur = 0;
+    cudaError_t e = cudaGetDevice(&cur);
+    if (e != cudaSuccess) return e;
+    if (cur != device && (e = cudaSetDevice(device)) != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)cluster);
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int v = 0;
+    e = cudaOccupancyMaxActiveClusters(&v, kernel, &cfg);
+    if (cur != device) cudaSetDevice(cur);
+    if (e != cudaSuccess) return e;
+    g_cluster_occupancy[key] = v;
+    *clusters = v;
+    return cudaSuccess;
+}
+
 }  // namespace mt
 
 using namespace mt;
@@ -278,12 +327,13 @@ mt_status_t forward_impl(int op, int xdt, int wdt, const void *X, const void *R,
     const bool ln = op == kLayer, add = op == kAddRms;
     if (!ln) { beta = nullptr; mean = nullptr; }
     if (!add) { R = nullptr; S = nullptr; }
-    if (!X || !gamma || !Y || !rstd || (ln && (!beta || !mean)) || (add && (!R || !S)))
-        return MT_ERR_INVALID_ARG;
     if (!valid_dtype(xdt) || !valid_dtype(wdt)) return MT_ERR_INVALID_ARG;
     mt_status_t s = check_shape(N, D);
     if (s != MT_OK) return s;
     if ((s = check_eps(eps)) != MT_OK) return s;
+    if (N == 0) return MT_OK;  // an empty batch: nothing is read or written
+    if (!X || !gamma || !Y || !rstd || (ln && (!beta || !mean)) || (add && (!R || !S)))
+        return MT_ERR_INVALID_ARG;
     const size_t act = (size_t)N * (size_t)D * dtype_bytes(xdt);
     const size_t par = (size_t)D * dtype_bytes(wdt), st = (size_t)N * 4;
     if (any_overlap({{S, act}, {Y, act}, {mean, st}, {rstd, st}},
@@ -317,11 +367,20 @@ mt_status_t backward_impl(int op, int xdt, int wdt, int gdt, const void *X, cons
     const bool ln = op == kLayer, add = op == kAddRms;
     if (!ln) { mean = nullptr; dbeta = nullptr; }
     if (!add) dS = nullptr;
-    if (!X || !gamma || !dY || !rstd || !dX || !dgamma || (ln && (!mean || !dbeta)))
-        return MT_ERR_INVALID_ARG;
     if (!valid_dtype(xdt) || !valid_dtype(wdt) || !valid_dtype(gdt)) return MT_ERR_INVALID_ARG;
     mt_status_t s = check_shape(N, D);
     if (s != MT_OK) return s;
+    if (N == 0) {
+        // an empty batch: the parameter gradients are empty sums, 0; nothing else is
+        // read or written and no workspace is needed
+        if (!dgamma || (ln && !dbeta) || (ln && dgamma == dbeta)) return MT_ERR_INVALID_ARG;
+        cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+        cudaError_t e = cudaMemsetAsync(dgamma, 0, (size_t)D * sizeof(float), st);
+        if (e == cudaSuccess && ln) e = cudaMemsetAsync(dbeta, 0, (size_t)D * sizeof(float), st);
+        return e == cudaSuccess ? MT_OK : cuda_fail(e);
+    }
+    if (!X || !gamma || !dY || !rstd || !dX || !dgamma || (ln && (!mean || !dbeta)))
+        return MT_ERR_INVALID_ARG;
     const size_t act = (size_t)N * (size_t)D * dtype_bytes(xdt);
     const size_t cot = (size_t)N * (size_t)D * dtype_bytes(gdt);
     const size_t par = (size_t)D * dtype_bytes(wdt), st = (size_t)N * 4, grad = (size_t)D * 4;
@@ -466,6 +525,10 @@ extern "C" mt_status_t mt_norm_backward_workspace_size(mt_norm_op_t op, int64_t 
     mt_status_t s = check_shape(N, D);
     if (s != MT_OK) return s;
     if (device < 0) return MT_ERR_INVALID_ARG;
+    if (N == 0) {  // an empty batch needs no workspace
+        *bytes = 0;
+        return MT_OK;
+    }
     const int kop = (op == MT_OP_RMSNORM) ? kRms : (op == MT_OP_LAYERNORM) ? kLayer : kAddRms;
     // The largest of the variants a call may take (vectorised or not, with or without
     // dS, any storage types), so one size fits every call with this op and shape.
@@ -480,7 +543,7 @@ extern "C" mt_status_t mt_norm_backward_workspace_size(mt_norm_op_t op, int64_t 
                         cudaError_t e = plan_backward(kop, N, (int)D, v == 1, xdt, wdt, gdt,
                                                       ds == 1, device, &p);
                         if (e != cudaSuccess) return cuda_fail(e);
-                        const size_t b = partial_bytes(kop, p.grid, (int)D);
+                        const size_t b = partial_bytes(kop, p.owners(), (int)D);
                         if (b > best) best = b;
                     }
                 }

@@ -49,6 +49,7 @@ struct FwdArgs {
     int D;
     float eps;
     int xdt, wdt;
+    int slice;            // cluster-split kernels: columns per CTA (a multiple of 8)
 };
 
 // X (or the saved S) and dX are stored as xdt, gamma as wdt, dY/dS as gdt.
@@ -65,6 +66,7 @@ struct BwdArgs {
     int64_t N;
     int D;
     int xdt, wdt, gdt;
+    int slice;            // cluster-split kernels: columns per CTA (a multiple of 8)
 };
 
 // ------------------------------------------------------------------ helpers ---
@@ -91,6 +93,92 @@ __device__ __forceinline__ void pdl_enter() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// ------------------------------------------------------------ cluster split ---
+// Rows wider than one CTA's slice run on a thread-block cluster: CTA r of the cluster
+// owns columns [r * slice, min(D, (r + 1) * slice)) of the cluster's rows, with the
+// same per-thread chunk layout inside its slice as a CTA that owns a whole row. A row
+// reduction first sums within each CTA (row_sum), then cluster_sum adds the CTAs'
+// totals through distributed shared memory in rank order 0, 1, ..., so every CTA of
+// the cluster ends with the bitwise-identical row total. The cluster barrier is the
+// hardware one (every CTA of a cluster is resident at once, so it always completes).
+
+__device__ __forceinline__ unsigned cluster_rank() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ unsigned cluster_size() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+// Release this thread's earlier memory accesses to the cluster / wait for every thread
+// of every CTA of the cluster to have arrived (acquiring their accesses).
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// The float at the same shared-memory offset as `local`, in the CTA of cluster rank r.
+__device__ __forceinline__ float ld_cluster(const float *local, unsigned r) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)), "r"(r));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+// Cluster-wide sum of NV per-CTA totals (every thread of the CTA holds them, bitwise
+// identical). xch: 2 x NV shared floats; alternate `buf` between consecutive calls (a
+// CTA rewrites a slot only after the next call's barrier, which every CTA reaches only
+// once it has read the slot). Every thread of every CTA of the cluster must call it.
+template <int NV>
+__device__ __forceinline__ void cluster_sum(float (&v)[NV], float *xch, int buf, unsigned n) {
+    float *slot = xch + buf * NV;
+    if (threadIdx.x == 0) {
+#pragma unroll
+        for (int i = 0; i < NV; ++i) slot[i] = v[i];
+    }
+    cluster_arrive();
+    cluster_wait();
+#pragma unroll
+    for (int i = 0; i < NV; ++i) v[i] = 0.f;
+    for (unsigned r = 0; r < n; ++r) {
+#pragma unroll
+        for (int i = 0; i < NV; ++i) v[i] += ld_cluster(slot + i, r);
+    }
+}
+
+// This CTA's column window and row owner. Not split: columns [0, D) and the plain CTA
+// index. Split: the CTA's slice, and the cluster index as the owner (cn = cluster size).
+template <bool CLU>
+struct Window {
+    int beg, end;
+    unsigned cn;
+    __device__ __forceinline__ Window(int D, int slice) {
+        if constexpr (CLU) {
+            cn = cluster_size();
+            beg = (int)cluster_rank() * slice;
+            end = min(D, beg + slice);
+        } else {
+            cn = 1;
+            beg = 0;
+            end = D;
+        }
+    }
+    __device__ __forceinline__ int64_t owner() const {
+        return CLU ? (int64_t)(blockIdx.x / cn) : (int64_t)blockIdx.x;
+    }
+    __device__ __forceinline__ int64_t owners() const {
+        return CLU ? (int64_t)(gridDim.x / cn) : (int64_t)gridDim.x;
+    }
+};
 
 // Barrier for one row group. NAMED: named barrier 1 + rg over the group's TPR threads,
 // so the row groups of a CTA do not wait for one another (the persistent backward, where
@@ -137,29 +225,32 @@ __device__ __forceinline__ void row_sum(float (&v)[NV], float *red, int buf, int
 // Scalar fallback for any alignment and any width: one row group per row, thread t
 // owning the CH columns k*TPR + t; types chosen at run time (a.xdt, a.wdt).
 // grid = ceil(N / RPC) CTAs of TPR*RPC threads.
-template <int OP, int TPR, int RPC, int CH>
+template <int OP, int TPR, int RPC, int CH, bool CLU = false>
 __global__ void __launch_bounds__(TPR * RPC)
 norm_fwd_kernel(const FwdArgs a) {
     pdl_enter();
     static_assert(TPR % 32 == 0 && TPR * RPC <= 1024, "bad launch shape");
+    static_assert(!CLU || RPC == 1, "a split row is one row group per CTA");
     constexpr int WPR = TPR / 32;
     __shared__ float red[2 * RPC * WPR];
+    __shared__ float xch[CLU ? 2 : 1];
 
     const int tid = threadIdx.x;
     const int rg = tid / TPR, t = tid % TPR, wir = t / 32, lane = tid % 32;
     const int D = a.D;
-    const int64_t row = (int64_t)blockIdx.x * RPC + rg;
-    const bool ok = row < a.N;
+    const Window<CLU> win(D, a.slice);
+    const int64_t row = CLU ? win.owner() : (int64_t)blockIdx.x * RPC + rg;
+    const bool ok = row < a.N;  // split rows: the grid is N clusters, so always true
     // A single-warp row group has no CTA barrier, so it may leave early; wider row
     // groups run masked (all loads read 0, nothing is stored) to reach the barriers.
     if (WPR == 1 && !ok) return;
     const int64_t off = (ok ? row : 0) * (int64_t)D;
-    const int lim = ok ? D : 0;  // masked row: every column counts as past the end
+    const int lim = ok ? win.end : 0;  // masked row: every column counts as past the end
 
     float x[CH];
 #pragma unroll
     for (int k = 0; k < CH; ++k) {
-        const int col = k * TPR + t;
+        const int col = win.beg + k * TPR + t;
         const bool v = col < lim;
         x[k] = v ? ld_elem_stream(a.X, off + col, a.xdt) : 0.f;
         if constexpr (OP == kAddRms) {
@@ -175,33 +266,39 @@ norm_fwd_kernel(const FwdArgs a) {
 #pragma unroll
         for (int k = 0; k < CH; ++k) s[0] += x[k];
         row_sum<TPR, RPC, 1>(s, red, 0, rg, wir, lane);
+        if constexpr (CLU) cluster_sum<1>(s, xch, 0, win.cn);
         mu = s[0] / (float)D;
     }
     float q[1] = {0.f};
 #pragma unroll
     for (int k = 0; k < CH; ++k) {
         // LayerNorm: centred second moment (two-pass, from registers)
-        const float d = (OP == kLayer) ? ((k * TPR + t) < lim ? x[k] - mu : 0.f) : x[k];
+        const float d = (OP == kLayer) ? ((win.beg + k * TPR + t) < lim ? x[k] - mu : 0.f) : x[k];
         q[0] += d * d;
     }
     row_sum<TPR, RPC, 1>(q, red, 1, rg, wir, lane);
+    if constexpr (CLU) {
+        cluster_sum<1>(q, xch, 1, win.cn);
+        cluster_arrive();  // done reading the other CTAs' slots (waited for before exit)
+    }
     const float rs = rsqrtf(q[0] / (float)D + a.eps);
     if (!ok) return;  // after the last barrier
-    if (t == 0) {
+    if (t == 0 && win.beg == 0) {
         a.rstd[row] = rs;
         if constexpr (OP == kLayer) a.mean[row] = mu;
     }
 
 #pragma unroll
     for (int k = 0; k < CH; ++k) {
-        const int col = k * TPR + t;
-        if (col >= D) continue;
+        const int col = win.beg + k * TPR + t;
+        if (col >= win.end) continue;
         const float g = ld_elem(a.gamma, col, a.wdt);
         float y;
         if constexpr (OP == kLayer) y = (x[k] - mu) * rs * g + ld_elem(a.beta, col, a.wdt);
         else y = x[k] * rs * g;
         st_elem(a.Y, off + col, y, a.xdt);
     }
+    if constexpr (CLU) cluster_wait();  // no CTA leaves while another may read its slots
 }
 
 // Forward for 16-byte-aligned rows (D % 8 == 0), one row group per row, fp32 pair
@@ -209,28 +306,31 @@ norm_fwd_kernel(const FwdArgs a) {
 // registers (as fp32 pairs) through the reductions and the apply. Activations are of
 // type XT, gamma/beta of type WT. MINB is the minimum number of resident CTAs per SM
 // asked of the compiler (it bounds the registers per thread; 0: the compiler's choice).
-template <int OP, int TPR, int RPC, int CH, int MINB, int XT, int WT>
+template <int OP, int TPR, int RPC, int CH, int MINB, int XT, int WT, bool CLU = false>
 __global__ void __launch_bounds__(TPR * RPC, MINB)
 norm_fwd_vec8_kernel(const FwdArgs a) {
     pdl_enter();
     static_assert(TPR % 32 == 0 && TPR * RPC <= 1024, "bad launch shape");
+    static_assert(!CLU || RPC == 1, "a split row is one row group per CTA");
     constexpr int WPR = TPR / 32;
     __shared__ float red[2 * RPC * WPR];
+    __shared__ float xch[CLU ? 2 : 1];
 
     const int tid = threadIdx.x;
     const int rg = tid / TPR, t = tid % TPR, wir = t / 32, lane = tid % 32;
     const int D = a.D;
     const float inv_d = 1.0f / (float)D;
-    const int64_t row = (int64_t)blockIdx.x * RPC + rg;
-    const bool ok = row < a.N;
+    const Window<CLU> win(D, a.slice);
+    const int64_t row = CLU ? win.owner() : (int64_t)blockIdx.x * RPC + rg;
+    const bool ok = row < a.N;  // split rows: the grid is N clusters, so always true
     if (WPR == 1 && !ok) return;  // no CTA barrier in a single-warp row group
     const int64_t off = (ok ? row : 0) * (int64_t)D;
 
     float2 x[CH][4];
 #pragma unroll
     for (int k = 0; k < CH; ++k) {
-        const int col = (k * TPR + t) * 8;
-        const bool v = ok && col < D;
+        const int col = win.beg + (k * TPR + t) * 8;
+        const bool v = ok && col < win.end;
         ld_chunk<XT, kStream>(as<XT>(a.X) + off + col, v, x[k]);
         if constexpr (OP == kAddRms) {
             float2 r[4];
@@ -249,13 +349,14 @@ norm_fwd_vec8_kernel(const FwdArgs a) {
             for (int p = 0; p < 4; ++p) s2 = __fadd2_rn(s2, x[k][p]);
         float s[1] = {s2.x + s2.y};
         row_sum<TPR, RPC, 1>(s, red, 0, rg, wir, lane);
+        if constexpr (CLU) cluster_sum<1>(s, xch, 0, win.cn);
         mu = s[0] * inv_d;
     }
     const float2 nmu = make_float2(-mu, -mu);
     float2 q2 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int k = 0; k < CH; ++k) {
-        if (!(ok && (k * TPR + t) * 8 < D)) continue;
+        if (!(ok && win.beg + (k * TPR + t) * 8 < win.end)) continue;
 #pragma unroll
         for (int p = 0; p < 4; ++p) {
             const float2 d = (OP == kLayer) ? __fadd2_rn(x[k][p], nmu) : x[k][p];
@@ -264,17 +365,21 @@ norm_fwd_vec8_kernel(const FwdArgs a) {
     }
     float q[1] = {q2.x + q2.y};
     row_sum<TPR, RPC, 1>(q, red, 1, rg, wir, lane);
+    if constexpr (CLU) {
+        cluster_sum<1>(q, xch, 1, win.cn);
+        cluster_arrive();  // done reading the other CTAs' slots (waited for before exit)
+    }
     const float rs = rsqrtf(q[0] * inv_d + a.eps);
     if (!ok) return;  // after the last barrier
-    if (t == 0) {
+    if (t == 0 && win.beg == 0) {
         a.rstd[row] = rs;
         if constexpr (OP == kLayer) a.mean[row] = mu;
     }
     const float2 rs2 = make_float2(rs, rs);
 #pragma unroll
     for (int k = 0; k < CH; ++k) {
-        const int col = (k * TPR + t) * 8;
-        if (col >= D) continue;
+        const int col = win.beg + (k * TPR + t) * 8;
+        if (col >= win.end) continue;
         float2 g[4], y[4];
         ld_param<WT>(as<WT>(a.gamma) + col, g);
         if constexpr (OP == kLayer) {
@@ -289,6 +394,7 @@ norm_fwd_vec8_kernel(const FwdArgs a) {
         }
         st_chunk<XT>(as<XT>(a.Y) + off + col, y);
     }
+    if constexpr (CLU) cluster_wait();  // no CTA leaves while another may read its slots
 }
 
 // The same forward for RMSNorm and LayerNorm with 2-byte activations (XT = fp16 or
@@ -296,31 +402,34 @@ norm_fwd_vec8_kernel(const FwdArgs a) {
 // half the registers of norm_fwd_vec8_kernel, so more CTAs (and more bytes in flight)
 // fit per SM, for one more conversion per pass. (The fused op normalises the unrounded
 // fp32 x + r, so it cannot keep 2-byte chunks.)
-template <int OP, int TPR, int RPC, int CH, int MINB, int XT, int WT>
+template <int OP, int TPR, int RPC, int CH, int MINB, int XT, int WT, bool CLU = false>
 __global__ void __launch_bounds__(TPR * RPC, MINB)
 norm_fwd_packed_kernel(const FwdArgs a) {
     pdl_enter();
     static_assert(TPR % 32 == 0 && TPR * RPC <= 1024, "bad launch shape");
     static_assert(OP == kRms || OP == kLayer, "the fused op keeps its fp32 sum");
     static_assert(XT == kF16 || XT == kBF16, "2-byte activations only");
+    static_assert(!CLU || RPC == 1, "a split row is one row group per CTA");
     constexpr int WPR = TPR / 32;
     __shared__ float red[2 * RPC * WPR];
+    __shared__ float xch[CLU ? 2 : 1];
     const auto *X = as<XT>(a.X);
 
     const int tid = threadIdx.x;
     const int rg = tid / TPR, t = tid % TPR, wir = t / 32, lane = tid % 32;
     const int D = a.D;
     const float inv_d = 1.0f / (float)D;
-    const int64_t row = (int64_t)blockIdx.x * RPC + rg;
-    const bool ok = row < a.N;
+    const Window<CLU> win(D, a.slice);
+    const int64_t row = CLU ? win.owner() : (int64_t)blockIdx.x * RPC + rg;
+    const bool ok = row < a.N;  // split rows: the grid is N clusters, so always true
     if (WPR == 1 && !ok) return;  // no CTA barrier in a single-warp row group
     const int64_t off = (ok ? row : 0) * (int64_t)D;
 
     uint4 raw[CH];
 #pragma unroll
     for (int k = 0; k < CH; ++k) {
-        const int col = (k * TPR + t) * 8;
-        raw[k] = (ok && col < D) ? ld_unit<kStream>(X + off + col) : make_uint4(0, 0, 0, 0);
+        const int col = win.beg + (k * TPR + t) * 8;
+        raw[k] = (ok && col < win.end) ? ld_unit<kStream>(X + off + col) : make_uint4(0, 0, 0, 0);
     }
     // Chunk k as fp32 pairs. Each pass widens the chunks again rather than keep fp32
     // copies of the row alive across the reductions. So that the compiler does not merge
@@ -346,13 +455,14 @@ norm_fwd_packed_kernel(const FwdArgs a) {
         }
         float s[1] = {s2.x + s2.y};
         row_sum<TPR, RPC, 1>(s, red, 0, rg, wir, lane);
+        if constexpr (CLU) cluster_sum<1>(s, xch, 0, win.cn);
         mu = s[0] * inv_d;
     }
     const float2 nmu = make_float2(-mu, -mu);
     float2 q2 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int k = 0; k < CH; ++k) {
-        if (!(ok && (k * TPR + t) * 8 < D)) continue;
+        if (!(ok && win.beg + (k * TPR + t) * 8 < win.end)) continue;
         float2 f[4];
         if constexpr (OP == kLayer) pairs(k, f, mu);
         else unpack_unit<XT>(raw[k], f);
@@ -364,9 +474,13 @@ norm_fwd_packed_kernel(const FwdArgs a) {
     }
     float q[1] = {q2.x + q2.y};
     row_sum<TPR, RPC, 1>(q, red, 1, rg, wir, lane);
+    if constexpr (CLU) {
+        cluster_sum<1>(q, xch, 1, win.cn);
+        cluster_arrive();  // done reading the other CTAs' slots (waited for before exit)
+    }
     const float rs = rsqrtf(q[0] * inv_d + a.eps);
     if (!ok) return;  // after the last barrier
-    if (t == 0) {
+    if (t == 0 && win.beg == 0) {
         a.rstd[row] = rs;
         if constexpr (OP == kLayer) a.mean[row] = mu;
     }
@@ -379,8 +493,8 @@ norm_fwd_packed_kernel(const FwdArgs a) {
     uint32_t chain = zero & __float_as_uint(rs);
 #pragma unroll
     for (int k = 0; k < CH; ++k) {
-        const int col = (k * TPR + t) * 8;
-        if (col >= D) continue;
+        const int col = win.beg + (k * TPR + t) * 8;
+        if (col >= win.end) continue;
         float2 f[4], g[4], y[4];
         pairs(k, f, rs);
         const int pc = col + (int)chain;
@@ -398,6 +512,7 @@ norm_fwd_packed_kernel(const FwdArgs a) {
         chain = zero & __float_as_uint(y[0].x);
         st_chunk<XT>(as<XT>(a.Y) + off + col, y);
     }
+    if constexpr (CLU) cluster_wait();  // no CTA leaves while another may read its slots
 }
 
 // ----------------------------------------------------------------- backward ---
@@ -406,20 +521,25 @@ norm_fwd_packed_kernel(const FwdArgs a) {
 // slots b*RPC + j*G*RPC (G = gridDim.x), row group rg taking row slot + rg.
 // Dynamic shared memory (RPC > 1): NV x D floats for the fixed-order combine. Compiled
 // for one resident CTA per SM, so the run-time type selection costs registers, not spills.
-template <int OP, int TPR, int RPC, int CH, bool HAS_DS>
+template <int OP, int TPR, int RPC, int CH, bool HAS_DS, bool CLU = false>
 __global__ void __launch_bounds__(TPR * RPC, 1)
 norm_bwd_kernel(const BwdArgs a) {
     pdl_enter();
     static_assert(TPR % 32 == 0 && TPR * RPC <= 1024, "bad launch shape");
+    static_assert(!CLU || RPC == 1, "a split row is one row group per CTA");
     constexpr int WPR = TPR / 32;
     constexpr int NV = (OP == kLayer) ? 2 : 1;
     __shared__ float red[2 * RPC * WPR * NV];
+    __shared__ float xch[CLU ? 2 * NV : 1];
     extern __shared__ float comb[];
 
     const int tid = threadIdx.x;
     const int rg = tid / TPR, t = tid % TPR, wir = t / 32, lane = tid % 32;
     const int D = a.D;
     const float inv_d = 1.0f / (float)D;
+    const Window<CLU> win(D, a.slice);
+    // split rows: every CTA of a cluster runs the cluster's rows (same count, same order)
+    const int64_t owner = win.owner(), owners = win.owners();
 
     float accg[CH];
     float accb[(OP == kLayer) ? CH : 1];
@@ -429,13 +549,12 @@ norm_bwd_kernel(const BwdArgs a) {
     for (int k = 0; k < ((OP == kLayer) ? CH : 1); ++k) accb[k] = 0.f;
 
     int buf = 0;
-    for (int64_t base = (int64_t)blockIdx.x * RPC; base < a.N;
-         base += (int64_t)gridDim.x * RPC, buf ^= 1) {
+    for (int64_t base = owner * RPC; base < a.N; base += owners * RPC, buf ^= 1) {
         const int64_t row = base + rg;
         const bool ok = row < a.N;
         if (WPR == 1 && !ok) continue;  // single-warp row group: no CTA barrier inside
         const int64_t off = (ok ? row : 0) * (int64_t)D;
-        const int lim = ok ? D : 0;
+        const int lim = ok ? win.end : 0;
         const float r = ok ? a.rstd[row] : 0.f;
         const float mu = (OP == kLayer && ok) ? a.mean[row] : 0.f;
 
@@ -446,7 +565,7 @@ norm_bwd_kernel(const BwdArgs a) {
         if constexpr (KEEP) {
 #pragma unroll
             for (int k = 0; k < CH; ++k) {
-                const int col = k * TPR + t;
+                const int col = win.beg + k * TPR + t;
                 xs[k] = col < lim ? ld_elem_stream(a.X, off + col, a.xdt) : 0.f;
                 dys[k] = col < lim ? ld_elem_stream(a.dY, off + col, a.gdt) : 0.f;
             }
@@ -458,7 +577,7 @@ norm_bwd_kernel(const BwdArgs a) {
         for (int i = 0; i < NV; ++i) v[i] = 0.f;
 #pragma unroll
         for (int k = 0; k < CH; ++k) {
-            const int col = k * TPR + t;
+            const int col = win.beg + k * TPR + t;
             const bool in = col < lim;
             const float gm = in ? ld_elem(a.gamma, col, a.wdt) : 0.f;
             float xv, dv;
@@ -475,6 +594,7 @@ norm_bwd_kernel(const BwdArgs a) {
             if constexpr (OP == kLayer) v[NV - 1] += g;
         }
         row_sum<TPR, RPC, NV>(v, red, buf, rg, wir, lane);
+        if constexpr (CLU) cluster_sum<NV>(v, xch, buf, win.cn);
         const float c = v[0] * inv_d;
         const float am = (OP == kLayer) ? v[NV - 1] * inv_d : 0.f;
         if (!ok) continue;
@@ -482,8 +602,8 @@ norm_bwd_kernel(const BwdArgs a) {
         // pass 2: dX and the parameter-gradient sums
 #pragma unroll
         for (int k = 0; k < CH; ++k) {
-            const int col = k * TPR + t;
-            if (col >= D) continue;
+            const int col = win.beg + k * TPR + t;
+            if (col >= win.end) continue;
             const float gm = ld_elem(a.gamma, col, a.wdt);
             float xv, dv;
             if constexpr (KEEP) {
@@ -505,16 +625,18 @@ norm_bwd_kernel(const BwdArgs a) {
 
     // Combine this CTA's row groups in the fixed order rg = 0, 1, ..., RPC-1 and
     // write one partial row per CTA. Thread t owns the same columns in every group.
-    float *pg = a.part_g + (size_t)blockIdx.x * D;
-    float *pb = (OP == kLayer) ? a.part_b + (size_t)blockIdx.x * D : nullptr;
+    if constexpr (CLU) cluster_arrive();  // done reading the other CTAs' slots
+    float *pg = a.part_g + (size_t)owner * D;
+    float *pb = (OP == kLayer) ? a.part_b + (size_t)owner * D : nullptr;
     if constexpr (RPC == 1) {
 #pragma unroll
         for (int k = 0; k < CH; ++k) {
-            const int col = k * TPR + t;
-            if (col >= D) continue;
+            const int col = win.beg + k * TPR + t;
+            if (col >= win.end) continue;
             pg[col] = accg[k];
             if constexpr (OP == kLayer) pb[col] = accb[k];
         }
+        if constexpr (CLU) cluster_wait();  // no CTA leaves while another may read its slots
     } else {
         float *cg = comb;
         float *cb = comb + D;

@@ -153,6 +153,29 @@ namespace mt {
     X(4096, 512, 1, 1, 4, 2)              \
     X(16384, 512, 1, 4, 3, 1)
 
+// Rows wider than MT_SLICE_COLS: a cluster of CL = 2, 4 or 8 CTAs per row (the smallest
+// that covers D), each CTA a slice of ceil(D / CL) columns (rounded up to 8) run with the
+// shape below, X(max slice, TPR, RPC, CH, ...): the 16384-column shape of each table.
+constexpr int kSliceCols = 16384;
+constexpr int kMaxCluster = 8;
+#define MT_FWD_WIDE_RMS(X) X(16384, 512, 1, 4, true, 3)
+#define MT_FWD_WIDE_VEC8(X) X(16384, 512, 1, 4, false, 0)
+#define MT_FWD_WIDE_SCALAR(X) X(16384, 1024, 1, 16)
+#define MT_BWD_WIDE_PIPE(X) X(16384, 512, 1, 4, 3, 1)
+#define MT_BWD_WIDE_PIPE_F32(X) X(8192, 512, 1, 2, 3, 1)
+#define MT_BWD_WIDE_SCALAR(X) X(16384, 512, 1, 32)
+
+// The cluster split of a D-column row over CTAs of at most `cap` columns: false when
+// more than kMaxCluster CTAs would be needed.
+inline bool wide_split(int D, int cap, int *cl, int *slice) {
+    int c = 2;
+    while ((int64_t)c * cap < D) c *= 2;
+    if (c > kMaxCluster) return false;
+    *cl = c;
+    *slice = (((D + c - 1) / c) + 7) / 8 * 8;
+    return true;
+}
+
 // Ring depth: the table's depth, cut so that the ring plus the parameter slots fit the
 // dynamic shared memory a CTA may use (227 KB per SM, shared by `ctas` resident CTAs);
 // 0 when not even two stages fit.
@@ -168,9 +191,13 @@ constexpr int pipe_stages(int base, size_t stage_bytes, size_t param_bytes, int 
 struct LaunchPlan {
     const void *kernel = nullptr;
     int threads = 0;
-    int grid = 0;       // forward: ceil(N / RPC); backward: persistent CTA count P
+    int grid = 0;       // CTAs. forward: ceil(N / RPC) (x cluster); backward: persistent
     size_t smem = 0;    // dynamic shared memory bytes
     int rows_per_cta = 0;
+    int cluster = 1;    // CTAs per cluster (> 1: a row split across the cluster)
+    int slice = 0;      // columns per CTA of a split row
+    // Row owners of a backward, one dgamma/dbeta partial row each.
+    int owners() const { return grid / cluster; }
 };
 
 // Host helpers defined in api.cu (cached per device; thread-safe).
@@ -180,6 +207,9 @@ cudaError_t launch_pdl(const LaunchPlan &p, void *arg, cudaStream_t stream);
 cudaError_t device_sm_count(int device, int *sms);
 cudaError_t cached_occupancy(const void *kernel, int threads, size_t smem, int device,
                              int *blocks_per_sm);
+// Clusters of `cluster` CTAs that can be resident at once (cached per kernel and shape).
+cudaError_t cached_cluster_occupancy(const void *kernel, int threads, size_t smem, int cluster,
+                                     int device, int *clusters);
 
 // Persistent grid: as many CTAs as fit on the device at once, at most one per row slot.
 inline cudaError_t persistent_grid(LaunchPlan *p, int64_t N, int device) {
@@ -191,6 +221,28 @@ inline cudaError_t persistent_grid(LaunchPlan *p, int64_t N, int device) {
     const int64_t slots = (N + p->rows_per_cta - 1) / p->rows_per_cta;
     const int64_t cap = (int64_t)sms * (int64_t)std::max(per_sm, 1);
     p->grid = (int)std::min(slots, cap);
+    return cudaSuccess;
+}
+
+// Persistent grid of clusters for a split row: as many clusters as fit at once, at most
+// one CTA per SM (which bounds the partial rows to SMs / cluster) and one per row.
+inline cudaError_t persistent_cluster_grid(LaunchPlan *p, int64_t N, int device) {
+    int per_sm = 0, sms = 0, fit = 0;
+    cudaError_t e = cached_occupancy(p->kernel, p->threads, p->smem, device, &per_sm);
+    if (e != cudaSuccess) return e;
+    if ((e = device_sm_count(device, &sms)) != cudaSuccess) return e;
+    e = cached_cluster_occupancy(p->kernel, p->threads, p->smem, p->cluster, device, &fit);
+    if (e != cudaSuccess) return e;
+    const int64_t owners = std::min<int64_t>({(int64_t)std::max(fit, 1),
+                                              (int64_t)std::max(sms / p->cluster, 1), N});
+    p->grid = (int)owners * p->cluster;
+    return cudaSuccess;
+}
+
+// Forward grid of a split row: one cluster per row.
+inline cudaError_t cluster_row_grid(LaunchPlan *p, int64_t N) {
+    if (N * p->cluster > (int64_t)INT32_MAX) return cudaErrorInvalidConfiguration;
+    p->grid = (int)N * p->cluster;
     return cudaSuccess;
 }
 
@@ -210,30 +262,45 @@ cudaError_t fwd_scalar_shape(int64_t N, LaunchPlan *p) {
     return cudaSuccess;
 }
 
+template <int OP, int TPR, int RPC, int CH>
+cudaError_t fwd_scalar_wide(int64_t N, int D, int cap, LaunchPlan *p) {
+    if (!wide_split(D, cap, &p->cluster, &p->slice)) return cudaErrorInvalidValue;
+    p->kernel = reinterpret_cast<const void *>(&norm_fwd_kernel<OP, TPR, RPC, CH, true>);
+    p->threads = TPR * RPC;
+    p->smem = 0;
+    p->rows_per_cta = RPC;
+    return cluster_row_grid(p, N);
+}
+
 template <int OP>
 cudaError_t fwd_plan_scalar(int64_t N, int D, LaunchPlan *p) {
 #define MT_TRY(maxd, tpr, rpc, ch) \
     if (D <= maxd) return fwd_scalar_shape<OP, tpr, rpc, ch>(N, p);
     MT_FWD_SHAPES_SCALAR(MT_TRY)
 #undef MT_TRY
-    return cudaErrorInvalidValue;
+#define MT_TRY(cap, tpr, rpc, ch) return fwd_scalar_wide<OP, tpr, rpc, ch>(N, D, cap, p);
+    MT_FWD_WIDE_SCALAR(MT_TRY)
+#undef MT_TRY
 }
 
 // The register floors (MINB) were set for 2-byte types; with fp32 activations or
-// parameters the compiler chooses (MINB 0), since the floors would force spills there.
-template <int OP, int XT, int WT, int TPR, int RPC, int CH, bool PACK, int MINB>
+// parameters the compiler chooses (MINB 0), since the floors would force spills there,
+// except that a split row's kernel asks for one resident CTA (MINB 1), without which
+// the compiler held the fp32 LayerNorm slice to 64 registers and spilled.
+template <int OP, int XT, int WT, int TPR, int RPC, int CH, bool PACK, int MINB, bool CLU = false>
 cudaError_t fwd_vec_shape(int64_t N, LaunchPlan *p) {
-    constexpr int minb = (XT == kF32 || WT == kF32) ? 0 : MINB;
+    constexpr int minb = (XT == kF32 || WT == kF32) ? (CLU ? 1 : 0) : MINB;
     if constexpr (PACK && OP != kAddRms && XT != kF32)
         p->kernel = reinterpret_cast<const void *>(
-            &norm_fwd_packed_kernel<OP, TPR, RPC, CH, minb, XT, WT>);
+            &norm_fwd_packed_kernel<OP, TPR, RPC, CH, minb, XT, WT, CLU>);
     else
         p->kernel = reinterpret_cast<const void *>(
-            &norm_fwd_vec8_kernel<OP, TPR, RPC, CH, minb, XT, WT>);
+            &norm_fwd_vec8_kernel<OP, TPR, RPC, CH, minb, XT, WT, CLU>);
     p->threads = TPR * RPC;
-    p->grid = (int)((N + RPC - 1) / RPC);
     p->smem = 0;
     p->rows_per_cta = RPC;
+    if constexpr (CLU) return cluster_row_grid(p, N);
+    p->grid = (int)((N + RPC - 1) / RPC);
     return cudaSuccess;
 }
 
@@ -252,7 +319,16 @@ cudaError_t fwd_plan_vec(int64_t N, int D, LaunchPlan *p) {
         MT_FWD_SHAPES_FUSED(MT_TRY)
     }
 #undef MT_TRY
-    return kNoVectorPlan;
+    // wider rows: split across a cluster
+#define MT_TRY(cap, tpr, rpc, ch, pack, minb)                                     \
+    if (!wide_split(D, cap, &p->cluster, &p->slice)) return kNoVectorPlan;       \
+    return fwd_vec_shape<OP, XT, WT, tpr, rpc, ch, pack, minb, true>(N, p);
+    if constexpr (OP == kRms && !SHORT) {
+        MT_FWD_WIDE_RMS(MT_TRY)
+    } else {
+        MT_FWD_WIDE_VEC8(MT_TRY)
+    }
+#undef MT_TRY
 }
 
 // ----------------------------------------------------------------- backward ---
@@ -267,17 +343,29 @@ cudaError_t bwd_scalar_shape(int64_t N, int D, int device, LaunchPlan *p) {
     return persistent_grid(p, N, device);
 }
 
+template <int OP, int TPR, int RPC, int CH, bool HAS_DS>
+cudaError_t bwd_scalar_wide(int64_t N, int D, int cap, int device, LaunchPlan *p) {
+    if (!wide_split(D, cap, &p->cluster, &p->slice)) return cudaErrorInvalidValue;
+    p->kernel = reinterpret_cast<const void *>(&norm_bwd_kernel<OP, TPR, RPC, CH, HAS_DS, true>);
+    p->threads = TPR * RPC;
+    p->smem = 0;
+    p->rows_per_cta = RPC;
+    return persistent_cluster_grid(p, N, device);
+}
+
 template <int OP, bool HAS_DS>
 cudaError_t bwd_plan_scalar(int64_t N, int D, int device, LaunchPlan *p) {
 #define MT_TRY(maxd, tpr, rpc, ch) \
     if (D <= maxd) return bwd_scalar_shape<OP, tpr, rpc, ch, HAS_DS>(N, D, device, p);
     MT_BWD_SHAPES_SCALAR(MT_TRY)
 #undef MT_TRY
-    return cudaErrorInvalidValue;
+#define MT_TRY(cap, tpr, rpc, ch) return bwd_scalar_wide<OP, tpr, rpc, ch, HAS_DS>(N, D, cap, device, p);
+    MT_BWD_WIDE_SCALAR(MT_TRY)
+#undef MT_TRY
 }
 
 template <int OP, int XT, int WT, int GT, int TPR, int RPC, int CH, int STAGES, bool HAS_DS,
-          int CTAS>
+          int CTAS, bool CLU = false>
 cudaError_t bwd_pipe_shape(int64_t N, int device, LaunchPlan *p) {
     constexpr int NPAR = (CH <= 2) ? 0 : 1;
     using G = PipeGeom<CH, XT, WT, GT>;
@@ -290,10 +378,11 @@ cudaError_t bwd_pipe_shape(int64_t N, int device, LaunchPlan *p) {
         using R = Ring<S, G::CK, TPR * RPC, G::UX, G::UG, HAS_DS, G::UW, NPAR>;
         static_assert(R::kBytes <= kMaxDynSmem, "ring too large");
         p->kernel = reinterpret_cast<const void *>(
-            &norm_bwd_pipe_kernel<OP, TPR, RPC, CH, S, HAS_DS, CTAS, XT, WT, GT>);
+            &norm_bwd_pipe_kernel<OP, TPR, RPC, CH, S, HAS_DS, CTAS, XT, WT, GT, CLU>);
         p->threads = TPR * RPC;
         p->smem = R::kBytes;
         p->rows_per_cta = RPC;
+        if constexpr (CLU) return persistent_cluster_grid(p, N, device);
         return persistent_grid(p, N, device);
     }
 }
@@ -320,7 +409,16 @@ cudaError_t bwd_plan_vec(int64_t N, int D, int device, LaunchPlan *p) {
         MT_BWD_PIPE_SHAPES_RMS(MT_TRY)
     }
 #undef MT_TRY
-    return kNoVectorPlan;
+    // wider rows: split across a cluster
+#define MT_TRY(cap, tpr, rpc, ch, st, ctas)                                                   \
+    if (!wide_split(D, cap, &p->cluster, &p->slice)) return kNoVectorPlan;                   \
+    return bwd_pipe_shape<OP, XT, WT, GT, tpr, rpc, ch, st, HAS_DS, ctas, true>(N, device, p);
+    if constexpr (XT == kF32 && WT == kF32 && GT == kF32) {
+        MT_BWD_WIDE_PIPE_F32(MT_TRY)
+    } else {
+        MT_BWD_WIDE_PIPE(MT_TRY)
+    }
+#undef MT_TRY
 }
 
 // ------------------------------------------------------------ entry points ---

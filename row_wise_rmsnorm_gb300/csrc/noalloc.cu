@@ -45,9 +45,11 @@ extern "C" mt_status_t mt_rmsnorm_backward_noalloc(const void *X, const void *ga
                                                    float *dgamma, int64_t N, int64_t D,
                                                    mt_stream_t stream) {
     // Argument errors are reported before any CUDA call, as for every other entry point.
-    if (!X || !gamma || !dY || !rstd || !dX || !dgamma) return MT_ERR_INVALID_ARG;
-    if (N < 1 || D < 1) return MT_ERR_INVALID_ARG;
+    if (N < 0 || D < 1) return MT_ERR_INVALID_ARG;
     if (D > MT_MAX_COLS || N > (int64_t)INT32_MAX) return MT_ERR_UNSUPPORTED;
+    if (N == 0)  // an empty batch: dgamma = 0, no scratch
+        return mt_rmsnorm_backward_ws(X, gamma, dY, rstd, dX, dgamma, N, D, nullptr, 0, stream);
+    if (!X || !gamma || !dY || !rstd || !dX || !dgamma) return MT_ERR_INVALID_ARG;
 
     int device = 0;
     cudaError_t e = cudaGetDevice(&device);

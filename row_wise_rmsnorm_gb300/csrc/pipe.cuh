@@ -26,10 +26,6 @@
 
 namespace mt {
 
-__device__ __forceinline__ uint32_t smem_addr(const void *p) {
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-
 // 16-byte global -> shared async copy, cached in L2 only.
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
@@ -87,20 +83,23 @@ struct PipeGeom {
     static constexpr int UW = chunk_units<WT, PPC>();
 };
 
-// Copy this thread's chunks of the parameter vector into its ring parameter slots.
+// Copy this thread's chunks of the parameter columns [beg, end) into its ring parameter
+// slots.
 template <class R, int WT, int PPC, int CK, int TPR, int THREADS>
-__device__ __forceinline__ void stage_param(uint4 *ring, const void *src, int D, int t, int tid) {
+__device__ __forceinline__ void stage_param(uint4 *ring, const void *src, int beg, int end, int t,
+                                            int tid) {
 #pragma unroll
     for (int k = 0; k < CK; ++k) {
-        const int col = (k * TPR + t) * 2 * PPC;
-        if (col < D) cp_chunk<WT, PPC, THREADS>(&ring[R::param(k, tid)], as<WT>(src) + col);
+        const int col = beg + (k * TPR + t) * 2 * PPC;
+        if (col < end) cp_chunk<WT, PPC, THREADS>(&ring[R::param(k, tid)], as<WT>(src) + col);
     }
 }
 
-// Iterations every row group of this CTA runs (uniform across the CTA).
-__device__ __forceinline__ int cta_iterations(int64_t N, int rpc) {
-    const int64_t base = (int64_t)blockIdx.x * rpc;
-    const int64_t stride = (int64_t)gridDim.x * rpc;
+// Iterations every row group of row owner `owner` (of `owners`) runs (uniform across the
+// CTA, and across a cluster that splits its rows).
+__device__ __forceinline__ int owner_iterations(int64_t N, int rpc, int64_t owner, int64_t owners) {
+    const int64_t base = owner * rpc;
+    const int64_t stride = owners * rpc;
     return base < N ? (int)((N - base + stride - 1) / stride) : 0;
 }
 
@@ -108,9 +107,11 @@ __device__ __forceinline__ int cta_iterations(int64_t N, int rpc) {
 // Dynamic shared memory: the ring (and gamma when CH > 2); after the row loop the ring
 // is reused for the fixed-order combine of the CTA's row groups (NV x D floats).
 // Compiled for CTAS resident CTAs per SM (it caps the registers per thread). X (or S) and
-// dX are of type XT, gamma of type WT, dY and dS of type GT.
+// dX are of type XT, gamma of type WT, dY and dS of type GT. CLU: rows split across a
+// cluster (kernels.cuh, "cluster split"); the cluster is the row owner and writes one
+// partial row, each CTA its slice of it.
 template <int OP, int TPR, int RPC, int CH, int STAGES, bool HAS_DS, int CTAS, int XT, int WT,
-          int GT>
+          int GT, bool CLU = false>
 __global__ void __launch_bounds__(TPR * RPC, CTAS)
 norm_bwd_pipe_kernel(const BwdArgs a) {
     constexpr int THREADS = TPR * RPC;
@@ -121,7 +122,9 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
     constexpr int PPC = G::PPC, EPC = G::EPC, CK = G::CK;
     using R = Ring<STAGES, CK, THREADS, G::UX, G::UG, HAS_DS, G::UW, KEEP ? 0 : 1>;
     static_assert(TPR % 32 == 0 && THREADS <= 1024, "bad launch shape");
+    static_assert(!CLU || RPC == 1, "a split row is one row group per CTA");
     __shared__ float red[2 * RPC * WPR * NV];
+    __shared__ float xch[CLU ? 2 * NV : 1];
     extern __shared__ __align__(16) uint4 ring[];
 
     pdl_enter();  // the dependent parameter reduction launches now and waits for this grid
@@ -130,19 +133,21 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
     const int rg = tid / TPR, t = tid % TPR, wir = t / 32, lane = tid % 32;
     const int D = a.D;
     const float inv_d = 1.0f / (float)D;
-    const int64_t stride = (int64_t)gridDim.x * RPC;
-    const int64_t first = (int64_t)blockIdx.x * RPC + rg;
-    const int iters = cta_iterations(a.N, RPC);
+    const Window<CLU> win(D, a.slice);
+    const int64_t owner = win.owner(), owners = win.owners();
+    const int64_t stride = owners * RPC;
+    const int64_t first = owner * RPC + rg;
+    const int iters = owner_iterations(a.N, RPC, owner, owners);
 
     float2 gam[KEEP ? CK : 1][PPC];
     if constexpr (KEEP) {
 #pragma unroll
         for (int k = 0; k < CK; ++k) {
-            const int col = (k * TPR + t) * EPC;
-            ld_chunk<WT, kReadOnly, PPC>(as<WT>(a.gamma) + col, col < D, gam[k]);
+            const int col = win.beg + (k * TPR + t) * EPC;
+            ld_chunk<WT, kReadOnly, PPC>(as<WT>(a.gamma) + col, col < win.end, gam[k]);
         }
     } else {
-        stage_param<R, WT, PPC, CK, TPR, THREADS>(ring, a.gamma, D, t, tid);
+        stage_param<R, WT, PPC, CK, TPR, THREADS>(ring, a.gamma, win.beg, win.end, t, tid);
     }
     cp_async_commit();
 
@@ -163,8 +168,8 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
             const int64_t off = row * (int64_t)D;
 #pragma unroll
             for (int k = 0; k < CK; ++k) {
-                const int col = (k * TPR + t) * EPC;
-                if (col < D) {
+                const int col = win.beg + (k * TPR + t) * EPC;
+                if (col < win.end) {
                     cp_chunk<XT, PPC, THREADS>(&ring[R::index(slot, 0, k, tid)], as<XT>(a.X) + off + col);
                     cp_chunk<GT, PPC, THREADS>(&ring[R::index(slot, 1, k, tid)], as<GT>(a.dY) + off + col);
                     if constexpr (HAS_DS)
@@ -217,7 +222,7 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
         float2 v0 = make_float2(0.f, 0.f), v1 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < CK; ++k) {
-            const bool v = ok && (k * TPR + t) * EPC < D;
+            const bool v = ok && win.beg + (k * TPR + t) * EPC < win.end;
             float2 xk[PPC], dk[PPC], g[PPC];
             if (v) {
                 load_xd(k, xk, dk);
@@ -247,6 +252,7 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
         vv[0] = v0.x + v0.y;
         if constexpr (OP == kLayer) vv[NV - 1] = v1.x + v1.y;
         row_sum<TPR, RPC, NV, true>(vv, red, buf, rg, wir, lane);
+        if constexpr (CLU) cluster_sum<NV>(vv, xch, buf, win.cn);
         const float c = r * vv[0] * inv_d;                           // mean_j g*xhat
         const float am = (OP == kLayer) ? vv[NV - 1] * inv_d : 0.f;  // mean_j g
         if (!ok) continue;
@@ -258,8 +264,8 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
         const float2 ra2 = make_float2(-r * am, -r * am);
 #pragma unroll
         for (int k = 0; k < CK; ++k) {
-            const int col = (k * TPR + t) * EPC;
-            if (col >= D) continue;
+            const int col = win.beg + (k * TPR + t) * EPC;
+            if (col >= win.end) continue;
             float2 xk[PPC], dk[PPC], g[PPC], o[PPC];
             if constexpr (KEEP) {
 #pragma unroll
@@ -285,16 +291,17 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
         }
     }
     cp_async_wait<0>();
+    if constexpr (CLU) cluster_arrive();  // done reading the other CTAs' slots
 
     // Partials: the CTA's row groups are combined in the fixed order rg = 0, 1, ... and
-    // one fp32 partial row per CTA is written.
-    float *pg = a.part_g + (size_t)blockIdx.x * D;
-    float *pb = (OP == kLayer) ? a.part_b + (size_t)blockIdx.x * D : nullptr;
+    // one fp32 partial row per row owner (CTA, or cluster) is written.
+    float *pg = a.part_g + (size_t)owner * D;
+    float *pb = (OP == kLayer) ? a.part_b + (size_t)owner * D : nullptr;
     if constexpr (RPC == 1) {
 #pragma unroll
         for (int k = 0; k < CK; ++k) {
-            const int col = (k * TPR + t) * EPC;
-            if (col >= D) continue;
+            const int col = win.beg + (k * TPR + t) * EPC;
+            if (col >= win.end) continue;
             float4 *g4 = reinterpret_cast<float4 *>(pg + col);
 #pragma unroll
             for (int q = 0; q < PPC / 2; ++q)
@@ -308,6 +315,7 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
                                         accb[k][2 * q + 1].y);
             }
         }
+        if constexpr (CLU) cluster_wait();  // no CTA leaves while another may read its slots
     } else {
         __syncthreads();  // every thread is done with the ring
         float2 *cg2 = reinterpret_cast<float2 *>(ring);

@@ -135,18 +135,20 @@ cudaError_t ce_plan(int64_t N, int D, bool vec8, int xdt, LaunchPlan *p) {
     return ce_plan_t<BWD, true, kF32>(N, D, p);
 }
 
+// N = 0 is a valid, empty batch.
 mt_status_t check_rows(int64_t N, int64_t D, int64_t max_cols) {
-    if (N < 1 || D < 1) return MT_ERR_INVALID_ARG;
+    if (N < 0 || D < 1) return MT_ERR_INVALID_ARG;
     if (D > max_cols || N > (int64_t)INT32_MAX) return MT_ERR_UNSUPPORTED;
     return MT_OK;
 }
 
 mt_status_t softmax_impl(bool bwd, int dt, const void *in, const void *dY, void *out, int64_t N,
                          int64_t D, int log_softmax, mt_stream_t stream) {
-    if (!in || !out || (bwd && !dY)) return MT_ERR_INVALID_ARG;
     if (!valid_dtype(dt)) return MT_ERR_INVALID_ARG;
-    mt_status_t s = check_rows(N, D, MT_MAX_COLS);
+    mt_status_t s = check_rows(N, D, MT_MAX_SOFTMAX_COLS);
     if (s != MT_OK) return s;
+    if (N == 0) return MT_OK;
+    if (!in || !out || (bwd && !dY)) return MT_ERR_INVALID_ARG;
     const size_t act = (size_t)N * (size_t)D * dtype_bytes(dt);
     if (overlaps({{out, act}}, {{in, act}, {dY, bwd ? act : 0}})) return MT_ERR_INVALID_ARG;
     SoftmaxArgs a{};
@@ -203,12 +205,21 @@ extern "C" mt_status_t mt_cross_entropy_forward(mt_dtype_t dtype, const void *lo
                                                 float *n_valid, mt_stream_t stream) {
     const int dt = (int)dtype;
     const bool reduce = reduction != MT_REDUCTION_NONE;
-    if (!logits || !targets || !loss_rows || !lse || (reduce && (!loss_out || !n_valid)))
-        return MT_ERR_INVALID_ARG;
     if (!valid_dtype(dt)) return MT_ERR_INVALID_ARG;
     mt_status_t s = check_ce_options((int)reduction, label_smoothing, z_loss);
     if (s != MT_OK) return s;
     if ((s = check_rows(N, D, MT_MAX_CE_COLS)) != MT_OK) return s;
+    if (reduce && (!loss_out || !n_valid || loss_out == n_valid)) return MT_ERR_INVALID_ARG;
+    if (N == 0) {
+        // an empty batch: the sum is 0, the mean over no valid row is 0 (as when every
+        // row is ignored), and no row is valid
+        if (!reduce) return MT_OK;
+        cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+        cudaError_t e = cudaMemsetAsync(loss_out, 0, sizeof(float), st);
+        if (e == cudaSuccess) e = cudaMemsetAsync(n_valid, 0, sizeof(float), st);
+        return e == cudaSuccess ? MT_OK : fail(e);
+    }
+    if (!logits || !targets || !loss_rows || !lse) return MT_ERR_INVALID_ARG;
     const size_t act = (size_t)N * (size_t)D * dtype_bytes(dt), row = (size_t)N * 4;
     if (!reduce) { loss_out = nullptr; n_valid = nullptr; }
     if (overlaps({{loss_rows, row}, {lse, row}, {loss_out, 4}, {n_valid, 4}},
@@ -259,13 +270,14 @@ extern "C" mt_status_t mt_cross_entropy_backward(mt_dtype_t dtype, const void *l
                                                  const float *n_valid, void *dlogits,
                                                  mt_stream_t stream) {
     const int dt = (int)dtype;
-    if (!logits || !targets || !lse || !dloss || !dlogits ||
-        (reduction == MT_REDUCTION_MEAN && !n_valid))
-        return MT_ERR_INVALID_ARG;
     if (!valid_dtype(dt)) return MT_ERR_INVALID_ARG;
     mt_status_t s = check_ce_options((int)reduction, label_smoothing, z_loss);
     if (s != MT_OK) return s;
     if ((s = check_rows(N, D, MT_MAX_CE_COLS)) != MT_OK) return s;
+    if (N == 0) return MT_OK;  // an empty batch: no logit gradient to write
+    if (!logits || !targets || !lse || !dloss || !dlogits ||
+        (reduction == MT_REDUCTION_MEAN && !n_valid))
+        return MT_ERR_INVALID_ARG;
     const size_t act = (size_t)N * (size_t)D * dtype_bytes(dt), row = (size_t)N * 4;
     const size_t dl = (reduction == MT_REDUCTION_NONE) ? row : 4;
     if (overlaps({{dlogits, act}}, {{logits, act}, {targets, (size_t)N * 8}, {lse, row},

@@ -70,7 +70,7 @@ def test_rmsnorm_forward_validation(lib, case):
     args = dict(X=A, g=B, Y=C, r=E, N=4, D=64, eps=1e-5)
     expect = INV
     if case == "null": args["X"] = None
-    if case == "n0": args["N"] = 0
+    if case == "n0": args["N"], expect = 0, mt.MT_OK  # an empty batch: no-op, no CUDA call
     if case == "d0": args["D"] = 0
     if case == "nneg": args["N"] = -3
     if case == "dwide": args["D"], expect = mt.MT_MAX_COLS + 1, UNS
@@ -90,8 +90,9 @@ def test_backward_validation(lib):
     N, D = 8, 64
     # RMSNorm backward: NULLs, shapes, dX aliasing dY, dgamma aliasing gamma
     assert lib.mt_rmsnorm_backward(A, B, C, E, F, None, N, D, None) == INV
-    assert lib.mt_rmsnorm_backward(A, B, C, E, F, G, 0, D, None) == INV
-    assert lib.mt_rmsnorm_backward(A, B, C, E, F, G, N, 20000, None) == UNS
+    assert lib.mt_rmsnorm_backward(A, B, C, E, F, G, -1, D, None) == INV
+    assert lib.mt_rmsnorm_backward(None, None, None, None, None, None, 0, D, None) == INV
+    assert lib.mt_rmsnorm_backward(A, B, C, E, F, G, N, mt.MT_MAX_COLS + 1, None) == UNS
     assert lib.mt_rmsnorm_backward(A, B, C, E, C, G, N, D, None) == INV
     assert lib.mt_rmsnorm_backward(A, B, C, E, F, B, N, D, None) == INV
     # _ws: NULL / misaligned / overlapping workspace
@@ -139,8 +140,8 @@ def test_explicit_dtype_validation(lib):
     # so use a valid eps and an invalid shape to stay away from CUDA)
     half = 2 * N * D
     assert fwd(RMS, F32, F32, A, None, B, None, None, A + half, None, E, N, D, 1e-5, None) == INV
-    assert fwd(RMS, F16, F16, A, None, B, None, None, A + half, None, E, N, 20000, 1e-5,
-               None) == UNS
+    assert fwd(RMS, F16, F16, A, None, B, None, None, A + half, None, E, N,
+               mt.MT_MAX_COLS + 1, 1e-5, None) == UNS
     # dY in fp32 overlapping dX placed right after an fp16-sized dY
     assert bwd(RMS, F16, F16, F32, A, B, C, None, None, E, C + half, G, None, N, D, None, 0,
                None) == INV
@@ -154,7 +155,10 @@ def test_softmax_and_cross_entropy_validation(lib):
     assert lib.mt_softmax_forward(F16, None, B, N, D, 0, None) == INV
     assert lib.mt_softmax_forward(5, A, B, N, D, 0, None) == INV
     assert lib.mt_softmax_forward(F16, A, A, N, D, 1, None) == INV          # in place
-    assert lib.mt_softmax_forward(F16, A, B, N, mt.MT_MAX_COLS + 1, 0, None) == UNS
+    assert lib.mt_softmax_forward(F16, A, B, N, mt.MT_MAX_SOFTMAX_COLS + 1, 0, None) == UNS
+    assert lib.mt_softmax_forward(F16, None, None, 0, D, 0, None) == mt.MT_OK      # empty batch
+    assert lib.mt_softmax_backward(F16, None, None, None, 0, D, 1, None) == mt.MT_OK
+    assert lib.mt_softmax_forward(F16, A, B, -1, D, 0, None) == INV
     assert lib.mt_softmax_backward(F32, A, None, C, N, D, 0, None) == INV
     assert lib.mt_softmax_backward(F32, A, B, B, N, D, 0, None) == INV      # dX aliases dY
     ce_f, ce_b = lib.mt_cross_entropy_forward, lib.mt_cross_entropy_backward
@@ -168,6 +172,12 @@ def test_softmax_and_cross_entropy_validation(lib):
     assert ce_f(F16, A, B, N, D, -100, 0.0, 0.0, NONE, C, C, None, None, None) == INV  # lse==rows
     assert ce_b(F16, A, B, C, N, D, -100, 0.0, 0.0, MEAN, E, None, G, None) == INV    # n_valid
     assert ce_b(F16, A, B, C, N, D, -100, 0.0, 0.0, NONE, E, None, A, None) == INV    # dX == X
+    # empty batch: NONE and the backward are no-ops (no CUDA call); SUM/MEAN still need
+    # their two distinct scalar outputs
+    assert ce_f(F16, None, None, 0, D, -100, 0.0, 0.0, NONE, None, None, None, None, None) == 0
+    assert ce_b(F16, None, None, None, 0, D, -100, 0.0, 0.0, MEAN, None, None, None, None) == 0
+    assert ce_f(F16, None, None, 0, D, -100, 0.0, 0.0, SUM, None, None, None, G, None) == INV
+    assert ce_f(F16, None, None, 0, D, -100, 0.0, 0.0, SUM, None, None, G, G, None) == INV
     assert lib.mt_last_cuda_error() == 0  # nothing reached CUDA
 
 
@@ -175,8 +185,11 @@ def test_workspace_size_validation(lib):
     out = ctypes.c_size_t(0)
     assert lib.mt_norm_backward_workspace_size(0, 8, 64, 0, None) == INV
     assert lib.mt_norm_backward_workspace_size(7, 8, 64, 0, ctypes.byref(out)) == INV
-    assert lib.mt_norm_backward_workspace_size(0, 0, 64, 0, ctypes.byref(out)) == INV
-    assert lib.mt_norm_backward_workspace_size(1, 8, 20000, 0, ctypes.byref(out)) == UNS
+    assert lib.mt_norm_backward_workspace_size(0, -1, 64, 0, ctypes.byref(out)) == INV
+    assert lib.mt_norm_backward_workspace_size(1, 8, mt.MT_MAX_COLS + 1, 0, ctypes.byref(out)) == UNS
+    out.value = 7
+    assert lib.mt_norm_backward_workspace_size(0, 0, 64, 0, ctypes.byref(out)) == mt.MT_OK
+    assert out.value == 0  # an empty batch needs no workspace
     assert lib.mt_norm_backward_workspace_size(2, 8, 64, -1, ctypes.byref(out)) == INV
     assert lib.mt_last_cuda_error() == 0  # nothing reached CUDA
 

@@ -6,9 +6,10 @@ import torch
 import workloads as W
 
 
-def test_five_workloads():
+def test_seven_workloads():
     assert W.WORKLOAD_ORDER == ["rmsnorm_17x257", "layernorm_128x1024", "rmsnorm_16384x4096",
-                                "add_rmsnorm_32768x4096", "layernorm_2048x16384"]
+                                "add_rmsnorm_32768x4096", "layernorm_2048x16384",
+                                "rmsnorm_4096x32768", "layernorm_1024x131072"]
 
 
 @pytest.mark.parametrize("name", W.WORKLOAD_ORDER)

@@ -29,7 +29,8 @@ def test_noalloc_rejects_bad_arguments_without_cuda():
     lib = mt.load()
     f = lib.mt_rmsnorm_backward_noalloc
     assert f(A, B, C, E, F, None, 8, 64, None) == mt.MT_ERR_INVALID_ARG
-    assert f(A, B, C, E, F, G, 0, 64, None) == mt.MT_ERR_INVALID_ARG
+    assert f(A, B, C, E, F, G, -1, 64, None) == mt.MT_ERR_INVALID_ARG
+    assert f(None, None, None, None, None, None, 0, 64, None) == mt.MT_ERR_INVALID_ARG
     assert f(A, B, C, E, F, G, 8, 0, None) == mt.MT_ERR_INVALID_ARG
     assert f(A, B, C, E, F, G, 8, mt.MT_MAX_COLS + 1, None) == mt.MT_ERR_UNSUPPORTED
 

@@ -10,7 +10,7 @@ rounded to its storage type (round-to-nearest-even; fp16 unless a call asks for
 bf16 or fp32 per role) before either side sees it. ``N(m, s)`` means mean m and
 standard deviation s.
 
-The five workloads (name: op, N x D, recipe):
+The seven workloads (name: op, N x D, recipe):
   rmsnorm_17x257        RMSNorm, ragged width. X, dY ~ N(0,1); gamma = 1 + 0.1 N(0,1); eps 1e-6.
   layernorm_128x1024    LayerNorm. X, dY ~ N(0,1); gamma = 1 + 0.1 N(0,1);
                         beta = 0.1 N(0,1); eps 1e-5.
@@ -22,6 +22,11 @@ The five workloads (name: op, N x D, recipe):
   layernorm_2048x16384  wide-row LayerNorm with a large mean (cancellation stress).
                         X = 50 + N(0,1); gamma = 1 + 0.1 N(0,1); beta = N(0, 0.1);
                         dY ~ N(0, 0.01); eps 1e-5.
+  rmsnorm_4096x32768    RMSNorm on rows wider than one CTA's slice (a cluster of 2 CTAs per
+                        row); the rmsnorm_16384x4096 recipe.
+  layernorm_1024x131072 LayerNorm at the widest supported row (a cluster of 8 CTAs per
+                        row). X, dY ~ N(0,1) and N(0, 0.01); gamma = 1 + 0.1 N(0,1);
+                        beta = N(0, 0.1); eps 1e-5.
 """
 from __future__ import annotations
 
@@ -59,6 +64,9 @@ WORKLOADS = {
         Workload("rmsnorm_16384x4096", RMSNORM, 16384, 4096, 1e-6, "row_scaled", 0.01),
         Workload("add_rmsnorm_32768x4096", ADD_RMSNORM, 32768, 4096, 1e-6, "normal", 0.01),
         Workload("layernorm_2048x16384", LAYERNORM, 2048, 16384, 1e-5, "shifted", 0.01,
+                 beta_std=0.1),
+        Workload("rmsnorm_4096x32768", RMSNORM, 4096, 32768, 1e-6, "row_scaled", 0.01),
+        Workload("layernorm_1024x131072", LAYERNORM, 1024, 131072, 1e-5, "normal", 0.01,
                  beta_std=0.1),
     )
 }
