@@ -138,6 +138,9 @@ __device__ __forceinline__ float ld_cluster(const float *local, unsigned r) {
 // identical). xch: 2 x NV shared floats; alternate `buf` between consecutive calls (a
 // CTA rewrites a slot only after the next call's barrier, which every CTA reaches only
 // once it has read the slot). Every thread of every CTA of the cluster must call it.
+// After the barrier, lane r of every warp reads CTA r's totals (one distributed
+// shared-memory load each) and a warp butterfly adds them: the same operands in the
+// same lanes everywhere, so every thread of the cluster gets the same bits.
 template <int NV>
 __device__ __forceinline__ void cluster_sum(float (&v)[NV], float *xch, int buf, unsigned n) {
     float *slot = xch + buf * NV;
@@ -147,12 +150,41 @@ __device__ __forceinline__ void cluster_sum(float (&v)[NV], float *xch, int buf,
     }
     cluster_arrive();
     cluster_wait();
+    const unsigned lane = threadIdx.x & 31u;
 #pragma unroll
-    for (int i = 0; i < NV; ++i) v[i] = 0.f;
-    for (unsigned r = 0; r < n; ++r) {
-#pragma unroll
-        for (int i = 0; i < NV; ++i) v[i] += ld_cluster(slot + i, r);
+    for (int i = 0; i < NV; ++i) v[i] = warp_sum(lane < n ? ld_cluster(slot + i, lane) : 0.f);
+}
+
+// LayerNorm statistics of a split row in one exchange. Each CTA has the sum s and the
+// centred second moment m2 (about its own slice mean) of its n columns. With the row
+// mean mu = (sum of the s) / D, the row's centred sum of squares is exactly
+//   sum over slices of ( m2 + n (s/n - mu)^2 )
+// (within-slice plus between-slice parts; Chan, Golub and LeVeque, "Algorithms for
+// computing the sample variance: analysis and recommendations", 1983), as stable as the
+// two-pass form since every term is a sum of squares about a mean. xch: 4 shared floats
+// (2 buffers of {s, m2}); v = {s, m2} in, {row mean, row centred sum of squares} out.
+// Same calling rules and lane-parallel combination as cluster_sum.
+__device__ __forceinline__ void cluster_ln_stats(float (&v)[2], float *xch, int buf, unsigned n,
+                                                 int D, int slice) {
+    float *slot = xch + buf * 2;
+    if (threadIdx.x == 0) {
+        slot[0] = v[0];
+        slot[1] = v[1];
     }
+    cluster_arrive();
+    cluster_wait();
+    const unsigned lane = threadIdx.x & 31u;
+    float sr = 0.f, m2r = 0.f, nr = 0.f;
+    if (lane < n) {
+        const int beg = (int)lane * slice;
+        nr = (float)max(0, min(D, beg + slice) - beg);
+        sr = ld_cluster(slot, lane);
+        m2r = ld_cluster(slot + 1, lane);
+    }
+    const float mu = warp_sum(sr) / (float)D;
+    const float dev = nr > 0.f ? sr / nr - mu : 0.f;
+    v[0] = mu;
+    v[1] = warp_sum(m2r + nr * dev * dev);
 }
 
 // This CTA's column window and row owner. Not split: columns [0, D) and the plain CTA
@@ -233,7 +265,7 @@ norm_fwd_kernel(const FwdArgs a) {
     static_assert(!CLU || RPC == 1, "a split row is one row group per CTA");
     constexpr int WPR = TPR / 32;
     __shared__ float red[2 * RPC * WPR];
-    __shared__ float xch[CLU ? 2 : 1];
+    __shared__ float xch[CLU ? 4 : 1];  // cluster_sum (2) or cluster_ln_stats (4)
 
     const int tid = threadIdx.x;
     const int rg = tid / TPR, t = tid % TPR, wir = t / 32, lane = tid % 32;
@@ -260,25 +292,31 @@ norm_fwd_kernel(const FwdArgs a) {
         }
     }
 
-    float mu = 0.f;
+    // LayerNorm: the mean, then the centred second moment (two passes, from registers).
+    // A split row centres on its slice's own mean and combines the slices afterwards.
+    float mu = 0.f, s[1] = {0.f};
     if constexpr (OP == kLayer) {
-        float s[1] = {0.f};
 #pragma unroll
         for (int k = 0; k < CH; ++k) s[0] += x[k];
         row_sum<TPR, RPC, 1>(s, red, 0, rg, wir, lane);
-        if constexpr (CLU) cluster_sum<1>(s, xch, 0, win.cn);
-        mu = s[0] / (float)D;
+        mu = s[0] / (float)(CLU ? max(win.end - win.beg, 1) : D);
     }
     float q[1] = {0.f};
 #pragma unroll
     for (int k = 0; k < CH; ++k) {
-        // LayerNorm: centred second moment (two-pass, from registers)
         const float d = (OP == kLayer) ? ((win.beg + k * TPR + t) < lim ? x[k] - mu : 0.f) : x[k];
         q[0] += d * d;
     }
     row_sum<TPR, RPC, 1>(q, red, 1, rg, wir, lane);
     if constexpr (CLU) {
-        cluster_sum<1>(q, xch, 1, win.cn);
+        if constexpr (OP == kLayer) {
+            float v[2] = {s[0], q[0]};
+            cluster_ln_stats(v, xch, 0, win.cn, D, a.slice);
+            mu = v[0];
+            q[0] = v[1];
+        } else {
+            cluster_sum<1>(q, xch, 0, win.cn);
+        }
         cluster_arrive();  // done reading the other CTAs' slots (waited for before exit)
     }
     const float rs = rsqrtf(q[0] / (float)D + a.eps);
@@ -314,7 +352,7 @@ norm_fwd_vec8_kernel(const FwdArgs a) {
     static_assert(!CLU || RPC == 1, "a split row is one row group per CTA");
     constexpr int WPR = TPR / 32;
     __shared__ float red[2 * RPC * WPR];
-    __shared__ float xch[CLU ? 2 : 1];
+    __shared__ float xch[CLU ? 4 : 1];  // cluster_sum (2) or cluster_ln_stats (4)
 
     const int tid = threadIdx.x;
     const int rg = tid / TPR, t = tid % TPR, wir = t / 32, lane = tid % 32;
@@ -340,19 +378,20 @@ norm_fwd_vec8_kernel(const FwdArgs a) {
             if (v) st_chunk<XT>(as<XT>(a.S) + off + col, x[k]);
         }
     }
-    float mu = 0.f;
+    // LayerNorm: the mean, then the centred second moment (two passes, from registers).
+    // A split row centres on its slice's own mean and combines the slices afterwards.
+    float mu = 0.f, s[1] = {0.f};
     if constexpr (OP == kLayer) {
         float2 s2 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < CH; ++k)
 #pragma unroll
             for (int p = 0; p < 4; ++p) s2 = __fadd2_rn(s2, x[k][p]);
-        float s[1] = {s2.x + s2.y};
+        s[0] = s2.x + s2.y;
         row_sum<TPR, RPC, 1>(s, red, 0, rg, wir, lane);
-        if constexpr (CLU) cluster_sum<1>(s, xch, 0, win.cn);
-        mu = s[0] * inv_d;
+        mu = CLU ? s[0] / (float)max(win.end - win.beg, 1) : s[0] * inv_d;
     }
-    const float2 nmu = make_float2(-mu, -mu);
+    float2 nmu = make_float2(-mu, -mu);
     float2 q2 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int k = 0; k < CH; ++k) {
@@ -366,7 +405,15 @@ norm_fwd_vec8_kernel(const FwdArgs a) {
     float q[1] = {q2.x + q2.y};
     row_sum<TPR, RPC, 1>(q, red, 1, rg, wir, lane);
     if constexpr (CLU) {
-        cluster_sum<1>(q, xch, 1, win.cn);
+        if constexpr (OP == kLayer) {
+            float v[2] = {s[0], q[0]};
+            cluster_ln_stats(v, xch, 0, win.cn, D, a.slice);
+            mu = v[0];
+            q[0] = v[1];
+            nmu = make_float2(-mu, -mu);
+        } else {
+            cluster_sum<1>(q, xch, 0, win.cn);
+        }
         cluster_arrive();  // done reading the other CTAs' slots (waited for before exit)
     }
     const float rs = rsqrtf(q[0] * inv_d + a.eps);
@@ -412,7 +459,7 @@ norm_fwd_packed_kernel(const FwdArgs a) {
     static_assert(!CLU || RPC == 1, "a split row is one row group per CTA");
     constexpr int WPR = TPR / 32;
     __shared__ float red[2 * RPC * WPR];
-    __shared__ float xch[CLU ? 2 : 1];
+    __shared__ float xch[CLU ? 4 : 1];  // cluster_sum (2) or cluster_ln_stats (4)
     const auto *X = as<XT>(a.X);
 
     const int tid = threadIdx.x;
@@ -443,7 +490,8 @@ norm_fwd_packed_kernel(const FwdArgs a) {
         unpack_unit<XT>(make_uint4(raw[k].x ^ key, raw[k].y ^ key, raw[k].z ^ key, raw[k].w ^ key), f);
     };
 
-    float mu = 0.f;
+    // LayerNorm: as in norm_fwd_vec8_kernel (a split row centres on its slice mean first)
+    float mu = 0.f, s[1] = {0.f};
     if constexpr (OP == kLayer) {
         float2 s2 = make_float2(0.f, 0.f);
 #pragma unroll
@@ -453,12 +501,11 @@ norm_fwd_packed_kernel(const FwdArgs a) {
 #pragma unroll
             for (int p = 0; p < 4; ++p) s2 = __fadd2_rn(s2, f[p]);
         }
-        float s[1] = {s2.x + s2.y};
+        s[0] = s2.x + s2.y;
         row_sum<TPR, RPC, 1>(s, red, 0, rg, wir, lane);
-        if constexpr (CLU) cluster_sum<1>(s, xch, 0, win.cn);
-        mu = s[0] * inv_d;
+        mu = CLU ? s[0] / (float)max(win.end - win.beg, 1) : s[0] * inv_d;
     }
-    const float2 nmu = make_float2(-mu, -mu);
+    float2 nmu = make_float2(-mu, -mu);
     float2 q2 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int k = 0; k < CH; ++k) {
@@ -475,7 +522,15 @@ norm_fwd_packed_kernel(const FwdArgs a) {
     float q[1] = {q2.x + q2.y};
     row_sum<TPR, RPC, 1>(q, red, 1, rg, wir, lane);
     if constexpr (CLU) {
-        cluster_sum<1>(q, xch, 1, win.cn);
+        if constexpr (OP == kLayer) {
+            float v[2] = {s[0], q[0]};
+            cluster_ln_stats(v, xch, 0, win.cn, D, a.slice);
+            mu = v[0];
+            q[0] = v[1];
+            nmu = make_float2(-mu, -mu);
+        } else {
+            cluster_sum<1>(q, xch, 0, win.cn);
+        }
         cluster_arrive();  // done reading the other CTAs' slots (waited for before exit)
     }
     const float rs = rsqrtf(q[0] * inv_d + a.eps);

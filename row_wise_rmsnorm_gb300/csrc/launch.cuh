@@ -153,15 +153,21 @@ namespace mt {
     X(4096, 512, 1, 1, 4, 2)              \
     X(16384, 512, 1, 4, 3, 1)
 
-// Rows wider than MT_SLICE_COLS: a cluster of CL = 2, 4 or 8 CTAs per row (the smallest
-// that covers D), each CTA a slice of ceil(D / CL) columns (rounded up to 8) run with the
-// shape below, X(max slice, TPR, RPC, CH, ...): the 16384-column shape of each table.
-constexpr int kSliceCols = 16384;
+// Rows wider than 16384 columns: a cluster of CL = 2, 4 or 8 CTAs per row, each CTA a
+// slice of ceil(D / CL) columns (rounded up to 8). The shapes below, X(max slice, TPR,
+// RPC, CH, ...), are tried in order; the first whose slice needs at most kMaxCluster CTAs
+// is taken (CL the smallest power of two that covers D with it).
 constexpr int kMaxCluster = 8;
+#ifndef MT_FWD_WIDE_RMS
 #define MT_FWD_WIDE_RMS(X) X(16384, 512, 1, 4, true, 3)
-#define MT_FWD_WIDE_VEC8(X) X(16384, 512, 1, 4, false, 0)
+#endif
+#ifndef MT_FWD_WIDE_VEC8
+#define MT_FWD_WIDE_VEC8(X) X(16384, 512, 1, 4, false, 2)
+#endif
 #define MT_FWD_WIDE_SCALAR(X) X(16384, 1024, 1, 16)
+#ifndef MT_BWD_WIDE_PIPE
 #define MT_BWD_WIDE_PIPE(X) X(16384, 512, 1, 4, 3, 1)
+#endif
 #define MT_BWD_WIDE_PIPE_F32(X) X(8192, 512, 1, 2, 3, 1)
 #define MT_BWD_WIDE_SCALAR(X) X(16384, 512, 1, 32)
 
@@ -320,15 +326,16 @@ cudaError_t fwd_plan_vec(int64_t N, int D, LaunchPlan *p) {
     }
 #undef MT_TRY
     // wider rows: split across a cluster
-#define MT_TRY(cap, tpr, rpc, ch, pack, minb)                                     \
-    if (!wide_split(D, cap, &p->cluster, &p->slice)) return kNoVectorPlan;       \
-    return fwd_vec_shape<OP, XT, WT, tpr, rpc, ch, pack, minb, true>(N, p);
+#define MT_TRY(cap, tpr, rpc, ch, pack, minb)        \
+    if (wide_split(D, cap, &p->cluster, &p->slice)) \
+        return fwd_vec_shape<OP, XT, WT, tpr, rpc, ch, pack, minb, true>(N, p);
     if constexpr (OP == kRms && !SHORT) {
         MT_FWD_WIDE_RMS(MT_TRY)
     } else {
         MT_FWD_WIDE_VEC8(MT_TRY)
     }
 #undef MT_TRY
+    return kNoVectorPlan;
 }
 
 // ----------------------------------------------------------------- backward ---
@@ -409,16 +416,20 @@ cudaError_t bwd_plan_vec(int64_t N, int D, int device, LaunchPlan *p) {
         MT_BWD_PIPE_SHAPES_RMS(MT_TRY)
     }
 #undef MT_TRY
-    // wider rows: split across a cluster
-#define MT_TRY(cap, tpr, rpc, ch, st, ctas)                                                   \
-    if (!wide_split(D, cap, &p->cluster, &p->slice)) return kNoVectorPlan;                   \
-    return bwd_pipe_shape<OP, XT, WT, GT, tpr, rpc, ch, st, HAS_DS, ctas, true>(N, device, p);
+    // wider rows: split across a cluster (a shape whose ring does not fit falls through)
+#define MT_TRY(cap, tpr, rpc, ch, st, ctas)                                                      \
+    if (wide_split(D, cap, &p->cluster, &p->slice)) {                                           \
+        const cudaError_t e =                                                                   \
+            bwd_pipe_shape<OP, XT, WT, GT, tpr, rpc, ch, st, HAS_DS, ctas, true>(N, device, p); \
+        if (e != kNoVectorPlan) return e;                                                       \
+    }
     if constexpr (XT == kF32 && WT == kF32 && GT == kF32) {
         MT_BWD_WIDE_PIPE_F32(MT_TRY)
     } else {
         MT_BWD_WIDE_PIPE(MT_TRY)
     }
 #undef MT_TRY
+    return kNoVectorPlan;
 }
 
 // ------------------------------------------------------------ entry points ---
