@@ -22,7 +22,11 @@
 //    needs no reduction: dX = g * ((1 + 2 z lse) exp(x - lse) - q). A last small kernel
 //    sums the per-row losses in a fixed order for the sum/mean reductions.
 //  * exp is __expf (the hardware exp2 path): relative error about 2^-21 for the ranges
-//    met here, well inside every output tolerance; log is logf, once per row.
+//    met here, well inside every output tolerance; log is logf, once per row. The
+//    cross-entropy loops, which are instruction-bound, write exp(x - m) as
+//    2^(x log2(e) - m log2(e)): one fp32x2 fused multiply-add for two arguments, then
+//    the hardware base-2 exponential (ex2.approx, relative error about 2^-22); the
+//    rounding of m log2(e) adds about |m| 2^-24 to the exponent.
 #pragma once
 
 #include "kernels.cuh"
@@ -241,6 +245,16 @@ softmax_scalar_kernel(const SoftmaxArgs a) {
 
 // ------------------------------------------------------------- cross-entropy ---
 
+constexpr float kLog2e = 1.4426950408889634f;  // log2(e)
+
+// 2^x by the hardware's approximate base-2 exponential (subnormal results flush to 0,
+// 2^-inf = 0).
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Chunks each cross-entropy thread loads before using the first (bytes in flight).
 #ifndef MT_CE_UNROLL
 #define MT_CE_UNROLL 4
@@ -288,25 +302,30 @@ __device__ __forceinline__ float chunk_elem(const float2 (&f)[4], int e) {
     return v;
 }
 
-// One CTA of TPR threads per row. VEC8: 8-element chunks (D % 8 == 0, aligned rows),
-// thread t taking chunks t, t + TPR, ...; otherwise single elements, same striding.
-// Every thread reads the row's target with its first logits; the thread that meets the
-// target column keeps its logit, so no load waits on another at the end of the row.
-template <int TPR, bool VEC8, int XT, int MINB>
-__global__ void __launch_bounds__(TPR, MINB)
+// A row group of TPR threads per row: one CTA per row, or, with one warp per row, RPC
+// rows (warps) per CTA. VEC8: 8-element chunks (D % 8 == 0, aligned rows), thread t
+// taking chunks t, t + TPR, ...; otherwise single elements, same striding. Every thread
+// reads the row's target with its first logits; the thread that meets the target column
+// keeps its logit, so no load waits on another at the end of the row.
+template <int TPR, int RPC, bool VEC8, int XT, int MINB>
+__global__ void __launch_bounds__(TPR * RPC, MINB)
 ce_fwd_kernel(const CeArgs a) {
     pdl_enter();
     constexpr int W = TPR / 32;
     static_assert(W <= 32 && (W & (W - 1)) == 0, "warps per row: a power of two up to 32");
-    __shared__ float sm_m[W], sm_s[W], sm_x[W], sm_t;
-    const int t = threadIdx.x, lane = t % 32, w = t / 32;
-    const int64_t row = blockIdx.x;
+    static_assert(W == 1 || RPC == 1, "several rows per CTA only with a warp per row");
+    __shared__ float sm_m[W], sm_s[W], sm_x[W], sm_t[RPC];
+    const int tid = threadIdx.x, t = tid % TPR, rg = tid / TPR, lane = tid % 32, w = t / 32;
+    const int64_t row = (int64_t)blockIdx.x * RPC + rg;
+    if (RPC > 1 && row >= a.N) return;  // a warp-wide row group: no CTA barrier below
     const int D = a.D;
     const int64_t off = row * (int64_t)D;
 
     MaxSum st{-INFINITY, 0.f};
     float sx = 0.f;
     if constexpr (VEC8) {
+        const float2 l2e = make_float2(kLog2e, kLog2e);
+        float2 sx2 = make_float2(0.f, 0.f);
         float2 f[kCeUnroll][4];
         ce_load<TPR, XT>(a.X, off, t, D, f);
         const int64_t tg = a.T[row];
@@ -316,32 +335,35 @@ ce_fwd_kernel(const CeArgs a) {
             for (int u = 0; u < kCeUnroll; ++u) {
                 const int c = c0 + u * TPR;
                 if (c * 8 >= D) continue;
-                float cm = -INFINITY;
-#pragma unroll
-                for (int p = 0; p < 4; ++p) cm = fmaxf(cm, fmaxf(f[u][p].x, f[u][p].y));
+                const float cm = fmaxf(fmaxf(fmaxf(f[u][0].x, f[u][0].y), fmaxf(f[u][1].x, f[u][1].y)),
+                                       fmaxf(fmaxf(f[u][2].x, f[u][2].y), fmaxf(f[u][3].x, f[u][3].y)));
                 const float m = fmaxf(st.m, cm);
                 const float ms = (m == -INFINITY) ? 0.f : m;   // all -inf so far: exps are 0
-                float cs = 0.f;
+                const float nb = -ms * kLog2e;
+                const float2 nb2 = make_float2(nb, nb);
+                float2 cs2 = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int p = 0; p < 4; ++p) {
-                    cs += __expf(f[u][p].x - ms) + __expf(f[u][p].y - ms);
-                    sx += f[u][p].x + f[u][p].y;
+                    const float2 e = __ffma2_rn(f[u][p], l2e, nb2);   // (x - ms) log2(e)
+                    cs2 = __fadd2_rn(cs2, make_float2(ex2(e.x), ex2(e.y)));
+                    sx2 = __fadd2_rn(sx2, f[u][p]);
                 }
-                st.s = st.s * __expf(st.m - ms) + cs;
+                st.s = st.s * ex2(fmaf(st.m, kLog2e, nb)) + (cs2.x + cs2.y);
                 st.m = m;
-                if (c == tc) sm_t = chunk_elem(f[u], (int)(tg & 7));
+                if (c == tc) sm_t[rg] = chunk_elem(f[u], (int)(tg & 7));
             }
             c0 += kCeUnroll * TPR;
             if (c0 * 8 >= D) break;
             ce_load<TPR, XT>(a.X, off, c0, D, f);
         }
+        sx = sx2.x + sx2.y;
     } else {
         const int64_t tg = a.T[row];
         for (int j = t; j < D; j += TPR) {
             const float v = ld_elem_stream(a.X, off + j, a.xdt);
             add_value(st, v);
             sx += v;
-            if (j == tg) sm_t = v;
+            if (j == tg) sm_t[rg] = v;
         }
     }
     // fixed-order combination: butterfly within each warp, then across the W warp results
@@ -352,20 +374,26 @@ ce_fwd_kernel(const CeArgs a) {
         st = (lane & o) ? combine(other, st) : combine(st, other);
         sx += __shfl_xor_sync(0xffffffffu, sx, o);
     }
-    if (lane == 0) {
-        sm_m[w] = st.m;
-        sm_s[w] = st.s;
-        sm_x[w] = sx;
-    }
-    __syncthreads();
-    if (w != 0) return;
-    MaxSum tot{lane < W ? sm_m[lane] : -INFINITY, lane < W ? sm_s[lane] : 0.f};
-    float tx = lane < W ? sm_x[lane] : 0.f;
+    MaxSum tot = st;
+    float tx = sx;
+    if constexpr (W == 1) {
+        __syncwarp();  // the target logit's owner wrote sm_t[rg]
+    } else {
+        if (lane == 0) {
+            sm_m[w] = st.m;
+            sm_s[w] = st.s;
+            sm_x[w] = sx;
+        }
+        __syncthreads();
+        if (w != 0) return;
+        tot = MaxSum{lane < W ? sm_m[lane] : -INFINITY, lane < W ? sm_s[lane] : 0.f};
+        tx = lane < W ? sm_x[lane] : 0.f;
 #pragma unroll
-    for (int o = W / 2; o > 0; o >>= 1) {
-        MaxSum other{__shfl_xor_sync(0xffffffffu, tot.m, o), __shfl_xor_sync(0xffffffffu, tot.s, o)};
-        tot = (lane & o) ? combine(other, tot) : combine(tot, other);
-        tx += __shfl_xor_sync(0xffffffffu, tx, o);
+        for (int o = W / 2; o > 0; o >>= 1) {
+            MaxSum other{__shfl_xor_sync(0xffffffffu, tot.m, o), __shfl_xor_sync(0xffffffffu, tot.s, o)};
+            tot = (lane & o) ? combine(other, tot) : combine(tot, other);
+            tx += __shfl_xor_sync(0xffffffffu, tx, o);
+        }
     }
     if (lane == 0) {
         const float l = tot.m + logf(tot.s);
@@ -377,7 +405,7 @@ ce_fwd_kernel(const CeArgs a) {
         } else if (tg < 0 || tg >= D) {
             loss = __int_as_float(0x7fc00000);
         } else {
-            loss = l - (1.f - a.eps) * sm_t - (a.eps / (float)D) * tx + a.z * l * l;
+            loss = l - (1.f - a.eps) * sm_t[rg] - (a.eps / (float)D) * tx + a.z * l * l;
         }
         a.loss[row] = loss;
     }
@@ -392,12 +420,13 @@ __device__ __forceinline__ float ce_row_grad(const CeArgs &a, int64_t row, int64
     return tg == a.ignore_index ? 0.f : g;
 }
 
-template <int TPR, bool VEC8, int XT, int MINB>
-__global__ void __launch_bounds__(TPR, MINB)
+template <int TPR, int RPC, bool VEC8, int XT, int MINB>
+__global__ void __launch_bounds__(TPR * RPC, MINB)
 ce_bwd_kernel(const CeArgs a) {
     pdl_enter();
-    const int t = threadIdx.x;
-    const int64_t row = blockIdx.x;
+    const int t = threadIdx.x % TPR;
+    const int64_t row = (int64_t)blockIdx.x * RPC + threadIdx.x / TPR;
+    if (row >= a.N) return;
     const int D = a.D;
     const int64_t off = row * (int64_t)D;
     if constexpr (VEC8) {
@@ -411,6 +440,9 @@ ce_bwd_kernel(const CeArgs a) {
         const float gq = g * a.eps / (float)D;            // g * (uniform part of q)
         const float gt = g * (1.f - a.eps);               // g * (target part of q)
         const int tc = (tg >= 0 && tg < D) ? (int)(tg >> 3) : -1;
+        const float2 l2e = make_float2(kLog2e, kLog2e);
+        const float2 nl2 = make_float2(-l * kLog2e, -l * kLog2e);
+        const float2 scale2 = make_float2(scale, scale), ngq2 = make_float2(-gq, -gq);
         for (int c0 = t;;) {
 #pragma unroll
             for (int u = 0; u < kCeUnroll; ++u) {
@@ -419,8 +451,8 @@ ce_bwd_kernel(const CeArgs a) {
                 float2 o[4];
 #pragma unroll
                 for (int p = 0; p < 4; ++p) {
-                    o[p].x = scale * __expf(f[u][p].x - l) - gq;
-                    o[p].y = scale * __expf(f[u][p].y - l) - gq;
+                    const float2 e = __ffma2_rn(f[u][p], l2e, nl2);   // (x - lse) log2(e)
+                    o[p] = __ffma2_rn(scale2, make_float2(ex2(e.x), ex2(e.y)), ngq2);
                 }
                 if (c == tc) {
                     const int e = (int)(tg & 7);
