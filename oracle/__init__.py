@@ -22,6 +22,8 @@ Sources for the formulas (page title, section):
     gradients; cross-entropy with ignore-index, none/sum/mean, label smoothing,
     z-loss. "Metal subgroup LayerNorm and cross-entropy report", "Structural
     repair exercised by cross-entropy": the per-row loss formula.
+  * tensorcore, "Training kernels", "Fused Norm + GEMV": Y = Norm(X) @ W with the
+    normalized rows kept unrounded.
 
 Parity pins: tests/test_oracle_pins.py pins every function here against finite
 differences, closed forms, invariants, the worked LayerNorm example of the
@@ -72,7 +74,9 @@ def _declare(lib):
                                                  ctypes.c_double, _dp, _dp]
     lib.oracle_cross_entropy_backward.argtypes = [_dp, _lp, _dp, _dp, _i64, _i64, _i64,
                                                   ctypes.c_double, ctypes.c_double, _dp]
-    for name in ("oracle_rmsnorm_forward", "oracle_rmsnorm_backward",
+    lib.oracle_norm_gemv.argtypes = [ctypes.c_int] + [_dp] * 7 + [_i64, _i64, _i64,
+                                                                   ctypes.c_double]
+    for name in ("oracle_norm_gemv", "oracle_rmsnorm_forward", "oracle_rmsnorm_backward",
                  "oracle_layernorm_forward", "oracle_layernorm_backward",
                  "oracle_add_rmsnorm_forward", "oracle_add_rmsnorm_backward",
                  "oracle_softmax_forward", "oracle_softmax_backward",
@@ -267,6 +271,24 @@ def cross_entropy_backward(X, T, lse, g, ignore_index=-100, label_smoothing=0.0,
                                       _p(lse), _p(g), N, D, int(ignore_index),
                                       float(label_smoothing), float(z_loss), _p(dX))
     return dX
+
+
+def norm_gemv(op, X, gamma, beta, W, eps, lib=None):
+    """Fused normalization + GEMV (tensorcore "Fused Norm + GEMV"): Y = Norm(X) @ W with the
+    normalized rows unrounded. op "rmsnorm" or "layernorm" (beta ignored for RMSNorm);
+    X [M, K], W [K, N]. -> (Y [M, N], Y_abs [M, N] = sum_k |xn_mk W_kn|), fp64."""
+    lib = lib or load_library()
+    code = {"rmsnorm": 0, "layernorm": 1}[op]
+    X, gamma, W = _f64(X), _f64(gamma), _f64(W)
+    beta = _f64(beta) if beta is not None else np.zeros_like(gamma)
+    M, K = _shape(X)
+    if W.ndim != 2 or W.shape[0] != K:
+        raise ValueError("W must be [K, N]")
+    N = int(W.shape[1])
+    Y, Ya, xn = np.empty((M, N)), np.empty((M, N)), np.empty(K)
+    lib.oracle_norm_gemv(code, _p(X), _p(gamma), _p(beta), _p(W), _p(Y), _p(Ya), _p(xn), M, N,
+                         K, float(eps))
+    return Y, Ya
 
 
 BF16_MAX = (2.0 - 2.0 ** -7) * 2.0 ** 127  # largest finite bfloat16

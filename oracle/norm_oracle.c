@@ -329,3 +329,39 @@ void oracle_cross_entropy_backward(const double *X, const int64_t *T,
         }
     }
 }
+
+/* ------------------------------------------------------------------------- */
+/* Fused normalization + GEMV. [tc] "Fused Norm + GEMV": Y = Norm(X, gamma[, beta]) @ W
+ * with X [M, K], W [K, N] (row k of W holds the weights of input feature k), Y [M, N];
+ * Norm is the RMSNorm forward (op 0) or the LayerNorm forward (op 1) above. The
+ * normalized row is used unrounded: the fused kernels apply it in registers during
+ * the accumulation and never store it.
+ *   xn_m  = Norm(x_m)                         (the forward above, one row)
+ *   Y_mn  = sum_k xn_mk * W_kn                (k ascending)
+ *   Y_abs_mn = sum_k |xn_mk * W_kn|           (the scale of the sum's rounding)
+ * xn: caller-provided scratch of K doubles.                                     */
+void oracle_norm_gemv(int op, const double *X, const double *gamma, const double *beta,
+                      const double *W, double *Y, double *Y_abs, double *xn,
+                      int64_t M, int64_t N, int64_t K, double eps)
+{
+    for (int64_t m = 0; m < M; ++m) {
+        double mean, rstd;
+        if (op == 0)
+            oracle_rmsnorm_forward(X + m * K, gamma, xn, &rstd, 1, K, eps);
+        else
+            oracle_layernorm_forward(X + m * K, gamma, beta, xn, &mean, &rstd, 1, K, eps);
+        double *y = Y + m * N, *ya = Y_abs + m * N;
+        for (int64_t n = 0; n < N; ++n) {
+            y[n] = 0.0;
+            ya[n] = 0.0;
+        }
+        for (int64_t k = 0; k < K; ++k) {
+            const double *w = W + k * N;
+            for (int64_t n = 0; n < N; ++n) {
+                double t = xn[k] * w[n];
+                y[n] += t;
+                ya[n] += fabs(t);
+            }
+        }
+    }
+}

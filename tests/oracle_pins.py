@@ -440,7 +440,65 @@ def pin_softmax_ce_closed_forms(lib):
     assert val == 0.0 and nv == 0.0, "mean over no valid row is 0"
 
 
+def pin_norm_gemv_torch(lib):
+    """torch's fp64 CPU rms_norm / layer_norm followed by a matmul (tensorcore "Fused Norm
+    + GEMV": Y = Norm(X, gamma[, beta]) @ W, W [K, N]), M = 3, K = 40, N = 24, and the
+    absolute-term sums against |xn| @ |W|."""
+    import torch
+    import torch.nn.functional as F
+
+    rng = np.random.default_rng(31)
+    M, K, N = 3, 40, 24
+    X = rng.standard_normal((M, K)) + 2.0
+    gamma = 1 + 0.1 * rng.standard_normal(K)
+    beta = 0.1 * rng.standard_normal(K)
+    W = rng.standard_normal((K, N))
+    t = lambda a: torch.tensor(a, dtype=torch.float64)
+    for op in ("rmsnorm", "layernorm"):
+        if op == "rmsnorm":
+            xn = F.rms_norm(t(X), (K,), weight=t(gamma), eps=1e-6)
+        else:
+            xn = F.layer_norm(t(X), (K,), weight=t(gamma), bias=t(beta), eps=1e-6)
+        Y, Ya = oracle.norm_gemv(op, X, gamma, beta, W, 1e-6, lib=lib)
+        _close(Y, (xn @ t(W)).numpy(), 1e-12, 1e-12, f"{op} gemv vs torch")
+        _close(Ya, (xn.abs() @ t(W).abs()).numpy(), 1e-12, 1e-12, f"{op} gemv |terms|")
+
+
+def pin_norm_gemv_closed_forms(lib):
+    """A hand-worked case and structural checks of Y = Norm(X) @ W:
+    * RMSNorm of x = [3, 4] (eps 0, gamma = [1, 2]) times W = [[1, 2], [3, 4]]:
+      ms = 12.5, xn = [3, 8] / sqrt(12.5), Y = [27, 38] / sqrt(12.5);
+    * a permutation matrix W (W[k, p(k)] = 1, p not an involution) moves feature k of the
+      normalized row to output column p(k): Y[:, p(k)] = Norm(X)[:, k] (an operand
+      transposition would apply p's inverse);
+    * LayerNorm of constant rows normalizes to beta, so Y = beta @ W for every row."""
+    Y, _ = oracle.norm_gemv("rmsnorm", [[3.0, 4.0]], [1.0, 2.0], None, [[1.0, 2.0], [3.0, 4.0]],
+                            0.0, lib=lib)
+    _close(Y, [[27 / np.sqrt(12.5), 38 / np.sqrt(12.5)]], 0, 1e-15, "hand-worked rmsnorm gemv")
+    rng = np.random.default_rng(32)
+    K = 7
+    perm = np.array([1, 2, 3, 4, 5, 6, 0])            # a 7-cycle
+    W = np.zeros((K, K))
+    W[np.arange(K), perm] = 1.0
+    X = rng.standard_normal((2, K))
+    gamma = 1 + 0.1 * rng.standard_normal(K)
+    beta = 0.1 * rng.standard_normal(K)
+    for op in ("rmsnorm", "layernorm"):
+        if op == "rmsnorm":
+            xn, _ = oracle.rmsnorm_forward(X, gamma, 1e-5, lib=lib)
+        else:
+            xn, _, _ = oracle.layernorm_forward(X, gamma, beta, 1e-5, lib=lib)
+        Y, _ = oracle.norm_gemv(op, X, gamma, beta, W, 1e-5, lib=lib)
+        _close(Y[:, perm], xn, 0, 1e-15, f"{op} gemv with a permutation")
+    Xc = np.full((3, K), 2.5)
+    Wr = rng.standard_normal((K, 5))
+    Y, _ = oracle.norm_gemv("layernorm", Xc, gamma, beta, Wr, 1e-5, lib=lib)
+    _close(Y, np.tile(beta @ Wr, (3, 1)), 1e-15, 1e-13, "layernorm gemv of constant rows")
+
+
 ALL_PINS = [
+    pin_norm_gemv_torch,
+    pin_norm_gemv_closed_forms,
     pin_fd_rmsnorm,
     pin_fd_layernorm,
     pin_fd_add_rmsnorm,

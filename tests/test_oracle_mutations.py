@@ -39,6 +39,12 @@ MUTATIONS = {
     "ce_grad_sign": ("* p - q);", "* p + q);"),
     "ce_ignored_row_not_zeroed": ("                dX[i * D + j] = 0.0;\n                continue;",
                                   "                ;"),
+    "gemv_column_reversed": ("double t = xn[k] * w[n];", "double t = xn[k] * w[N - 1 - n];"),
+    "gemv_first_feature_dropped": ("for (int64_t k = 0; k < K; ++k) {\n            const double *w",
+                                   "for (int64_t k = 1; k < K; ++k) {\n            const double *w"),
+    "gemv_layernorm_as_rmsnorm": ("        if (op == 0)\n            oracle_rmsnorm_forward",
+                                  "        if (op >= 0)\n            oracle_rmsnorm_forward"),
+    "gemv_abs_terms_signed": ("ya[n] += fabs(t);", "ya[n] += t;"),
 }
 
 
