@@ -429,6 +429,85 @@ def max_over_ranks(value: float, device=None) -> float:
     return float(t.item())
 
 
+# Softmax / cross-entropy workloads: name -> (runner, N, D, storage type name).
+ROW_OPS = {
+    "softmax_16384x4096_f16": ("softmax", 16384, 4096, "float16"),
+    "cross_entropy_4096x32768_bf16": ("cross_entropy", 4096, 32768, "bfloat16"),
+}
+
+
+def row_op_line(name, device, steps, warmup, stream, peak):
+    """Forward and backward of one ROW_OPS workload, back to back over two buffer sets."""
+    import torch
+    kind, N, D, tname = ROW_OPS[name]
+    cls = SoftmaxRunner if kind == "softmax" else CrossEntropyRunner
+    r2 = [cls(N, D, device, i, getattr(torch, tname)) for i in range(2)]
+    f2, b2, _ = time_ops(r2, steps, warmup, stream)
+    fg = r2[0].fwd_bytes / (statistics.mean(f2) * 1e-3) / 1e9
+    bg = r2[0].bwd_bytes / (statistics.mean(b2) * 1e-3) / 1e9
+    return {"row_op": name, "forward_gbs": round(fg, 2), "backward_gbs": round(bg, 2),
+            "forward_frac_of_measured": round(fg / peak, 4),
+            "backward_frac_of_measured": round(bg / peak, 4),
+            "forward_us": round(1e3 * statistics.mean(f2), 3),
+            "backward_us": round(1e3 * statistics.mean(b2), 3),
+            "compulsory_bytes": {"forward": r2[0].fwd_bytes, "backward": r2[0].bwd_bytes}}
+
+
+# Fused normalization + GEMV for decode: name -> (op, M, K, N). K x N = 4096 x 12288 is a
+# Llama-7B fused QKV projection (three 4096 x 4096 weights side by side).
+GEMV_OPS = {
+    "rmsnorm_gemv_m1_4096x12288": ("rmsnorm", 1, 4096, 12288),
+    "rmsnorm_gemv_m4_4096x12288": ("rmsnorm", 4, 4096, 12288),
+    "layernorm_gemv_m4_4096x12288": ("layernorm", 4, 4096, 12288),
+    "rmsnorm_gemv_m4_4096x4096": ("rmsnorm", 4, 4096, 4096),
+}
+
+
+def gemv_line(name, device, steps, warmup, stream, peak):
+    """CUDA-event time of the fused norm + GEMV, back to back over enough weight sets that
+    together they hold three times the L2 (so every call streams its W from HBM).
+    Compulsory bytes: W (2KN), X (2MK), gamma (2K), beta (2K, LayerNorm) and Y (2MN)."""
+    import torch
+    import row_wise_rmsnorm_gb300 as mt
+    op, M, K, N = GEMV_OPS[name]
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    nsets = max(2, -(-3 * l2 // (2 * K * N)))
+    sets = []
+    for i in range(nsets):
+        g = torch.Generator(device=device)
+        g.manual_seed(i)
+        x = torch.randn((M, K), generator=g, device=device).half()
+        gamma = (1 + 0.1 * torch.randn(K, generator=g, device=device)).half()
+        beta = (0.1 * torch.randn(K, generator=g, device=device)).half()
+        w = (torch.randn((K, N), generator=g, device=device) / K ** 0.5).half()
+        sets.append((x, gamma, beta, w, torch.empty((M, N), dtype=torch.float16, device=device)))
+
+    def call(j):
+        x, gamma, beta, w, y = sets[j % nsets]
+        if op == "rmsnorm":
+            mt.mt_fused_rmsnorm_gemv(x, gamma, w, y, M, N, K, 1e-5, stream)
+        else:
+            mt.mt_fused_layernorm_gemv(x, gamma, beta, w, y, M, N, K, 1e-5, stream)
+
+    for j in range(warmup):
+        call(j)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    torch.cuda.synchronize()
+    ev[0].record(stream)
+    for j in range(steps):
+        call(j)
+        ev[j + 1].record(stream)
+    torch.cuda.synchronize()
+    ts = [ev[j].elapsed_time(ev[j + 1]) for j in range(steps)]
+    nbytes = 2 * K * N + 2 * M * K + 2 * K * (2 if op == "layernorm" else 1) + 2 * M * N
+    ms = statistics.mean(ts)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"gemv": name, "us": round(1e3 * ms, 3), "us_median": round(1e3 * statistics.median(ts), 3),
+            "gbs": round(gbs, 2), "frac_of_measured": round(gbs / peak, 4),
+            "compulsory_bytes": nbytes, "M": M, "K": K, "N": N,
+            "gflops": round(2 * M * K * N / (ms * 1e-3) / 1e9, 1)}
+
+
 # --------------------------------------------------------------- main ---
 
 def main(argv=None):
@@ -442,6 +521,12 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-others", action="store_true",
                     help="skip the per-op numbers of the other large workloads")
+    ap.add_argument("--gemv", choices=list(GEMV_OPS),
+                    help="time only this fused norm + GEMV workload (a side measurement) and "
+                         "print its own line")
+    ap.add_argument("--row-op", choices=list(ROW_OPS),
+                    help="time only this softmax / cross-entropy workload (a side measurement, "
+                         "e.g. for a profiler) and print its own line")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -467,6 +552,13 @@ def main(argv=None):
     stream = torch.cuda.current_stream()
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     peak, peak_src = measured_peak_gbs()
+    if args.row_op or args.gemv:
+        line = (row_op_line(args.row_op, device, args.steps, args.warmup, stream, peak)
+                if args.row_op else gemv_line(args.gemv, device, args.steps, args.warmup, stream,
+                                              peak))
+        if rank == 0:
+            print(json.dumps(line))
+        return 0
     sets = [OpRunner(args.workload, device, seed=2 * rank + i) for i in range(2)]
     runner = sets[0]
     w = runner.w
@@ -544,22 +636,19 @@ def main(argv=None):
     # The row softmax and the per-row cross-entropy (the next row-reduction family).
     row_ops = {}
     if not args.no_others and rank == 0:
-        for name, cls, N, D, tdt in (("softmax_16384x4096_f16", SoftmaxRunner, 16384, 4096,
-                                      torch.float16),
-                                     ("cross_entropy_4096x32768_bf16", CrossEntropyRunner, 4096,
-                                      32768, torch.bfloat16)):
-            r2 = [cls(N, D, device, i, tdt) for i in range(2)]
-            f2, b2, _ = time_ops(r2, max(50, args.steps // 10), args.warmup, stream)
-            fg = r2[0].fwd_bytes / (statistics.mean(f2) * 1e-3) / 1e9
-            bg = r2[0].bwd_bytes / (statistics.mean(b2) * 1e-3) / 1e9
-            row_ops[name] = {"forward_gbs": round(fg, 2), "backward_gbs": round(bg, 2),
-                             "forward_frac_of_measured": round(fg / peak, 4),
-                             "backward_frac_of_measured": round(bg / peak, 4),
-                             "forward_us": round(1e3 * statistics.mean(f2), 3),
-                             "backward_us": round(1e3 * statistics.mean(b2), 3),
-                             "compulsory_bytes": {"forward": r2[0].fwd_bytes,
-                                                  "backward": r2[0].bwd_bytes}}
-            del r2
+        for name in ROW_OPS:
+            row_ops[name] = row_op_line(name, device, max(50, args.steps // 10), args.warmup,
+                                        stream, peak)
+            del row_ops[name]["row_op"]
+            torch.cuda.empty_cache()
+
+    # Fused normalization + GEMV (decode).
+    gemv = {}
+    if not args.no_others and rank == 0:
+        for name in GEMV_OPS:
+            gemv[name] = gemv_line(name, device, max(50, args.steps // 10), args.warmup, stream,
+                                   peak)
+            del gemv[name]["gemv"]
             torch.cuda.empty_cache()
 
     e2e = None
@@ -612,6 +701,7 @@ def main(argv=None):
         "other_workloads": others,
         "storage_types": {"workload": args.workload, **dtypes},
         "row_ops": row_ops,
+        "norm_gemv": gemv,
     }
     if rank == 0:
         print(json.dumps(line))

@@ -6,8 +6,9 @@
  *   LayerNorm                     mt_layernorm_forward / mt_layernorm_backward
  *   fused residual-add + RMSNorm  mt_add_rmsnorm_forward / mt_add_rmsnorm_backward
  * with explicit storage types (mt_norm_forward_ex / mt_norm_backward_ex), and on the same
- * row skeleton a row softmax / log-softmax (mt_softmax_*) and a per-row cross-entropy
- * (mt_cross_entropy_*).
+ * row skeleton a row softmax / log-softmax (mt_softmax_*), a per-row cross-entropy
+ * (mt_cross_entropy_*) and, for decode, normalization fused into the GEMV that consumes
+ * it (mt_fused_rmsnorm_gemv / mt_fused_layernorm_gemv).
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -278,6 +279,33 @@ mt_status_t mt_cross_entropy_backward(mt_dtype_t dtype, const void *logits,
                                       float z_loss, mt_reduction_t reduction,
                                       const float *dloss, const float *n_valid, void *dlogits,
                                       mt_stream_t stream);
+
+/* ------------------------------------------ fused normalization + GEMV (decode) ---
+ * [tc] "Fused Norm + GEMV":  Y = Norm(X, gamma[, beta]) @ W  for the small batches of a
+ * decode step, with Norm the RMSNorm (eps inside the square root, zero-offset weight) or
+ * LayerNorm (centred population variance) forward above. The normalized rows are
+ * applied in registers during the accumulation and never stored, so there is no
+ * x_norm round trip; the statistics are not returned (inference only, as on the page).
+ *   X:     [M, K] fp16 (row-major)          gamma, beta: [K] fp16
+ *   W:     [K, N] fp16 (row-major; row k holds the weights of input feature k)
+ *   Y:     [M, N] fp16 (row-major)          Y_mn = sum_k Norm(x_m)_k * W_kn
+ * Arithmetic fp32 (statistics, normalized values, products, sums); Y rounded to fp16,
+ * nearest even. The sums over k run in a fixed order, so Y is bitwise identical run to
+ * run on the same device and shape. Any alignment (N % 8 == 0 with a 16-byte aligned W
+ * takes 16-byte loads).
+ * Bounds: 0 <= M <= MT_MAX_GEMV_ROWS, 1 <= K <= MT_MAX_GEMV_K, 0 <= N <= 2^31 - 1; M = 0
+ * or N = 0 is a no-op (pointers may be NULL). Errors: MT_ERR_INVALID_ARG for a NULL
+ * pointer, a negative size, K < 1, eps not finite or not > 0, or Y overlapping an
+ * input; MT_ERR_UNSUPPORTED past the bounds.                                       */
+#define MT_MAX_GEMV_ROWS 8
+#define MT_MAX_GEMV_K 32768
+
+mt_status_t mt_fused_rmsnorm_gemv(const void *X, const void *gamma, const void *W, void *Y,
+                                  int64_t M, int64_t N, int64_t K, float eps,
+                                  mt_stream_t stream);
+mt_status_t mt_fused_layernorm_gemv(const void *X, const void *gamma, const void *beta,
+                                    const void *W, void *Y, int64_t M, int64_t N, int64_t K,
+                                    float eps, mt_stream_t stream);
 
 /* ----------------------------------------------- backward without allocation ---
  * No counterpart on the pages: this entry point exists for callers that cannot

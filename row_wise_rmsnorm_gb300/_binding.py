@@ -29,6 +29,8 @@ MT_REDUCTION_NONE, MT_REDUCTION_SUM, MT_REDUCTION_MEAN = 0, 1, 2
 MT_MAX_CE_COLS = 262144
 MT_MAX_COLS = 131072
 MT_MAX_SOFTMAX_COLS = 16384
+MT_MAX_GEMV_ROWS = 8
+MT_MAX_GEMV_K = 32768
 
 # Every exported symbol of include/mt_norm.h.
 EXPORTED = (
@@ -38,6 +40,7 @@ EXPORTED = (
     "mt_norm_forward_ex", "mt_norm_backward_ex",
     "mt_softmax_forward", "mt_softmax_backward",
     "mt_cross_entropy_forward", "mt_cross_entropy_backward",
+    "mt_fused_rmsnorm_gemv", "mt_fused_layernorm_gemv",
     "mt_rmsnorm_backward_noalloc",
     "mt_norm_backward_workspace_size", "mt_last_cuda_error", "mt_status_string",
     "mt_norm_version",
@@ -78,6 +81,8 @@ _SIGS = {
     "mt_softmax_backward": [ctypes.c_int, _P, _P, _P, _I64, _I64, ctypes.c_int, _P],
     "mt_cross_entropy_forward": [ctypes.c_int, _P, _P, _I64, _I64, _I64, _F, _F, ctypes.c_int,
                                  _P, _P, _P, _P, _P],
+    "mt_fused_rmsnorm_gemv": [_P, _P, _P, _P, _I64, _I64, _I64, _F, _P],
+    "mt_fused_layernorm_gemv": [_P, _P, _P, _P, _P, _I64, _I64, _I64, _F, _P],
     "mt_cross_entropy_backward": [ctypes.c_int, _P, _P, _P, _I64, _I64, _I64, _F, _F,
                                   ctypes.c_int, _P, _P, _P, _P],
     "mt_rmsnorm_backward_noalloc": [_P, _P, _P, _P, _P, _P, _I64, _I64, _P],
@@ -232,6 +237,16 @@ def mt_cross_entropy_backward(dtype, logits, targets, lse, N, D, ignore_index, l
                                             ignore_index, label_smoothing, z_loss, reduction,
                                             _ptr(dloss), _ptr(n_valid), _ptr(dlogits),
                                             _stream(stream)), "mt_cross_entropy_backward")
+
+
+def mt_fused_rmsnorm_gemv(X, gamma, W, Y, M, N, K, eps, stream=None):
+    _check(load().mt_fused_rmsnorm_gemv(_ptr(X), _ptr(gamma), _ptr(W), _ptr(Y), M, N, K, eps,
+                                        _stream(stream)), "mt_fused_rmsnorm_gemv")
+
+
+def mt_fused_layernorm_gemv(X, gamma, beta, W, Y, M, N, K, eps, stream=None):
+    _check(load().mt_fused_layernorm_gemv(_ptr(X), _ptr(gamma), _ptr(beta), _ptr(W), _ptr(Y), M, N,
+                                          K, eps, _stream(stream)), "mt_fused_layernorm_gemv")
 
 
 def mt_rmsnorm_backward_noalloc(X, gamma, dY, rstd, dX, dgamma, N, D, stream=None):
@@ -441,3 +456,17 @@ def cross_entropy_backward(logits, targets, lse, dloss, n_valid=None, ignore_ind
     mt_cross_entropy_backward(dtype_code(logits.dtype), logits, targets, lse, n, d, ignore_index,
                               label_smoothing, z_loss, _REDUCTIONS[reduction], dloss, n_valid, dx)
     return dx
+
+
+def norm_gemv(x, gamma, w, beta=None, eps=1e-5):
+    """Y = Norm(x, gamma[, beta]) @ w for a decode batch: RMSNorm when beta is None, else
+    LayerNorm. x [M, K], w [K, N], all fp16 on the device -> Y [M, N] fp16."""
+    import torch
+    m, k = x.shape
+    n = w.shape[1]
+    y = _new(x, (m, n), torch.float16)
+    if beta is None:
+        mt_fused_rmsnorm_gemv(x, gamma, w, y, m, n, k, eps)
+    else:
+        mt_fused_layernorm_gemv(x, gamma, beta, w, y, m, n, k, eps)
+    return y

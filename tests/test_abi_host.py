@@ -42,7 +42,7 @@ def test_header_is_plain_c():
 
 def test_exports_every_declared_symbol(lib):
     decl = declared_functions()
-    assert len(decl) == 20
+    assert len(decl) == 22
     assert sorted(mt.EXPORTED) == decl
     out = subprocess.run(["nm", "-D", "--defined-only", mt.library_path()], capture_output=True,
                          text=True, check=True).stdout
@@ -178,6 +178,24 @@ def test_softmax_and_cross_entropy_validation(lib):
     assert ce_b(F16, None, None, None, 0, D, -100, 0.0, 0.0, MEAN, None, None, None, None) == 0
     assert ce_f(F16, None, None, 0, D, -100, 0.0, 0.0, SUM, None, None, None, G, None) == INV
     assert ce_f(F16, None, None, 0, D, -100, 0.0, 0.0, SUM, None, None, G, G, None) == INV
+    assert lib.mt_last_cuda_error() == 0  # nothing reached CUDA
+
+
+def test_norm_gemv_validation(lib):
+    """mt_fused_rmsnorm_gemv / mt_fused_layernorm_gemv: argument errors before any CUDA
+    call; M = 0 and N = 0 are no-ops."""
+    f_rms, f_ln = lib.mt_fused_rmsnorm_gemv, lib.mt_fused_layernorm_gemv
+    M, N, K = 4, 64, 128
+    assert f_rms(None, B, C, E, M, N, K, 1e-5, None) == INV
+    assert f_ln(A, B, None, C, E, M, N, K, 1e-5, None) == INV        # beta
+    assert f_rms(A, B, C, E, -1, N, K, 1e-5, None) == INV
+    assert f_rms(A, B, C, E, M, N, 0, 1e-5, None) == INV
+    assert f_rms(A, B, C, E, M, N, K, 0.0, None) == INV
+    assert f_rms(A, B, C, E, mt.MT_MAX_GEMV_ROWS + 1, N, K, 1e-5, None) == UNS
+    assert f_rms(A, B, C, E, M, N, mt.MT_MAX_GEMV_K + 1, 1e-5, None) == UNS
+    assert f_rms(A, B, C, C + 8, M, N, K, 1e-5, None) == INV          # Y inside W
+    assert f_rms(None, None, None, None, 0, N, K, 1e-5, None) == mt.MT_OK
+    assert f_ln(None, None, None, None, None, M, 0, K, 1e-5, None) == mt.MT_OK
     assert lib.mt_last_cuda_error() == 0  # nothing reached CUDA
 
 
