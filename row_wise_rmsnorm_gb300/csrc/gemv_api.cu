@@ -2,6 +2,7 @@
 // (include/mt_norm.h documents the contracts; gemv.cuh the kernel).
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 
@@ -12,19 +13,13 @@
 namespace mt {
 namespace {
 
-// Features per CTA at most: two 8-feature chunks per thread (kGemvSliceChunks); the
-// normalized slice (slice x 8 rows x 4 bytes) stays within 128 KB of shared memory.
+// Input features per slice at most (two 8-feature chunks per thread build its normalized
+// rows).
 constexpr int kGemvMaxSlice = kGemvSliceChunks * 8 * kGemvWarps * 32;
 
-// Features per CTA for a cluster of cl: ceil(K / cl) rounded up to whole 8-feature chunks.
-int gemv_slice(int K, int cl) { return ((K + cl - 1) / cl + 7) / 8 * 8; }
-// W ring stages per thread (features in flight + 1), and the CTAs per SM the launch
-// shape aims for.
+// W ring stages per thread (features in flight + 1).
 #ifndef MT_GEMV_STAGES
 #define MT_GEMV_STAGES 12
-#endif
-#ifndef MT_GEMV_CTAS_PER_SM
-#define MT_GEMV_CTAS_PER_SM 2
 #endif
 constexpr int kGemvStages = MT_GEMV_STAGES;
 
@@ -40,32 +35,21 @@ bool overlap(const void *a, size_t na, const void *b, size_t nb) {
 }
 
 template <int OP, int MT, int LPF, bool VEC>
-const void *gemv_kernel() {
-    return reinterpret_cast<const void *>(&norm_gemv_kernel<OP, MT, LPF, kGemvStages, VEC>);
+void gemv_set(int slice, LaunchPlan *p) {
+    p->kernel = reinterpret_cast<const void *>(&norm_gemv_kernel<OP, MT, LPF, kGemvStages, VEC>);
+    p->smem = gemv_smem<MT, LPF, kGemvStages>(slice);
 }
 
 template <int OP, int MT>
-cudaError_t gemv_pick(int lpf, bool vec, int slice, LaunchPlan *p) {
-    if (!vec) {
-        p->kernel = gemv_kernel<OP, MT, 32, false>();
-        p->smem = gemv_smem<MT, 32, kGemvStages>(slice);
-        return cudaSuccess;
-    }
-    if (lpf == 32) {
-        p->kernel = gemv_kernel<OP, MT, 32, true>();
-        p->smem = gemv_smem<MT, 32, kGemvStages>(slice);
-    } else if (lpf == 16) {
-        p->kernel = gemv_kernel<OP, MT, 16, true>();
-        p->smem = gemv_smem<MT, 16, kGemvStages>(slice);
-    } else {
-        p->kernel = gemv_kernel<OP, MT, 8, true>();
-        p->smem = gemv_smem<MT, 8, kGemvStages>(slice);
-    }
-    return cudaSuccess;
+void gemv_pick(int lpf, bool vec, int slice, LaunchPlan *p) {
+    if (!vec) return gemv_set<OP, MT, 32, false>(slice, p);  // per-element W loads
+    if (lpf == 32) return gemv_set<OP, MT, 32, true>(slice, p);
+    if (lpf == 16) return gemv_set<OP, MT, 16, true>(slice, p);
+    return gemv_set<OP, MT, 8, true>(slice, p);
 }
 
 template <int OP>
-cudaError_t gemv_pick_rows(int M, int lpf, bool vec, int slice, LaunchPlan *p) {
+void gemv_pick_rows(int M, int lpf, bool vec, int slice, LaunchPlan *p) {
     switch (M) {
         case 1: return gemv_pick<OP, 1>(lpf, vec, slice, p);
         case 2: return gemv_pick<OP, 2>(lpf, vec, slice, p);
@@ -75,41 +59,58 @@ cudaError_t gemv_pick_rows(int M, int lpf, bool vec, int slice, LaunchPlan *p) {
     }
 }
 
-// Launch shape: the widest column tile (lanes per feature 32, 16, 8) and the smallest
-// cluster along K that give at least MT_GEMV_CTAS_PER_SM CTAs per SM, with at most kGemvMaxSlice
-// features per CTA and, where K allows, at least four features per feature group.
+// Split-K launch shape: tiles of 8 * LPF columns (LPF 32 for N >= 1024, narrower for
+// narrow outputs; 32 for per-element loads), and the number of slices (each thread
+// keeping at least four features, each slice at most kGemvMaxSlice of them) whose grid
+// fills its last wave of resident CTAs best; ties go to fewer, longer CTAs.
 cudaError_t gemv_plan(int op, int M, int N, int K, bool vec, int device, LaunchPlan *p,
-                      int *slice) {
+                      int *slice, int *ks, int *ntiles) {
     int sms = 0;
     cudaError_t e = device_sm_count(device, &sms);
     if (e != cudaSuccess) return e;
-    const int64_t want = MT_GEMV_CTAS_PER_SM * (int64_t)sms;
-    int lpf = 32;
-    if (vec) {
-        while (lpf > 8 && (int64_t)((N + 8 * lpf - 1) / (8 * lpf)) * kMaxCluster < want) lpf /= 2;
-    }
+    const int lpf = !vec ? 32 : N >= 1024 ? 32 : N >= 256 ? 16 : 8;
     const int64_t tiles = (N + 8 * lpf - 1) / (8 * lpf);
     const int fg = kGemvWarps * (32 / lpf);
-    int cl = 1;
-    while (cl < kMaxCluster && (tiles * cl < want || gemv_slice(K, cl) > kGemvMaxSlice)) cl *= 2;
-    while (cl > 1 && gemv_slice(K, cl) < 4 * fg && gemv_slice(K, cl / 2) <= kGemvMaxSlice)
-        cl /= 2;
-    *slice = gemv_slice(K, cl);
-    if (*slice > kGemvMaxSlice || tiles * cl > (int64_t)INT32_MAX) return cudaErrorInvalidValue;
-    e = (op == kRms) ? gemv_pick_rows<kRms>(M, lpf, vec, *slice, p)
-                     : gemv_pick_rows<kLayer>(M, lpf, vec, *slice, p);
-    if (e != cudaSuccess) return e;
+    const int64_t kmin = std::max<int64_t>(1, (K + kGemvMaxSlice - 1) / kGemvMaxSlice);
+    const int64_t kmax = std::max<int64_t>(kmin, (K + 4 * fg - 1) / (4 * fg));
+    auto slice_of = [&](int64_t k) { return (int)(((K + k - 1) / k + 7) / 8 * 8); };
+    // resident CTAs (the shared memory differs little with the slice: take the largest)
+    if (op == kRms) gemv_pick_rows<kRms>(M, lpf, vec, slice_of(kmin), p);
+    else gemv_pick_rows<kLayer>(M, lpf, vec, slice_of(kmin), p);
+    int per_sm = 0;
+    if ((e = cached_occupancy(p->kernel, kGemvWarps * 32, p->smem, device, &per_sm)) != cudaSuccess)
+        return e;
+    const int64_t cap = (int64_t)std::max(per_sm, 1) * sms;
+    int64_t best_k = kmin;
+    double best_fill = -1.0;
+    for (int64_t k = kmin; k <= std::min<int64_t>(kmax, 4 * cap); ++k) {
+        const int64_t kk = (K + slice_of(k) - 1) / slice_of(k);  // slices actually used
+        const int64_t ctas = tiles * kk;
+        if (ctas > 8 * cap) break;
+        const double fill = (double)ctas / (double)(((ctas + cap - 1) / cap) * cap);
+        if (fill > best_fill + 1e-9) {
+            best_fill = fill;
+            best_k = kk;
+        }
+    }
+    const int sl = slice_of(best_k);
+    const int64_t k = (K + sl - 1) / sl;
+    if (sl > kGemvMaxSlice || tiles * k > (int64_t)INT32_MAX) return cudaErrorInvalidValue;
+    if (op == kRms) gemv_pick_rows<kRms>(M, lpf, vec, sl, p);
+    else gemv_pick_rows<kLayer>(M, lpf, vec, sl, p);
     p->threads = kGemvWarps * 32;
-    p->grid = (int)(tiles * cl);
-    p->cluster = cl;
+    p->grid = (int)(tiles * k);
     p->rows_per_cta = M;
-    int per_sm = 0;  // raises the kernel's dynamic shared memory limit to p->smem
+    *slice = sl;
+    *ks = (int)k;
+    *ntiles = (int)tiles;
+    // raises the kernel's dynamic shared memory limit to p->smem
     return cached_occupancy(p->kernel, p->threads, p->smem, device, &per_sm);
 }
 
 mt_status_t norm_gemv_impl(int op, const void *X, const void *gamma, const void *beta,
                            const void *W, void *Y, int64_t M, int64_t N, int64_t K, float eps,
-                           mt_stream_t stream) {
+                           mt_stream_t stream_in) {
     if (M < 0 || N < 0 || K < 1) return MT_ERR_INVALID_ARG;
     if (M > MT_MAX_GEMV_ROWS || K > MT_MAX_GEMV_K || N > (int64_t)INT32_MAX)
         return MT_ERR_UNSUPPORTED;
@@ -121,6 +122,7 @@ mt_status_t norm_gemv_impl(int op, const void *X, const void *gamma, const void 
         overlap(Y, ybytes, op == kLayer ? beta : nullptr, (size_t)K * 2) ||
         overlap(Y, ybytes, W, (size_t)K * (size_t)N * 2))
         return MT_ERR_INVALID_ARG;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_in);
     int device = 0;
     cudaError_t e = cudaGetDevice(&device);
     if (e != cudaSuccess) return gemv_fail(e);
@@ -128,8 +130,16 @@ mt_status_t norm_gemv_impl(int op, const void *X, const void *gamma, const void 
     const bool a16 = (((uintptr_t)X | (uintptr_t)gamma | (uintptr_t)(op == kLayer ? beta : gamma)) &
                       15u) == 0;
     LaunchPlan p;
-    int slice = 0;
-    if ((e = gemv_plan(op, (int)M, (int)N, (int)K, vec, device, &p, &slice)) != cudaSuccess)
+    int slice = 0, ks = 0, tiles = 0;
+    if ((e = gemv_plan(op, (int)M, (int)N, (int)K, vec, device, &p, &slice, &ks, &tiles)) !=
+        cudaSuccess)
+        return gemv_fail(e);
+    // stream-ordered scratch: the statistics, the tile counters, the fp32 partial rows
+    const size_t stats_bytes = 256;
+    const size_t count_bytes = ((size_t)tiles * sizeof(unsigned) + 255) / 256 * 256;
+    const size_t part_bytes = (size_t)ks * (size_t)M * (size_t)N * sizeof(float);
+    void *ws = nullptr;
+    if ((e = cudaMallocAsync(&ws, stats_bytes + count_bytes + part_bytes, stream)) != cudaSuccess)
         return gemv_fail(e);
     GemvArgs a{};
     a.X = X;
@@ -137,13 +147,26 @@ mt_status_t norm_gemv_impl(int op, const void *X, const void *gamma, const void 
     a.beta = op == kLayer ? beta : gamma;
     a.W = W;
     a.Y = Y;
+    a.stats = static_cast<float *>(ws);
+    a.count = reinterpret_cast<unsigned *>(static_cast<char *>(ws) + stats_bytes);
+    a.part = reinterpret_cast<float *>(static_cast<char *>(ws) + stats_bytes + count_bytes);
+    a.tiles = tiles;
     a.M = (int)M;
     a.N = (int)N;
     a.K = (int)K;
     a.slice = slice;
+    a.ks = ks;
     a.eps = eps;
     a.xvec = (K % 8 == 0) && a16;
-    e = launch_pdl(p, &a, reinterpret_cast<cudaStream_t>(stream));
+    LaunchPlan st;
+    st.kernel = op == kRms ? reinterpret_cast<const void *>(&gemv_stats_kernel<kRms>)
+                           : reinterpret_cast<const void *>(&gemv_stats_kernel<kLayer>);
+    st.threads = kGemvStatsThreads;
+    st.grid = (int)M;
+    e = launch_pdl(st, &a, stream);
+    if (e == cudaSuccess) e = launch_pdl(p, &a, stream);
+    const cudaError_t fe = cudaFreeAsync(ws, stream);
+    if (e == cudaSuccess) e = fe;
     return e == cudaSuccess ? MT_OK : gemv_fail(e);
 }
 
