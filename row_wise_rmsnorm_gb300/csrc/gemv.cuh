@@ -66,10 +66,17 @@ __host__ __device__ constexpr int gemv_mp() { return MT <= 4 ? 4 : 8; }
 
 // Shared memory of a GEMV launch: the normalized slice, then the W ring (S stages of one
 // 16-byte chunk per thread), reused after the stream for the warps' partial sums.
+#ifndef MT_GEMV_CPL
+#define MT_GEMV_CPL 1
+#endif
+// 16-byte chunks per lane and feature: lane l's chunks sit 8 * LPF columns apart, so each
+// warp load instruction still covers 16 * LPF contiguous bytes.
+constexpr int kGemvCpl = MT_GEMV_CPL;
+
 template <int MT, int LPF, int S>
 constexpr size_t gemv_smem(int slice) {
-    const size_t ring = (size_t)S * kGemvWarps * 32 * 16;
-    const size_t red = (size_t)kGemvWarps * MT * (8 * LPF) * sizeof(float);
+    const size_t ring = (size_t)S * kGemvCpl * kGemvWarps * 32 * 16;
+    const size_t red = (size_t)kGemvWarps * MT * (8 * LPF * kGemvCpl) * sizeof(float);
     return (size_t)slice * gemv_mp<MT>() * sizeof(float) + (ring > red ? ring : red);
 }
 
@@ -170,7 +177,8 @@ norm_gemv_kernel(const GemvArgs a) {
     constexpr int THREADS = kGemvWarps * 32;
     constexpr int G = 32 / LPF;              // features per warp step
     constexpr int FG = kGemvWarps * G;       // feature groups per CTA
-    constexpr int TILE = 8 * LPF;            // output columns per CTA
+    constexpr int CPL = kGemvCpl;            // chunks per lane and feature
+    constexpr int TILE = 8 * LPF * CPL;      // output columns per CTA
     constexpr int MP = gemv_mp<MT>();
     static_assert(OP == kRms || OP == kLayer, "RMSNorm or LayerNorm");
     static_assert(MT >= 1 && MT <= kGemvMaxRows && (LPF == 32 || LPF == 16 || LPF == 8), "shape");
@@ -184,8 +192,7 @@ norm_gemv_kernel(const GemvArgs a) {
     const int tile = (int)(blockIdx.x % ntiles), ks = (int)(blockIdx.x / ntiles);
     const int kbeg = ks * a.slice, kend = min(K, kbeg + a.slice);
     const int f = w * G + lane / LPF;                 // this thread's feature group
-    const int col = tile * TILE + (lane % LPF) * 8;   // first of its 8 columns
-    const bool cok = col < N;
+    const int col = tile * TILE + (lane % LPF) * 8;   // first column of its chunk 0
     const int nk = kbeg + f < kend ? (kend - kbeg - f + FG - 1) / FG : 0;  // its features
     const __half *W = static_cast<const __half *>(a.W);
     float *xn = gsm;                                                      // [slice][MP]
@@ -194,9 +201,13 @@ norm_gemv_kernel(const GemvArgs a) {
     // start the W stream (before the wait: no earlier kernel of the chain writes W)
     auto issue = [&](int i) {
         if constexpr (VEC) {
-            if (i < nk && cok)
-                cp_async16(smem_addr(&ring[(i % S) * THREADS + tid]),
-                           W + (int64_t)(kbeg + f + i * FG) * N + col);
+            if (i < nk) {
+#pragma unroll
+                for (int c = 0; c < CPL; ++c)
+                    if (col + c * 8 * LPF < N)
+                        cp_async16(smem_addr(&ring[((i % S) * CPL + c) * THREADS + tid]),
+                                   W + (int64_t)(kbeg + f + i * FG) * N + col + c * 8 * LPF);
+            }
             cp_async_commit();
         }
     };
@@ -253,23 +264,30 @@ norm_gemv_kernel(const GemvArgs a) {
     __syncthreads();
 
     // stream: acc[m][p] += xn[k][m] * W[k][col + 2p .. 2p+1], features ascending
-    float2 acc[MT][4];
+    float2 acc[CPL][MT][4];
 #pragma unroll
-    for (int m = 0; m < MT; ++m)
+    for (int c = 0; c < CPL; ++c)
 #pragma unroll
-        for (int p = 0; p < 4; ++p) acc[m][p] = make_float2(0.f, 0.f);
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+            for (int p = 0; p < 4; ++p) acc[c][m][p] = make_float2(0.f, 0.f);
     for (int i = 0; i < nk; ++i) {
-        uint4 raw;
+        uint4 raw[CPL];
         if constexpr (VEC) {
             issue(i + S - 1);
-            cp_async_wait<S - 1>();  // this thread's copy of feature i has landed
-            raw = ring[(i % S) * THREADS + tid];
+            cp_async_wait<S - 1>();  // this thread's copies of feature i have landed
+#pragma unroll
+            for (int c = 0; c < CPL; ++c)
+                raw[c] = col + c * 8 * LPF < N ? ring[((i % S) * CPL + c) * THREADS + tid]
+                                               : make_uint4(0, 0, 0, 0);
         } else {
-            raw = cok ? gemv_ld_w<false>(W, kbeg + f + (int64_t)i * FG, N, col) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int c = 0; c < CPL; ++c)
+                raw[c] = col + c * 8 * LPF < N
+                             ? gemv_ld_w<false>(W, kbeg + f + (int64_t)i * FG, N, col + c * 8 * LPF)
+                             : make_uint4(0, 0, 0, 0);
         }
         const int kl = f + i * FG;  // feature index within the slice
-        float2 wf[4];
-        unpack_unit<kF16>(raw, wf);
         float xv[MP];
 #pragma unroll
         for (int q = 0; q < MP / 4; ++q) {
@@ -280,10 +298,15 @@ norm_gemv_kernel(const GemvArgs a) {
             xv[4 * q + 3] = t.w;
         }
 #pragma unroll
-        for (int m = 0; m < MT; ++m) {
-            const float2 x2 = make_float2(xv[m], xv[m]);
+        for (int c = 0; c < CPL; ++c) {
+            float2 wf[4];
+            unpack_unit<kF16>(raw[c], wf);
 #pragma unroll
-            for (int p = 0; p < 4; ++p) acc[m][p] = __ffma2_rn(x2, wf[p], acc[m][p]);
+            for (int m = 0; m < MT; ++m) {
+                const float2 x2 = make_float2(xv[m], xv[m]);
+#pragma unroll
+                for (int p = 0; p < 4; ++p) acc[c][m][p] = __ffma2_rn(x2, wf[p], acc[c][m][p]);
+            }
         }
     }
     if constexpr (VEC) cp_async_wait<0>();
@@ -293,21 +316,26 @@ norm_gemv_kernel(const GemvArgs a) {
 #pragma unroll
     for (int o = LPF; o < 32; o <<= 1)
 #pragma unroll
-        for (int m = 0; m < MT; ++m)
+        for (int c = 0; c < CPL; ++c)
 #pragma unroll
-            for (int p = 0; p < 4; ++p) {
-                acc[m][p].x += __shfl_xor_sync(0xffffffffu, acc[m][p].x, o);
-                acc[m][p].y += __shfl_xor_sync(0xffffffffu, acc[m][p].y, o);
-            }
+            for (int m = 0; m < MT; ++m)
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    acc[c][m][p].x += __shfl_xor_sync(0xffffffffu, acc[c][m][p].x, o);
+                    acc[c][m][p].y += __shfl_xor_sync(0xffffffffu, acc[c][m][p].y, o);
+                }
     __syncthreads();  // every thread is done with its ring slots
     float *wpart = reinterpret_cast<float *>(ring);  // [kGemvWarps][MT][TILE]
     if (lane < LPF) {
 #pragma unroll
-        for (int m = 0; m < MT; ++m) {
-            float4 *dst = reinterpret_cast<float4 *>(wpart + ((size_t)w * MT + m) * TILE + (lane % LPF) * 8);
-            dst[0] = make_float4(acc[m][0].x, acc[m][0].y, acc[m][1].x, acc[m][1].y);
-            dst[1] = make_float4(acc[m][2].x, acc[m][2].y, acc[m][3].x, acc[m][3].y);
-        }
+        for (int c = 0; c < CPL; ++c)
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                float4 *dst = reinterpret_cast<float4 *>(wpart + ((size_t)w * MT + m) * TILE +
+                                                         lane * 8 + c * 8 * LPF);
+                dst[0] = make_float4(acc[c][m][0].x, acc[c][m][0].y, acc[c][m][1].x, acc[c][m][1].y);
+                dst[1] = make_float4(acc[c][m][2].x, acc[c][m][2].y, acc[c][m][3].x, acc[c][m][3].y);
+            }
     }
     __syncthreads();
     for (int idx = tid; idx < M * TILE; idx += THREADS) {

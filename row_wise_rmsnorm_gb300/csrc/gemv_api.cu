@@ -69,7 +69,7 @@ cudaError_t gemv_plan(int op, int M, int N, int K, bool vec, int device, LaunchP
     cudaError_t e = device_sm_count(device, &sms);
     if (e != cudaSuccess) return e;
     const int lpf = !vec ? 32 : N >= 1024 ? 32 : N >= 256 ? 16 : 8;
-    const int64_t tiles = (N + 8 * lpf - 1) / (8 * lpf);
+    const int64_t tiles = (N + 8 * lpf * kGemvCpl - 1) / (8 * lpf * kGemvCpl);
     const int fg = kGemvWarps * (32 / lpf);
     const int64_t kmin = std::max<int64_t>(1, (K + kGemvMaxSlice - 1) / kGemvMaxSlice);
     const int64_t kmax = std::max<int64_t>(kmin, (K + 4 * fg - 1) / (4 * fg));
