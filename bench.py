@@ -297,41 +297,94 @@ def time_ops(sets, steps: int, warmup: int, stream):
     return fwd, bwd, total
 
 
-def e2e_run(name: str, device, steps: int, warmup: int, seed: int):
+E2E_COPY_STREAMS = 1  # measured on GB300: 1, 2, 4, 8 streams per direction: 404, 391, 378, 283 GB/s
+
+
+def e2e_run(name: str, device, steps: int, warmup: int, seed: int,
+            copy_streams: int = E2E_COPY_STREAMS):
     """Same metric through the public API with pinned-host inputs/outputs: every step
     copies X, gamma, dY (and R, dS / beta) host->device, runs forward + backward, and
-    copies Y, stats, dX, dgamma (and S / dbeta) back. CUDA events bracket the step."""
+    copies Y, stats, dX, dgamma (and S / dbeta) back to pinned host memory.
+
+    Steps are pipelined the way a serving or training loop would run them: copy-in
+    streams, a compute stream and copy-out streams, with two device buffer sets, so the
+    copy-in of step s runs beside the compute of step s-1 and the copy-out of step s-2.
+    Each tensor's copy is split by rows over `copy_streams` streams per direction (one
+    cudaMemcpyAsync each), so several copy engines share it. Events order every step's
+    three stages and keep a buffer set from being refilled before its previous step's
+    outputs are out. The timed region runs from before the first copy-in to after the
+    last copy-out."""
     import torch
-    r = OpRunner(name, device, seed)
-    ins = {k: v.cpu().pin_memory() for k, v in r.t.items()}
-    outs_dev = [r.Y, r.rstd, r.dX, r.dg] + [x for x in (r.mean, r.db, r.S) if x is not None]
-    outs_host = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in outs_dev]
+    sets = [OpRunner(name, device, seed + i) for i in range(2)]
+    ins = {k: v.cpu().pin_memory() for k, v in sets[0].t.items()}
+
+    def outs(r):
+        return [r.Y, r.rstd, r.dX, r.dg] + [x for x in (r.mean, r.db, r.S) if x is not None]
+
+    outs_host = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in outs(sets[0])]
     h2d = sum(v.numel() * v.element_size() for v in ins.values())
-    d2h = sum(x.numel() * x.element_size() for x in outs_dev)
-    stream = torch.cuda.current_stream()
+    d2h = sum(x.numel() * x.element_size() for x in outs(sets[0]))
+    P = max(1, copy_streams)
+    s_in = [torch.cuda.Stream(device=device) for _ in range(P)]
+    s_out = [torch.cuda.Stream(device=device) for _ in range(P)]
+    s_comp = torch.cuda.Stream(device=device)
+    total = warmup + steps
+    in_done = [[torch.cuda.Event() for _ in range(P)] for _ in range(total)]
+    comp_done = [torch.cuda.Event() for _ in range(total)]
+    out_done = [[torch.cuda.Event() for _ in range(P)] for _ in range(total)]
 
-    def step():
-        for k, v in ins.items():
-            r.t[k].copy_(v, non_blocking=True)
-        r.forward(stream)
-        r.backward(stream)
-        for hd, dv in zip(outs_host, outs_dev):
-            hd.copy_(dv, non_blocking=True)
+    def pieces(t):
+        return t.chunk(P, dim=0) if t.dim() > 0 and t.shape[0] >= P else [t] + [None] * (P - 1)
 
-    for _ in range(warmup):
-        step()
+    def copy_all(dsts, srcs, streams, done):
+        for i, st in enumerate(streams):
+            with torch.cuda.stream(st):
+                for d, s_ in zip(dsts, srcs):
+                    dp, sp = pieces(d)[i], pieces(s_)[i]
+                    if dp is not None:
+                        dp.copy_(sp, non_blocking=True)
+            done[i].record(st)
+
+    def step(j):
+        r = sets[j % 2]
+        if j >= 2:
+            for st in s_in:
+                st.wait_event(comp_done[j - 2])  # this set's inputs are consumed
+        copy_all([r.t[k] for k in ins], list(ins.values()), s_in, in_done[j])
+        for ev in in_done[j]:
+            s_comp.wait_event(ev)
+        if j >= 2:
+            for ev in out_done[j - 2]:
+                s_comp.wait_event(ev)            # this set's outputs are copied out
+        with torch.cuda.stream(s_comp):
+            r.forward(s_comp)
+            r.backward(s_comp)
+        comp_done[j].record(s_comp)
+        for st in s_out:
+            st.wait_event(comp_done[j])
+        copy_all(outs_host, outs(r), s_out, out_done[j])
+
+    for j in range(warmup):
+        step(j)
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(steps):
-        step()
-    b.record(stream)
+    a.record(s_in[0])
+    for st in s_in[1:] + s_out + [s_comp]:
+        st.wait_event(a)
+    for j in range(warmup, total):
+        step(j)
+    for st in s_out[1:]:
+        s_out[0].wait_stream(st)
+    b.record(s_out[0])
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / steps
+    r = sets[0]
     gbs = (r.fwd_bytes + r.bwd_bytes) / (ms * 1e-3) / 1e9
-    del r
+    del sets, r
     return {"value": round(gbs, 2), "unit": "GB/s", "ms_per_step": round(ms, 4),
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "pipeline": (f"{P} copy-in streams, a compute stream, {P} copy-out streams, two "
+                         "device buffer sets")}
 
 
 # ------------------------------------------------------------ CPU oracle ---
