@@ -19,6 +19,9 @@
 //    fp32 registers across its rows; at the end the CTA's row groups are combined in
 //    a fixed order and one fp32 partial row per CTA is written. A second small
 //    kernel sums the partials column by column in ascending CTA order. No atomics.
+//  * Rows wider than one CTA's slice run on a thread-block cluster (see "cluster
+//    split" below): the same per-thread layout inside each CTA's column window, plus
+//    one exchange of the CTAs' row sums through distributed shared memory.
 //
 // Formulas (page title, section): meTile "Kernel coverage and training scope",
 // "Exact native normalization contract"; tensorcore "Training kernels",
