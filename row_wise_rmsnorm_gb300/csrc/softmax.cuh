@@ -255,11 +255,8 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-// Chunks each cross-entropy thread loads before using the first (bytes in flight).
-#ifndef MT_CE_UNROLL
-#define MT_CE_UNROLL 4
-#endif
-constexpr int kCeUnroll = MT_CE_UNROLL;
+// Each cross-entropy thread loads UN chunks (a kernel template parameter, set per shape)
+// before using the first: the bytes in flight.
 
 // Running (maximum, sum of exp(x - maximum)) state and its order-fixed combination. A
 // state whose maximum is -inf has seen only -inf logits (masked columns) and sums to 0.
@@ -280,14 +277,53 @@ __device__ __forceinline__ void add_value(MaxSum &st, float x) {
     }
 }
 
-// Loads the kCeUnroll chunks c0, c0 + TPR, ... of one row (zeros past the end).
-template <int TPR, int XT>
+// Loads the UN chunks c0, c0 + TPR, ... of one row (zeros past the end).
+template <int TPR, int XT, int UN>
 __device__ __forceinline__ void ce_load(const void *X, int64_t off, int c0, int D,
-                                        float2 (&f)[kCeUnroll][4]) {
+                                        float2 (&f)[UN][4]) {
 #pragma unroll
-    for (int u = 0; u < kCeUnroll; ++u) {
+    for (int u = 0; u < UN; ++u) {
         const int c = c0 + u * TPR;
         ld_chunk<XT, kStream>(as<XT>(X) + off + c * 8, c * 8 < D, f[u]);
+    }
+}
+
+// The 16-byte units of the UN chunks c0, c0 + TPR, ... of one row, as loaded; chunks
+// past the end read as -inf (they must not raise the running maximum).
+template <int TPR, int XT, int UN>
+__device__ __forceinline__ void ce_load_raw(const void *X, int64_t off, int c0, int D,
+                                            uint4 (&raw)[UN][chunk_units<XT>()]) {
+    constexpr uint32_t kNegInf = (XT == kF32) ? 0xff800000u : (XT == kBF16) ? 0xff80ff80u : 0xfc00fc00u;
+#pragma unroll
+    for (int u = 0; u < UN; ++u) {
+        const int c = c0 + u * TPR;
+#pragma unroll
+        for (int q = 0; q < chunk_units<XT>(); ++q)
+            raw[u][q] = c * 8 < D ? ld_unit<kStream>(as<XT>(X) + off + c * 8 + q * (8 / chunk_units<XT>()))
+                                  : make_uint4(kNegInf, kNegInf, kNegInf, kNegInf);
+    }
+}
+
+// Maximum of one loaded chunk: 2-byte types with packed two-lane max instructions on the
+// loaded words (a maximum is exact, so this equals the fp32 maximum of the widened
+// values), fp32 lane by lane.
+template <int XT>
+__device__ __forceinline__ float chunk_max(const uint4 (&r)[chunk_units<XT>()]) {
+    if constexpr (XT == kF32) {
+        float m = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < chunk_units<XT>(); ++q)
+            m = fmaxf(m, fmaxf(fmaxf(__uint_as_float(r[q].x), __uint_as_float(r[q].y)),
+                               fmaxf(__uint_as_float(r[q].z), __uint_as_float(r[q].w))));
+        return m;
+    } else if constexpr (XT == kBF16) {
+        auto w = [](uint32_t v) { return *reinterpret_cast<const __nv_bfloat162 *>(&v); };
+        const __nv_bfloat162 m = __hmax2(__hmax2(w(r[0].x), w(r[0].y)), __hmax2(w(r[0].z), w(r[0].w)));
+        return __bfloat162float(__hmax(m.x, m.y));
+    } else {
+        auto w = [](uint32_t v) { return *reinterpret_cast<const __half2 *>(&v); };
+        const __half2 m = __hmax2(__hmax2(w(r[0].x), w(r[0].y)), __hmax2(w(r[0].z), w(r[0].w)));
+        return __half2float(__hmax(m.x, m.y));
     }
 }
 
@@ -307,7 +343,7 @@ __device__ __forceinline__ float chunk_elem(const float2 (&f)[4], int e) {
 // taking chunks t, t + TPR, ...; otherwise single elements, same striding. Every thread
 // reads the row's target with its first logits; the thread that meets the target column
 // keeps its logit, so no load waits on another at the end of the row.
-template <int TPR, int RPC, bool VEC8, int XT, int MINB>
+template <int TPR, int RPC, bool VEC8, int XT, int MINB, int UN>
 __global__ void __launch_bounds__(TPR * RPC, MINB)
 ce_fwd_kernel(const CeArgs a) {
     pdl_enter();
@@ -324,37 +360,44 @@ ce_fwd_kernel(const CeArgs a) {
     MaxSum st{-INFINITY, 0.f};
     float sx = 0.f;
     if constexpr (VEC8) {
+        // per batch of UN chunks: one running-maximum update (from the chunks'
+        // packed maxima), then the exponentials of the valid chunks
+        constexpr int CU = chunk_units<XT>();
         const float2 l2e = make_float2(kLog2e, kLog2e);
         float2 sx2 = make_float2(0.f, 0.f);
-        float2 f[kCeUnroll][4];
-        ce_load<TPR, XT>(a.X, off, t, D, f);
+        uint4 raw[UN][CU];
+        ce_load_raw<TPR, XT, UN>(a.X, off, t, D, raw);
         const int64_t tg = a.T[row];
         const int tc = (tg >= 0 && tg < D) ? (int)(tg >> 3) : -1;   // chunk holding the target
         for (int c0 = t;;) {
+            float bm = chunk_max<XT>(raw[0]);
 #pragma unroll
-            for (int u = 0; u < kCeUnroll; ++u) {
+            for (int u = 1; u < UN; ++u) bm = fmaxf(bm, chunk_max<XT>(raw[u]));
+            const float m = fmaxf(st.m, bm);
+            const float ms = (m == -INFINITY) ? 0.f : m;   // all -inf so far: exps are 0
+            const float nb = -ms * kLog2e;
+            const float2 nb2 = make_float2(nb, nb);
+            st.s *= ex2(fmaf(st.m, kLog2e, nb));
+            st.m = m;
+            float2 cs2 = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int u = 0; u < UN; ++u) {
                 const int c = c0 + u * TPR;
                 if (c * 8 >= D) continue;
-                const float cm = fmaxf(fmaxf(fmaxf(f[u][0].x, f[u][0].y), fmaxf(f[u][1].x, f[u][1].y)),
-                                       fmaxf(fmaxf(f[u][2].x, f[u][2].y), fmaxf(f[u][3].x, f[u][3].y)));
-                const float m = fmaxf(st.m, cm);
-                const float ms = (m == -INFINITY) ? 0.f : m;   // all -inf so far: exps are 0
-                const float nb = -ms * kLog2e;
-                const float2 nb2 = make_float2(nb, nb);
-                float2 cs2 = make_float2(0.f, 0.f);
+                float2 f[4];
+                unpack_chunk<XT, 4>(raw[u], 1, f);
 #pragma unroll
                 for (int p = 0; p < 4; ++p) {
-                    const float2 e = __ffma2_rn(f[u][p], l2e, nb2);   // (x - ms) log2(e)
+                    const float2 e = __ffma2_rn(f[p], l2e, nb2);   // (x - ms) log2(e)
                     cs2 = __fadd2_rn(cs2, make_float2(ex2(e.x), ex2(e.y)));
-                    sx2 = __fadd2_rn(sx2, f[u][p]);
+                    sx2 = __fadd2_rn(sx2, f[p]);
                 }
-                st.s = st.s * ex2(fmaf(st.m, kLog2e, nb)) + (cs2.x + cs2.y);
-                st.m = m;
-                if (c == tc) sm_t[rg] = chunk_elem(f[u], (int)(tg & 7));
+                if (c == tc) sm_t[rg] = chunk_elem(f, (int)(tg & 7));
             }
-            c0 += kCeUnroll * TPR;
+            st.s += cs2.x + cs2.y;
+            c0 += UN * TPR;
             if (c0 * 8 >= D) break;
-            ce_load<TPR, XT>(a.X, off, c0, D, f);
+            ce_load_raw<TPR, XT, UN>(a.X, off, c0, D, raw);
         }
         sx = sx2.x + sx2.y;
     } else {
@@ -420,7 +463,7 @@ __device__ __forceinline__ float ce_row_grad(const CeArgs &a, int64_t row, int64
     return tg == a.ignore_index ? 0.f : g;
 }
 
-template <int TPR, int RPC, bool VEC8, int XT, int MINB>
+template <int TPR, int RPC, bool VEC8, int XT, int MINB, int UN>
 __global__ void __launch_bounds__(TPR * RPC, MINB)
 ce_bwd_kernel(const CeArgs a) {
     pdl_enter();
@@ -431,8 +474,8 @@ ce_bwd_kernel(const CeArgs a) {
     const int64_t off = row * (int64_t)D;
     if constexpr (VEC8) {
         // the first logits are requested before the per-row scalars are waited on
-        float2 f[kCeUnroll][4];
-        ce_load<TPR, XT>(a.X, off, t, D, f);
+        float2 f[UN][4];
+        ce_load<TPR, XT, UN>(a.X, off, t, D, f);
         const int64_t tg = a.T[row];
         const float g = ce_row_grad(a, row, tg);
         const float l = a.lse[row];
@@ -445,7 +488,7 @@ ce_bwd_kernel(const CeArgs a) {
         const float2 scale2 = make_float2(scale, scale), ngq2 = make_float2(-gq, -gq);
         for (int c0 = t;;) {
 #pragma unroll
-            for (int u = 0; u < kCeUnroll; ++u) {
+            for (int u = 0; u < UN; ++u) {
                 const int c = c0 + u * TPR;
                 if (c * 8 >= D) continue;
                 float2 o[4];
@@ -464,9 +507,9 @@ ce_bwd_kernel(const CeArgs a) {
                 }
                 st_chunk<XT>(as<XT>(a.dX) + off + c * 8, o);
             }
-            c0 += kCeUnroll * TPR;
+            c0 += UN * TPR;
             if (c0 * 8 >= D) break;
-            ce_load<TPR, XT>(a.X, off, c0, D, f);
+            ce_load<TPR, XT, UN>(a.X, off, c0, D, f);
         }
     } else {
         const int64_t tg = a.T[row];

@@ -28,26 +28,28 @@ namespace {
     X(4096, 256, 1, 16)             \
     X(16384, 1024, 1, 16)
 
-// Cross-entropy: X(max_D, TPR, RPC, MINB): a row group of TPR threads per row, RPC rows per
-// CTA (one-warp row groups only), MINB a floor on resident CTAs per SM for the register
-// allocator (0: the compiler's choice). Narrow row groups with many chunks per thread,
-// narrower still in the forward (whose per-element work is larger): each entry measured
-// on GB300 against its neighbours (forward of 4096 x 32768 bf16: 128 threads 55.8 us,
-// 256 threads 59.3 us, 512 threads 92.5 us; forward of 16384 x 4096: one warp per row,
-// four rows per CTA, 35.2 us, 64 threads 39.0 us, 256 threads 80.1 us).
+// Cross-entropy: X(max_D, TPR, RPC, MINB, UN): a row group of TPR threads per row, RPC
+// rows per CTA (one-warp row groups only), MINB a floor on resident CTAs per SM for the
+// register allocator (0: the compiler's choice), UN chunks in flight per thread. Narrow
+// row groups with many chunks per thread, narrower still in the forward (whose
+// per-element work is larger): each entry measured on GB300 against its neighbours
+// (forward of 4096 x 32768 bf16: 128 threads 55.8 us, 256 threads 59.3 us, 512 threads
+// 92.5 us, and 8 chunks in flight 54.1 us against 4; forward of 16384 x 4096: one warp
+// per row, four rows per CTA, 35.2 us, 64 threads 39.0 us, 256 threads 80.1 us; 8 chunks
+// in flight lose at 1024 columns: 53.4 us against 47.3 us for 65536 rows).
 #ifndef MT_CE_FWD_SHAPES
 #define MT_CE_FWD_SHAPES(X) \
-    X(1024, 32, 2, 0)       \
-    X(4096, 32, 4, 0)       \
-    X(16384, 64, 1, 0)      \
-    X(MT_MAX_CE_COLS, 128, 1, 0)
+    X(1024, 32, 2, 0, 4)    \
+    X(4096, 32, 4, 0, 4)    \
+    X(16384, 64, 1, 0, 8)   \
+    X(MT_MAX_CE_COLS, 128, 1, 0, 8)
 #endif
 #ifndef MT_CE_BWD_SHAPES
 #define MT_CE_BWD_SHAPES(X) \
-    X(1024, 32, 4, 0)       \
-    X(4096, 64, 1, 0)       \
-    X(16384, 128, 1, 0)     \
-    X(MT_MAX_CE_COLS, 256, 1, 0)
+    X(1024, 32, 4, 0, 4)    \
+    X(4096, 64, 1, 0, 8)    \
+    X(16384, 128, 1, 0, 8)  \
+    X(MT_MAX_CE_COLS, 256, 1, 0, 4)
 #endif
 
 mt_status_t fail(cudaError_t e) {
@@ -126,12 +128,12 @@ cudaError_t softmax_plan(int64_t N, int D, bool vec8, int xdt, LaunchPlan *p) {
 
 template <bool BWD, bool VEC8, int XT>
 cudaError_t ce_plan_t(int64_t N, int D, LaunchPlan *p) {
-#define MT_TRY(maxd, tpr, rpc, minb)                                                                \
+#define MT_TRY(maxd, tpr, rpc, minb, un)                                                            \
     if (D <= maxd) {                                                                                \
         if constexpr (BWD)                                                                          \
-            p->kernel = reinterpret_cast<const void *>(&ce_bwd_kernel<tpr, rpc, VEC8, XT, minb>);   \
+            p->kernel = reinterpret_cast<const void *>(&ce_bwd_kernel<tpr, rpc, VEC8, XT, minb, un>); \
         else                                                                                        \
-            p->kernel = reinterpret_cast<const void *>(&ce_fwd_kernel<tpr, rpc, VEC8, XT, minb>);   \
+            p->kernel = reinterpret_cast<const void *>(&ce_fwd_kernel<tpr, rpc, VEC8, XT, minb, un>); \
         p->threads = tpr * rpc;                                                                     \
         p->grid = (int)((N + rpc - 1) / rpc);                                                       \
         p->rows_per_cta = rpc;                                                                      \
