@@ -48,7 +48,8 @@ def _run(op, x, gamma, beta, w, eps):
     return mt.norm_gemv(x, gamma, w, beta if op == "layernorm" else None, eps)
 
 
-SHAPES = [(64, 8), (257, 100), (1024, 4096), (4096, 1000), (2048, 12288), (32768, 256)]
+SHAPES = [(64, 8), (257, 100), (1024, 4096), (4096, 1000), (2048, 12288), (32768, 256),
+          (32768, 4096)]
 
 
 @pytest.mark.parametrize("KN", SHAPES, ids=lambda s: f"K{s[0]}-N{s[1]}")
