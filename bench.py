@@ -430,7 +430,26 @@ def oracle_baseline(name: str, budget_s: float = 10.0):
     return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"first {rows} of {w.N} rows of {name}, forward + backward, {reps} "
                       f"pass(es), fp64 single-threaded C, {secs:.2f} s",
-            "rows_per_s": round(reps * rows / secs, 1)}
+            "rows_per_s": round(reps * rows / secs, 1),
+            "host_cores": os.cpu_count(), "host_cpu": host_cpu()}
+
+
+def host_cpu() -> str:
+    """The host CPU as /proc/cpuinfo names it (model name, or the Arm implementer and
+    part numbers), else the machine type."""
+    import platform
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+    except OSError:
+        return platform.machine()
+    for key in ("model name", "Model name"):
+        for line in info.splitlines():
+            if line.startswith(key):
+                return line.split(":", 1)[1].strip()
+    parts = sorted({line.split(":", 1)[1].strip() for line in info.splitlines()
+                    if line.startswith(("CPU implementer", "CPU part"))})
+    return f"{platform.machine()} ({', '.join(parts)})" if parts else platform.machine()
 
 
 def run_reference(args):
@@ -641,7 +660,10 @@ def main(argv=None):
     def op_line(nbytes, times):
         ms = statistics.mean(times)
         gbs = nbytes / (ms * 1e-3) / 1e9
+        q = sorted(times)
         return {"us": round(1e3 * ms, 3), "us_median": round(1e3 * statistics.median(times), 3),
+                "us_p10": round(1e3 * q[len(q) // 10], 3),
+                "us_p90": round(1e3 * q[min(len(q) - 1, (9 * len(q)) // 10)], 3),
                 "gbs": round(gbs, 2), "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
                 "frac_of_measured": round(gbs / peak, 4), "rows_per_s": round(w.N / (ms * 1e-3), 1),
                 "compulsory_bytes": nbytes}

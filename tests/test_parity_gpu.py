@@ -263,3 +263,32 @@ def test_cached_plans_survive_alternating_widths(op):
             d[k].copy_(v.to(DEV))
         got = gpu_run(op, d, 1e-5)
         compare(op, got, oracle_run(op, t, 1e-5), t["X"], tag=f"{op} D={D} shift={shift}")
+
+
+def test_fused_backward_both_readings_of_s():
+    """The fused backward differentiates at the saved activation. This library's reading
+    (the primary parity check) takes the stored fp16 S; the other reading takes the exact
+    fp32 sum x + r. Both oracle variants are computed here: the GPU dX matches the stored-S
+    reading within the fp16 tolerance, and its distance from the exact-sum reading is
+    reported and bounded by the effect of S's rounding (half an fp16 ulp of S, carried
+    through dX's dependence on x)."""
+    N, D = 64, 4096
+    t = W.generate(W.ADD_RMSNORM, N, D, seed=9, dy_std=1.0)
+    got = gpu_run(W.ADD_RMSNORM, to_dev(t), 1e-6)
+    torch.cuda.synchronize()
+    X, R, gamma, dY, dS = (f64(t[k]) for k in ("X", "R", "gamma", "dY", "dS"))
+    _, S_exact, rstd = oracle.add_rmsnorm_forward(X, R, gamma, 1e-6)
+    S16 = oracle.round_fp16(S_exact).astype(np.float64)
+    dX_saved, _, _ = oracle.add_rmsnorm_backward(S16, gamma, dY, dS, rstd)
+    dX_exact, _, _ = oracle.add_rmsnorm_backward(S_exact, gamma, dY, dS, rstd)
+    g = f64(got["dX"])
+    err_saved = np.abs(g - dX_saved)
+    assert np.all(err_saved <= 2e-3 + 2e-3 * np.abs(dX_saved)), err_saved.max()
+    err_exact = np.abs(g - dX_exact)
+    gap = np.abs(dX_saved - dX_exact)
+    print(f"fused dX: max |gpu - stored-S reading| {err_saved.max():.3e}, "
+          f"max |gpu - exact-sum reading| {err_exact.max():.3e}, "
+          f"max |stored-S - exact-sum| {gap.max():.3e}")
+    # S's rounding moves x by at most 2^-11 |s|; dX depends on x through r^2 c / D terms
+    # and r * g * x_hat terms, so the readings differ by a small multiple of that
+    assert np.all(err_exact <= 2e-3 + 2e-3 * np.abs(dX_exact) + 4 * gap), err_exact.max()
