@@ -391,6 +391,74 @@ def e2e_run(name: str, device, steps: int, warmup: int, seed: int,
 
 # ------------------------------------------------------------ CPU oracle ---
 
+_SHARD = {}
+
+
+def _shard_init(name: str, rows: int, lo: int, hi: int):
+    """Worker start-up for the all-cores baseline: draw the workload's first `rows` rows
+    (the same draw as the single-core run) and keep this worker's rows lo..hi-1."""
+    sys.path.insert(0, ROOT)
+    import numpy as np  # noqa: F401
+    t = W.generate_workload(name, rows=rows)
+    _SHARD.update(name=name, a={k: (v.double().numpy()[lo:hi] if v.dim() == 2 else v.double().numpy())
+                               for k, v in t.items()})
+
+
+def _shard_run(_):
+    """One forward + backward of this worker's rows with the oracle; returns its dgamma
+    (and dbeta) partial sums for the fixed-order combine."""
+    import numpy as np
+    import oracle
+    w = W.WORKLOADS[_SHARD["name"]]
+    a = _SHARD["a"]
+    eps = float(np.float32(w.eps))
+    if w.op == W.RMSNORM:
+        _, rstd = oracle.rmsnorm_forward(a["X"], a["gamma"], eps)
+        return oracle.rmsnorm_backward(a["X"], a["gamma"], a["dY"], rstd)[1]
+    if w.op == W.LAYERNORM:
+        _, mean, rstd = oracle.layernorm_forward(a["X"], a["gamma"], a["beta"], eps)
+        r = oracle.layernorm_backward(a["X"], a["gamma"], a["dY"], mean, rstd)
+        return r[1], r[3]
+    _, s_, rstd = oracle.add_rmsnorm_forward(a["X"], a["R"], a["gamma"], eps)
+    s16 = oracle.round_fp16(s_).astype(np.float64)
+    return oracle.add_rmsnorm_backward(s16, a["gamma"], a["dY"], a["dS"], rstd)[1]
+
+
+def oracle_baseline_all_cores(name: str, rows: int, passes: int = 3):
+    """The same per-row oracle code on every host core: one spawned process per core, each
+    with a contiguous shard of the first `rows` rows; the shards' dgamma (dbeta) partials
+    are added in shard order. Reported beside the single-core baseline, not instead of it."""
+    import multiprocessing as mp
+    import numpy as np
+    cores = os.cpu_count() or 1
+    ctx = mp.get_context("spawn")  # never fork a process that holds a CUDA context
+    bounds = [(rows * i // cores, rows * (i + 1) // cores) for i in range(cores)]
+    pools = [ctx.Pool(1, initializer=_shard_init, initargs=(name, rows, lo, hi)) for lo, hi in bounds]
+    try:
+        for pl in pools:  # warm: library compiled and loaded, inputs drawn
+            pl.apply(_shard_run, (0,))
+        t0 = time.perf_counter()
+        for _ in range(passes):
+            parts = [pl.apply_async(_shard_run, (0,)) for pl in pools]
+            res = [r.get() for r in parts]
+            total = res[0]
+            for r_ in res[1:]:  # fixed shard order
+                total = tuple(x + y for x, y in zip(total, r_)) if isinstance(total, tuple) else total + r_
+        secs = time.perf_counter() - t0
+    finally:
+        for pl in pools:
+            pl.close()
+            pl.join()
+    w = W.WORKLOADS[name]
+    nbytes = passes * (W.compulsory_bytes(w.op, "forward", rows, w.D)
+                       + W.compulsory_bytes(w.op, "backward", rows, w.D))
+    return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": cores,
+            "kind": "oracle, row shards on every core",
+            "sample": f"first {rows} of {w.N} rows of {name}, forward + backward, {passes} "
+                      f"pass(es), {cores} processes, {secs:.2f} s",
+            "rows_per_s": round(passes * rows / secs, 1)}
+
+
 def oracle_step_seconds(name: str, rows: int, seed: int = 0):
     """Wall time of one oracle forward + backward over `rows` rows of the workload."""
     import numpy as np
@@ -735,9 +803,10 @@ def main(argv=None):
             e2e["ms_per_step"] = round(max_over_ranks(e2e["ms_per_step"], device), 4)
             e2e["value"] = round(world * step_bytes / (e2e["ms_per_step"] * 1e-3) / 1e9, 2)
 
-    cpu = None
+    cpu = cpu_all = None
     if rank == 0 and world >= 1 and not args.no_cpu_baseline and args.gpus == 1:
         cpu = oracle_baseline(args.workload)
+        cpu_all = oracle_baseline_all_cores(args.workload, W.WORKLOADS[args.workload].N)
 
     dom_line = ops[dom]
     traffic = recorded_traffic(args.workload, dom)
@@ -771,6 +840,7 @@ def main(argv=None):
                      "frac": dom_line["frac_of_measured"], "traffic": traffic,
                      "algorithmic_bytes_per_launch": dom_line["compulsory_bytes"]},
         "cpu_baseline": cpu,
+        "cpu_baseline_all_cores": cpu_all,
         "e2e": e2e,
         "gpu_launches": args.steps * 3,
         "clocks": clocks.summary(),
