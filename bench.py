@@ -424,7 +424,7 @@ def _shard_run(_):
     return oracle.add_rmsnorm_backward(s16, a["gamma"], a["dY"], a["dS"], rstd)[1]
 
 
-def oracle_baseline_all_cores(name: str, rows: int, passes: int = 3):
+def oracle_baseline_all_cores(name: str, rows: int, passes: int = 20):
     """The same per-row oracle code on every host core: one spawned process per core, each
     with a contiguous shard of the first `rows` rows; the shards' dgamma (dbeta) partials
     are added in shard order. Reported beside the single-core baseline, not instead of it."""
