@@ -574,6 +574,7 @@ def max_over_ranks(value: float, device=None) -> float:
 # Softmax / cross-entropy workloads: name -> (runner, N, D, storage type name).
 ROW_OPS = {
     "softmax_16384x4096_f16": ("softmax", 16384, 4096, "float16"),
+    "softmax_256x262144_f16": ("softmax", 256, 262144, "float16"),
     "cross_entropy_4096x32768_bf16": ("cross_entropy", 4096, 32768, "bfloat16"),
 }
 

@@ -84,8 +84,11 @@ typedef struct CUstream_st *mt_stream_t;
  * memory in a fixed order, so results stay bitwise reproducible. */
 #define MT_MAX_COLS 131072
 
-/* Widest row of the softmax / log-softmax (register-resident rows). */
-#define MT_MAX_SOFTMAX_COLS 16384
+/* Widest row of the softmax / log-softmax: [meTile] training_losses bounds last-axis
+ * softmax to 1..262144 columns. Rows up to 16384 columns stay in registers (one read,
+ * one write); wider rows run two passes over the row on one CTA (a running maximum and
+ * sum of exponentials, then the outputs; the second read mostly hits L2). */
+#define MT_MAX_SOFTMAX_COLS 262144
 
 /* ---------------------------------------------------------------- RMSNorm ---
  * [tc] "RMSnorm -- Llama-style", Math; [meTile] contract (zero-offset weight):

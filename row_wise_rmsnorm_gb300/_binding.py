@@ -28,7 +28,7 @@ MT_DTYPE_F16, MT_DTYPE_BF16, MT_DTYPE_F32 = 0, 1, 2
 MT_REDUCTION_NONE, MT_REDUCTION_SUM, MT_REDUCTION_MEAN = 0, 1, 2
 MT_MAX_CE_COLS = 262144
 MT_MAX_COLS = 131072
-MT_MAX_SOFTMAX_COLS = 16384
+MT_MAX_SOFTMAX_COLS = 262144
 MT_MAX_GEMV_ROWS = 8
 MT_MAX_GEMV_K = 32768
 

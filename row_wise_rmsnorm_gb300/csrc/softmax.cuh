@@ -290,7 +290,7 @@ __device__ __forceinline__ void ce_load(const void *X, int64_t off, int c0, int 
 
 // The 16-byte units of the UN chunks c0, c0 + TPR, ... of one row, as loaded; chunks
 // past the end read as -inf (they must not raise the running maximum).
-template <int TPR, int XT, int UN>
+template <int TPR, int XT, int UN, int H = kStream>
 __device__ __forceinline__ void ce_load_raw(const void *X, int64_t off, int c0, int D,
                                             uint4 (&raw)[UN][chunk_units<XT>()]) {
     constexpr uint32_t kNegInf = (XT == kF32) ? 0xff800000u : (XT == kBF16) ? 0xff80ff80u : 0xfc00fc00u;
@@ -299,7 +299,7 @@ __device__ __forceinline__ void ce_load_raw(const void *X, int64_t off, int c0, 
         const int c = c0 + u * TPR;
 #pragma unroll
         for (int q = 0; q < chunk_units<XT>(); ++q)
-            raw[u][q] = c * 8 < D ? ld_unit<kStream>(as<XT>(X) + off + c * 8 + q * (8 / chunk_units<XT>()))
+            raw[u][q] = c * 8 < D ? ld_unit<H>(as<XT>(X) + off + c * 8 + q * (8 / chunk_units<XT>()))
                                   : make_uint4(kNegInf, kNegInf, kNegInf, kNegInf);
     }
 }
@@ -521,6 +521,203 @@ ce_bwd_kernel(const CeArgs a) {
         for (int j = t; j < D; j += TPR) {
             const float v = ld_elem_stream(a.X, off + j, a.xdt);
             st_elem(a.dX, off + j, scale * __expf(v - l) - gq - (j == tg ? gt : 0.f), a.xdt);
+        }
+    }
+}
+
+// ------------------------------------------------ softmax of wide rows (streaming) ---
+// Rows wider than the register-resident softmax kernels hold (D > 16384; up to the
+// 262144 columns of the meTile training_losses bounds): one CTA of TPR threads per row,
+// two passes over the row, every combination in a fixed order.
+//  * Forward: pass 1 keeps the running (maximum, sum of exp) state of the cross-entropy
+//    forward (packed chunk maxima, one update per batch of UN chunks) and the CTA combines
+//    it into lse = m + log(s); pass 2 reads the row again (mostly from L2: pass 1 reads
+//    with the default cache policy) and writes y = exp(x - lse), or x - lse.
+//  * Backward: pass 1 reduces sum dY*Y (softmax) or sum dY (log-softmax); pass 2 writes
+//    dX = Y*(dY - sum) or dY - exp(Y)*sum.
+
+// Block-wide fixed-order combination of the (maximum, sum) states; every thread gets the
+// total (every warp combines the same operands in the same lanes).
+template <int TPR>
+__device__ __forceinline__ MaxSum block_maxsum(MaxSum st, float *sm_m, float *sm_s) {
+    constexpr int W = TPR / 32;
+    const int lane = threadIdx.x % 32, w = threadIdx.x / 32;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        MaxSum other{__shfl_xor_sync(0xffffffffu, st.m, o), __shfl_xor_sync(0xffffffffu, st.s, o)};
+        st = (lane & o) ? combine(other, st) : combine(st, other);
+    }
+    if (lane == 0) {
+        sm_m[w] = st.m;
+        sm_s[w] = st.s;
+    }
+    __syncthreads();
+    MaxSum tot{sm_m[lane & (W - 1)], sm_s[lane & (W - 1)]};  // W aligned groups, same operands
+#pragma unroll
+    for (int o = W / 2; o > 0; o >>= 1) {
+        MaxSum other{__shfl_xor_sync(0xffffffffu, tot.m, o), __shfl_xor_sync(0xffffffffu, tot.s, o)};
+        tot = (lane & o) ? combine(other, tot) : combine(tot, other);
+    }
+    return tot;
+}
+
+template <int TPR, bool VEC8, int XT, bool LOG, int UN>
+__global__ void __launch_bounds__(TPR)
+softmax_stream_fwd_kernel(const SoftmaxArgs a) {
+    pdl_enter();
+    constexpr int W = TPR / 32;
+    static_assert(W <= 32 && (W & (W - 1)) == 0, "warps per row: a power of two up to 32");
+    __shared__ float sm_m[W], sm_s[W];
+    const int t = threadIdx.x;
+    const int64_t row = blockIdx.x;
+    const int D = a.D;
+    const int64_t off = row * (int64_t)D;
+
+    MaxSum st{-INFINITY, 0.f};
+    if constexpr (VEC8) {
+        constexpr int CU = chunk_units<XT>();
+        const float2 l2e = make_float2(kLog2e, kLog2e);
+        uint4 raw[UN][CU];
+        ce_load_raw<TPR, XT, UN, kReadOnly>(a.X, off, t, D, raw);
+        for (int c0 = t;;) {
+            float bm = chunk_max<XT>(raw[0]);
+#pragma unroll
+            for (int u = 1; u < UN; ++u) bm = fmaxf(bm, chunk_max<XT>(raw[u]));
+            const float m = fmaxf(st.m, bm);
+            const float ms = (m == -INFINITY) ? 0.f : m;
+            const float nb = -ms * kLog2e;
+            const float2 nb2 = make_float2(nb, nb);
+            st.s *= ex2(fmaf(st.m, kLog2e, nb));
+            st.m = m;
+            float2 cs2 = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int u = 0; u < UN; ++u) {
+                if ((c0 + u * TPR) * 8 >= D) continue;
+                float2 f[4];
+                unpack_chunk<XT, 4>(raw[u], 1, f);
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    const float2 e = __ffma2_rn(f[p], l2e, nb2);
+                    cs2 = __fadd2_rn(cs2, make_float2(ex2(e.x), ex2(e.y)));
+                }
+            }
+            st.s += cs2.x + cs2.y;
+            c0 += UN * TPR;
+            if (c0 * 8 >= D) break;
+            ce_load_raw<TPR, XT, UN, kReadOnly>(a.X, off, c0, D, raw);
+        }
+    } else {
+        for (int j = t; j < D; j += TPR) add_value(st, ld_elem(a.X, off + j, a.xdt));
+    }
+    const MaxSum tot = block_maxsum<TPR>(st, sm_m, sm_s);
+    const float lse = tot.m + logf(tot.s);
+
+    if constexpr (VEC8) {
+        const float2 l2e = make_float2(kLog2e, kLog2e);
+        const float2 nl2 = make_float2(-lse * kLog2e, -lse * kLog2e);
+        const float2 nlse = make_float2(-lse, -lse);
+        for (int c0 = t; c0 * 8 < D; c0 += UN * TPR) {
+            float2 f[UN][4];
+#pragma unroll
+            for (int u = 0; u < UN; ++u) {
+                const int c = c0 + u * TPR;
+                ld_chunk<XT, kStream>(as<XT>(a.X) + off + c * 8, c * 8 < D, f[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < UN; ++u) {
+                const int c = c0 + u * TPR;
+                if (c * 8 >= D) continue;
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    if constexpr (LOG) {
+                        f[u][p] = __fadd2_rn(f[u][p], nlse);
+                    } else {
+                        const float2 e = __ffma2_rn(f[u][p], l2e, nl2);  // (x - lse) log2(e)
+                        f[u][p] = make_float2(ex2(e.x), ex2(e.y));
+                    }
+                }
+                st_chunk<XT>(as<XT>(a.Y) + off + c * 8, f[u]);
+            }
+        }
+    } else {
+        for (int j = t; j < D; j += TPR) {
+            const float v = ld_elem_stream(a.X, off + j, a.xdt);
+            st_elem(a.Y, off + j, LOG ? v - lse : __expf(v - lse), a.xdt);
+        }
+    }
+}
+
+template <int TPR, bool VEC8, int XT, bool LOG, int UN>
+__global__ void __launch_bounds__(TPR)
+softmax_stream_bwd_kernel(const SoftmaxArgs a) {
+    pdl_enter();
+    constexpr int WPR = TPR / 32;
+    __shared__ float red[2 * WPR];
+    const int t = threadIdx.x, lane = t % 32, w = t / 32;
+    const int64_t row = blockIdx.x;
+    const int D = a.D;
+    const int64_t off = row * (int64_t)D;
+
+    // pass 1: sum dY*Y (softmax) or sum dY (log-softmax)
+    float v[1] = {0.f};
+    if constexpr (VEC8) {
+        float2 acc = make_float2(0.f, 0.f);
+        for (int c0 = t; c0 * 8 < D; c0 += UN * TPR) {
+            float2 yv[UN][4], gv[UN][4];
+#pragma unroll
+            for (int u = 0; u < UN; ++u) {
+                const int c = c0 + u * TPR;
+                ld_chunk<XT, kReadOnly>(as<XT>(a.dY) + off + c * 8, c * 8 < D, gv[u]);
+                if constexpr (!LOG) ld_chunk<XT, kReadOnly>(as<XT>(a.X) + off + c * 8, c * 8 < D, yv[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < UN; ++u)
+#pragma unroll
+                for (int p = 0; p < 4; ++p)
+                    acc = LOG ? __fadd2_rn(acc, gv[u][p]) : __ffma2_rn(gv[u][p], yv[u][p], acc);
+        }
+        v[0] = acc.x + acc.y;
+    } else {
+        for (int j = t; j < D; j += TPR) {
+            const float g = ld_elem(a.dY, off + j, a.gdt);
+            v[0] += LOG ? g : g * ld_elem(a.X, off + j, a.xdt);
+        }
+    }
+    row_sum<TPR, 1, 1>(v, red, 0, 0, w, lane);
+    const float c = v[0];
+
+    // pass 2: dX
+    if constexpr (VEC8) {
+        const float2 nc = make_float2(-c, -c);
+        for (int c0 = t; c0 * 8 < D; c0 += UN * TPR) {
+            float2 yk[UN][4], gk[UN][4];
+#pragma unroll
+            for (int u = 0; u < UN; ++u) {
+                const int ch = c0 + u * TPR;
+                ld_chunk<XT, kStream>(as<XT>(a.X) + off + ch * 8, ch * 8 < D, yk[u]);
+                ld_chunk<XT, kStream>(as<XT>(a.dY) + off + ch * 8, ch * 8 < D, gk[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < UN; ++u) {
+                const int ch = c0 + u * TPR;
+                if (ch * 8 >= D) continue;
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    if constexpr (LOG) {
+                        const float2 e = make_float2(__expf(yk[u][p].x), __expf(yk[u][p].y));
+                        gk[u][p] = __ffma2_rn(e, nc, gk[u][p]);                    // dY - exp(Y) c
+                    } else {
+                        gk[u][p] = __fmul2_rn(yk[u][p], __fadd2_rn(gk[u][p], nc));  // Y (dY - c)
+                    }
+                }
+                st_chunk<XT>(as<XT>(a.Y) + off + ch * 8, gk[u]);
+            }
+        }
+    } else {
+        for (int j = t; j < D; j += TPR) {
+            const float y = ld_elem_stream(a.X, off + j, a.xdt);
+            const float g = ld_elem_stream(a.dY, off + j, a.gdt);
+            st_elem(a.Y, off + j, LOG ? g - __expf(y) * c : y * (g - c), a.xdt);
         }
     }
 }

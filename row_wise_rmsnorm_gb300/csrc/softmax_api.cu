@@ -22,6 +22,23 @@ namespace {
     X(4096, 128, 1, 4)            \
     X(16384, 512, 1, 4)
 #endif
+// Rows wider than 16384 (up to MT_MAX_SOFTMAX_COLS): the two-pass streaming kernels,
+// X(max_D, TPR, UN): one CTA of TPR threads per row, UN chunks (or elements) in flight
+// per thread and operand (the backward loads two operands). Measured on GB300 (fp16,
+// forward / backward): 1024 x 65536 at 512 threads 53.2 / 94.2 us, 256 threads 54.8 /
+// 94.4, 128 threads 60.4 / 105.8; 256 x 262144 at 1024 threads 61.0 / 97.2 us, 512
+// threads 63.0 / 105.7; 2048 x 32768 backward at 256 threads 73.3 us, 512 threads 74.1.
+#ifndef MT_SOFTMAX_SHAPES_STREAM_FWD
+#define MT_SOFTMAX_SHAPES_STREAM_FWD(X) \
+    X(65536, 512, 4)                    \
+    X(MT_MAX_SOFTMAX_COLS, 1024, 2)
+#endif
+#ifndef MT_SOFTMAX_SHAPES_STREAM_BWD
+#define MT_SOFTMAX_SHAPES_STREAM_BWD(X) \
+    X(32768, 256, 4)                    \
+    X(65536, 512, 2)                    \
+    X(MT_MAX_SOFTMAX_COLS, 1024, 2)
+#endif
 #define MT_SOFTMAX_SHAPES_SCALAR(X) \
     X(256, 32, 4, 8)                \
     X(1024, 32, 4, 32)              \
@@ -116,8 +133,36 @@ cudaError_t softmax_plan_scalar(int64_t N, int D, LaunchPlan *p) {
     return cudaErrorInvalidValue;
 }
 
+template <bool BWD, bool LOG, bool VEC8, int XT>
+cudaError_t softmax_plan_stream(int64_t N, int D, LaunchPlan *p) {
+#define MT_TRY(maxd, tpr, un)                                                                       \
+    if (D <= maxd) {                                                                                \
+        if constexpr (BWD)                                                                          \
+            p->kernel = reinterpret_cast<const void *>(&softmax_stream_bwd_kernel<tpr, VEC8, XT, LOG, un>); \
+        else                                                                                        \
+            p->kernel = reinterpret_cast<const void *>(&softmax_stream_fwd_kernel<tpr, VEC8, XT, LOG, un>); \
+        p->threads = tpr;                                                                           \
+        p->grid = (int)N;                                                                           \
+        p->rows_per_cta = 1;                                                                        \
+        return cudaSuccess;                                                                         \
+    }
+    if constexpr (BWD) {
+        MT_SOFTMAX_SHAPES_STREAM_BWD(MT_TRY)
+    } else {
+        MT_SOFTMAX_SHAPES_STREAM_FWD(MT_TRY)
+    }
+#undef MT_TRY
+    return cudaErrorInvalidValue;
+}
+
 template <bool BWD, bool LOG>
 cudaError_t softmax_plan(int64_t N, int D, bool vec8, int xdt, LaunchPlan *p) {
+    if (D > 16384) {
+        if (!vec8) return softmax_plan_stream<BWD, LOG, false, kF32>(N, D, p);  // types at run time
+        if (xdt == kF16) return softmax_plan_stream<BWD, LOG, true, kF16>(N, D, p);
+        if (xdt == kBF16) return softmax_plan_stream<BWD, LOG, true, kBF16>(N, D, p);
+        return softmax_plan_stream<BWD, LOG, true, kF32>(N, D, p);
+    }
     if (vec8) {
         if (xdt == kF16) return softmax_plan_vec<BWD, LOG, kF16>(N, D, p);
         if (xdt == kBF16) return softmax_plan_vec<BWD, LOG, kBF16>(N, D, p);

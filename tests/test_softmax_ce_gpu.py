@@ -5,7 +5,7 @@ loss checklists; "Metal subgroup LayerNorm and cross-entropy report", cross-entr
 Inputs are seeded and synthetic: softmax rows N(0, 3^2) (peaked rows), cotangents N(0, 1);
 logits N(0, 2^2) with uniform random targets and a few ignored rows. Shapes: the report's
 cross-entropy shapes (1x127, 17x257, 128x1024, 64x4096), ragged widths for the scalar
-paths, and vocabulary-wide rows up to the 262144-column bound.
+paths, and rows up to the 262144-column bound for both softmax and cross-entropy.
 
 Tolerances: softmax outputs and gradients use the storage type's output tolerance
 (parity.OUT_TOL); cross-entropy losses and lse (fp32, computed from the stored logits)
@@ -38,7 +38,11 @@ def _gen(shape, std, dtype, seed):
 
 # -------------------------------------------------------------------- softmax ---
 
-SM_SHAPES = [(1, 127), (17, 257), (96, 1024), (40, 4104), (9, 16384), (300, 64)]
+# up to 16384 columns the row stays in registers; wider rows (to the meTile bound of
+# 262144) take the two-pass streaming kernels: 256-thread rows up to 65536 columns,
+# 512-thread rows above, a ragged width on the scalar path
+SM_SHAPES = [(1, 127), (17, 257), (96, 1024), (40, 4104), (9, 16384), (300, 64),
+             (4, 16392), (6, 65536), (3, 65544), (5, 50001), (3, 131072), (2, 262144)]
 
 
 @pytest.mark.parametrize("log", [False, True], ids=["softmax", "log_softmax"])
@@ -61,8 +65,9 @@ def test_softmax_parity(dtype, shape, log):
         assert np.all(np.abs(s - 1.0) <= D * OUT_TOL[dtype][0] + 1e-6), "rows sum to one"
 
 
-def test_softmax_misaligned_and_deterministic():
-    N, D = 33, 1024
+@pytest.mark.parametrize("D", [1024, 40000], ids=["regs", "stream"])
+def test_softmax_misaligned_and_deterministic(D):
+    N = 33 if D <= 16384 else 3
     x = _gen((N, D), 3.0, F16, 4)
     buf = torch.empty(N * D + 1, dtype=F16, device="cuda")
     xs = buf[1:].view(N, D)
@@ -71,6 +76,15 @@ def test_softmax_misaligned_and_deterministic():
     b = mt.softmax_forward(x)
     check_out(a, oracle.softmax_forward(f64(x)), F16, "misaligned softmax")
     assert torch.equal(mt.softmax_forward(x), b), "softmax not deterministic"
+    dy = _gen((N, D), 1.0, F16, 5)
+    dys = torch.empty(N * D + 1, dtype=F16, device="cuda")[1:].view(N, D)
+    dys.copy_(dy)
+    ys = torch.empty(N * D + 1, dtype=F16, device="cuda")[1:].view(N, D)
+    ys.copy_(a)
+    g = mt.softmax_backward(ys, dys)
+    check_out(g, oracle.softmax_backward(f64(a), f64(dy)), F16, "misaligned softmax backward")
+    assert torch.equal(mt.softmax_backward(a, dy), mt.softmax_backward(a, dy)), \
+        "softmax backward not deterministic"
 
 
 # -------------------------------------------------------------- cross-entropy ---
