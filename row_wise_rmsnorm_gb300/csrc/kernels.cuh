@@ -19,14 +19,18 @@
 //    fp32 registers across its rows; at the end the CTA's row groups are combined in
 //    a fixed order and one fp32 partial row per CTA is written. A second small
 //    kernel sums the partials column by column in ascending CTA order. No atomics.
-//  * Rows wider than one CTA's slice run on a thread-block cluster (see "cluster
-//    split" below): the same per-thread layout inside each CTA's column window, plus
-//    one exchange of the CTAs' row sums through distributed shared memory.
+//  * Rows wider than 16384 columns: the aligned forward streams the row twice on one
+//    CTA (norm_fwd_stream_kernel; the second read mostly hits L2); the backward and
+//    the scalar forward run on a thread-block cluster (see "cluster split" below): the
+//    same per-thread layout inside each CTA's column window, plus one exchange of the
+//    CTAs' row sums through distributed shared memory.
 //
 // Formulas (page title, section): meTile "Kernel coverage and training scope",
 // "Exact native normalization contract"; tensorcore "Training kernels",
 // "RMSnorm -- Llama-style" and "LayerNorm -- standard".
 #pragma once
+
+#include <type_traits>
 
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -347,31 +351,28 @@ norm_fwd_kernel(const FwdArgs a) {
 // registers (as fp32 pairs) through the reductions and the apply. Activations are of
 // type XT, gamma/beta of type WT. MINB is the minimum number of resident CTAs per SM
 // asked of the compiler (it bounds the registers per thread; 0: the compiler's choice).
-template <int OP, int TPR, int RPC, int CH, int MINB, int XT, int WT, bool CLU = false>
+template <int OP, int TPR, int RPC, int CH, int MINB, int XT, int WT>
 __global__ void __launch_bounds__(TPR * RPC, MINB)
 norm_fwd_vec8_kernel(const FwdArgs a) {
     pdl_enter();
     static_assert(TPR % 32 == 0 && TPR * RPC <= 1024, "bad launch shape");
-    static_assert(!CLU || RPC == 1, "a split row is one row group per CTA");
     constexpr int WPR = TPR / 32;
     __shared__ float red[2 * RPC * WPR];
-    __shared__ float xch[CLU ? 4 : 1];  // cluster_sum (2) or cluster_ln_stats (4)
 
     const int tid = threadIdx.x;
     const int rg = tid / TPR, t = tid % TPR, wir = t / 32, lane = tid % 32;
     const int D = a.D;
     const float inv_d = 1.0f / (float)D;
-    const Window<CLU> win(D, a.slice);
-    const int64_t row = CLU ? win.owner() : (int64_t)blockIdx.x * RPC + rg;
-    const bool ok = row < a.N;  // split rows: the grid is N clusters, so always true
+    const int64_t row = (int64_t)blockIdx.x * RPC + rg;
+    const bool ok = row < a.N;
     if (WPR == 1 && !ok) return;  // no CTA barrier in a single-warp row group
     const int64_t off = (ok ? row : 0) * (int64_t)D;
 
     float2 x[CH][4];
 #pragma unroll
     for (int k = 0; k < CH; ++k) {
-        const int col = win.beg + (k * TPR + t) * 8;
-        const bool v = ok && col < win.end;
+        const int col = (k * TPR + t) * 8;
+        const bool v = ok && col < D;
         ld_chunk<XT, kStream>(as<XT>(a.X) + off + col, v, x[k]);
         if constexpr (OP == kAddRms) {
             float2 r[4];
@@ -382,7 +383,6 @@ norm_fwd_vec8_kernel(const FwdArgs a) {
         }
     }
     // LayerNorm: the mean, then the centred second moment (two passes, from registers).
-    // A split row centres on its slice's own mean and combines the slices afterwards.
     float mu = 0.f, s[1] = {0.f};
     if constexpr (OP == kLayer) {
         float2 s2 = make_float2(0.f, 0.f);
@@ -392,13 +392,13 @@ norm_fwd_vec8_kernel(const FwdArgs a) {
             for (int p = 0; p < 4; ++p) s2 = __fadd2_rn(s2, x[k][p]);
         s[0] = s2.x + s2.y;
         row_sum<TPR, RPC, 1>(s, red, 0, rg, wir, lane);
-        mu = CLU ? s[0] / (float)max(win.end - win.beg, 1) : s[0] * inv_d;
+        mu = s[0] * inv_d;
     }
     float2 nmu = make_float2(-mu, -mu);
     float2 q2 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int k = 0; k < CH; ++k) {
-        if (!(ok && win.beg + (k * TPR + t) * 8 < win.end)) continue;
+        if (!(ok && (k * TPR + t) * 8 < D)) continue;
 #pragma unroll
         for (int p = 0; p < 4; ++p) {
             const float2 d = (OP == kLayer) ? __fadd2_rn(x[k][p], nmu) : x[k][p];
@@ -407,29 +407,17 @@ norm_fwd_vec8_kernel(const FwdArgs a) {
     }
     float q[1] = {q2.x + q2.y};
     row_sum<TPR, RPC, 1>(q, red, 1, rg, wir, lane);
-    if constexpr (CLU) {
-        if constexpr (OP == kLayer) {
-            float v[2] = {s[0], q[0]};
-            cluster_ln_stats(v, xch, 0, win.cn, D, a.slice);
-            mu = v[0];
-            q[0] = v[1];
-            nmu = make_float2(-mu, -mu);
-        } else {
-            cluster_sum<1>(q, xch, 0, win.cn);
-        }
-        cluster_arrive();  // done reading the other CTAs' slots (waited for before exit)
-    }
     const float rs = rsqrtf(q[0] * inv_d + a.eps);
     if (!ok) return;  // after the last barrier
-    if (t == 0 && win.beg == 0) {
+    if (t == 0) {
         a.rstd[row] = rs;
         if constexpr (OP == kLayer) a.mean[row] = mu;
     }
     const float2 rs2 = make_float2(rs, rs);
 #pragma unroll
     for (int k = 0; k < CH; ++k) {
-        const int col = win.beg + (k * TPR + t) * 8;
-        if (col >= win.end) continue;
+        const int col = (k * TPR + t) * 8;
+        if (col >= D) continue;
         float2 g[4], y[4];
         ld_param<WT>(as<WT>(a.gamma) + col, g);
         if constexpr (OP == kLayer) {
@@ -444,7 +432,6 @@ norm_fwd_vec8_kernel(const FwdArgs a) {
         }
         st_chunk<XT>(as<XT>(a.Y) + off + col, y);
     }
-    if constexpr (CLU) cluster_wait();  // no CTA leaves while another may read its slots
 }
 
 // The same forward for RMSNorm and LayerNorm with 2-byte activations (XT = fp16 or
@@ -452,34 +439,31 @@ norm_fwd_vec8_kernel(const FwdArgs a) {
 // half the registers of norm_fwd_vec8_kernel, so more CTAs (and more bytes in flight)
 // fit per SM, for one more conversion per pass. (The fused op normalises the unrounded
 // fp32 x + r, so it cannot keep 2-byte chunks.)
-template <int OP, int TPR, int RPC, int CH, int MINB, int XT, int WT, bool CLU = false>
+template <int OP, int TPR, int RPC, int CH, int MINB, int XT, int WT>
 __global__ void __launch_bounds__(TPR * RPC, MINB)
 norm_fwd_packed_kernel(const FwdArgs a) {
     pdl_enter();
     static_assert(TPR % 32 == 0 && TPR * RPC <= 1024, "bad launch shape");
     static_assert(OP == kRms || OP == kLayer, "the fused op keeps its fp32 sum");
     static_assert(XT == kF16 || XT == kBF16, "2-byte activations only");
-    static_assert(!CLU || RPC == 1, "a split row is one row group per CTA");
     constexpr int WPR = TPR / 32;
     __shared__ float red[2 * RPC * WPR];
-    __shared__ float xch[CLU ? 4 : 1];  // cluster_sum (2) or cluster_ln_stats (4)
     const auto *X = as<XT>(a.X);
 
     const int tid = threadIdx.x;
     const int rg = tid / TPR, t = tid % TPR, wir = t / 32, lane = tid % 32;
     const int D = a.D;
     const float inv_d = 1.0f / (float)D;
-    const Window<CLU> win(D, a.slice);
-    const int64_t row = CLU ? win.owner() : (int64_t)blockIdx.x * RPC + rg;
-    const bool ok = row < a.N;  // split rows: the grid is N clusters, so always true
+    const int64_t row = (int64_t)blockIdx.x * RPC + rg;
+    const bool ok = row < a.N;
     if (WPR == 1 && !ok) return;  // no CTA barrier in a single-warp row group
     const int64_t off = (ok ? row : 0) * (int64_t)D;
 
     uint4 raw[CH];
 #pragma unroll
     for (int k = 0; k < CH; ++k) {
-        const int col = win.beg + (k * TPR + t) * 8;
-        raw[k] = (ok && col < win.end) ? ld_unit<kStream>(X + off + col) : make_uint4(0, 0, 0, 0);
+        const int col = (k * TPR + t) * 8;
+        raw[k] = (ok && col < D) ? ld_unit<kStream>(X + off + col) : make_uint4(0, 0, 0, 0);
     }
     // Chunk k as fp32 pairs. Each pass widens the chunks again rather than keep fp32
     // copies of the row alive across the reductions. So that the compiler does not merge
@@ -493,7 +477,7 @@ norm_fwd_packed_kernel(const FwdArgs a) {
         unpack_unit<XT>(make_uint4(raw[k].x ^ key, raw[k].y ^ key, raw[k].z ^ key, raw[k].w ^ key), f);
     };
 
-    // LayerNorm: as in norm_fwd_vec8_kernel (a split row centres on its slice mean first)
+    // LayerNorm: as in norm_fwd_vec8_kernel
     float mu = 0.f, s[1] = {0.f};
     if constexpr (OP == kLayer) {
         float2 s2 = make_float2(0.f, 0.f);
@@ -506,13 +490,13 @@ norm_fwd_packed_kernel(const FwdArgs a) {
         }
         s[0] = s2.x + s2.y;
         row_sum<TPR, RPC, 1>(s, red, 0, rg, wir, lane);
-        mu = CLU ? s[0] / (float)max(win.end - win.beg, 1) : s[0] * inv_d;
+        mu = s[0] * inv_d;
     }
     float2 nmu = make_float2(-mu, -mu);
     float2 q2 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int k = 0; k < CH; ++k) {
-        if (!(ok && win.beg + (k * TPR + t) * 8 < win.end)) continue;
+        if (!(ok && (k * TPR + t) * 8 < D)) continue;
         float2 f[4];
         if constexpr (OP == kLayer) pairs(k, f, mu);
         else unpack_unit<XT>(raw[k], f);
@@ -524,21 +508,9 @@ norm_fwd_packed_kernel(const FwdArgs a) {
     }
     float q[1] = {q2.x + q2.y};
     row_sum<TPR, RPC, 1>(q, red, 1, rg, wir, lane);
-    if constexpr (CLU) {
-        if constexpr (OP == kLayer) {
-            float v[2] = {s[0], q[0]};
-            cluster_ln_stats(v, xch, 0, win.cn, D, a.slice);
-            mu = v[0];
-            q[0] = v[1];
-            nmu = make_float2(-mu, -mu);
-        } else {
-            cluster_sum<1>(q, xch, 0, win.cn);
-        }
-        cluster_arrive();  // done reading the other CTAs' slots (waited for before exit)
-    }
     const float rs = rsqrtf(q[0] * inv_d + a.eps);
     if (!ok) return;  // after the last barrier
-    if (t == 0 && win.beg == 0) {
+    if (t == 0) {
         a.rstd[row] = rs;
         if constexpr (OP == kLayer) a.mean[row] = mu;
     }
@@ -551,8 +523,8 @@ norm_fwd_packed_kernel(const FwdArgs a) {
     uint32_t chain = zero & __float_as_uint(rs);
 #pragma unroll
     for (int k = 0; k < CH; ++k) {
-        const int col = win.beg + (k * TPR + t) * 8;
-        if (col >= win.end) continue;
+        const int col = (k * TPR + t) * 8;
+        if (col >= D) continue;
         float2 f[4], g[4], y[4];
         pairs(k, f, rs);
         const int pc = col + (int)chain;
@@ -570,7 +542,131 @@ norm_fwd_packed_kernel(const FwdArgs a) {
         chain = zero & __float_as_uint(y[0].x);
         st_chunk<XT>(as<XT>(a.Y) + off + col, y);
     }
-    if constexpr (CLU) cluster_wait();  // no CTA leaves while another may read its slots
+}
+
+// --------------------------------------------------- wide rows, streamed ---
+// Forward for aligned rows wider than a CTA holds in registers (D > 16384): one CTA of
+// TPR threads per row, two passes over the row; chunk c (8 elements) belongs to thread
+// c % TPR, UN chunks in flight per thread and operand. Pass 1 reads the row with the
+// default cache policy (so pass 2 mostly finds it in L2; the fused op also writes S) and
+// reduces it: RMSNorm and the fused op the sum of squares; LayerNorm, per thread, the
+// count, sum and centred sum of squares of its elements, one batch of UN chunks at a time
+// (each batch centred on its own mean, then merged by the update of Chan, Golub and
+// LeVeque), and the row's centred sum of squares as sum_t (m2_t + n_t (s_t / n_t - mu)^2),
+// as stable as the two-pass form. Pass 2 reads the row again (the fused op re-adds x + r,
+// the same fp32 value as pass 1) and applies.
+template <int OP, int TPR, int UN, int XT, int WT>
+__global__ void __launch_bounds__(TPR)
+norm_fwd_stream_kernel(const FwdArgs a) {
+    pdl_enter();
+    static_assert(TPR % 32 == 0 && TPR <= 1024, "bad launch shape");
+    constexpr int WPR = TPR / 32;
+    __shared__ float red[2 * WPR];
+    const int t = threadIdx.x, wir = t / 32, lane = t % 32;
+    const int D = a.D;
+    const float inv_d = 1.0f / (float)D;
+    const int64_t row = blockIdx.x;
+    const int64_t off = row * (int64_t)D;
+
+    auto load = [&](int c0, float2 (&x)[UN][4], auto hint, bool keep_s) {
+        constexpr int H = decltype(hint)::value;
+#pragma unroll
+        for (int u = 0; u < UN; ++u) {
+            const int c = c0 + u * TPR;
+            const bool v = c * 8 < D;
+            ld_chunk<XT, H>(as<XT>(a.X) + off + c * 8, v, x[u]);
+            if constexpr (OP == kAddRms) {
+                float2 r[4];
+                ld_chunk<XT, H>(as<XT>(a.R) + off + c * 8, v, r);
+#pragma unroll
+                for (int p = 0; p < 4; ++p) x[u][p] = __fadd2_rn(x[u][p], r[p]);
+                if (keep_s && v) st_chunk<XT>(as<XT>(a.S) + off + c * 8, x[u]);
+            }
+        }
+    };
+
+    float n = 0.f, s = 0.f, m2 = 0.f;   // LayerNorm: this thread's count, sum, centred sum of squares
+    float2 q2 = make_float2(0.f, 0.f);  // RMSNorm, fused op: the sum of squares (chunks past D are 0)
+    for (int c0 = t; c0 * 8 < D; c0 += UN * TPR) {
+        float2 x[UN][4];
+        load(c0, x, std::integral_constant<int, kReadOnly>{}, true);
+        if constexpr (OP == kLayer) {
+            float2 b2 = make_float2(0.f, 0.f);
+            int nv = 0;
+#pragma unroll
+            for (int u = 0; u < UN; ++u) {
+                nv += ((c0 + u * TPR) * 8 < D) ? 8 : 0;
+#pragma unroll
+                for (int p = 0; p < 4; ++p) b2 = __fadd2_rn(b2, x[u][p]);
+            }
+            const float nb = (float)nv, bs = b2.x + b2.y, bm = bs / nb;  // nv >= 8: chunk c0 is in the row
+            const float2 nbm = make_float2(-bm, -bm);
+            float2 d2 = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int u = 0; u < UN; ++u) {
+                if ((c0 + u * TPR) * 8 >= D) continue;
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    const float2 d = __fadd2_rn(x[u][p], nbm);
+                    d2 = __ffma2_rn(d, d, d2);
+                }
+            }
+            const float bm2 = d2.x + d2.y;
+            if (n == 0.f) {
+                m2 = bm2;
+            } else {
+                const float dl = bm - s / n;
+                m2 += bm2 + dl * dl * (n * nb / (n + nb));
+            }
+            s += bs;
+            n += nb;
+        } else {
+#pragma unroll
+            for (int u = 0; u < UN; ++u)
+#pragma unroll
+                for (int p = 0; p < 4; ++p) q2 = __ffma2_rn(x[u][p], x[u][p], q2);
+        }
+    }
+    float mu = 0.f, q[1];
+    if constexpr (OP == kLayer) {
+        float v[1] = {s};
+        row_sum<TPR, 1, 1>(v, red, 0, 0, wir, lane);
+        mu = v[0] * inv_d;
+        const float dev = n > 0.f ? s / n - mu : 0.f;
+        q[0] = m2 + n * dev * dev;
+    } else {
+        q[0] = q2.x + q2.y;
+    }
+    row_sum<TPR, 1, 1>(q, red, 1, 0, wir, lane);
+    const float rs = rsqrtf(q[0] * inv_d + a.eps);
+    if (t == 0) {
+        a.rstd[row] = rs;
+        if constexpr (OP == kLayer) a.mean[row] = mu;
+    }
+
+    const float2 rs2 = make_float2(rs, rs), nmu = make_float2(-mu, -mu);
+    for (int c0 = t; c0 * 8 < D; c0 += UN * TPR) {
+        float2 x[UN][4];
+        load(c0, x, std::integral_constant<int, kStream>{}, false);
+#pragma unroll
+        for (int u = 0; u < UN; ++u) {
+            const int col = (c0 + u * TPR) * 8;
+            if (col >= D) continue;
+            float2 g[4], y[4];
+            ld_param<WT>(as<WT>(a.gamma) + col, g);
+            if constexpr (OP == kLayer) {
+                float2 b[4];
+                ld_param<WT>(as<WT>(a.beta) + col, b);
+#pragma unroll
+                for (int p = 0; p < 4; ++p)
+                    y[p] = __ffma2_rn(__fmul2_rn(__fadd2_rn(x[u][p], nmu), rs2), g[p], b[p]);
+            } else {
+#pragma unroll
+                for (int p = 0; p < 4; ++p) y[p] = __fmul2_rn(__fmul2_rn(x[u][p], rs2), g[p]);
+            }
+            st_chunk<XT>(as<XT>(a.Y) + off + col, y);
+        }
+    }
 }
 
 // ----------------------------------------------------------------- backward ---

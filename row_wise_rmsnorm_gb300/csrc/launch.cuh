@@ -7,7 +7,8 @@
 // list. The first shape whose width covers D is taken. Forward rows up to 1024 wide get
 // one warp each (four rows per CTA, two for the fused op at 1024); wider rows get a row
 // group of 64-512 threads, one row per CTA (on GB300 this beat a persistent pipelined
-// forward at every width measured). The aligned backward is persistent and pipelined
+// forward at every width measured); aligned rows wider than 16384 are streamed twice
+// by one CTA each. The aligned backward is persistent and pipelined
 // (pipe.cuh), with few CTAs so that the dgamma/dbeta partials stay small.
 //
 // Storage types: activations XT, parameters WT, cotangents GT (dtype.cuh). The full
@@ -22,6 +23,7 @@
 #include <algorithm>
 
 #include "kernels.cuh"
+#include "mt_norm.h"
 #include "pipe.cuh"
 
 namespace mt {
@@ -153,17 +155,26 @@ namespace mt {
     X(4096, 512, 1, 1, 4, 2)              \
     X(16384, 512, 1, 4, 3, 1)
 
-// Rows wider than 16384 columns: a cluster of CL = 2, 4 or 8 CTAs per row, each CTA a
+// Aligned rows wider than 16384 columns, forward: the two-pass streaming kernel, one CTA
+// per row, X(max_D, TPR, UN). Each entry gives whole batches of UN chunks per thread at
+// the width it was measured on (24576: 12 chunks per thread; 32768 and 65536: 8 and 16).
+// Measured on GB300 against the cluster split the backward keeps (fp16 forward): RMSNorm
+// 4096 x 32768 108.0 -> 90.1 us, LayerNorm 1024 x 131072 189.1 -> 137.6 us, fused op
+// 2048 x 65536 239.8 -> 199.7 us, LayerNorm 4096 x 24576 139.9 -> 77.5 us (256 threads;
+// 89.9 us at 512).
+#ifndef MT_FWD_STREAM_SHAPES
+#define MT_FWD_STREAM_SHAPES(X) \
+    X(24576, 256, 4)            \
+    X(65536, 512, 4)            \
+    X(MT_MAX_COLS, 1024, 2)
+#endif
+
+// Rows wider than 16384 columns that are not streamed (the backward; forwards of rows that
+// are misaligned or not a multiple of 8 wide): a cluster of CL = 2, 4 or 8 CTAs per row, each CTA a
 // slice of ceil(D / CL) columns (rounded up to 8). The shapes below, X(max slice, TPR,
 // RPC, CH, ...), are tried in order; the first whose slice needs at most kMaxCluster CTAs
 // is taken (CL the smallest power of two that covers D with it).
 constexpr int kMaxCluster = 8;
-#ifndef MT_FWD_WIDE_RMS
-#define MT_FWD_WIDE_RMS(X) X(16384, 512, 1, 4, true, 3)
-#endif
-#ifndef MT_FWD_WIDE_VEC8
-#define MT_FWD_WIDE_VEC8(X) X(16384, 512, 1, 4, false, 2)
-#endif
 #define MT_FWD_WIDE_SCALAR(X) X(16384, 1024, 1, 16)
 #ifndef MT_BWD_WIDE_PIPE
 #define MT_BWD_WIDE_PIPE(X) X(16384, 512, 1, 4, 3, 1)
@@ -290,23 +301,30 @@ cudaError_t fwd_plan_scalar(int64_t N, int D, LaunchPlan *p) {
 }
 
 // The register floors (MINB) were set for 2-byte types; with fp32 activations or
-// parameters the compiler chooses (MINB 0), since the floors would force spills there,
-// except that a split row's kernel asks for one resident CTA (MINB 1), without which
-// the compiler held the fp32 LayerNorm slice to 64 registers and spilled.
-template <int OP, int XT, int WT, int TPR, int RPC, int CH, bool PACK, int MINB, bool CLU = false>
+// parameters the compiler chooses (MINB 0), since the floors would force spills there.
+template <int OP, int XT, int WT, int TPR, int RPC, int CH, bool PACK, int MINB>
 cudaError_t fwd_vec_shape(int64_t N, LaunchPlan *p) {
-    constexpr int minb = (XT == kF32 || WT == kF32) ? (CLU ? 1 : 0) : MINB;
+    constexpr int minb = (XT == kF32 || WT == kF32) ? 0 : MINB;
     if constexpr (PACK && OP != kAddRms && XT != kF32)
         p->kernel = reinterpret_cast<const void *>(
-            &norm_fwd_packed_kernel<OP, TPR, RPC, CH, minb, XT, WT, CLU>);
+            &norm_fwd_packed_kernel<OP, TPR, RPC, CH, minb, XT, WT>);
     else
         p->kernel = reinterpret_cast<const void *>(
-            &norm_fwd_vec8_kernel<OP, TPR, RPC, CH, minb, XT, WT, CLU>);
+            &norm_fwd_vec8_kernel<OP, TPR, RPC, CH, minb, XT, WT>);
     p->threads = TPR * RPC;
     p->smem = 0;
     p->rows_per_cta = RPC;
-    if constexpr (CLU) return cluster_row_grid(p, N);
     p->grid = (int)((N + RPC - 1) / RPC);
+    return cudaSuccess;
+}
+
+template <int OP, int XT, int WT, int TPR, int UN>
+cudaError_t fwd_stream_shape(int64_t N, LaunchPlan *p) {
+    p->kernel = reinterpret_cast<const void *>(&norm_fwd_stream_kernel<OP, TPR, UN, XT, WT>);
+    p->threads = TPR;
+    p->smem = 0;
+    p->rows_per_cta = 1;
+    p->grid = (int)N;
     return cudaSuccess;
 }
 
@@ -325,15 +343,10 @@ cudaError_t fwd_plan_vec(int64_t N, int D, LaunchPlan *p) {
         MT_FWD_SHAPES_FUSED(MT_TRY)
     }
 #undef MT_TRY
-    // wider rows: split across a cluster
-#define MT_TRY(cap, tpr, rpc, ch, pack, minb)        \
-    if (wide_split(D, cap, &p->cluster, &p->slice)) \
-        return fwd_vec_shape<OP, XT, WT, tpr, rpc, ch, pack, minb, true>(N, p);
-    if constexpr (OP == kRms && !SHORT) {
-        MT_FWD_WIDE_RMS(MT_TRY)
-    } else {
-        MT_FWD_WIDE_VEC8(MT_TRY)
-    }
+    // wider rows: streamed, one CTA per row
+#define MT_TRY(maxd, tpr, un) \
+    if (D <= maxd) return fwd_stream_shape<OP, XT, WT, tpr, un>(N, p);
+    MT_FWD_STREAM_SHAPES(MT_TRY)
 #undef MT_TRY
     return kNoVectorPlan;
 }
