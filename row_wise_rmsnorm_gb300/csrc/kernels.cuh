@@ -545,6 +545,10 @@ norm_fwd_packed_kernel(const FwdArgs a) {
 }
 
 // --------------------------------------------------- wide rows, streamed ---
+// Chunks in flight per thread for the streaming kernels: a table's UN counts 16-byte
+// chunks of a 2-byte type; fp32 chunks are 32 bytes, so fp32 rows take half as many.
+__host__ __device__ constexpr int stream_un(int xt, int un) { return xt == kF32 ? (un + 1) / 2 : un; }
+
 // Forward for aligned rows wider than a CTA holds in registers (D > 16384): one CTA of
 // TPR threads per row, two passes over the row; chunk c (8 elements) belongs to thread
 // c % TPR, UN chunks in flight per thread and operand. Pass 1 reads the row with the
@@ -554,9 +558,10 @@ norm_fwd_packed_kernel(const FwdArgs a) {
 // (each batch centred on its own mean, then merged by the update of Chan, Golub and
 // LeVeque), and the row's centred sum of squares as sum_t (m2_t + n_t (s_t / n_t - mu)^2),
 // as stable as the two-pass form. Pass 2 reads the row again (the fused op re-adds x + r,
-// the same fp32 value as pass 1) and applies.
-template <int OP, int TPR, int UN, int XT, int WT>
-__global__ void __launch_bounds__(TPR)
+// the same fp32 value as pass 1) and applies. MINB: resident CTAs per SM asked of the
+// compiler (a register cap).
+template <int OP, int TPR, int UN, int MINB, int XT, int WT>
+__global__ void __launch_bounds__(TPR, MINB)
 norm_fwd_stream_kernel(const FwdArgs a) {
     pdl_enter();
     static_assert(TPR % 32 == 0 && TPR <= 1024, "bad launch shape");

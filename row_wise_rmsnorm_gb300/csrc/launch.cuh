@@ -61,9 +61,10 @@ namespace mt {
     X(1024, 64, 2, 2, false, 16)       \
     X(2048, 128, 1, 2, false, 12)      \
     X(4096, 512, 1, 1, false, 4)       \
-    X(8192, 512, 1, 2, false, 3)       \
-    X(16384, 512, 1, 4, false, 0)
+    X(8192, 512, 1, 2, false, 3)
 #endif
+// (The fused op's 16384-wide rows take the streaming kernel below: 4096 x 16384 in 83.1
+// us against 96.2 us for the register-resident row, which holds the fp32 sum x + r.)
 // Short forward table (fp32 parameters with 2-byte activations), every op.
 #define MT_FWD_SHAPES_SHORT(X)         \
     X(1024, 32, 4, 4, false, 0)        \
@@ -155,18 +156,25 @@ namespace mt {
     X(4096, 512, 1, 1, 4, 2)              \
     X(16384, 512, 1, 4, 3, 1)
 
-// Aligned rows wider than 16384 columns, forward: the two-pass streaming kernel, one CTA
-// per row, X(max_D, TPR, UN). Each entry gives whole batches of UN chunks per thread at
-// the width it was measured on (24576: 12 chunks per thread; 32768 and 65536: 8 and 16).
+// Aligned rows wider than the tables above cover, forward (every op past 16384 columns, the
+// fused op past 8192): the two-pass streaming kernel, one CTA per row, X(max_D, TPR, UN,
+// MINB), MINB the resident-CTA floor per SM the kernel is compiled for (1: none); fp32
+// rows take half as many chunks in flight (stream_un: the same bytes).
+// Each entry gives whole batches of UN chunks per thread at the width it was measured on
+// (16384: 4 chunks per thread; 24576: 12; 32768 and 65536: 8 and 16). At 16384 columns
+// the register-resident RMSNorm and LayerNorm rows stay faster (RMSNorm 8192 x 16384
+// 81.2 us against 84.2 streamed, LayerNorm 2048 x 16384 29.6 against 35.1).
 // Measured on GB300 against the cluster split the backward keeps (fp16 forward): RMSNorm
 // 4096 x 32768 108.0 -> 90.1 us, LayerNorm 1024 x 131072 189.1 -> 137.6 us, fused op
 // 2048 x 65536 239.8 -> 199.7 us, LayerNorm 4096 x 24576 139.9 -> 77.5 us (256 threads;
-// 89.9 us at 512).
+// 89.9 us at 512); 1024 x 131072 at 1024 threads with 4 chunks 124.4 us, 2 chunks 135.6.
+// Floors of 2 or 4 resident CTAs per SM did not help.
 #ifndef MT_FWD_STREAM_SHAPES
 #define MT_FWD_STREAM_SHAPES(X) \
-    X(24576, 256, 4)            \
-    X(65536, 512, 4)            \
-    X(MT_MAX_COLS, 1024, 2)
+    X(16384, 512, 2, 1)         \
+    X(24576, 256, 4, 1)         \
+    X(65536, 512, 4, 1)         \
+    X(MT_MAX_COLS, 1024, 4, 1)
 #endif
 
 // Rows wider than 16384 columns that are not streamed (the backward; forwards of rows that
@@ -318,9 +326,10 @@ cudaError_t fwd_vec_shape(int64_t N, LaunchPlan *p) {
     return cudaSuccess;
 }
 
-template <int OP, int XT, int WT, int TPR, int UN>
+template <int OP, int XT, int WT, int TPR, int UN, int MINB>
 cudaError_t fwd_stream_shape(int64_t N, LaunchPlan *p) {
-    p->kernel = reinterpret_cast<const void *>(&norm_fwd_stream_kernel<OP, TPR, UN, XT, WT>);
+    p->kernel = reinterpret_cast<const void *>(
+        &norm_fwd_stream_kernel<OP, TPR, stream_un(XT, UN), MINB, XT, WT>);
     p->threads = TPR;
     p->smem = 0;
     p->rows_per_cta = 1;
@@ -344,8 +353,8 @@ cudaError_t fwd_plan_vec(int64_t N, int D, LaunchPlan *p) {
     }
 #undef MT_TRY
     // wider rows: streamed, one CTA per row
-#define MT_TRY(maxd, tpr, un) \
-    if (D <= maxd) return fwd_stream_shape<OP, XT, WT, tpr, un>(N, p);
+#define MT_TRY(maxd, tpr, un, minb) \
+    if (D <= maxd) return fwd_stream_shape<OP, XT, WT, tpr, un, minb>(N, p);
     MT_FWD_STREAM_SHAPES(MT_TRY)
 #undef MT_TRY
     return kNoVectorPlan;

@@ -536,6 +536,16 @@ ce_bwd_kernel(const CeArgs a) {
 //  * Backward: pass 1 reduces sum dY*Y (softmax) or sum dY (log-softmax); pass 2 writes
 //    dX = Y*(dY - sum) or dY - exp(Y)*sum.
 
+// The 16-byte units of chunk c of the row at `off`, as loaded (zeros past the end).
+template <int XT, int H>
+__device__ __forceinline__ void ld_raw_chunk(const void *base, int64_t off, int c, int D,
+                                             uint4 (&r)[chunk_units<XT>()]) {
+    constexpr int CU = chunk_units<XT>();
+#pragma unroll
+    for (int q = 0; q < CU; ++q)
+        r[q] = c * 8 < D ? ld_unit<H>(as<XT>(base) + off + c * 8 + q * (8 / CU)) : make_uint4(0, 0, 0, 0);
+}
+
 // Block-wide fixed-order combination of the (maximum, sum) states; every thread gets the
 // total (every warp combines the same operands in the same lanes).
 template <int TPR>
@@ -561,8 +571,8 @@ __device__ __forceinline__ MaxSum block_maxsum(MaxSum st, float *sm_m, float *sm
     return tot;
 }
 
-template <int TPR, bool VEC8, int XT, bool LOG, int UN>
-__global__ void __launch_bounds__(TPR)
+template <int TPR, bool VEC8, int XT, bool LOG, int UN, int MINB>
+__global__ void __launch_bounds__(TPR, MINB)
 softmax_stream_fwd_kernel(const SoftmaxArgs a) {
     pdl_enter();
     constexpr int W = TPR / 32;
@@ -616,27 +626,26 @@ softmax_stream_fwd_kernel(const SoftmaxArgs a) {
         const float2 l2e = make_float2(kLog2e, kLog2e);
         const float2 nl2 = make_float2(-lse * kLog2e, -lse * kLog2e);
         const float2 nlse = make_float2(-lse, -lse);
+        constexpr int CU = chunk_units<XT>();
         for (int c0 = t; c0 * 8 < D; c0 += UN * TPR) {
-            float2 f[UN][4];
-#pragma unroll
-            for (int u = 0; u < UN; ++u) {
-                const int c = c0 + u * TPR;
-                ld_chunk<XT, kStream>(as<XT>(a.X) + off + c * 8, c * 8 < D, f[u]);
-            }
+            uint4 raw[UN][CU];
+            ce_load_raw<TPR, XT, UN>(a.X, off, c0, D, raw);
 #pragma unroll
             for (int u = 0; u < UN; ++u) {
                 const int c = c0 + u * TPR;
                 if (c * 8 >= D) continue;
+                float2 f[4];
+                unpack_chunk<XT, 4>(raw[u], 1, f);
 #pragma unroll
                 for (int p = 0; p < 4; ++p) {
                     if constexpr (LOG) {
-                        f[u][p] = __fadd2_rn(f[u][p], nlse);
+                        f[p] = __fadd2_rn(f[p], nlse);
                     } else {
-                        const float2 e = __ffma2_rn(f[u][p], l2e, nl2);  // (x - lse) log2(e)
-                        f[u][p] = make_float2(ex2(e.x), ex2(e.y));
+                        const float2 e = __ffma2_rn(f[p], l2e, nl2);  // (x - lse) log2(e)
+                        f[p] = make_float2(ex2(e.x), ex2(e.y));
                     }
                 }
-                st_chunk<XT>(as<XT>(a.Y) + off + c * 8, f[u]);
+                st_chunk<XT>(as<XT>(a.Y) + off + c * 8, f);
             }
         }
     } else {
@@ -647,8 +656,8 @@ softmax_stream_fwd_kernel(const SoftmaxArgs a) {
     }
 }
 
-template <int TPR, bool VEC8, int XT, bool LOG, int UN>
-__global__ void __launch_bounds__(TPR)
+template <int TPR, bool VEC8, int XT, bool LOG, int UN, int MINB>
+__global__ void __launch_bounds__(TPR, MINB)
 softmax_stream_bwd_kernel(const SoftmaxArgs a) {
     pdl_enter();
     constexpr int WPR = TPR / 32;
@@ -658,23 +667,28 @@ softmax_stream_bwd_kernel(const SoftmaxArgs a) {
     const int D = a.D;
     const int64_t off = row * (int64_t)D;
 
-    // pass 1: sum dY*Y (softmax) or sum dY (log-softmax)
+    // pass 1: sum dY*Y (softmax) or sum dY (log-softmax). The chunks in flight stay as
+    // loaded (16-byte units) until used: half the registers of fp32 pairs for 2-byte types.
+    constexpr int CU = chunk_units<XT>();
     float v[1] = {0.f};
     if constexpr (VEC8) {
         float2 acc = make_float2(0.f, 0.f);
         for (int c0 = t; c0 * 8 < D; c0 += UN * TPR) {
-            float2 yv[UN][4], gv[UN][4];
+            uint4 yr[LOG ? 1 : UN][CU], gr[UN][CU];
 #pragma unroll
             for (int u = 0; u < UN; ++u) {
-                const int c = c0 + u * TPR;
-                ld_chunk<XT, kReadOnly>(as<XT>(a.dY) + off + c * 8, c * 8 < D, gv[u]);
-                if constexpr (!LOG) ld_chunk<XT, kReadOnly>(as<XT>(a.X) + off + c * 8, c * 8 < D, yv[u]);
+                ld_raw_chunk<XT, kReadOnly>(a.dY, off, c0 + u * TPR, D, gr[u]);
+                if constexpr (!LOG) ld_raw_chunk<XT, kReadOnly>(a.X, off, c0 + u * TPR, D, yr[u]);
             }
 #pragma unroll
-            for (int u = 0; u < UN; ++u)
+            for (int u = 0; u < UN; ++u) {
+                float2 gv[4], yv[4];
+                unpack_chunk<XT, 4>(gr[u], 1, gv);
+                if constexpr (!LOG) unpack_chunk<XT, 4>(yr[u], 1, yv);
 #pragma unroll
                 for (int p = 0; p < 4; ++p)
-                    acc = LOG ? __fadd2_rn(acc, gv[u][p]) : __ffma2_rn(gv[u][p], yv[u][p], acc);
+                    acc = LOG ? __fadd2_rn(acc, gv[p]) : __ffma2_rn(gv[p], yv[p], acc);
+            }
         }
         v[0] = acc.x + acc.y;
     } else {
@@ -690,27 +704,29 @@ softmax_stream_bwd_kernel(const SoftmaxArgs a) {
     if constexpr (VEC8) {
         const float2 nc = make_float2(-c, -c);
         for (int c0 = t; c0 * 8 < D; c0 += UN * TPR) {
-            float2 yk[UN][4], gk[UN][4];
+            uint4 yr[UN][CU], gr[UN][CU];
 #pragma unroll
             for (int u = 0; u < UN; ++u) {
-                const int ch = c0 + u * TPR;
-                ld_chunk<XT, kStream>(as<XT>(a.X) + off + ch * 8, ch * 8 < D, yk[u]);
-                ld_chunk<XT, kStream>(as<XT>(a.dY) + off + ch * 8, ch * 8 < D, gk[u]);
+                ld_raw_chunk<XT, kStream>(a.X, off, c0 + u * TPR, D, yr[u]);
+                ld_raw_chunk<XT, kStream>(a.dY, off, c0 + u * TPR, D, gr[u]);
             }
 #pragma unroll
             for (int u = 0; u < UN; ++u) {
                 const int ch = c0 + u * TPR;
                 if (ch * 8 >= D) continue;
+                float2 yk[4], gk[4];
+                unpack_chunk<XT, 4>(yr[u], 1, yk);
+                unpack_chunk<XT, 4>(gr[u], 1, gk);
 #pragma unroll
                 for (int p = 0; p < 4; ++p) {
                     if constexpr (LOG) {
-                        const float2 e = make_float2(__expf(yk[u][p].x), __expf(yk[u][p].y));
-                        gk[u][p] = __ffma2_rn(e, nc, gk[u][p]);                    // dY - exp(Y) c
+                        const float2 e = make_float2(__expf(yk[p].x), __expf(yk[p].y));
+                        gk[p] = __ffma2_rn(e, nc, gk[p]);                 // dY - exp(Y) c
                     } else {
-                        gk[u][p] = __fmul2_rn(yk[u][p], __fadd2_rn(gk[u][p], nc));  // Y (dY - c)
+                        gk[p] = __fmul2_rn(yk[p], __fadd2_rn(gk[p], nc));  // Y (dY - c)
                     }
                 }
-                st_chunk<XT>(as<XT>(a.Y) + off + ch * 8, gk[u]);
+                st_chunk<XT>(as<XT>(a.Y) + off + ch * 8, gk);
             }
         }
     } else {

@@ -23,21 +23,24 @@ namespace {
     X(16384, 512, 1, 4)
 #endif
 // Rows wider than 16384 (up to MT_MAX_SOFTMAX_COLS): the two-pass streaming kernels,
-// X(max_D, TPR, UN): one CTA of TPR threads per row, UN chunks (or elements) in flight
-// per thread and operand (the backward loads two operands). Measured on GB300 (fp16,
-// forward / backward): 1024 x 65536 at 512 threads 53.2 / 94.2 us, 256 threads 54.8 /
-// 94.4, 128 threads 60.4 / 105.8; 256 x 262144 at 1024 threads 61.0 / 97.2 us, 512
-// threads 63.0 / 105.7; 2048 x 32768 backward at 256 threads 73.3 us, 512 threads 74.1.
+// X(max_D, TPR, UN, MINB): one CTA of TPR threads per row, UN chunks (or elements) in
+// flight per thread and operand (the backward loads two operands; fp32 rows take half as
+// many chunks, the same bytes), MINB the resident-CTA floor per SM the kernel is compiled
+// for (1: none). Measured on GB300 (forward / backward, us): 2048 x 32768 fp16 47.0 / 73.6
+// (backward at 256 threads 77.3); 1024 x 65536 fp16 52.8 / 92.8 (256 threads 54.8 / 94.4,
+// 128 threads 60.4 / 105.8); 512 x 131072 bf16 forward 56.5 at 2 chunks, 62.5 at 4;
+// 256 x 262144 fp16 forward 58.1 - 61.5 at 4 chunks, 61.5 at 2, 63.0 at 512 threads;
+// floors of 2 or 4 resident CTAs per SM did not help.
 #ifndef MT_SOFTMAX_SHAPES_STREAM_FWD
 #define MT_SOFTMAX_SHAPES_STREAM_FWD(X) \
-    X(65536, 512, 4)                    \
-    X(MT_MAX_SOFTMAX_COLS, 1024, 2)
+    X(65536, 512, 4, 1)                 \
+    X(131072, 1024, 2, 1)               \
+    X(MT_MAX_SOFTMAX_COLS, 1024, 4, 1)
 #endif
 #ifndef MT_SOFTMAX_SHAPES_STREAM_BWD
 #define MT_SOFTMAX_SHAPES_STREAM_BWD(X) \
-    X(32768, 256, 4)                    \
-    X(65536, 512, 2)                    \
-    X(MT_MAX_SOFTMAX_COLS, 1024, 2)
+    X(65536, 512, 2, 1)                 \
+    X(MT_MAX_SOFTMAX_COLS, 1024, 4, 1)
 #endif
 #define MT_SOFTMAX_SHAPES_SCALAR(X) \
     X(256, 32, 4, 8)                \
@@ -135,12 +138,12 @@ cudaError_t softmax_plan_scalar(int64_t N, int D, LaunchPlan *p) {
 
 template <bool BWD, bool LOG, bool VEC8, int XT>
 cudaError_t softmax_plan_stream(int64_t N, int D, LaunchPlan *p) {
-#define MT_TRY(maxd, tpr, un)                                                                       \
+#define MT_TRY(maxd, tpr, un, minb)                                                                 \
     if (D <= maxd) {                                                                                \
         if constexpr (BWD)                                                                          \
-            p->kernel = reinterpret_cast<const void *>(&softmax_stream_bwd_kernel<tpr, VEC8, XT, LOG, un>); \
+            p->kernel = reinterpret_cast<const void *>(&softmax_stream_bwd_kernel<tpr, VEC8, XT, LOG, stream_un(XT, un), minb>); \
         else                                                                                        \
-            p->kernel = reinterpret_cast<const void *>(&softmax_stream_fwd_kernel<tpr, VEC8, XT, LOG, un>); \
+            p->kernel = reinterpret_cast<const void *>(&softmax_stream_fwd_kernel<tpr, VEC8, XT, LOG, stream_un(XT, un), minb>); \
         p->threads = tpr;                                                                           \
         p->grid = (int)N;                                                                           \
         p->rows_per_cta = 1;                                                                        \
