@@ -556,9 +556,12 @@ __host__ __device__ constexpr int stream_un(int xt, int un) { return xt == kF32 
 // reduces it: RMSNorm and the fused op the sum of squares; LayerNorm, per thread, the
 // count, sum and centred sum of squares of its elements, one batch of UN chunks at a time
 // (each batch centred on its own mean, then merged by the update of Chan, Golub and
-// LeVeque), and the row's centred sum of squares as sum_t (m2_t + n_t (s_t / n_t - mu)^2),
-// as stable as the two-pass form. Pass 2 reads the row again (the fused op re-adds x + r,
-// the same fp32 value as pass 1) and applies. MINB: resident CTAs per SM asked of the
+// LeVeque), and the row's centred sum of squares as sum_t (m2_t + n_t (s_t / n_t - mu)^2).
+// LayerNorm works on x - k, k the row's first element, so that every mean in these sums
+// is of the row's spread, not of its offset from zero: a row with mean 1000 and standard
+// deviation 0.1 keeps its variance digits, and the apply takes (x - k) - mean(x - k),
+// so its outputs keep theirs too. Pass 2 reads the row again (the fused op re-adds
+// x + r, the same fp32 value as pass 1) and applies. MINB: resident CTAs per SM asked of the
 // compiler (a register cap).
 template <int OP, int TPR, int UN, int MINB, int XT, int WT>
 __global__ void __launch_bounds__(TPR, MINB)
@@ -590,8 +593,11 @@ norm_fwd_stream_kernel(const FwdArgs a) {
         }
     };
 
-    float n = 0.f, s = 0.f, m2 = 0.f;   // LayerNorm: this thread's count, sum, centred sum of squares
+    // LayerNorm: this thread's count, sum and centred sum of squares of x - k
+    float n = 0.f, s = 0.f, m2 = 0.f;
     float2 q2 = make_float2(0.f, 0.f);  // RMSNorm, fused op: the sum of squares (chunks past D are 0)
+    const float k = (OP == kLayer) ? ld_elem(a.X, off, XT) : 0.f;
+    const float2 nk = make_float2(-k, -k);
     for (int c0 = t; c0 * 8 < D; c0 += UN * TPR) {
         float2 x[UN][4];
         load(c0, x, std::integral_constant<int, kReadOnly>{}, true);
@@ -600,9 +606,13 @@ norm_fwd_stream_kernel(const FwdArgs a) {
             int nv = 0;
 #pragma unroll
             for (int u = 0; u < UN; ++u) {
-                nv += ((c0 + u * TPR) * 8 < D) ? 8 : 0;
+                if ((c0 + u * TPR) * 8 >= D) continue;
+                nv += 8;
 #pragma unroll
-                for (int p = 0; p < 4; ++p) b2 = __fadd2_rn(b2, x[u][p]);
+                for (int p = 0; p < 4; ++p) {
+                    x[u][p] = __fadd2_rn(x[u][p], nk);
+                    b2 = __fadd2_rn(b2, x[u][p]);
+                }
             }
             const float nb = (float)nv, bs = b2.x + b2.y, bm = bs / nb;  // nv >= 8: chunk c0 is in the row
             const float2 nbm = make_float2(-bm, -bm);
@@ -632,7 +642,7 @@ norm_fwd_stream_kernel(const FwdArgs a) {
                 for (int p = 0; p < 4; ++p) q2 = __ffma2_rn(x[u][p], x[u][p], q2);
         }
     }
-    float mu = 0.f, q[1];
+    float mu = 0.f, q[1];  // LayerNorm: mu = mean(x - k)
     if constexpr (OP == kLayer) {
         float v[1] = {s};
         row_sum<TPR, 1, 1>(v, red, 0, 0, wir, lane);
@@ -646,7 +656,7 @@ norm_fwd_stream_kernel(const FwdArgs a) {
     const float rs = rsqrtf(q[0] * inv_d + a.eps);
     if (t == 0) {
         a.rstd[row] = rs;
-        if constexpr (OP == kLayer) a.mean[row] = mu;
+        if constexpr (OP == kLayer) a.mean[row] = k + mu;
     }
 
     const float2 rs2 = make_float2(rs, rs), nmu = make_float2(-mu, -mu);
@@ -663,8 +673,10 @@ norm_fwd_stream_kernel(const FwdArgs a) {
                 float2 b[4];
                 ld_param<WT>(as<WT>(a.beta) + col, b);
 #pragma unroll
-                for (int p = 0; p < 4; ++p)
-                    y[p] = __ffma2_rn(__fmul2_rn(__fadd2_rn(x[u][p], nmu), rs2), g[p], b[p]);
+                for (int p = 0; p < 4; ++p) {
+                    const float2 d = __fadd2_rn(__fadd2_rn(x[u][p], nk), nmu);  // (x - k) - mu
+                    y[p] = __ffma2_rn(__fmul2_rn(d, rs2), g[p], b[p]);
+                }
             } else {
 #pragma unroll
                 for (int p = 0; p < 4; ++p) y[p] = __fmul2_rn(__fmul2_rn(x[u][p], rs2), g[p]);

@@ -65,6 +65,27 @@ def test_softmax_parity(dtype, shape, log):
         assert np.all(np.abs(s - 1.0) <= D * OUT_TOL[dtype][0] + 1e-6), "rows sum to one"
 
 
+@pytest.mark.parametrize("D", [4096, 65536, 262144])
+def test_softmax_masked_columns(D):
+    """-inf logits (masked columns), a row whose maximum is its last element, and a
+    row whose first columns are all masked: the running maximum starts at -inf and
+    masked entries come out as exactly 0."""
+    N = 3
+    x = _gen((N, D), 3.0, F32, 6)
+    x[0, ::3] = float("-inf")
+    x[1, -1] = 40.0
+    x[2, : D // 2] = float("-inf")
+    for log in (False, True):
+        y = mt.softmax_forward(x, log)
+        torch.cuda.synchronize()
+        Y, got = oracle.softmax_forward(f64(x), log), f64(y)
+        fin = np.isfinite(Y)   # log-softmax of a masked column is -inf on both sides
+        assert np.array_equal(np.isfinite(got), fin) and np.all(got[~fin] == -np.inf)
+        check_out(got[fin], Y[fin], F32, f"masked softmax(log={log}) {D}")
+        if not log:
+            assert torch.all(y[0, ::3] == 0) and torch.all(y[2, : D // 2] == 0)
+
+
 @pytest.mark.parametrize("D", [1024, 40000], ids=["regs", "stream"])
 def test_softmax_misaligned_and_deterministic(D):
     N = 33 if D <= 16384 else 3

@@ -1,13 +1,16 @@
-"""Rows wider than 16384 columns (split across a thread-block cluster) and the empty
-batch, against the fp64 oracle on the same stored inputs.
+"""Rows wider than 16384 columns and the empty batch, against the fp64 oracle on the
+same stored inputs.
 
 The pages bound a row to 8192 columns (meTile "Exact native normalization contract");
-the library widens the bound to 131072. A row of more than 16384 columns runs on a
+the library widens the bound to 131072. An aligned row of more than 16384 columns runs
+its forward on one CTA in two passes (LayerNorm merging per-thread centred sums by
+Chan's update); the backward, and the forward of misaligned or ragged rows, run on a
 cluster of 2, 4 or 8 CTAs, each a slice of the row, adding the CTAs' row sums in a fixed
-order, so the oracle's definitions apply unchanged. The widths cover each cluster size
-(16392 and 24576: 2 CTAs; 40000 and 65536: 4; 131072: 8), ragged widths and misaligned
-rows (the scalar kernels, also split), every op, the storage types, more rows than
-resident clusters (the persistent backward loops), and N = 0.
+order. The oracle's definitions apply unchanged. The widths cover each cluster size
+(16392 and 24576: 2 CTAs; 40000 and 65536: 4; 131072: 8) and each streaming shape,
+ragged widths and misaligned rows (the scalar kernels, also split), every op, the
+storage types, more rows than resident clusters (the persistent backward loops), rows
+far from zero mean, and N = 0.
 """
 import numpy as np
 import pytest
@@ -16,7 +19,7 @@ import torch
 import oracle
 import row_wise_rmsnorm_gb300 as mt
 import workloads as W
-from parity import STORAGE, check_out, compare_ex, f64, gpu_run_ex, oracle_run
+from parity import STORAGE, check_out, check_rstd, compare_ex, f64, gpu_run_ex, oracle_run
 
 pytestmark = pytest.mark.gpu
 
@@ -74,6 +77,28 @@ def test_wide_many_rows(op):
     torch.cuda.synchronize()
     ref = oracle_run(op, t, 1e-5, x_storage="f16")
     compare_ex(op, got, ref, t["X"], tag=f"{op} {N}x{D}")
+
+
+@pytest.mark.parametrize("D", [40000, 131072])
+def test_wide_layernorm_offset_rows(D):
+    """fp32 rows with mean 1000 and standard deviation 0.1 through the streamed forward:
+    the sum of squares minus the squared sum would lose every digit of the variance in
+    fp32. rstd to the usual 1e-5, the saved mean to one fp32 rounding of |mean|, Y to the
+    fp32 output tolerance. (The backward is not checked here: it takes x - mean with the
+    fp32 mean the interface saves, which at |mean| / std = 1e4 moves x-hat by about
+    ulp(1000) * rstd = 6e-4, beyond the fp32 tolerances.)"""
+    N = 3
+    t = _inputs(W.LAYERNORM, N, D, (F32, F32, F32))
+    g = torch.Generator(device="cuda")
+    g.manual_seed(11)
+    t["X"] = 1000.0 + 0.1 * torch.randn(N, D, generator=g, device="cuda")
+    got = gpu_run_ex(W.LAYERNORM, t, 1e-5)
+    torch.cuda.synchronize()
+    ref = oracle_run(W.LAYERNORM, t, 1e-5, x_storage="f32")
+    check_rstd(got["rstd"], ref["rstd"], f"offset rows rstd {N}x{D}")
+    mu, mref = f64(got["mean"]), f64(ref["mean"])
+    assert np.all(np.abs(mu - mref) <= 2.0 ** -23 * np.abs(mref)), (mu - mref)
+    check_out(got["Y"], ref["Y"], F32, f"offset rows Y {N}x{D}")
 
 
 def test_wide_fused_without_residual_cotangent():
