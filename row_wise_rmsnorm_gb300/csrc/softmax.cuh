@@ -40,6 +40,7 @@ struct SoftmaxArgs {
     int64_t N;
     int D;
     int xdt, gdt;    // storage types (scalar fallback): X/Y/dX, and dY
+    int slice;       // cluster-split streaming kernels: columns per CTA (a multiple of 8)
 };
 
 struct CeArgs {
@@ -535,6 +536,12 @@ ce_bwd_kernel(const CeArgs a) {
 //    with the default cache policy) and writes y = exp(x - lse), or x - lse.
 //  * Backward: pass 1 reduces sum dY*Y (softmax) or sum dY (log-softmax); pass 2 writes
 //    dX = Y*(dY - sum) or dY - exp(Y)*sum.
+//  * CLU (backward): a row is split over a thread-block cluster, CTA r taking columns
+//    [r*slice, (r+1)*slice); the CTAs' sums are exchanged once through distributed
+//    shared memory and added in rank order (cluster_sum), so every CTA gets the same
+//    bits. Fewer rows are then in flight at once (the second read finds its slice in L2
+//    more often), and a few hundred rows still make many CTAs. (The same split of the
+//    forward measured slower on GB300: 256 x 262144 fp16 61.4 -> 68.8 - 92.8 us.)
 
 // The 16-byte units of chunk c of the row at `off`, as loaded (zeros past the end).
 template <int XT, int H>
@@ -656,16 +663,19 @@ softmax_stream_fwd_kernel(const SoftmaxArgs a) {
     }
 }
 
-template <int TPR, bool VEC8, int XT, bool LOG, int UN, int MINB>
+template <int TPR, bool VEC8, int XT, bool LOG, int UN, int MINB, bool CLU = false>
 __global__ void __launch_bounds__(TPR, MINB)
 softmax_stream_bwd_kernel(const SoftmaxArgs a) {
     pdl_enter();
     constexpr int WPR = TPR / 32;
     __shared__ float red[2 * WPR];
+    __shared__ float xch[1];  // cluster_sum's slot
     const int t = threadIdx.x, lane = t % 32, w = t / 32;
-    const int64_t row = blockIdx.x;
-    const int D = a.D;
-    const int64_t off = row * (int64_t)D;
+    // this CTA's columns: the row, or its slice of a split row, as a row of D columns
+    const Window<CLU> win(a.D, a.slice);
+    const int64_t row = win.owner();
+    const int D = max(win.end - win.beg, 0);
+    const int64_t off = row * (int64_t)a.D + win.beg;
 
     // pass 1: sum dY*Y (softmax) or sum dY (log-softmax). The chunks in flight stay as
     // loaded (16-byte units) until used: half the registers of fp32 pairs for 2-byte types.
@@ -698,6 +708,10 @@ softmax_stream_bwd_kernel(const SoftmaxArgs a) {
         }
     }
     row_sum<TPR, 1, 1>(v, red, 0, 0, w, lane);
+    if constexpr (CLU) {
+        cluster_sum<1>(v, xch, 0, win.cn);
+        cluster_arrive();  // done reading the other CTAs' slots (waited for before exit)
+    }
     const float c = v[0];
 
     // pass 2: dX
@@ -736,6 +750,7 @@ softmax_stream_bwd_kernel(const SoftmaxArgs a) {
             st_elem(a.Y, off + j, LOG ? g - __expf(y) * c : y * (g - c), a.xdt);
         }
     }
+    if constexpr (CLU) cluster_wait();  // no CTA leaves while another may read its slots
 }
 
 // Fixed-order reduction of the per-row losses for sum/mean: one block; thread i sums rows

@@ -39,8 +39,9 @@ def _gen(shape, std, dtype, seed):
 # -------------------------------------------------------------------- softmax ---
 
 # up to 16384 columns the row stays in registers; wider rows (to the meTile bound of
-# 262144) take the two-pass streaming kernels: 256-thread rows up to 65536 columns,
-# 512-thread rows above, a ragged width on the scalar path
+# 262144) take the two-pass streaming kernels: one CTA per row, except the backward of
+# rows wider than 65536, split over a cluster (65544 and 131072: 4 CTAs, 262144: 8); a
+# ragged width on the scalar path
 SM_SHAPES = [(1, 127), (17, 257), (96, 1024), (40, 4104), (9, 16384), (300, 64),
              (4, 16392), (6, 65536), (3, 65544), (5, 50001), (3, 131072), (2, 262144)]
 
@@ -86,7 +87,7 @@ def test_softmax_masked_columns(D):
             assert torch.all(y[0, ::3] == 0) and torch.all(y[2, : D // 2] == 0)
 
 
-@pytest.mark.parametrize("D", [1024, 40000], ids=["regs", "stream"])
+@pytest.mark.parametrize("D", [1024, 40000, 70000], ids=["regs", "stream", "stream_split"])
 def test_softmax_misaligned_and_deterministic(D):
     N = 33 if D <= 16384 else 3
     x = _gen((N, D), 3.0, F16, 4)
