@@ -78,10 +78,12 @@ struct CUstream_st;
 typedef struct CUstream_st *mt_stream_t;
 
 /* Widest supported row of the normalizations. [meTile] bounds rows to 1..8192 columns;
- * this library extends the bound to 131072. Rows up to 16384 columns run on one CTA;
- * wider rows are split across a thread-block cluster of 2, 4 or 8 CTAs (one slice of
- * at most 16384 columns each) that add their row sums through distributed shared
- * memory in a fixed order, so results stay bitwise reproducible. */
+ * this library extends the bound to 131072. Rows up to 16384 columns run on one CTA.
+ * Wider rows: the forward of an aligned row (D % 8 == 0, 16-byte row bases) reads the
+ * row twice on one CTA (a reduction pass, then the apply); the backward, and the
+ * forward of other rows, split the row across a thread-block cluster of 2, 4 or 8 CTAs
+ * (one slice of at most 16384 columns each) that add their row sums through
+ * distributed shared memory in a fixed order. Results stay bitwise reproducible. */
 #define MT_MAX_COLS 131072
 
 /* Widest row of the softmax / log-softmax: [meTile] training_losses bounds last-axis
