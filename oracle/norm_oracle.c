@@ -18,8 +18,8 @@
  *             normalization contract": the three forward formulas, population
  *             variance of the centred row, the fused op normalising the unrounded
  *             FP32 sum, the residual-output cotangent added to both input
- *             gradients, backward differentiating the real-valued formula with
- *             the saved statistics.
+ *             gradients, the backward being the exact derivative of the
+ *             forward formula, taken at the saved fp32 statistics.
  *   [tc]      "Training kernels" (tensorcore docs), sections "RMSnorm -- Llama-style"
  *             (Math: rms(x) = sqrt(mean(x^2) + eps), y = x / rms * gamma) and
  *             "LayerNorm -- standard" (mean and inverse standard deviation saved
@@ -61,8 +61,8 @@ void oracle_rmsnorm_forward(const double *X, const double *gamma,
 }
 
 /* RMSNorm backward: derivative of the forward above for the loss
- * L = sum_ij dY_ij * y_ij, at the saved rstd ([meTile] contract: backward
- * differentiates the real-valued formula with saved statistics).
+ * L = sum_ij dY_ij * y_ij, at the saved rstd ([meTile] contract: the backward is the
+ * exact derivative of the forward formula at the saved statistics).
  *   xhat_ij = x_ij * rstd_i,   g_ij = dY_ij * gamma_j
  *   c_i     = (1/D) sum_j g_ij * xhat_ij
  *   dX_ij   = rstd_i * (g_ij - xhat_ij * c_i)
@@ -223,10 +223,11 @@ void oracle_add_rmsnorm_backward(const double *S, const double *gamma,
  *   [meTile]  "Kernel coverage and training scope", "Reduction and attention
  *             parity checklist" (softmax and log-softmax with input gradients)
  *             and "Loss parity checklist" / the native training_losses notes
- *             (cross-entropy row loss and logit gradients with ignore-index,
- *             none/sum/mean reduction, uniform label smoothing, squared
- *             log-sum-exp z-loss; mean over valid rows; maxima and
- *             log-denominators saved for the backward).
+ *             (cross-entropy row loss and logit gradients: an index whose rows
+ *             are skipped, losses per row, summed or averaged over the rows
+ *             kept, label smoothing spread evenly over the classes, a penalty
+ *             on the squared log-sum-exp; maxima and log-denominators kept
+ *             for the backward).
  *   [report]  "Metal subgroup LayerNorm and cross-entropy report", section
  *             "Structural repair exercised by cross-entropy": peak = max,
  *             total = sum exp(logit - peak), loss = log(total) + peak - selected.

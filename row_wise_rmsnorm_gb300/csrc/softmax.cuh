@@ -4,9 +4,10 @@
 // Sources (page title, section): tensorcore "Training kernels", "Softmax -- standalone,
 // row-wise" (subtract the row maximum, exponentiate, sum, divide; backward from Y and
 // dY); meTile "Kernel coverage and training scope", the reduction and loss checklists
-// (softmax / log-softmax with input gradients; cross-entropy with integer targets,
-// ignore-index, none/sum/mean reduction, uniform label smoothing, squared log-sum-exp
-// z-loss, maxima and log-denominators saved for the backward); "Metal subgroup
+// (softmax / log-softmax with input gradients; cross-entropy with integer targets, an
+// index whose rows are skipped, losses left per row or summed or averaged, label
+// smoothing spread evenly over the classes, a penalty on the squared log-sum-exp, and
+// the maxima and log-denominators kept for the backward); "Metal subgroup
 // LayerNorm and cross-entropy report", "Structural repair exercised by cross-entropy"
 // (loss = log(total) + peak - selected).
 //
