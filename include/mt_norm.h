@@ -244,10 +244,11 @@ mt_status_t mt_softmax_backward(mt_dtype_t dtype, const void *Y, const void *dY,
 
 /* ---------------------------------------------------------- cross-entropy ---
  * [meTile] loss checklist and training_losses notes: per-row cross-entropy of logits
- * with integer class targets, ignore-index, none/sum/mean reduction (mean over the
- * rows whose target is not ignore_index; 0 when there is none), uniform label
- * smoothing and the squared log-sum-exp z-loss; maxima and log-denominators saved for
- * the backward. ["Metal subgroup LayerNorm and cross-entropy report", "Structural
+ * with integer class targets; rows whose target equals ignore_index are skipped;
+ * the row losses are returned as they are, summed, or averaged (over the rows not
+ * skipped; 0 when there is none); label smoothing spreads its mass evenly over the
+ * classes; a z-loss penalises the squared log-sum-exp; the log-denominators are kept
+ * for the backward. ["Metal subgroup LayerNorm and cross-entropy report", "Structural
  * repair exercised by cross-entropy"]: loss = log(total) + peak - selected.
  *   lse_i  = log(sum_j exp(X_ij))                 (computed from the row maximum)
  *   q_ij   = (1 - label_smoothing) [j == t_i] + label_smoothing / D

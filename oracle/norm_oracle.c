@@ -22,7 +22,7 @@
  *             forward formula, taken at the saved fp32 statistics.
  *   [tc]      "Training kernels" (tensorcore docs), sections "RMSnorm -- Llama-style"
  *             (Math: rms(x) = sqrt(mean(x^2) + eps), y = x / rms * gamma) and
- *             "LayerNorm -- standard" (mean and inverse standard deviation saved
+ *             "LayerNorm -- standard" (the mean and rstd kept
  *             for backward).
  *   The backward expressions below are the derivative of those forward formulas;
  *   the test suite pins them against central finite differences.
