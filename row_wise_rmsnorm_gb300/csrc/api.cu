@@ -92,6 +92,11 @@ cudaError_t launch_pdl(const LaunchPlan &p, void *arg, cudaStream_t stream) {
     cfg.numAttrs = 1;
     if (p.cluster > 1) {
         if (p.grid % p.cluster != 0) return cudaErrorInvalidConfiguration;
+        if (p.cluster > 8) {  // a non-portable cluster size: the kernel opts in
+            const cudaError_t e =
+                cudaFuncSetAttribute(p.kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (e != cudaSuccess) return e;
+        }
         attr[1].id = cudaLaunchAttributeClusterDimension;
         attr[1].val.clusterDim.x = (unsigned)p.cluster;
         attr[1].val.clusterDim.y = 1;
@@ -300,7 +305,9 @@ cudaError_t cached_cluster_occupancy(const void *kernel, int threads, size_t sme
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int v = 0;
-    e = cudaOccupancyMaxActiveClusters(&v, kernel, &cfg);
+    if (cluster > 8)  // a non-portable cluster size: the kernel opts in first
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&v, kernel, &cfg);
     if (cur != device) cudaSetDevice(cur);
     if (e != cudaSuccess) return e;
     g_cluster_occupancy[key] = v;

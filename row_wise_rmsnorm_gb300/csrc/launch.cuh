@@ -183,6 +183,10 @@ namespace mt {
 // RPC, CH, ...), are tried in order; the first whose slice needs at most kMaxCluster CTAs
 // is taken (CL the smallest power of two that covers D with it).
 constexpr int kMaxCluster = 8;
+// The all-fp32 backward's slices are 8192 columns (two ring stages of 16384 fp32 columns
+// do not fit), so its widest rows need 16 CTAs: a non-portable cluster size, which the
+// kernel opts into; where 16-CTA clusters cannot be resident the scalar kernel runs.
+constexpr int kMaxClusterF32Bwd = 16;
 #define MT_FWD_WIDE_SCALAR(X) X(16384, 1024, 1, 16)
 #ifndef MT_BWD_WIDE_PIPE
 #define MT_BWD_WIDE_PIPE(X) X(16384, 512, 1, 4, 3, 1)
@@ -191,11 +195,11 @@ constexpr int kMaxCluster = 8;
 #define MT_BWD_WIDE_SCALAR(X) X(16384, 512, 1, 32)
 
 // The cluster split of a D-column row over CTAs of at most `cap` columns: false when
-// more than kMaxCluster CTAs would be needed.
-inline bool wide_split(int D, int cap, int *cl, int *slice) {
+// more than max_cl CTAs would be needed.
+inline bool wide_split(int D, int cap, int *cl, int *slice, int max_cl = kMaxCluster) {
     int c = 2;
     while ((int64_t)c * cap < D) c *= 2;
-    if (c > kMaxCluster) return false;
+    if (c > max_cl) return false;
     *cl = c;
     *slice = (((D + c - 1) / c) + 7) / 8 * 8;
     return true;
@@ -212,6 +216,10 @@ constexpr int pipe_stages(int base, size_t stage_bytes, size_t param_bytes, int 
                       ? (int)((kMaxDynSmem / ctas - param_bytes) / stage_bytes)
                       : base);
 }
+
+// Returned by a vector plan for a dtype combination or shape it does not cover: the
+// caller takes the scalar kernel.
+constexpr cudaError_t kNoVectorPlan = cudaErrorNotSupported;
 
 struct LaunchPlan {
     const void *kernel = nullptr;
@@ -258,6 +266,7 @@ inline cudaError_t persistent_cluster_grid(LaunchPlan *p, int64_t N, int device)
     if ((e = device_sm_count(device, &sms)) != cudaSuccess) return e;
     e = cached_cluster_occupancy(p->kernel, p->threads, p->smem, p->cluster, device, &fit);
     if (e != cudaSuccess) return e;
+    if (fit == 0 && p->cluster > kMaxCluster) return kNoVectorPlan;  // not resident: scalar
     const int64_t owners = std::min<int64_t>({(int64_t)std::max(fit, 1),
                                               (int64_t)std::max(sms / p->cluster, 1), N});
     p->grid = (int)owners * p->cluster;
@@ -270,10 +279,6 @@ inline cudaError_t cluster_row_grid(LaunchPlan *p, int64_t N) {
     p->grid = (int)N * p->cluster;
     return cudaSuccess;
 }
-
-// Returned by a vector plan for a dtype combination or shape it does not cover: the
-// caller takes the scalar kernel.
-constexpr cudaError_t kNoVectorPlan = cudaErrorNotSupported;
 
 // ------------------------------------------------------------------ forward ---
 
@@ -439,8 +444,9 @@ cudaError_t bwd_plan_vec(int64_t N, int D, int device, LaunchPlan *p) {
     }
 #undef MT_TRY
     // wider rows: split across a cluster (a shape whose ring does not fit falls through)
+    constexpr int max_cl = (XT == kF32 && WT == kF32 && GT == kF32) ? kMaxClusterF32Bwd : kMaxCluster;
 #define MT_TRY(cap, tpr, rpc, ch, st, ctas)                                                      \
-    if (wide_split(D, cap, &p->cluster, &p->slice)) {                                           \
+    if (wide_split(D, cap, &p->cluster, &p->slice, max_cl)) {                                   \
         const cudaError_t e =                                                                   \
             bwd_pipe_shape<OP, XT, WT, GT, tpr, rpc, ch, st, HAS_DS, ctas, true>(N, device, p); \
         if (e != kNoVectorPlan) return e;                                                       \

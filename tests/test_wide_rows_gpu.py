@@ -57,7 +57,7 @@ COMBOS = [(BF16, BF16, BF16), (F32, F32, F32), (F16, F32, F32), (BF16, F32, BF16
 @pytest.mark.parametrize("op", OPS)
 def test_wide_storage_types(op, combo, D):
     """Every family of the split kernels: matching 2-byte types, all fp32 (its backward
-    slices are 8192 columns, and 131072 columns take the scalar kernels), fp32
+    slices are 8192 columns, so 131072 columns take 16-CTA clusters), fp32
     parameters or cotangents."""
     N = 3
     t = _inputs(op, N, D, combo)
