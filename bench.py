@@ -40,9 +40,29 @@ import workloads as W  # noqa: E402
 METRIC = ("achieved HBM GB/s (% of ~8 TB/s) and rows/s, norm fwd+bwd at N×D fp16")
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-DEFAULT_WORKLOAD = "rmsnorm_16384x4096"
-LARGE_WORKLOADS = ["rmsnorm_16384x4096", "add_rmsnorm_32768x4096", "layernorm_2048x16384",
-                   "rmsnorm_4096x32768", "layernorm_1024x131072"]
+# The headline is the largest workload that fits one GPU: the fused residual-add + RMSNorm
+# over 32768 x 4096 (about 1.07 GB read and written per direction).
+DEFAULT_WORKLOAD = "add_rmsnorm_32768x4096"
+# The three large workloads the >= 80 % bar applies to; each gets its own roofline block.
+GATED_WORKLOADS = ["rmsnorm_16384x4096", "add_rmsnorm_32768x4096", "layernorm_2048x16384"]
+LARGE_WORKLOADS = GATED_WORKLOADS + ["rmsnorm_4096x32768", "layernorm_1024x131072"]
+
+# The kernels each call of a workload launches (fp16 storage), for the roofline blocks.
+# The backward is one user-visible call: the row kernel then the fixed-order reduction.
+KERNELS = {
+    ("rmsnorm_16384x4096", "forward"): ["norm_fwd_packed_kernel"],
+    ("rmsnorm_16384x4096", "backward"): ["norm_bwd_pipe_kernel", "param_reduce_kernel"],
+    ("add_rmsnorm_32768x4096", "forward"): ["norm_fwd_vec8_kernel"],
+    ("add_rmsnorm_32768x4096", "backward"): ["norm_bwd_pipe_kernel", "param_reduce_kernel"],
+    ("layernorm_2048x16384", "forward"): ["norm_fwd_vec8_kernel"],
+    ("layernorm_2048x16384", "backward"): ["norm_bwd_pipe_kernel", "param_reduce_kernel"],
+    ("rmsnorm_4096x32768", "forward"): ["norm_fwd_stream_kernel"],
+    ("rmsnorm_4096x32768", "backward"): ["norm_bwd_pipe_kernel (2-CTA clusters)",
+                                         "param_reduce_kernel"],
+    ("layernorm_1024x131072", "forward"): ["norm_fwd_stream_kernel"],
+    ("layernorm_1024x131072", "backward"): ["norm_bwd_pipe_kernel (8-CTA clusters)",
+                                            "param_reduce_kernel"],
+}
 CSRC = os.path.join(ROOT, "row_wise_rmsnorm_gb300", "csrc")
 
 
@@ -84,57 +104,141 @@ def recorded_traffic(workload: str, kernel: str):
 
 
 class ClockSampler:
-    """nvidia-smi clock/throttle samples every 200 ms while the timed region runs."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """SM clock, power and clock-event reasons while the timed region runs, read through
+    NVML (the library nvidia-smi itself uses; read-only queries) every millisecond from a
+    background thread, plus one synchronous sample as soon as the timed work is enqueued
+    (`mark()`), so that even a region of a few milliseconds carries its own clock record.
+    Falls back to `nvidia-smi -lms 200` when NVML cannot be loaded."""
+    REASONS = ((0x8, "hw_slowdown"), (0x40, "hw_thermal_slowdown"),
+               (0x20, "sw_thermal_slowdown"), (0x4, "sw_power_cap"))
+    SMI_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                  "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
+    def __init__(self, device, period_s: float = 0.001):
+        self.device = device
+        self.period = period_s
+        self.rows = []
+        self.nvml = None
+        self.handle = None
         self.proc = None
+        self.source = None
+
+    # -- NVML through ctypes
+    def _open_nvml(self):
+        import ctypes
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+        except OSError:
+            return False
+        if lib.nvmlInit_v2() != 0:
+            return False
+        h = ctypes.c_void_p()
+        ok = False
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(self.device).uuid)
+            key = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            ok = lib.nvmlDeviceGetHandleByUUID(key.encode(), ctypes.byref(h)) == 0
+        except Exception:  # noqa: BLE001 - any failure falls back to the index
+            ok = False
+        if not ok:
+            idx = self.device.index or 0
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+            ids = [v for v in vis.split(",") if v.strip().isdigit()]
+            if idx < len(ids):
+                idx = int(ids[idx])
+            ok = lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(idx), ctypes.byref(h)) == 0
+        if not ok:
+            return False
+        self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        self.nvml, self.handle = lib, h
+        mx = ctypes.c_uint(0)
+        lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))
+        self.max_mhz = mx.value
+        return True
+
+    def sample(self, tag="thread"):
+        import ctypes
+        if self.nvml is None:
+            return
+        sm, pw, rs = ctypes.c_uint(0), ctypes.c_uint(0), ctypes.c_ulonglong(0)
+        if self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(sm)) != 0:
+            return
+        self.nvml.nvmlDeviceGetPowerUsage(self.handle, ctypes.byref(pw))
+        self.reasons_fn(self.handle, ctypes.byref(rs))
+        self.rows.append(dict(t=time.perf_counter(), sm=float(sm.value), smax=float(self.max_mhz),
+                              power=pw.value / 1000.0, mask=int(rs.value), tag=tag))
+
+    def mark(self):
+        """One synchronous sample (call right after enqueuing the timed work)."""
+        self.sample("sync")
+
+    def _loop(self):
+        while not self._stop.is_set():
+            self.sample()
+            self._stop.wait(self.period)
 
     def __enter__(self):
-        try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except OSError:
-            self.proc = None
+        import threading
+        if self._open_nvml():
+            self.source = "nvml, 1 ms"
+            self._stop = threading.Event()
+            self._thread = threading.Thread(target=self._loop, daemon=True)
+            self.t0 = time.perf_counter()
+            self._thread.start()
+        else:
+            self.source = "nvidia-smi, 200 ms"
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", f"--id={self.device.index or 0}",
+                     f"--query-gpu={self.SMI_FIELDS}", "--format=csv,noheader,nounits",
+                     "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except OSError:
+                self.proc = None
+            self.t0 = time.perf_counter()
         return self
 
     def __exit__(self, *exc):
-        self.out = ""
+        self.t1 = time.perf_counter()
+        if self.nvml is not None:
+            self._stop.set()
+            self._thread.join(timeout=5)
+            self.nvml.nvmlShutdown()
+            return
+        out = ""
         if self.proc is not None:
             self.proc.terminate()
             try:
-                self.out, _ = self.proc.communicate(timeout=5)
+                out, _ = self.proc.communicate(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-                self.out, _ = self.proc.communicate()
-
-    def summary(self):
-        rows = []
-        for r in csv.reader(io.StringIO(getattr(self, "out", "") or "")):
+                out, _ = self.proc.communicate()
+        for r in csv.reader(io.StringIO(out or "")):
             if len(r) < 9:
                 continue
             try:
-                rows.append(dict(sm=float(r[1]), smax=float(r[2]), power=float(r[3]),
-                                 hw=r[5].strip(), hwt=r[6].strip(), swt=r[7].strip(),
-                                 pcap=r[8].strip()))
+                mask = sum(bit for (bit, _), col in zip(self.REASONS, (5, 6, 7, 8))
+                           if r[col].strip().lower() == "active")
+                self.rows.append(dict(t=0.0, sm=float(r[1]), smax=float(r[2]), power=float(r[3]),
+                                      mask=mask, tag="smi"))
             except ValueError:
                 continue
+
+    def summary(self):
+        rows = self.rows
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
-        reasons = []
-        for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
-                          ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
-            if any(x[key].lower() == "active" for x in rows):
-                reasons.append(name)
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0,
+                    "source": self.source}
+        reasons = [name for bit, name in self.REASONS if any(x["mask"] & bit for x in rows)]
         return {"sm_mhz": statistics.median(x["sm"] for x in rows),
+                "sm_mhz_min": min(x["sm"] for x in rows),
                 "sm_max_mhz": max(x["smax"] for x in rows),
-                "power_w_max": max(x["power"] for x in rows),
-                "reasons": reasons, "samples": len(rows)}
+                "power_w_max": round(max(x["power"] for x in rows), 1),
+                "reasons": reasons, "samples": len(rows),
+                "sync_samples": sum(1 for x in rows if x["tag"] == "sync"),
+                "source": self.source}
 
 
 # ------------------------------------------------------------ GPU arm ---
@@ -272,11 +376,12 @@ class CrossEntropyRunner:
                                           self.dx, stream)
 
 
-def time_ops(sets, steps: int, warmup: int, stream):
+def time_ops(sets, steps: int, warmup: int, stream, on_enqueued=None):
     """CUDA-event times (ms) of `steps` back-to-back steps, each a forward on buffer set
     s % n and a backward on set (s + 1) % n: a backward never finds in L2 the rows its
     step's forward just read, and the write-backs one call leaves in L2 are paid by the
-    next timed call. Returns per-step forward and backward times and the total."""
+    next timed call. `on_enqueued` runs once every timed step is enqueued, while the GPU
+    works through them. Returns per-step forward and backward times and the total."""
     import torch
     n = len(sets)
     for r in sets:
@@ -292,6 +397,8 @@ def time_ops(sets, steps: int, warmup: int, stream):
         ev[2 * s + 1].record(stream)
         sets[(s + 1) % n].backward(stream)
         ev[2 * s + 2].record(stream)
+    if on_enqueued is not None:
+        on_enqueued()
     torch.cuda.synchronize()
     fwd = [ev[2 * s].elapsed_time(ev[2 * s + 1]) for s in range(steps)]
     bwd = [ev[2 * s + 1].elapsed_time(ev[2 * s + 2]) for s in range(steps)]
@@ -459,14 +566,27 @@ def oracle_baseline_all_cores(name: str, rows: int, passes: int = 20):
             "rows_per_s": round(passes * rows / secs, 1)}
 
 
+_ORACLE_INPUTS = {}
+
+
+def _oracle_inputs(name: str, rows: int, seed: int):
+    """The first `rows` rows of the workload as fp64 arrays, drawn once per (name, rows,
+    seed) and kept: repeated timing steps reuse them instead of drawing them again."""
+    key = (name, rows, seed)
+    if key not in _ORACLE_INPUTS:
+        _ORACLE_INPUTS.clear()
+        t = W.generate_workload(name, rows=rows, seed=seed)
+        _ORACLE_INPUTS[key] = {k: v.double().numpy() for k, v in t.items()}
+    return _ORACLE_INPUTS[key]
+
+
 def oracle_step_seconds(name: str, rows: int, seed: int = 0):
     """Wall time of one oracle forward + backward over `rows` rows of the workload."""
     import numpy as np
     sys.path.insert(0, ROOT)
     import oracle
     w = W.WORKLOADS[name]
-    t = W.generate_workload(name, rows=rows, seed=seed)
-    a = {k: v.double().numpy() for k, v in t.items()}
+    a = _oracle_inputs(name, rows, seed)
     eps = float(np.float32(w.eps))
     t0 = time.perf_counter()
     if w.op == W.RMSNORM:
@@ -520,6 +640,17 @@ def host_cpu() -> str:
     return f"{platform.machine()} ({', '.join(parts)})" if parts else platform.machine()
 
 
+def bench_config(name: str, world: int = 1) -> dict:
+    """The workload description both arms print (the same keys and values)."""
+    w = W.WORKLOADS[name]
+    return {"workload": name, "op": w.op, "N": w.N, "D": w.D, "eps": w.eps,
+            "step": "forward + backward",
+            "l2": ("not flushed: inputs larger than L2; steps run back to back, the forward on "
+                   "one buffer set and the backward on another (2 sets) so no call re-reads what "
+                   "the previous one touched, and write-backs are paid inside the timed region"),
+            "parallelism": f"{world} independent replica(s)"}
+
+
 def run_reference(args):
     """--impl reference: the oracle on host cores, K steps of a bounded row sample."""
     rank = int(os.environ.get("RANK", "0"))
@@ -527,8 +658,8 @@ def run_reference(args):
         return 0
     name = args.workload
     w = W.WORKLOADS[name]
-    t1 = oracle_step_seconds(name, min(w.N, 16))
-    per_row = t1 / min(w.N, 16)
+    probe = min(w.N, 512)
+    per_row = oracle_step_seconds(name, probe) / probe
     per_step_budget = max(0.02, 60.0 / max(1, args.steps + args.warmup))
     rows = int(max(1, min(w.N, per_step_budget / max(per_row, 1e-9))))
     for _ in range(args.warmup):
@@ -546,10 +677,9 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * secs / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": name, "op": w.op, "N": w.N, "D": w.D, "eps": w.eps,
-                   "rows_per_step": rows},
+        "config": bench_config(name, args.gpus),
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "rows_per_step": rows},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -712,9 +842,10 @@ def main(argv=None):
         torch.cuda.synchronize()
 
     barrier()
-    with ClockSampler(local) as clocks:
+    with ClockSampler(device) as clocks:
         t0 = time.perf_counter()
-        fwd, bwd, total_ms = time_ops(sets, args.steps, args.warmup, stream)
+        fwd, bwd, total_ms = time_ops(sets, args.steps, args.warmup, stream,
+                                      on_enqueued=clocks.mark)
         barrier()
         wall = time.perf_counter() - t0
     fwd_ms = statistics.mean(fwd)
@@ -739,11 +870,20 @@ def main(argv=None):
 
     ops = {"forward": op_line(runner.fwd_bytes, fwd), "backward": op_line(runner.bwd_bytes, bwd)}
     dom = "backward" if bwd_ms >= fwd_ms else "forward"
-    dom_name = {"forward": f"{w.op} forward (norm_fwd_kernel, 1 launch)",
-                "backward": f"{w.op} backward (norm_bwd_kernel + param_reduce_kernel, 2 launches)"}
     del runner, sets
     torch.cuda.empty_cache()
 
+    def roofline_block(name, direction, line):
+        """One kernel call's roofline entry: algorithmic (compulsory) bytes per call over
+        its mean CUDA-event time, against the measured copy peak and 8 TB/s."""
+        return {"bound": "hbm", "kernels": KERNELS.get((name, direction)),
+                "achieved": line["gbs"], "peak": peak, "unit": "GB/s",
+                "frac": line["frac_of_measured"], "frac_of_8tbs": line["frac_of_8tbs"],
+                "us": line["us"], "rows_per_s": line["rows_per_s"],
+                "algorithmic_bytes_per_launch": line["compulsory_bytes"],
+                "traffic": recorded_traffic(name, direction)}
+
+    rooflines = {args.workload: {d: roofline_block(args.workload, d, ops[d]) for d in ops}}
     others = {}
     if not args.no_others and rank == 0:
         for name in LARGE_WORKLOADS:
@@ -752,11 +892,21 @@ def main(argv=None):
             r2 = [OpRunner(name, device, seed=i) for i in range(2)]
             f2, b2, _ = time_ops(r2, max(50, args.steps // 10), args.warmup, stream)
             r2 = r2[0]
-            others[name] = {
-                "forward_gbs": round(r2.fwd_bytes / (statistics.mean(f2) * 1e-3) / 1e9, 2),
-                "backward_gbs": round(r2.bwd_bytes / (statistics.mean(b2) * 1e-3) / 1e9, 2),
-                "forward_us": round(1e3 * statistics.mean(f2), 3),
-                "backward_us": round(1e3 * statistics.mean(b2), 3)}
+            w2 = r2.w
+            lines = {}
+            for d, nbytes, ts in (("forward", r2.fwd_bytes, f2), ("backward", r2.bwd_bytes, b2)):
+                ms = statistics.mean(ts)
+                gbs = nbytes / (ms * 1e-3) / 1e9
+                lines[d] = {"us": round(1e3 * ms, 3), "gbs": round(gbs, 2),
+                            "frac_of_measured": round(gbs / peak, 4),
+                            "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
+                            "rows_per_s": round(w2.N / (ms * 1e-3), 1), "compulsory_bytes": nbytes}
+            others[name] = {"forward_gbs": lines["forward"]["gbs"],
+                            "backward_gbs": lines["backward"]["gbs"],
+                            "forward_us": lines["forward"]["us"],
+                            "backward_us": lines["backward"]["us"]}
+            if name in GATED_WORKLOADS:
+                rooflines[name] = {d: roofline_block(name, d, lines[d]) for d in lines}
             del r2
             torch.cuda.empty_cache()
 
@@ -799,7 +949,7 @@ def main(argv=None):
 
     e2e = None
     if not args.no_e2e:
-        e2e = e2e_run(args.workload, device, max(5, min(50, args.steps // 40)), 3, seed=rank)
+        e2e = e2e_run(args.workload, device, max(20, min(50, args.steps // 40)), 3, seed=rank)
         if world > 1:
             e2e["ms_per_step"] = round(max_over_ranks(e2e["ms_per_step"], device), 4)
             e2e["value"] = round(world * step_bytes / (e2e["ms_per_step"] * 1e-3) / 1e9, 2)
@@ -807,10 +957,10 @@ def main(argv=None):
     cpu = cpu_all = None
     if rank == 0 and world >= 1 and not args.no_cpu_baseline and args.gpus == 1:
         cpu = oracle_baseline(args.workload)
-        cpu_all = oracle_baseline_all_cores(args.workload, W.WORKLOADS[args.workload].N)
+        cpu_all = oracle_baseline_all_cores(args.workload,
+                                            min(W.WORKLOADS[args.workload].N, 8192))
 
-    dom_line = ops[dom]
-    traffic = recorded_traffic(args.workload, dom)
+    dom_block = rooflines[args.workload][dom]
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -828,22 +978,18 @@ def main(argv=None):
         "dtype": "f32",
         "storage": "f16",
         "data": "synthetic",
-        "config": {"workload": args.workload, "op": w.op, "N": w.N, "D": w.D, "eps": w.eps,
-                   "step": "forward + backward",
-                   "l2": (f"not flushed: inputs larger than L2 ({l2 >> 20} MiB); steps run back "
-                          "to back, the forward on one buffer set and the backward on another "
-                          "(2 sets) so no call re-reads what the previous one touched, and "
-                          "write-backs are paid inside the timed region"),
-                   "parallelism": f"{world} independent replica(s)"},
+        "config": bench_config(args.workload, world),
+        "l2_note": (f"inputs larger than L2 ({l2 >> 20} MiB)"),
         "ops": ops,
-        "roofline": {"bound": "hbm", "kernel": dom_name[dom], "achieved": dom_line["gbs"],
-                     "peak": peak, "peak_source": peak_src, "unit": "GB/s",
-                     "frac": dom_line["frac_of_measured"], "traffic": traffic,
-                     "algorithmic_bytes_per_launch": dom_line["compulsory_bytes"]},
+        "roofline": {"bound": "hbm", "kernel": f"{w.op} {dom}: " + " + ".join(KERNELS[(args.workload, dom)]),
+                     "achieved": dom_block["achieved"], "peak": peak, "peak_source": peak_src,
+                     "unit": "GB/s", "frac": dom_block["frac"], "traffic": dom_block["traffic"],
+                     "algorithmic_bytes_per_launch": dom_block["algorithmic_bytes_per_launch"]},
+        "rooflines": rooflines,
         "cpu_baseline": cpu,
         "cpu_baseline_all_cores": cpu_all,
         "e2e": e2e,
-        "gpu_launches": args.steps * 3,
+        "gpu_launches": args.steps * 3,  # per step: the forward, the backward row kernel, the reduction
         "clocks": clocks.summary(),
         "timed_region_wall_s": round(wall, 3),
         "other_workloads": others,

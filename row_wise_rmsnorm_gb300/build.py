@@ -91,6 +91,37 @@ def build(force: bool = False, verbose: bool = False) -> str:
     return LIB
 
 
+HOOKS_LIB = os.path.join(BUILD, "libmt_norm_hooks.so")
+HOOKS_SOURCE = os.path.join(CSRC, "api.cu")
+
+
+def build_test_hooks() -> str:
+    """Build the test-only variant libmt_norm_hooks.so: the library with api.cu compiled
+    with -DMT_TEST_HOOKS (host-side launch-failure injection, mt_test_*), every other
+    object shared with libmt_norm.so. The product library never contains the hooks."""
+    build()
+    nvcc = _nvcc()
+    objdir = os.path.join(BUILD, "obj")
+    hookdir = os.path.join(BUILD, "hooks")
+    os.makedirs(hookdir, exist_ok=True)
+    hobj = os.path.join(hookdir, "api.o")
+    if _stale(hobj, [HOOKS_SOURCE] + _headers() + [__file__]):
+        cmd = [nvcc, *NVCC_FLAGS, "-DMT_TEST_HOOKS", "-c", HOOKS_SOURCE, "-o", hobj]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed for the test-hook api.cu:\n{r.stderr}")
+    objs = [hobj] + [os.path.join(objdir, os.path.basename(s)[:-3] + ".o") for s in sources()
+                     if os.path.basename(s) != "api.cu"]
+    if _stale(HOOKS_LIB, objs):
+        tmp = HOOKS_LIB + f".tmp{os.getpid()}"
+        r = subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True,
+                           text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"link failed:\n{r.stderr}")
+        os.replace(tmp, HOOKS_LIB)
+    return HOOKS_LIB
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--force", action="store_true")

@@ -79,6 +79,8 @@ std::map<std::tuple<const void *, int, size_t, int, int>, int> g_cluster_occupan
 // in kernels.cuh).
 cudaError_t launch_pdl(const LaunchPlan &p, void *arg, cudaStream_t stream) {
     if (p.kernel == nullptr || p.grid < 1) return cudaErrorInvalidConfiguration;
+    const cudaError_t h = launch_hook();
+    if (h != cudaSuccess) return h;
     void *args[] = {arg};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.grid);
@@ -91,12 +93,9 @@ cudaError_t launch_pdl(const LaunchPlan &p, void *arg, cudaStream_t stream) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (p.cluster > 1) {
+        // (a non-portable cluster size was opted into when the plan was made:
+        // cached_cluster_occupancy)
         if (p.grid % p.cluster != 0) return cudaErrorInvalidConfiguration;
-        if (p.cluster > 8) {  // a non-portable cluster size: the kernel opts in
-            const cudaError_t e =
-                cudaFuncSetAttribute(p.kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-            if (e != cudaSuccess) return e;
-        }
         attr[1].id = cudaLaunchAttributeClusterDimension;
         attr[1].val.clusterDim.x = (unsigned)p.cluster;
         attr[1].val.clusterDim.y = 1;
@@ -199,8 +198,8 @@ mt_status_t run_backward(int op, BwdArgs a, bool vec8, float *dgamma, float *dbe
         // runs and starts reading only after the backward grid has completed. The wide
         // form is used when its 128-column blocks still give one block per SM.
         int sms = 0;
-        e = device_sm_count(device, &sms);
-        if (e != cudaSuccess) return cuda_fail(e);
+        e = device_sm_count(device, &sms);  // cached by the plan: cannot fail here
+        if (e != cudaSuccess) sms = 1;
         const int arrays = num_partial_arrays(op);
         const bool wide = (a.D % 4 == 0) && ((a.D + 127) / 128) * arrays >= sms;
         cudaLaunchConfig_t cfg = {};
@@ -215,10 +214,12 @@ mt_status_t run_backward(int op, BwdArgs a, bool vec8, float *dgamma, float *dbe
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         const float *cpart = part;
-        e = wide ? cudaLaunchKernelEx(&cfg, param_reduce_kernel<4, kReduceWideWarps>, cpart, prow,
-                                      a.D, dgamma, dbeta)
-                 : cudaLaunchKernelEx(&cfg, param_reduce_kernel<1, kReduceNarrowWarps>, cpart,
-                                      prow, a.D, dgamma, dbeta);
+        e = launch_hook();
+        if (e == cudaSuccess)
+            e = wide ? cudaLaunchKernelEx(&cfg, param_reduce_kernel<4, kReduceWideWarps>, cpart,
+                                          prow, a.D, dgamma, dbeta)
+                     : cudaLaunchKernelEx(&cfg, param_reduce_kernel<1, kReduceNarrowWarps>,
+                                          cpart, prow, a.D, dgamma, dbeta);
         if (e != cudaSuccess) st = cuda_fail(e);
     }
     if (own_ws) {
@@ -231,6 +232,27 @@ mt_status_t run_backward(int op, BwdArgs a, bool vec8, float *dgamma, float *dbe
 }  // namespace
 
 void record_cuda_error(cudaError_t e) { g_last_cuda_error = (int)e; }
+
+#ifdef MT_TEST_HOOKS
+// Test build only (-DMT_TEST_HOOKS, libmt_norm_hooks.so): host-side failure injection.
+// mt_test_fail_launch(skip, err) arms a one-shot failure: the launch that comes after
+// `skip` further launches returns `err` without launching anything, as a failing
+// cudaLaunchKernelEx would. Nothing on the GPU is made to fail.
+namespace {
+std::mutex g_hook_mu;
+int g_hook_skip = -1;  // < 0: disarmed
+cudaError_t g_hook_err = cudaSuccess;
+}  // namespace
+
+cudaError_t launch_hook() {
+    std::lock_guard<std::mutex> lock(g_hook_mu);
+    if (g_hook_skip < 0) return cudaSuccess;
+    if (g_hook_skip-- > 0) return cudaSuccess;
+    return g_hook_err;
+}
+#else
+cudaError_t launch_hook() { return cudaSuccess; }
+#endif
 
 cudaError_t device_sm_count(int device, int *sms) {
     std::lock_guard<std::mutex> lock(g_cache_mu);
@@ -305,9 +327,22 @@ cudaError_t cached_cluster_occupancy(const void *kernel, int threads, size_t sme
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int v = 0;
-    if (cluster > 8)  // a non-portable cluster size: the kernel opts in first
+    if (cluster > kMaxCluster) {
+        // A non-portable cluster size: the kernel opts in here, once per kernel and
+        // device (the attribute persists, so launches need not set it again). A device
+        // or driver that refuses the opt-in or the occupancy query for this size cannot
+        // run the clusters: that is recorded as 0 resident clusters (the planner then
+        // takes the scalar kernel) and the error is cleared, not returned.
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&v, kernel, &cfg);
+        if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&v, kernel, &cfg);
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            v = 0;
+            e = cudaSuccess;
+        }
+    } else {
+        e = cudaOccupancyMaxActiveClusters(&v, kernel, &cfg);
+    }
     if (cur != device) cudaSetDevice(cur);
     if (e != cudaSuccess) return e;
     g_cluster_occupancy[key] = v;
@@ -562,6 +597,32 @@ extern "C" mt_status_t mt_norm_backward_workspace_size(mt_norm_op_t op, int64_t 
 }
 
 extern "C" int mt_last_cuda_error(void) { return g_last_cuda_error; }
+
+#ifdef MT_TEST_HOOKS
+extern "C" void mt_test_fail_launch(int skip, int error) {
+    std::lock_guard<std::mutex> lock(g_hook_mu);
+    g_hook_skip = skip;
+    g_hook_err = (cudaError_t)error;
+}
+
+// 1 while an injected failure is still armed.
+extern "C" int mt_test_failure_armed(void) {
+    std::lock_guard<std::mutex> lock(g_hook_mu);
+    return g_hook_skip >= 0;
+}
+
+// Bytes in use in the memory pool stream-ordered allocations on `device` draw from.
+extern "C" int mt_test_pool_used_bytes(int device, unsigned long long *bytes) {
+    cudaMemPool_t pool;
+    cudaError_t e = cudaDeviceGetMemPool(&pool, device);
+    if (e == cudaSuccess) {
+        unsigned long long v = 0;  // the attribute is a 64-bit unsigned integer
+        e = cudaMemPoolGetAttribute(pool, cudaMemPoolAttrUsedMemCurrent, &v);
+        *bytes = (unsigned long long)v;
+    }
+    return (int)e;
+}
+#endif
 
 extern "C" const char *mt_status_string(mt_status_t status) {
     switch (status) {

@@ -235,6 +235,9 @@ struct LaunchPlan {
 
 // Host helpers defined in api.cu (cached per device; thread-safe).
 void record_cuda_error(cudaError_t e);  // what mt_last_cuda_error() reports on this thread
+// Called before every kernel launch: cudaSuccess, except in the test build (compiled with
+// MT_TEST_HOOKS), where an armed injected failure is returned instead of launching.
+cudaError_t launch_hook();
 // Launch p.kernel(*arg) on `stream` with the programmatic-stream-serialization attribute.
 cudaError_t launch_pdl(const LaunchPlan &p, void *arg, cudaStream_t stream);
 cudaError_t device_sm_count(int device, int *sms);

@@ -343,8 +343,10 @@ extern "C" mt_status_t mt_cross_entropy_forward(mt_dtype_t dtype, const void *lo
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         const float *cl = loss_rows;
-        e = cudaLaunchKernelEx(&cfg, ce_loss_reduce_kernel<B>, cl, targets, N, ignore_index,
-                               (int)reduction, loss_out, n_valid);
+        e = launch_hook();
+        if (e == cudaSuccess)
+            e = cudaLaunchKernelEx(&cfg, ce_loss_reduce_kernel<B>, cl, targets, N, ignore_index,
+                                   (int)reduction, loss_out, n_valid);
         if (e != cudaSuccess) return fail(e);
     }
     return MT_OK;

@@ -1,6 +1,6 @@
 """bench.py's reference arm on the host cores: `--impl reference` times the fp64 oracle
 on a bounded sample of the bench workload and prints one JSON line with the same metric,
-unit and workload as the GPU arm, plus its own cpu_baseline and e2e. Runs without a GPU;
+unit and workload description as the GPU arm, plus its own cpu_baseline and e2e. Runs without a GPU;
 this checks the line's contract, not the number."""
 import json
 import os
@@ -23,7 +23,11 @@ def test_reference_arm_line():
         assert k in d, k
     assert d["steps"] == 1 and d["warmup"] == 3 and d["higher_is_better"] is True
     assert d["value"] > 0 and d["unit"] == "GB/s"
-    assert d["config"]["workload"] == "rmsnorm_16384x4096"
+    sys.path.insert(0, ROOT)
+    import bench
+    # the GPU arm prints bench_config(workload, world): the same keys and values
+    assert d["config"] == bench.bench_config(bench.DEFAULT_WORKLOAD, 1)
+    assert d["config"]["workload"] == "add_rmsnorm_32768x4096"
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
     e = d["e2e"]

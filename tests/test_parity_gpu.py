@@ -60,6 +60,32 @@ def test_full_size_workloads(name):
     host = {k: v.cpu() for k, v in t.items()}
     ref = oracle_run(w.op, host, w.eps, rows=rows)
     compare(w.op, got, ref, host["X"], rows=rows, tag=name)
+    # The cotangents of these workloads are N(0, 0.01), so dX is about 1e-2 and the fixed
+    # atol of 2e-3 alone would be a loose bound; dX is also held relative to its largest
+    # magnitude: fp16 storage of dX costs 2^-11 of |dX| at most, the fp32 arithmetic far less.
+    sel = torch.as_tensor(rows, device=DEV)
+    err = np.abs(f64(got["dX"][sel]) - ref["dX"])
+    rel = float(err.max() / np.abs(ref["dX"]).max())
+    print(f"{name}: dX max|err|/max|ref| = {rel:.3e} (max|ref| {np.abs(ref['dX']).max():.3e})")
+    assert rel <= 2e-3, f"{name}: dX max|err|/max|ref| = {rel:.3e}"
+
+
+@pytest.mark.parametrize("N,D", [(1000, 4096), (300, 16384)])
+def test_layernorm_large_mean_fp16_strict(N, D):
+    """fp16 LayerNorm of rows with a large mean and unit spread (X = 50 + N(0,1), the
+    cancellation case of the 2048x16384 workload) under unit cotangents dY ~ N(0,1), so
+    that dX is O(1) and the fp16 tolerance is tight. Every element of Y, dX, mean and rstd
+    and every column of dgamma/dbeta is checked against the oracle. N is chosen so that
+    the persistent backward's CTAs each run several rows."""
+    t = W.generate(W.LAYERNORM, N, D, seed=29, x_kind="shifted", dy_std=1.0, beta_std=0.1)
+    got = gpu_run(W.LAYERNORM, to_dev(t), 1e-5)
+    torch.cuda.synchronize()
+    ref = oracle_run(W.LAYERNORM, t, 1e-5)
+    compare(W.LAYERNORM, got, ref, t["X"], tag=f"layernorm mean 50 fp16 {N}x{D}")
+    err = np.abs(f64(got["dX"]) - ref["dX"])
+    rel = float(err.max() / np.abs(ref["dX"]).max())
+    print(f"layernorm mean 50 {N}x{D}: dX max|err|/max|ref| = {rel:.3e}")
+    assert rel <= 2e-3
 
 
 def test_fused_without_residual_cotangent():

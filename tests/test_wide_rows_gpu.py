@@ -67,6 +67,25 @@ def test_wide_storage_types(op, combo, D):
     compare_ex(op, got, ref, t["X"], tag=f"{op} {N}x{D} {_name(combo)}")
 
 
+@pytest.mark.parametrize("D", [65544, 100000])
+@pytest.mark.parametrize("op", OPS)
+def test_wide_all_fp32_sixteen_cta_clusters(op, D):
+    """All-fp32 backwards of rows wider than 65536 columns take 16-CTA clusters of
+    8192-column slices. At these ragged widths the last slice is short (65544: slices of
+    4104 columns, the last 3984; 100000: 6256, the last 6160), and with 40 rows every
+    resident cluster runs several rows and sums them into its partial row. Every output
+    against the oracle, and a second run bit for bit."""
+    N = 40
+    t = _inputs(op, N, D, (F32, F32, F32), seed=5)
+    got = gpu_run_ex(op, t, 1e-5)
+    again = gpu_run_ex(op, t, 1e-5)
+    torch.cuda.synchronize()
+    ref = oracle_run(op, t, 1e-5, x_storage="f32")
+    compare_ex(op, got, ref, t["X"], tag=f"{op} {N}x{D} f32 16-CTA")
+    for k in got:
+        assert torch.equal(got[k].view(torch.int32), again[k].view(torch.int32)), k
+
+
 @pytest.mark.parametrize("op", OPS)
 def test_wide_many_rows(op):
     """More rows than resident clusters: every cluster of the persistent backward runs
