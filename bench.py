@@ -6,10 +6,14 @@ A step is one forward and one backward of the workload's op (every stage of the 
 row load, reduction, statistics, apply, backward row pass, dgamma/dbeta partials and
 their fixed-order reduction) on device-resident inputs. The metric is achieved HBM
 throughput: compulsory bytes (fp16 activations read and written once, fp32 stats and
-parameter gradients) divided by the CUDA-event time of the two calls, plus rows/s.
+parameter gradients) divided by the CUDA-event time of a step, plus rows/s.
 Steps run back to back with no flush: the forward of step s uses buffer set s % 2 and
 its backward set (s + 1) % 2, so no call finds in L2 the rows the previous call just
-touched, and each call pays for the write-backs the previous one left behind.
+touched, and each call pays for the write-backs the previous one left behind. Events
+mark only the start and the end of the K timed steps (an event between two calls would
+stop the second from being scheduled while the first drains, which a training loop
+does not do). Each call's own time (the roofline entries) comes from a separate loop of
+that call alone, back to back, timed the same way.
 
 One JSON line is printed by rank 0. Under torchrun (N > 1) every rank runs its own
 replica of the workload (weak scaling; the path has no cross-rank exchange in this
@@ -376,12 +380,14 @@ class CrossEntropyRunner:
                                           self.dx, stream)
 
 
-def time_ops(sets, steps: int, warmup: int, stream, on_enqueued=None):
-    """CUDA-event times (ms) of `steps` back-to-back steps, each a forward on buffer set
-    s % n and a backward on set (s + 1) % n: a backward never finds in L2 the rows its
-    step's forward just read, and the write-backs one call leaves in L2 are paid by the
-    next timed call. `on_enqueued` runs once every timed step is enqueued, while the GPU
-    works through them. Returns per-step forward and backward times and the total."""
+def time_steps(sets, steps: int, warmup: int, stream, on_enqueued=None) -> float:
+    """Mean CUDA-event time (ms) of one step over `steps` back-to-back steps. Step s runs
+    the forward on buffer set s % n and the backward on set (s + 1) % n, so no call finds
+    in L2 the rows the previous call touched and each call pays for the write-backs the
+    previous one left dirty. Events mark only the start and the end of the steps: an
+    event recorded between two kernels would keep the second from being scheduled while
+    the first drains (programmatic dependent launch), a gap no training loop has.
+    `on_enqueued` runs once every timed step is enqueued, while the GPU works on them."""
     import torch
     n = len(sets)
     for r in sets:
@@ -389,21 +395,47 @@ def time_ops(sets, steps: int, warmup: int, stream, on_enqueued=None):
     for s in range(warmup):
         sets[s % n].forward(stream)
         sets[(s + 1) % n].backward(stream)
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * steps + 1)]
+    a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
-    ev[0].record(stream)
+    a.record(stream)
     for s in range(steps):
         sets[s % n].forward(stream)
-        ev[2 * s + 1].record(stream)
         sets[(s + 1) % n].backward(stream)
-        ev[2 * s + 2].record(stream)
+    z.record(stream)
     if on_enqueued is not None:
         on_enqueued()
     torch.cuda.synchronize()
-    fwd = [ev[2 * s].elapsed_time(ev[2 * s + 1]) for s in range(steps)]
-    bwd = [ev[2 * s + 1].elapsed_time(ev[2 * s + 2]) for s in range(steps)]
-    total = ev[0].elapsed_time(ev[2 * steps])
-    return fwd, bwd, total
+    return a.elapsed_time(z) / steps
+
+
+def time_calls(sets, direction: str, calls: int, warmup: int, stream, chunks: int = 10) -> dict:
+    """Per-call CUDA-event time (ms) of one direction ("forward" or "backward") over
+    `calls` back-to-back calls alternating the buffer sets, in `chunks` runs with events
+    at their ends: the mean over all calls and each chunk's mean (the spread)."""
+    import torch
+    n = len(sets)
+    fn = [getattr(r, direction) for r in sets]
+    for i in range(warmup):
+        fn[i % n](stream)
+    per = max(1, calls // chunks)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(chunks + 1)]
+    torch.cuda.synchronize()
+    ev[0].record(stream)
+    for c in range(chunks):
+        for i in range(per):
+            fn[(c * per + i) % n](stream)
+        ev[c + 1].record(stream)
+    torch.cuda.synchronize()
+    ch = [ev[c].elapsed_time(ev[c + 1]) / per for c in range(chunks)]
+    return {"mean": ev[0].elapsed_time(ev[chunks]) / (per * chunks), "chunks": ch,
+            "calls": per * chunks}
+
+
+def time_ops(sets, steps: int, warmup: int, stream):
+    """Forward and backward per-call times (ms), each from its own back-to-back loop."""
+    calls = max(steps, 100)
+    return (time_calls(sets, "forward", calls, warmup, stream),
+            time_calls(sets, "backward", calls, warmup, stream))
 
 
 E2E_COPY_STREAMS = 1  # measured on GB300: 1, 2, 4, 8 streams per direction: 404, 391, 378, 283 GB/s
@@ -715,14 +747,14 @@ def row_op_line(name, device, steps, warmup, stream, peak):
     kind, N, D, tname = ROW_OPS[name]
     cls = SoftmaxRunner if kind == "softmax" else CrossEntropyRunner
     r2 = [cls(N, D, device, i, getattr(torch, tname)) for i in range(2)]
-    f2, b2, _ = time_ops(r2, steps, warmup, stream)
-    fg = r2[0].fwd_bytes / (statistics.mean(f2) * 1e-3) / 1e9
-    bg = r2[0].bwd_bytes / (statistics.mean(b2) * 1e-3) / 1e9
+    f2, b2 = time_ops(r2, steps, warmup, stream)
+    fg = r2[0].fwd_bytes / (f2["mean"] * 1e-3) / 1e9
+    bg = r2[0].bwd_bytes / (b2["mean"] * 1e-3) / 1e9
     return {"row_op": name, "forward_gbs": round(fg, 2), "backward_gbs": round(bg, 2),
             "forward_frac_of_measured": round(fg / peak, 4),
             "backward_frac_of_measured": round(bg / peak, 4),
-            "forward_us": round(1e3 * statistics.mean(f2), 3),
-            "backward_us": round(1e3 * statistics.mean(b2), 3),
+            "forward_us": round(1e3 * f2["mean"], 3),
+            "backward_us": round(1e3 * b2["mean"], 3),
             "compulsory_bytes": {"forward": r2[0].fwd_bytes, "backward": r2[0].bwd_bytes}}
 
 
@@ -764,18 +796,22 @@ def gemv_line(name, device, steps, warmup, stream, peak):
 
     for j in range(warmup):
         call(j)
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    # back-to-back calls in chunks, events only at the chunks' ends (see time_steps)
+    chunks, per = 10, max(1, max(steps, 100) // 10)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(chunks + 1)]
     torch.cuda.synchronize()
     ev[0].record(stream)
-    for j in range(steps):
-        call(j)
-        ev[j + 1].record(stream)
+    for c in range(chunks):
+        for j in range(per):
+            call(c * per + j)
+        ev[c + 1].record(stream)
     torch.cuda.synchronize()
-    ts = [ev[j].elapsed_time(ev[j + 1]) for j in range(steps)]
+    ts = [ev[c].elapsed_time(ev[c + 1]) / per for c in range(chunks)]
     nbytes = 2 * K * N + 2 * M * K + 2 * K * (2 if op == "layernorm" else 1) + 2 * M * N
-    ms = statistics.mean(ts)
+    ms = ev[0].elapsed_time(ev[chunks]) / (per * chunks)
     gbs = nbytes / (ms * 1e-3) / 1e9
-    return {"gemv": name, "us": round(1e3 * ms, 3), "us_median": round(1e3 * statistics.median(ts), 3),
+    return {"gemv": name, "us": round(1e3 * ms, 3), "us_chunk_min": round(1e3 * min(ts), 3),
+            "us_chunk_max": round(1e3 * max(ts), 3),
             "gbs": round(gbs, 2), "frac_of_measured": round(gbs / peak, 4),
             "compulsory_bytes": nbytes, "M": M, "K": K, "N": N,
             "gflops": round(2 * M * K * N / (ms * 1e-3) / 1e9, 1)}
@@ -844,31 +880,30 @@ def main(argv=None):
     barrier()
     with ClockSampler(device) as clocks:
         t0 = time.perf_counter()
-        fwd, bwd, total_ms = time_ops(sets, args.steps, args.warmup, stream,
-                                      on_enqueued=clocks.mark)
+        step_ms = time_steps(sets, args.steps, args.warmup, stream, on_enqueued=clocks.mark)
         barrier()
         wall = time.perf_counter() - t0
-    fwd_ms = statistics.mean(fwd)
-    bwd_ms = statistics.mean(bwd)
-    step_ms = total_ms / args.steps
     step_ms = max_over_ranks(step_ms, device)
+    # each call's own time, from back-to-back loops of that call alone
+    fwd, bwd = time_ops(sets, args.steps, args.warmup, stream)
+    fwd_ms, bwd_ms = fwd["mean"], bwd["mean"]
 
     step_bytes = runner.fwd_bytes + runner.bwd_bytes
     value = world * step_bytes / (step_ms * 1e-3) / 1e9
     rows_s = world * w.N / (step_ms * 1e-3)
 
-    def op_line(nbytes, times):
-        ms = statistics.mean(times)
+    def op_line(nbytes, t, rows):
+        ms = t["mean"]
         gbs = nbytes / (ms * 1e-3) / 1e9
-        q = sorted(times)
-        return {"us": round(1e3 * ms, 3), "us_median": round(1e3 * statistics.median(times), 3),
-                "us_p10": round(1e3 * q[len(q) // 10], 3),
-                "us_p90": round(1e3 * q[min(len(q) - 1, (9 * len(q)) // 10)], 3),
+        return {"us": round(1e3 * ms, 3),
+                "us_chunk_min": round(1e3 * min(t["chunks"]), 3),
+                "us_chunk_max": round(1e3 * max(t["chunks"]), 3), "calls": t["calls"],
                 "gbs": round(gbs, 2), "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
-                "frac_of_measured": round(gbs / peak, 4), "rows_per_s": round(w.N / (ms * 1e-3), 1),
+                "frac_of_measured": round(gbs / peak, 4), "rows_per_s": round(rows / (ms * 1e-3), 1),
                 "compulsory_bytes": nbytes}
 
-    ops = {"forward": op_line(runner.fwd_bytes, fwd), "backward": op_line(runner.bwd_bytes, bwd)}
+    ops = {"forward": op_line(runner.fwd_bytes, fwd, w.N),
+           "backward": op_line(runner.bwd_bytes, bwd, w.N)}
     dom = "backward" if bwd_ms >= fwd_ms else "forward"
     del runner, sets
     torch.cuda.empty_cache()
@@ -890,17 +925,11 @@ def main(argv=None):
             if name == args.workload:
                 continue
             r2 = [OpRunner(name, device, seed=i) for i in range(2)]
-            f2, b2, _ = time_ops(r2, max(50, args.steps // 10), args.warmup, stream)
+            f2, b2 = time_ops(r2, args.steps, args.warmup, stream)
             r2 = r2[0]
             w2 = r2.w
-            lines = {}
-            for d, nbytes, ts in (("forward", r2.fwd_bytes, f2), ("backward", r2.bwd_bytes, b2)):
-                ms = statistics.mean(ts)
-                gbs = nbytes / (ms * 1e-3) / 1e9
-                lines[d] = {"us": round(1e3 * ms, 3), "gbs": round(gbs, 2),
-                            "frac_of_measured": round(gbs / peak, 4),
-                            "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
-                            "rows_per_s": round(w2.N / (ms * 1e-3), 1), "compulsory_bytes": nbytes}
+            lines = {"forward": op_line(r2.fwd_bytes, f2, w2.N),
+                     "backward": op_line(r2.bwd_bytes, b2, w2.N)}
             others[name] = {"forward_gbs": lines["forward"]["gbs"],
                             "backward_gbs": lines["backward"]["gbs"],
                             "forward_us": lines["forward"]["us"],
@@ -915,16 +944,16 @@ def main(argv=None):
     if not args.no_others and rank == 0:
         for dname, tdt in (("bf16", torch.bfloat16), ("f32", torch.float32)):
             r2 = [OpRunner(args.workload, device, seed=i, dtype=tdt) for i in range(2)]
-            f2, b2, _ = time_ops(r2, max(50, args.steps // 10), args.warmup, stream)
+            f2, b2 = time_ops(r2, args.steps, args.warmup, stream)
             r2 = r2[0]
-            fg = r2.fwd_bytes / (statistics.mean(f2) * 1e-3) / 1e9
-            bg = r2.bwd_bytes / (statistics.mean(b2) * 1e-3) / 1e9
+            fg = r2.fwd_bytes / (f2["mean"] * 1e-3) / 1e9
+            bg = r2.bwd_bytes / (b2["mean"] * 1e-3) / 1e9
             dtypes[dname] = {
                 "forward_gbs": round(fg, 2), "backward_gbs": round(bg, 2),
                 "forward_frac_of_measured": round(fg / peak, 4),
                 "backward_frac_of_measured": round(bg / peak, 4),
-                "forward_us": round(1e3 * statistics.mean(f2), 3),
-                "backward_us": round(1e3 * statistics.mean(b2), 3),
+                "forward_us": round(1e3 * f2["mean"], 3),
+                "backward_us": round(1e3 * b2["mean"], 3),
                 "compulsory_bytes": {"forward": r2.fwd_bytes, "backward": r2.bwd_bytes}}
             del r2
             torch.cuda.empty_cache()
@@ -933,8 +962,7 @@ def main(argv=None):
     row_ops = {}
     if not args.no_others and rank == 0:
         for name in ROW_OPS:
-            row_ops[name] = row_op_line(name, device, max(50, args.steps // 10), args.warmup,
-                                        stream, peak)
+            row_ops[name] = row_op_line(name, device, args.steps, args.warmup, stream, peak)
             del row_ops[name]["row_op"]
             torch.cuda.empty_cache()
 
@@ -942,8 +970,7 @@ def main(argv=None):
     gemv = {}
     if not args.no_others and rank == 0:
         for name in GEMV_OPS:
-            gemv[name] = gemv_line(name, device, max(50, args.steps // 10), args.warmup, stream,
-                                   peak)
+            gemv[name] = gemv_line(name, device, args.steps, args.warmup, stream, peak)
             del gemv[name]["gemv"]
             torch.cuda.empty_cache()
 

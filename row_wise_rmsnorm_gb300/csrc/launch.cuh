@@ -44,6 +44,11 @@ namespace mt {
     X(8192, 256, 1, 4, true, 6)        \
     X(16384, 512, 1, 4, true, 3)
 #endif
+// LayerNorm rows of 8192 and 16384 columns: 256-thread row groups with the row packed in
+// registers and 5 / 4 resident CTAs per SM (back to back on GB300: LayerNorm 2048 x 16384
+// forward 26.5 -> 24.4 us against 512 threads with the row as fp32 pairs, where 5 CTAs per
+// SM or 1024-thread rows lost; 4096 x 8192 26.8 us with 512 threads and 4 CTAs, 23.8 us
+// with 6 CTAs, which spills, 23.9 us with 5).
 #ifndef MT_FWD_SHAPES_LAYER
 #define MT_FWD_SHAPES_LAYER(X)         \
     X(256, 32, 4, 1, false, 0)         \
@@ -51,8 +56,8 @@ namespace mt {
     X(1024, 32, 4, 4, false, 0)        \
     X(2048, 128, 1, 2, true, 16)       \
     X(4096, 64, 1, 8, true, 8)         \
-    X(8192, 512, 1, 2, true, 4)        \
-    X(16384, 512, 1, 4, false, 0)
+    X(8192, 256, 1, 4, true, 5)        \
+    X(16384, 256, 1, 8, true, 4)
 #endif
 #ifndef MT_FWD_SHAPES_FUSED
 #define MT_FWD_SHAPES_FUSED(X)         \

@@ -318,3 +318,4 @@ def test_fused_backward_both_readings_of_s():
     # S's rounding moves x by at most 2^-11 |s|; dX depends on x through r^2 c / D terms
     # and r * g * x_hat terms, so the readings differ by a small multiple of that
     assert np.all(err_exact <= 2e-3 + 2e-3 * np.abs(dX_exact) + 4 * gap), err_exact.max()
+
