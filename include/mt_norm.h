@@ -350,6 +350,20 @@ mt_status_t mt_norm_backward_workspace_size(mt_norm_op_t op, int64_t N, int64_t 
 /* cudaError_t value of the most recent MT_ERR_CUDA on the calling thread (0 if none). */
 int mt_last_cuda_error(void);
 
+/* The backward of a row split across a thread-block cluster (aligned rows wider than one
+ * CTA's slice) exchanges its CTAs' row sums through distributed shared memory, each CTA
+ * waiting on its own mbarrier for its peers' sums. Every such wait is bounded: one that
+ * has not completed after 200 ms of device time gives up, the kernel ORs an error bit
+ * into a status word of the device, skips the rows' remaining work and runs to its end,
+ * so that no wait can hang the GPU; the call's outputs are then incomplete.
+ * mt_device_wait_errors copies the word of CUDA device `device` to *flags (0: no wait has
+ * ever given up; MT_WAIT_ERR_CLUSTER: a split row's exchange did) and, when `clear` is
+ * non-zero, resets it. It synchronizes with the device (blocking copies). Errors:
+ * MT_ERR_INVALID_ARG for a NULL `flags` or a negative device, MT_ERR_CUDA if a CUDA call
+ * fails.                                                                            */
+#define MT_WAIT_ERR_CLUSTER 1u
+mt_status_t mt_device_wait_errors(int device, unsigned *flags, int clear);
+
 /* Static, human-readable name of a status code. */
 const char *mt_status_string(mt_status_t status);
 

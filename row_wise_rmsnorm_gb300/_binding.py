@@ -43,8 +43,9 @@ EXPORTED = (
     "mt_fused_rmsnorm_gemv", "mt_fused_layernorm_gemv",
     "mt_rmsnorm_backward_noalloc",
     "mt_norm_backward_workspace_size", "mt_last_cuda_error", "mt_status_string",
-    "mt_norm_version",
+    "mt_norm_version", "mt_device_wait_errors",
 )
+MT_WAIT_ERR_CLUSTER = 1
 MT_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -89,6 +90,7 @@ _SIGS = {
     "mt_norm_backward_workspace_size": [ctypes.c_int, _I64, _I64, ctypes.c_int,
                                         ctypes.POINTER(_SZ)],
     "mt_last_cuda_error": [],
+    "mt_device_wait_errors": [ctypes.c_int, ctypes.POINTER(ctypes.c_uint), ctypes.c_int],
     "mt_status_string": [ctypes.c_int],
     "mt_norm_version": [],
 }
@@ -270,6 +272,14 @@ def mt_norm_backward_workspace_size(op, N, D, device=0) -> int:
 
 def mt_last_cuda_error() -> int:
     return load().mt_last_cuda_error()
+
+
+def mt_device_wait_errors(device: int = 0, clear: bool = False) -> int:
+    """Error bits of the device's bounded waits (0: none has given up); see the header."""
+    v = ctypes.c_uint(0)
+    _check(load().mt_device_wait_errors(int(device), ctypes.byref(v), 1 if clear else 0),
+           "mt_device_wait_errors")
+    return v.value
 
 
 def mt_status_string(status: int) -> str:

@@ -189,6 +189,11 @@ mt_status_t run_backward(int op, BwdArgs a, bool vec8, float *dgamma, float *dbe
     } else if (ws_bytes < need) {
         return MT_ERR_UNSUPPORTED;
     }
+    if (p.waits && (e = device_status_word(device, &a.status)) != cudaSuccess) {
+        const mt_status_t fail = cuda_fail(e);
+        if (own_ws) cudaFreeAsync(workspace, stream);
+        return fail;
+    }
     float *part = static_cast<float *>(workspace);
     a.part_g = part;
     a.part_b = (op == kLayer) ? part + (size_t)prow * (size_t)a.D : nullptr;
@@ -232,6 +237,36 @@ mt_status_t run_backward(int op, BwdArgs a, bool vec8, float *dgamma, float *dbe
 }  // namespace
 
 void record_cuda_error(cudaError_t e) { g_last_cuda_error = (int)e; }
+
+}  // namespace mt
+
+// Error bits of the kernels' bounded waits (kErrClusterWait), one word per device that
+// loads the library; kernels receive its address (device_status_word) and OR bits in.
+static __device__ unsigned g_mt_device_status;
+
+namespace mt {
+
+cudaError_t device_status_word(int device, unsigned **word) {
+    static std::mutex mu;
+    static std::map<int, unsigned *> cache;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(device);
+    if (it != cache.end()) {
+        *word = it->second;
+        return cudaSuccess;
+    }
+    int cur = 0;
+    cudaError_t e = cudaGetDevice(&cur);
+    if (e != cudaSuccess) return e;
+    if (cur != device && (e = cudaSetDevice(device)) != cudaSuccess) return e;
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_mt_device_status);
+    if (cur != device) cudaSetDevice(cur);
+    if (e != cudaSuccess) return e;
+    cache[device] = static_cast<unsigned *>(p);
+    *word = static_cast<unsigned *>(p);
+    return cudaSuccess;
+}
 
 #ifdef MT_TEST_HOOKS
 // Test build only (-DMT_TEST_HOOKS, libmt_norm_hooks.so): host-side failure injection.
@@ -597,6 +632,20 @@ extern "C" mt_status_t mt_norm_backward_workspace_size(mt_norm_op_t op, int64_t 
 }
 
 extern "C" int mt_last_cuda_error(void) { return g_last_cuda_error; }
+
+extern "C" mt_status_t mt_device_wait_errors(int device, unsigned *flags, int clear) {
+    if (flags == nullptr || device < 0) return MT_ERR_INVALID_ARG;
+    unsigned *word = nullptr;
+    cudaError_t e = device_status_word(device, &word);
+    if (e != cudaSuccess) return cuda_fail(e);
+    int cur = 0;
+    if ((e = cudaGetDevice(&cur)) != cudaSuccess) return cuda_fail(e);
+    if (cur != device && (e = cudaSetDevice(device)) != cudaSuccess) return cuda_fail(e);
+    e = cudaMemcpy(flags, word, sizeof(unsigned), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && clear) e = cudaMemset(word, 0, sizeof(unsigned));
+    if (cur != device) cudaSetDevice(cur);
+    return e == cudaSuccess ? MT_OK : cuda_fail(e);
+}
 
 #ifdef MT_TEST_HOOKS
 extern "C" void mt_test_fail_launch(int skip, int error) {

@@ -74,6 +74,7 @@ struct BwdArgs {
     int D;
     int xdt, wdt, gdt;
     int slice;            // cluster-split kernels: columns per CTA (a multiple of 8)
+    unsigned *status;     // split rows: error bits of bounded waits (device memory)
 };
 
 // ------------------------------------------------------------------ helpers ---
@@ -192,6 +193,148 @@ __device__ __forceinline__ void cluster_ln_stats(float (&v)[2], float *xch, int 
     const float dev = nr > 0.f ? sr / nr - mu : 0.f;
     v[0] = mu;
     v[1] = warp_sum(m2r + nr * dev * dev);
+}
+
+// ------------------------------------------------------ push exchange ---
+// The pipelined backward of a split row exchanges its CTAs' row sums by pushing them
+// instead of meeting at the cluster barrier: after its CTA-level reduction, thread 0 of
+// every CTA writes the CTA's totals (two floats) into its slot of each peer's buffer with
+// st.async, an asynchronous store into distributed shared memory that completes 8 bytes
+// of transactions on the peer's mbarrier, and arrives on its own mbarrier expecting
+// (cn - 1) * 8 bytes. Each CTA waits only on its own mbarrier until its peers' totals are
+// in, and adds the cn totals in rank order (every CTA the same operands in the same
+// order: the same bits). A CTA waits for data, not for its peers to reach a barrier, and
+// no store is fenced.
+// Two buffers alternate by row. A CTA pushes row j + 2 into the buffer of row j only
+// after receiving every peer's row j + 1 totals, which each peer pushed after all its
+// threads had passed the row j wait and read the row j buffer (a CTA barrier lies
+// between), so a buffer is never overwritten before it is read and no transaction of
+// row j + 2 can land in the phase of row j.
+//
+// Every wait is bounded (kWaitLimitNs of global time): a wait that gives up ORs
+// kErrClusterWait into the launch's status word (read on the host with
+// mt_device_wait_errors), and the thread skips its remaining waits; the kernel runs to
+// its end, so no wait can hang the GPU.
+constexpr unsigned kErrClusterWait = 1u;
+constexpr unsigned long long kWaitLimitNs = 200ull * 1000ull * 1000ull;  // 200 ms
+constexpr int kMaxPushCluster = 16;
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+
+// Makes this thread's mbarrier initialisations visible across the cluster.
+__device__ __forceinline__ void mbar_init_fence() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Arrive on this CTA's mbarrier and add `bytes` to the phase's expected transactions.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// True once the phase with parity `parity` of the local mbarrier has completed (acquire at
+// cluster scope).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, unsigned parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// mbar_try_wait_cluster until it succeeds or kWaitLimitNs have passed (then false).
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t *bar, unsigned parity) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait_cluster(bar, parity))
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    return true;
+}
+
+// The shared::cluster address of `local`'s counterpart in the CTA of cluster rank r.
+__device__ __forceinline__ uint32_t cluster_map(const void *local, unsigned r) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)), "r"(r));
+    return remote;
+}
+
+// Store two floats at `addr` (another CTA's shared memory, 8-byte aligned), completing 8
+// bytes of transactions on that CTA's mbarrier at `bar`.
+__device__ __forceinline__ void st_async_f2(uint32_t addr, float x, float y, uint32_t bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];"
+        ::"r"(addr), "f"(x), "f"(y), "r"(bar)
+        : "memory");
+}
+
+struct PushExchange {
+    uint64_t bar[2];                           // one per row buffer
+    __align__(8) float in[2][kMaxPushCluster][2];  // [buffer][rank of the sender][value]
+};
+
+// The exchange state of this CTA (static shared memory of the kernels that call it only).
+__device__ __forceinline__ PushExchange &push_exchange() {
+    __shared__ __align__(8) PushExchange px;
+    return px;
+}
+
+// Thread 0 initialises the exchange; every thread of every CTA of the cluster must then
+// pass one cluster barrier before the first push (cluster_push_init does both).
+__device__ __forceinline__ void cluster_push_init(PushExchange &px) {
+    if (threadIdx.x == 0) {
+        mbar_init(&px.bar[0], 1);
+        mbar_init(&px.bar[1], 1);
+        mbar_init_fence();
+    }
+    cluster_arrive();
+    cluster_wait();
+}
+
+// Cluster-wide sum of the NV (1 or 2) per-CTA totals in v (bitwise identical in every
+// thread of the CTA) for the cluster's j-th row. Every thread of every CTA of the cluster
+// calls it once per row, and between two calls every thread of the CTA passes a CTA
+// barrier. `live`: this thread's waits have not given up so far; returns false if this
+// wait gave up (the totals are then incomplete).
+template <int NV>
+__device__ __forceinline__ bool cluster_push_sum(float (&v)[NV], PushExchange &px, int j,
+                                                 unsigned cn, unsigned rank, bool live) {
+    static_assert(NV == 1 || NV == 2, "one or two values per row");
+    const int buf = j & 1;
+    if (threadIdx.x == 0) {
+        const float y = (NV == 2) ? v[NV - 1] : 0.f;
+        for (unsigned r = 0; r < cn; ++r) {
+            if (r == rank) continue;
+            st_async_f2(cluster_map(&px.in[buf][rank][0], r), v[0], y,
+                        cluster_map(&px.bar[buf], r));
+        }
+        mbar_arrive_expect_tx(&px.bar[buf], (cn - 1) * 8u);
+    }
+    const bool ok = live && mbar_wait_cluster_bounded(&px.bar[buf], (unsigned)(j >> 1) & 1u);
+    float t[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) t[i] = 0.f;
+    for (unsigned r = 0; r < cn; ++r)
+#pragma unroll
+        for (int i = 0; i < NV; ++i) t[i] += (r == rank) ? v[i] : px.in[buf][r][i];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) v[i] = t[i];
+    return ok;
 }
 
 // This CTA's column window and row owner. Not split: columns [0, D) and the plain CTA

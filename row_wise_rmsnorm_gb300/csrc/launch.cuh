@@ -238,6 +238,7 @@ struct LaunchPlan {
     int rows_per_cta = 0;
     int cluster = 1;    // CTAs per cluster (> 1: a row split across the cluster)
     int slice = 0;      // columns per CTA of a split row
+    bool waits = false; // the kernel has bounded waits: pass it the device status word
     // Row owners of a backward, one dgamma/dbeta partial row each.
     int owners() const { return grid / cluster; }
 };
@@ -255,6 +256,8 @@ cudaError_t cached_occupancy(const void *kernel, int threads, size_t smem, int d
 // Clusters of `cluster` CTAs that can be resident at once (cached per kernel and shape).
 cudaError_t cached_cluster_occupancy(const void *kernel, int threads, size_t smem, int cluster,
                                      int device, int *clusters);
+// Address of the device's status word: the error bits of bounded waits (cached per device).
+cudaError_t device_status_word(int device, unsigned **word);
 
 // Persistent grid: as many CTAs as fit on the device at once, at most one per row slot.
 inline cudaError_t persistent_grid(LaunchPlan *p, int64_t N, int device) {
@@ -428,6 +431,7 @@ cudaError_t bwd_pipe_shape(int64_t N, int device, LaunchPlan *p) {
         p->threads = TPR * RPC;
         p->smem = R::kBytes;
         p->rows_per_cta = RPC;
+        p->waits = CLU;  // the split row's push exchange
         if constexpr (CLU) return persistent_cluster_grid(p, N, device);
         return persistent_grid(p, N, device);
     }

@@ -4,8 +4,9 @@
 // of the next STAGES-1 rows into a shared-memory ring with cp.async (L2 only, no L1
 // allocation), then reads them back for the current row. A thread only ever reads what
 // it copied itself, so cp.async.wait_group alone orders the ring: no mbarrier, no
-// cross-thread or cross-CTA wait. Bytes in flight per SM are set by the ring depth
-// (STAGES x streamed arrays x row slice), not by registers.
+// cross-thread wait. Bytes in flight per SM are set by the ring depth (STAGES x streamed
+// arrays x row slice), not by registers. A row split across a cluster exchanges its CTAs'
+// row sums by the bounded push exchange of kernels.cuh.
 //
 // Ownership. Row assignment is static: CTA b runs row slots b*RPC + j*G*RPC
 // (G = gridDim.x, j = 0, 1, ...), row group rg taking slot + rg. Thread t of a row group
@@ -123,17 +124,22 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
     using R = Ring<STAGES, CK, THREADS, G::UX, G::UG, HAS_DS, G::UW, KEEP ? 0 : 1>;
     static_assert(TPR % 32 == 0 && THREADS <= 1024, "bad launch shape");
     static_assert(!CLU || RPC == 1, "a split row is one row group per CTA");
+    // (the push exchange relies on the CTA barrier inside row_sum: TPR > 32)
+    static_assert(!CLU || TPR > 32, "a split row's row group spans several warps");
     __shared__ float red[2 * RPC * WPR * NV];
-    __shared__ float xch[CLU ? 2 * NV : 1];
     extern __shared__ __align__(16) uint4 ring[];
-
-    pdl_enter();  // the dependent parameter reduction launches now and waits for this grid
 
     const int tid = threadIdx.x;
     const int rg = tid / TPR, t = tid % TPR, wir = t / 32, lane = tid % 32;
     const int D = a.D;
     const float inv_d = 1.0f / (float)D;
     const Window<CLU> win(D, a.slice);
+    const unsigned rank = CLU ? cluster_rank() : 0u;
+    if constexpr (CLU) cluster_push_init(push_exchange());
+    bool live = true;  // split rows: no wait of this thread has given up
+
+    pdl_enter();  // the dependent parameter reduction launches now and waits for this grid
+
     const int64_t owner = win.owner(), owners = win.owners();
     const int64_t stride = owners * RPC;
     const int64_t first = owner * RPC + rg;
@@ -252,10 +258,15 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
         vv[0] = v0.x + v0.y;
         if constexpr (OP == kLayer) vv[NV - 1] = v1.x + v1.y;
         row_sum<TPR, RPC, NV, true>(vv, red, buf, rg, wir, lane);
-        if constexpr (CLU) cluster_sum<NV>(vv, xch, buf, win.cn);
+        if constexpr (CLU) {
+            if (!cluster_push_sum<NV>(vv, push_exchange(), j, win.cn, rank, live) && live) {
+                atomicOr(a.status, kErrClusterWait);
+                live = false;
+            }
+        }
         const float c = r * vv[0] * inv_d;                           // mean_j g*xhat
         const float am = (OP == kLayer) ? vv[NV - 1] * inv_d : 0.f;  // mean_j g
-        if (!ok) continue;
+        if (!ok || !live) continue;
 
         // pass 2: dX = r*g - r*a - (r*c)*xhat (+ dS), xhat = (x - mean)*r, and the
         // parameter-gradient sums dgamma += dY*xhat, dbeta += dY
@@ -291,7 +302,9 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
         }
     }
     cp_async_wait<0>();
-    if constexpr (CLU) cluster_arrive();  // done reading the other CTAs' slots
+    // split rows: this CTA's pushes are issued; no CTA leaves before the cluster's last
+    // pushes into its buffers have landed (waited for below, after the partial rows)
+    if constexpr (CLU) cluster_arrive();
 
     // Partials: the CTA's row groups are combined in the fixed order rg = 0, 1, ... and
     // one fp32 partial row per row owner (CTA, or cluster) is written.
@@ -315,7 +328,7 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
                                         accb[k][2 * q + 1].y);
             }
         }
-        if constexpr (CLU) cluster_wait();  // no CTA leaves while another may read its slots
+        if constexpr (CLU) cluster_wait();
     } else {
         __syncthreads();  // every thread is done with the ring
         float2 *cg2 = reinterpret_cast<float2 *>(ring);

@@ -16,7 +16,7 @@ NAMES = ["MT_OK", "MT_ERR_INVALID_ARG", "MT_ERR_UNSUPPORTED", "MT_ERR_CUDA",
          "MT_DTYPE_F16", "MT_DTYPE_BF16", "MT_DTYPE_F32",
          "MT_REDUCTION_NONE", "MT_REDUCTION_SUM", "MT_REDUCTION_MEAN",
          "MT_MAX_COLS", "MT_MAX_SOFTMAX_COLS", "MT_MAX_CE_COLS",
-         "MT_MAX_GEMV_ROWS", "MT_MAX_GEMV_K", "MT_NOALLOC_SCRATCH_BYTES"]
+         "MT_MAX_GEMV_ROWS", "MT_MAX_GEMV_K", "MT_NOALLOC_SCRATCH_BYTES", "MT_WAIT_ERR_CLUSTER"]
 
 
 def test_header_constants_match_binding(tmp_path):

@@ -86,6 +86,24 @@ def test_wide_all_fp32_sixteen_cta_clusters(op, D):
         assert torch.equal(got[k].view(torch.int32), again[k].view(torch.int32)), k
 
 
+def test_split_row_exchange_waits_never_give_up():
+    """The split-row backward exchanges row sums by pushing them into the peers' shared
+    memory and waiting, bounded, on the CTA's own mbarrier. Over every cluster size (2, 4,
+    8 and the all-fp32 16) and many rows per cluster, the outputs match the oracle and the
+    device's wait-error word stays 0."""
+    mt.mt_device_wait_errors(0, clear=True)
+    for op, N, D, combo in [(W.RMSNORM, 200, 24576, (F16, F16, F16)),
+                            (W.LAYERNORM, 120, 65536, (BF16, BF16, BF16)),
+                            (W.ADD_RMSNORM, 60, 131072, (F16, F16, F16)),
+                            (W.LAYERNORM, 40, 131072, (F32, F32, F32))]:
+        t = _inputs(op, N, D, combo, seed=9)
+        got = gpu_run_ex(op, t, 1e-5)
+        torch.cuda.synchronize()
+        ref = oracle_run(op, t, 1e-5, x_storage=STORAGE[combo[0]])
+        compare_ex(op, got, ref, t["X"], tag=f"{op} {N}x{D} {_name(combo)} exchange")
+    assert mt.mt_device_wait_errors(0) == 0
+
+
 @pytest.mark.parametrize("op", OPS)
 def test_wide_many_rows(op):
     """More rows than resident clusters: every cluster of the persistent backward runs
