@@ -329,7 +329,12 @@ mt_status_t mt_fused_layernorm_gemv(const void *X, const void *gamma, const void
  * between calls, but calls that overlap on the GPU race on it and must not be made.
  * A shape whose dgamma partials (one fp32 row of D per persistent CTA, or per cluster
  * of a split row) exceed MT_NOALLOC_SCRATCH_BYTES returns MT_ERR_UNSUPPORTED and
- * launches nothing; every shape up to MT_MAX_COLS columns fits on a 152-SM GB300.    */
+ * launches nothing; on a 152-SM GB300 every shape up to MT_MAX_COLS columns fits (the
+ * largest need is about 10 MB: rows of 16383 columns on the scalar kernel, one partial row
+ * per SM, and split rows of up to 131072 columns, one per cluster).
+ * A device reset (cudaDeviceReset) unloads the library's device code, so the cached
+ * address no longer names the array: after a reset of a device, this entry point must not
+ * be called on it again in the same process.                                         */
 #define MT_NOALLOC_SCRATCH_BYTES (16u << 20)
 
 mt_status_t mt_rmsnorm_backward_noalloc(const void *X, const void *gamma, const void *dY,
