@@ -579,17 +579,29 @@ __device__ __forceinline__ MaxSum block_maxsum(MaxSum st, float *sm_m, float *sm
     return tot;
 }
 
-template <int TPR, bool VEC8, int XT, bool LOG, int UN, int MINB>
+// CIT > 0 (aligned rows): the first CIT batches of UN chunks a thread loads in the first
+// pass are also kept in shared memory (CIT * UN * TPR 16-byte units per chunk unit, the
+// dynamic shared memory of the launch), and the second pass takes them from there: only
+// the rest of the row, the part read last, is read again from global memory, where it is
+// the most likely to still be in L2. The shared memory also leaves one CTA per SM, so
+// fewer rows are between their two passes at a time.
+template <int TPR, bool VEC8, int XT, bool LOG, int UN, int MINB, int CIT = 0>
 __global__ void __launch_bounds__(TPR, MINB)
 softmax_stream_fwd_kernel(const SoftmaxArgs a) {
     pdl_enter();
     constexpr int W = TPR / 32;
     static_assert(W <= 32 && (W & (W - 1)) == 0, "warps per row: a power of two up to 32");
+    static_assert(CIT == 0 || VEC8, "the row cache holds aligned chunks");
     __shared__ float sm_m[W], sm_s[W];
+    extern __shared__ __align__(16) uint4 xcache[];  // [CIT][UN][CU][TPR]
     const int t = threadIdx.x;
     const int64_t row = blockIdx.x;
     const int D = a.D;
     const int64_t off = row * (int64_t)D;
+    constexpr int CU0 = VEC8 ? chunk_units<XT>() : 1;
+    auto cache_at = [&](int it, int u, int q) -> uint4 & {
+        return xcache[((it * UN + u) * CU0 + q) * TPR + t];
+    };
 
     MaxSum st{-INFINITY, 0.f};
     if constexpr (VEC8) {
@@ -597,7 +609,13 @@ softmax_stream_fwd_kernel(const SoftmaxArgs a) {
         const float2 l2e = make_float2(kLog2e, kLog2e);
         uint4 raw[UN][CU];
         ce_load_raw<TPR, XT, UN, kReadOnly>(a.X, off, t, D, raw);
-        for (int c0 = t;;) {
+        for (int c0 = t, it = 0;; ++it) {
+            if (it < CIT) {
+#pragma unroll
+                for (int u = 0; u < UN; ++u)
+#pragma unroll
+                    for (int q = 0; q < CU; ++q) cache_at(it, u, q) = raw[u][q];
+            }
             float bm = chunk_max<XT>(raw[0]);
 #pragma unroll
             for (int u = 1; u < UN; ++u) bm = fmaxf(bm, chunk_max<XT>(raw[u]));
@@ -635,9 +653,16 @@ softmax_stream_fwd_kernel(const SoftmaxArgs a) {
         const float2 nl2 = make_float2(-lse * kLog2e, -lse * kLog2e);
         const float2 nlse = make_float2(-lse, -lse);
         constexpr int CU = chunk_units<XT>();
-        for (int c0 = t; c0 * 8 < D; c0 += UN * TPR) {
+        for (int c0 = t, it = 0; c0 * 8 < D; c0 += UN * TPR, ++it) {
             uint4 raw[UN][CU];
-            ce_load_raw<TPR, XT, UN>(a.X, off, c0, D, raw);
+            if (it < CIT) {
+#pragma unroll
+                for (int u = 0; u < UN; ++u)
+#pragma unroll
+                    for (int q = 0; q < CU; ++q) raw[u][q] = cache_at(it, u, q);
+            } else {
+                ce_load_raw<TPR, XT, UN>(a.X, off, c0, D, raw);
+            }
 #pragma unroll
             for (int u = 0; u < UN; ++u) {
                 const int c = c0 + u * TPR;

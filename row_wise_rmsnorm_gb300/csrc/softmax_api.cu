@@ -31,11 +31,14 @@ namespace {
 // 128 threads 60.4 / 105.8); 512 x 131072 bf16 forward 56.5 at 2 chunks, 62.5 at 4;
 // 256 x 262144 fp16 forward 58.1 - 61.5 at 4 chunks, 61.5 at 2, 63.0 at 512 threads;
 // floors of 2 or 4 resident CTAs per SM did not help.
+// The forward's entries add CIT, the batches of UN chunks per thread kept in shared memory
+// between the passes (softmax_stream_fwd_kernel; 0: none): rows wider than 131072 keep
+// their first 3 of 8 batches (192 KB of an fp16 row), one CTA per SM.
 #ifndef MT_SOFTMAX_SHAPES_STREAM_FWD
 #define MT_SOFTMAX_SHAPES_STREAM_FWD(X) \
-    X(65536, 512, 4, 1)                 \
-    X(131072, 1024, 2, 1)               \
-    X(MT_MAX_SOFTMAX_COLS, 1024, 4, 1)
+    X(65536, 512, 4, 1, 0)              \
+    X(131072, 1024, 2, 1, 0)            \
+    X(MT_MAX_SOFTMAX_COLS, 1024, 4, 1, 3)
 #endif
 // Backward of rows wider than 65536: split over a thread-block cluster of CL = 2, 4 or 8
 // CTAs (the smallest power of two whose slices of ceil(D / CL) columns fit the cap),
@@ -158,21 +161,37 @@ cudaError_t softmax_plan_stream(int64_t N, int D, LaunchPlan *p) {
     }
 #define MT_TRY(maxd, tpr, un, minb)                                                                 \
     if (D <= maxd) {                                                                                \
-        if constexpr (BWD)                                                                          \
-            p->kernel = reinterpret_cast<const void *>(&softmax_stream_bwd_kernel<tpr, VEC8, XT, LOG, stream_un(XT, un), minb>); \
-        else                                                                                        \
-            p->kernel = reinterpret_cast<const void *>(&softmax_stream_fwd_kernel<tpr, VEC8, XT, LOG, stream_un(XT, un), minb>); \
+        p->kernel = reinterpret_cast<const void *>(&softmax_stream_bwd_kernel<tpr, VEC8, XT, LOG, stream_un(XT, un), minb>); \
         p->threads = tpr;                                                                           \
         p->grid = (int)N;                                                                           \
         p->rows_per_cta = 1;                                                                        \
         return cudaSuccess;                                                                         \
     }
+#define MT_TRY_F(maxd, tpr, un, minb, cit)                                                          \
+    if (D <= maxd) {                                                                                \
+        constexpr int cu = VEC8 ? chunk_units<XT>() : 1;                                            \
+        constexpr int c = VEC8 ? cit : 0;                                                           \
+        p->kernel = reinterpret_cast<const void *>(                                                 \
+            &softmax_stream_fwd_kernel<tpr, VEC8, XT, LOG, stream_un(XT, un), minb, c>);            \
+        p->threads = tpr;                                                                           \
+        p->grid = (int)N;                                                                           \
+        p->rows_per_cta = 1;                                                                        \
+        p->smem = (size_t)c * stream_un(XT, un) * cu * tpr * 16;                                    \
+        if (p->smem > 0) {                                                                          \
+            int device = 0, per_sm = 0;                                                             \
+            cudaError_t e = cudaGetDevice(&device);                                                 \
+            if (e == cudaSuccess) e = cached_occupancy(p->kernel, tpr, p->smem, device, &per_sm);   \
+            return e;                                                                               \
+        }                                                                                           \
+        return cudaSuccess;                                                                         \
+    }
     if constexpr (BWD) {
         MT_SOFTMAX_SHAPES_STREAM_BWD(MT_TRY)
     } else {
-        MT_SOFTMAX_SHAPES_STREAM_FWD(MT_TRY)
+        MT_SOFTMAX_SHAPES_STREAM_FWD(MT_TRY_F)
     }
 #undef MT_TRY
+#undef MT_TRY_F
     return cudaErrorInvalidValue;
 }
 
