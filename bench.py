@@ -58,7 +58,7 @@ KERNELS = {
     ("rmsnorm_16384x4096", "backward"): ["norm_bwd_pipe_kernel", "param_reduce_kernel"],
     ("add_rmsnorm_32768x4096", "forward"): ["norm_fwd_vec8_kernel"],
     ("add_rmsnorm_32768x4096", "backward"): ["norm_bwd_pipe_kernel", "param_reduce_kernel"],
-    ("layernorm_2048x16384", "forward"): ["norm_fwd_vec8_kernel"],
+    ("layernorm_2048x16384", "forward"): ["norm_fwd_packed_kernel"],
     ("layernorm_2048x16384", "backward"): ["norm_bwd_pipe_kernel", "param_reduce_kernel"],
     ("rmsnorm_4096x32768", "forward"): ["norm_fwd_stream_kernel"],
     ("rmsnorm_4096x32768", "backward"): ["norm_bwd_pipe_kernel (2-CTA clusters)",

@@ -102,6 +102,35 @@ __device__ __forceinline__ void pdl_enter() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// L2 warm-up, issued before pdl_enter(): a CTA that becomes resident while the previous
+// kernel in the stream is still finishing asks L2 for the first bytes it will read, so
+// that DRAM works during that kernel's tail instead of idling. prefetch.global.L2 returns
+// no data to the thread. Global memory is coherent at L2, so a line fetched here that the
+// previous kernel then writes holds the written bytes when the loads after the wait read
+// it: the prefetch changes timing only. Threads t = 0 .. n-1 cover the 128-byte lines of
+// the n_elem elements at p.
+template <typename T>
+__device__ __forceinline__ void prefetch_l2(const T *p, int n_elem, int t, int n) {
+    const char *c = reinterpret_cast<const char *>(p);
+    const int64_t bytes = (int64_t)n_elem * (int64_t)sizeof(T);
+    for (int64_t b = (int64_t)t * 128; b < bytes; b += (int64_t)n * 128)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(c + b));
+}
+// The same for the row-in-registers forwards, with a trip count known at compile time:
+// a row group of TPR threads whose threads own CH 8-element chunks each spans at most
+// CH*8*sizeof(T)*TPR bytes, so thread t asks for lines t, t + TPR, ... of the row at p.
+template <int TPR, int CH, typename T>
+__device__ __forceinline__ void prefetch_l2_row(const T *p, int D, int t) {
+    constexpr int kLines = (CH * 8 * (int)sizeof(T) + 127) / 128;  // per thread
+    const char *c = reinterpret_cast<const char *>(p);
+    const int bytes = D * (int)sizeof(T);
+#pragma unroll
+    for (int i = 0; i < kLines; ++i) {
+        const int b = (i * TPR + t) * 128;
+        if (b < bytes) asm volatile("prefetch.global.L2 [%0];" ::"l"(c + b));
+    }
+}
+
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return (uint32_t)__cvta_generic_to_shared(p);
 }
@@ -497,7 +526,6 @@ norm_fwd_kernel(const FwdArgs a) {
 template <int OP, int TPR, int RPC, int CH, int MINB, int XT, int WT>
 __global__ void __launch_bounds__(TPR * RPC, MINB)
 norm_fwd_vec8_kernel(const FwdArgs a) {
-    pdl_enter();
     static_assert(TPR % 32 == 0 && TPR * RPC <= 1024, "bad launch shape");
     constexpr int WPR = TPR / 32;
     __shared__ float red[2 * RPC * WPR];
@@ -508,6 +536,12 @@ norm_fwd_vec8_kernel(const FwdArgs a) {
     const float inv_d = 1.0f / (float)D;
     const int64_t row = (int64_t)blockIdx.x * RPC + rg;
     const bool ok = row < a.N;
+    // (not at 16 CTAs of 128 threads: in 32 registers a thread its addresses spill)
+    if (ok && MINB * TPR * RPC < 2048) {
+        prefetch_l2_row<TPR, CH>(as<XT>(a.X) + row * (int64_t)D, D, t);
+        if constexpr (OP == kAddRms) prefetch_l2_row<TPR, CH>(as<XT>(a.R) + row * (int64_t)D, D, t);
+    }
+    pdl_enter();
     if (WPR == 1 && !ok) return;  // no CTA barrier in a single-warp row group
     const int64_t off = (ok ? row : 0) * (int64_t)D;
 
@@ -585,7 +619,6 @@ norm_fwd_vec8_kernel(const FwdArgs a) {
 template <int OP, int TPR, int RPC, int CH, int MINB, int XT, int WT>
 __global__ void __launch_bounds__(TPR * RPC, MINB)
 norm_fwd_packed_kernel(const FwdArgs a) {
-    pdl_enter();
     static_assert(TPR % 32 == 0 && TPR * RPC <= 1024, "bad launch shape");
     static_assert(OP == kRms || OP == kLayer, "the fused op keeps its fp32 sum");
     static_assert(XT == kF16 || XT == kBF16, "2-byte activations only");
@@ -599,6 +632,8 @@ norm_fwd_packed_kernel(const FwdArgs a) {
     const float inv_d = 1.0f / (float)D;
     const int64_t row = (int64_t)blockIdx.x * RPC + rg;
     const bool ok = row < a.N;
+    if (ok) prefetch_l2_row<TPR, CH>(X + row * (int64_t)D, D, t);
+    pdl_enter();
     if (WPR == 1 && !ok) return;  // no CTA barrier in a single-warp row group
     const int64_t off = (ok ? row : 0) * (int64_t)D;
 
@@ -709,7 +744,6 @@ __host__ __device__ constexpr int stream_un(int xt, int un) { return xt == kF32 
 template <int OP, int TPR, int UN, int MINB, int XT, int WT>
 __global__ void __launch_bounds__(TPR, MINB)
 norm_fwd_stream_kernel(const FwdArgs a) {
-    pdl_enter();
     static_assert(TPR % 32 == 0 && TPR <= 1024, "bad launch shape");
     constexpr int WPR = TPR / 32;
     __shared__ float red[2 * WPR];
@@ -718,6 +752,9 @@ norm_fwd_stream_kernel(const FwdArgs a) {
     const float inv_d = 1.0f / (float)D;
     const int64_t row = blockIdx.x;
     const int64_t off = row * (int64_t)D;
+    prefetch_l2(as<XT>(a.X) + off, min(D, UN * TPR * 8), t, TPR);  // pass 1's first batch
+    if constexpr (OP == kAddRms) prefetch_l2(as<XT>(a.R) + off, min(D, UN * TPR * 8), t, TPR);
+    pdl_enter();
 
     auto load = [&](int c0, float2 (&x)[UN][4], auto hint, bool keep_s) {
         constexpr int H = decltype(hint)::value;

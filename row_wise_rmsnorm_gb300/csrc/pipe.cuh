@@ -138,12 +138,23 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
     if constexpr (CLU) cluster_push_init(push_exchange());
     bool live = true;  // split rows: no wait of this thread has given up
 
-    pdl_enter();  // the dependent parameter reduction launches now and waits for this grid
-
     const int64_t owner = win.owner(), owners = win.owners();
     const int64_t stride = owners * RPC;
     const int64_t first = owner * RPC + rg;
     const int iters = owner_iterations(a.N, RPC, owner, owners);
+    // L2 warm-up of the rows the ring is first filled with (kernels.cuh, prefetch_l2)
+#pragma unroll
+    for (int j = 0; j < STAGES - 1; ++j) {
+        const int64_t row = first + (int64_t)j * stride;
+        if (j < iters && row < a.N) {
+            const int64_t off = row * (int64_t)D + win.beg;
+            prefetch_l2(as<XT>(a.X) + off, win.end - win.beg, t, TPR);
+            prefetch_l2(as<GT>(a.dY) + off, win.end - win.beg, t, TPR);
+            if constexpr (HAS_DS) prefetch_l2(as<GT>(a.dS) + off, win.end - win.beg, t, TPR);
+        }
+    }
+
+    pdl_enter();  // the dependent parameter reduction launches now and waits for this grid
 
     float2 gam[KEEP ? CK : 1][PPC];
     if constexpr (KEEP) {

@@ -85,7 +85,6 @@ __device__ __forceinline__ float row_max(float v, float *red, int buf, int rg, i
 template <int TPR, int RPC, int CH, bool LOG, int XT>
 __global__ void __launch_bounds__(TPR * RPC)
 softmax_fwd_vec8_kernel(const SoftmaxArgs a) {
-    pdl_enter();
     constexpr int WPR = TPR / 32;
     __shared__ float red[2 * RPC * WPR];
     const int tid = threadIdx.x;
@@ -93,6 +92,8 @@ softmax_fwd_vec8_kernel(const SoftmaxArgs a) {
     const int D = a.D;
     const int64_t row = (int64_t)blockIdx.x * RPC + rg;
     const bool ok = row < a.N;
+    if (ok) prefetch_l2_row<TPR, CH>(as<XT>(a.X) + row * (int64_t)D, D, t);
+    pdl_enter();
     if (WPR == 1 && !ok) return;
     const int64_t off = (ok ? row : 0) * (int64_t)D;
 
@@ -141,7 +142,6 @@ softmax_fwd_vec8_kernel(const SoftmaxArgs a) {
 template <int TPR, int RPC, int CH, bool LOG, int XT>
 __global__ void __launch_bounds__(TPR * RPC)
 softmax_bwd_vec8_kernel(const SoftmaxArgs a) {
-    pdl_enter();
     constexpr int WPR = TPR / 32;
     __shared__ float red[2 * RPC * WPR];
     const int tid = threadIdx.x;
@@ -149,6 +149,11 @@ softmax_bwd_vec8_kernel(const SoftmaxArgs a) {
     const int D = a.D;
     const int64_t row = (int64_t)blockIdx.x * RPC + rg;
     const bool ok = row < a.N;
+    if (ok) {
+        prefetch_l2_row<TPR, CH>(as<XT>(a.X) + row * (int64_t)D, D, t);
+        prefetch_l2_row<TPR, CH>(as<XT>(a.dY) + row * (int64_t)D, D, t);
+    }
+    pdl_enter();
     if (WPR == 1 && !ok) return;
     const int64_t off = (ok ? row : 0) * (int64_t)D;
 
@@ -348,13 +353,16 @@ __device__ __forceinline__ float chunk_elem(const float2 (&f)[4], int e) {
 template <int TPR, int RPC, bool VEC8, int XT, int MINB, int UN>
 __global__ void __launch_bounds__(TPR * RPC, MINB)
 ce_fwd_kernel(const CeArgs a) {
-    pdl_enter();
     constexpr int W = TPR / 32;
     static_assert(W <= 32 && (W & (W - 1)) == 0, "warps per row: a power of two up to 32");
     static_assert(W == 1 || RPC == 1, "several rows per CTA only with a warp per row");
     __shared__ float sm_m[W], sm_s[W], sm_x[W], sm_t[RPC];
     const int tid = threadIdx.x, t = tid % TPR, rg = tid / TPR, lane = tid % 32, w = t / 32;
     const int64_t row = (int64_t)blockIdx.x * RPC + rg;
+    // the first batch of UN chunks a thread (aligned rows only: the scalar form's XT
+    // stands for a type read at run time)
+    if (VEC8 && row < a.N) prefetch_l2(as<XT>(a.X) + row * (int64_t)a.D, min(a.D, UN * TPR * 8), t, TPR);
+    pdl_enter();
     if (RPC > 1 && row >= a.N) return;  // a warp-wide row group: no CTA barrier below
     const int D = a.D;
     const int64_t off = row * (int64_t)D;
@@ -468,9 +476,12 @@ __device__ __forceinline__ float ce_row_grad(const CeArgs &a, int64_t row, int64
 template <int TPR, int RPC, bool VEC8, int XT, int MINB, int UN>
 __global__ void __launch_bounds__(TPR * RPC, MINB)
 ce_bwd_kernel(const CeArgs a) {
-    pdl_enter();
     const int t = threadIdx.x % TPR;
     const int64_t row = (int64_t)blockIdx.x * RPC + threadIdx.x / TPR;
+    // the first batch of UN chunks a thread (aligned rows only: the scalar form's XT
+    // stands for a type read at run time)
+    if (VEC8 && row < a.N) prefetch_l2(as<XT>(a.X) + row * (int64_t)a.D, min(a.D, UN * TPR * 8), t, TPR);
+    pdl_enter();
     if (row >= a.N) return;
     const int D = a.D;
     const int64_t off = row * (int64_t)D;
@@ -588,7 +599,6 @@ __device__ __forceinline__ MaxSum block_maxsum(MaxSum st, float *sm_m, float *sm
 template <int TPR, bool VEC8, int XT, bool LOG, int UN, int MINB, int CIT = 0>
 __global__ void __launch_bounds__(TPR, MINB)
 softmax_stream_fwd_kernel(const SoftmaxArgs a) {
-    pdl_enter();
     constexpr int W = TPR / 32;
     static_assert(W <= 32 && (W & (W - 1)) == 0, "warps per row: a power of two up to 32");
     static_assert(CIT == 0 || VEC8, "the row cache holds aligned chunks");
@@ -598,6 +608,8 @@ softmax_stream_fwd_kernel(const SoftmaxArgs a) {
     const int64_t row = blockIdx.x;
     const int D = a.D;
     const int64_t off = row * (int64_t)D;
+    if constexpr (VEC8) prefetch_l2(as<XT>(a.X) + off, min(D, UN * TPR * 8), t, TPR);  // (see ce_fwd_kernel)
+    pdl_enter();
     constexpr int CU0 = VEC8 ? chunk_units<XT>() : 1;
     auto cache_at = [&](int it, int u, int q) -> uint4 & {
         return xcache[((it * UN + u) * CU0 + q) * TPR + t];
@@ -692,7 +704,6 @@ softmax_stream_fwd_kernel(const SoftmaxArgs a) {
 template <int TPR, bool VEC8, int XT, bool LOG, int UN, int MINB, bool CLU = false>
 __global__ void __launch_bounds__(TPR, MINB)
 softmax_stream_bwd_kernel(const SoftmaxArgs a) {
-    pdl_enter();
     constexpr int WPR = TPR / 32;
     __shared__ float red[2 * WPR];
     __shared__ float xch[1];  // cluster_sum's slot
@@ -702,6 +713,11 @@ softmax_stream_bwd_kernel(const SoftmaxArgs a) {
     const int64_t row = win.owner();
     const int D = max(win.end - win.beg, 0);
     const int64_t off = row * (int64_t)a.D + win.beg;
+    if constexpr (VEC8) {  // (see ce_fwd_kernel)
+        prefetch_l2(as<XT>(a.X) + off, min(D, UN * TPR * 8), t, TPR);
+        prefetch_l2(as<XT>(a.dY) + off, min(D, UN * TPR * 8), t, TPR);
+    }
+    pdl_enter();
 
     // pass 1: sum dY*Y (softmax) or sum dY (log-softmax). The chunks in flight stay as
     // loaded (16-byte units) until used: half the registers of fp32 pairs for 2-byte types.
