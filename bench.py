@@ -7,9 +7,11 @@ row load, reduction, statistics, apply, backward row pass, dgamma/dbeta partials
 their fixed-order reduction) on device-resident inputs. The metric is achieved HBM
 throughput: compulsory bytes (fp16 activations read and written once, fp32 stats and
 parameter gradients) divided by the CUDA-event time of a step, plus rows/s.
-Steps run back to back with no flush: the forward of step s uses buffer set s % 2 and
-its backward set (s + 1) % 2, so no call finds in L2 the rows the previous call just
-touched, and each call pays for the write-backs the previous one left behind. Events
+Steps run back to back with no flush: the forward of step s uses buffer set s % n and
+its backward set (s + 1) % n, with n = 2 when one set exceeds L2 and more for smaller
+workloads (the n sets together hold at least three times L2), so no call finds in L2
+the rows an earlier call touched, and each call pays for the write-backs the previous
+one left behind. Events
 mark only the start and the end of the K timed steps (an event between two calls would
 stop the second from being scheduled while the first drains, which a training loop
 does not do). Each call's own time (the roofline entries) comes from a separate loop of
@@ -672,14 +674,25 @@ def host_cpu() -> str:
     return f"{platform.machine()} ({', '.join(parts)})" if parts else platform.machine()
 
 
+def n_buffer_sets(name: str, l2: int) -> int:
+    """Buffer sets the timed loops rotate through: 2 when one step's arrays exceed L2, more
+    for smaller workloads, so that together they hold at least three times L2 and no call
+    finds its inputs in L2 (the same rule as the norm + GEMV's weight sets)."""
+    w = W.WORKLOADS[name]
+    per_set = (W.compulsory_bytes(w.op, "forward", w.N, w.D)
+               + W.compulsory_bytes(w.op, "backward", w.N, w.D))
+    return int(max(2, min(4096, -(-3 * l2 // per_set))))
+
+
 def bench_config(name: str, world: int = 1) -> dict:
     """The workload description both arms print (the same keys and values)."""
     w = W.WORKLOADS[name]
     return {"workload": name, "op": w.op, "N": w.N, "D": w.D, "eps": w.eps,
             "step": "forward + backward",
-            "l2": ("not flushed: inputs larger than L2; steps run back to back, the forward on "
-                   "one buffer set and the backward on another (2 sets) so no call re-reads what "
-                   "the previous one touched, and write-backs are paid inside the timed region"),
+            "l2": ("not flushed: steps run back to back, rotating the forward and the backward "
+                   "over buffer sets that together hold more than L2 (2 sets when one set alone "
+                   "exceeds L2), so no call re-reads what an earlier one left in L2, and "
+                   "write-backs are paid inside the timed region"),
             "parallelism": f"{world} independent replica(s)"}
 
 
@@ -868,7 +881,8 @@ def main(argv=None):
         if rank == 0:
             print(json.dumps(line))
         return 0
-    sets = [OpRunner(args.workload, device, seed=2 * rank + i) for i in range(2)]
+    nsets = n_buffer_sets(args.workload, l2)
+    sets = [OpRunner(args.workload, device, seed=nsets * rank + i) for i in range(nsets)]
     runner = sets[0]
     w = runner.w
 
@@ -943,7 +957,7 @@ def main(argv=None):
     dtypes = {}
     if not args.no_others and rank == 0:
         for dname, tdt in (("bf16", torch.bfloat16), ("f32", torch.float32)):
-            r2 = [OpRunner(args.workload, device, seed=i, dtype=tdt) for i in range(2)]
+            r2 = [OpRunner(args.workload, device, seed=i, dtype=tdt) for i in range(nsets)]
             f2, b2 = time_ops(r2, args.steps, args.warmup, stream)
             r2 = r2[0]
             fg = r2.fwd_bytes / (f2["mean"] * 1e-3) / 1e9
@@ -1006,9 +1020,12 @@ def main(argv=None):
         "storage": "f16",
         "data": "synthetic",
         "config": bench_config(args.workload, world),
-        "l2_note": (f"inputs larger than L2 ({l2 >> 20} MiB)"),
+        "l2_note": (f"{nsets} buffer sets of {step_bytes >> 20} MiB "
+                    f"of compulsory traffic each against {l2 >> 20} MiB of L2"),
         "ops": ops,
-        "roofline": {"bound": "hbm", "kernel": f"{w.op} {dom}: " + " + ".join(KERNELS[(args.workload, dom)]),
+        "roofline": {"bound": "hbm", "kernel": f"{w.op} {dom}: " + " + ".join(
+            KERNELS.get((args.workload, dom), ["the row kernel"] + (["param_reduce_kernel"]
+                                                                    if dom == "backward" else []))),
                      "achieved": dom_block["achieved"], "peak": peak, "peak_source": peak_src,
                      "unit": "GB/s", "frac": dom_block["frac"], "traffic": dom_block["traffic"],
                      "algorithmic_bytes_per_launch": dom_block["algorithmic_bytes_per_launch"]},
