@@ -312,39 +312,44 @@ __device__ __forceinline__ void st_async_f2(uint32_t addr, float x, float y, uin
         : "memory");
 }
 
+// NB row buffers, used by rows j with j % NB = buffer (parity of the buffer's mbarrier
+// phase: (j / NB) & 1). NB = 2 when a CTA waits for row j's totals before it pushes row
+// j + 1; NB = 4 when it pushes row j + 1 before it waits for row j (the software-pipelined
+// backward, whose safety argument is at cluster_collect).
+template <int NB>
 struct PushExchange {
-    uint64_t bar[2];                           // one per row buffer
-    __align__(8) float in[2][kMaxPushCluster][2];  // [buffer][rank of the sender][value]
+    uint64_t bar[NB];                           // one per row buffer
+    __align__(8) float in[NB][kMaxPushCluster][2];  // [buffer][rank of the sender][value]
 };
 
 // The exchange state of this CTA (static shared memory of the kernels that call it only).
-__device__ __forceinline__ PushExchange &push_exchange() {
-    __shared__ __align__(8) PushExchange px;
+template <int NB>
+__device__ __forceinline__ PushExchange<NB> &push_exchange() {
+    __shared__ __align__(8) PushExchange<NB> px;
     return px;
 }
 
 // Thread 0 initialises the exchange; every thread of every CTA of the cluster must then
 // pass one cluster barrier before the first push (cluster_push_init does both).
-__device__ __forceinline__ void cluster_push_init(PushExchange &px) {
+template <int NB>
+__device__ __forceinline__ void cluster_push_init(PushExchange<NB> &px) {
     if (threadIdx.x == 0) {
-        mbar_init(&px.bar[0], 1);
-        mbar_init(&px.bar[1], 1);
+#pragma unroll
+        for (int b = 0; b < NB; ++b) mbar_init(&px.bar[b], 1);
         mbar_init_fence();
     }
     cluster_arrive();
     cluster_wait();
 }
 
-// Cluster-wide sum of the NV (1 or 2) per-CTA totals in v (bitwise identical in every
-// thread of the CTA) for the cluster's j-th row. Every thread of every CTA of the cluster
-// calls it once per row, and between two calls every thread of the CTA passes a CTA
-// barrier. `live`: this thread's waits have not given up so far; returns false if this
-// wait gave up (the totals are then incomplete).
-template <int NV>
-__device__ __forceinline__ bool cluster_push_sum(float (&v)[NV], PushExchange &px, int j,
-                                                 unsigned cn, unsigned rank, bool live) {
+// Push this CTA's NV (1 or 2) totals of the cluster's j-th row (bitwise identical in every
+// thread of the CTA) into every peer's buffer j % NB, and arrive on the CTA's own barrier
+// of that buffer expecting the peers' (cn - 1) pushes. Thread 0 does the work.
+template <int NB, int NV>
+__device__ __forceinline__ void cluster_push(const float (&v)[NV], PushExchange<NB> &px, int j,
+                                             unsigned cn, unsigned rank) {
     static_assert(NV == 1 || NV == 2, "one or two values per row");
-    const int buf = j & 1;
+    const int buf = j % NB;
     if (threadIdx.x == 0) {
         const float y = (NV == 2) ? v[NV - 1] : 0.f;
         for (unsigned r = 0; r < cn; ++r) {
@@ -354,7 +359,29 @@ __device__ __forceinline__ bool cluster_push_sum(float (&v)[NV], PushExchange &p
         }
         mbar_arrive_expect_tx(&px.bar[buf], (cn - 1) * 8u);
     }
-    const bool ok = live && mbar_wait_cluster_bounded(&px.bar[buf], (unsigned)(j >> 1) & 1u);
+}
+
+// Wait (bounded) until every peer's totals of row j are in buffer j % NB, then replace v
+// (this CTA's own totals of row j) by the cluster's sum in rank order 0, 1, ... (the same
+// operands in the same order in every CTA: the same bits). `live`: this thread's waits have
+// not given up so far; returns false if this wait gave up (the totals are incomplete).
+//
+// Buffer reuse. A CTA pushes row j into its peers' buffer j % NB, which last held row
+// j - NB; a peer's threads read that row in their cluster_collect of row j - NB. With
+// NB = 2 (push row j, then collect row j, each row in turn): a CTA pushes row j only after
+// collecting row j - 1, whose pushes each peer made after all its threads had collected
+// row j - 2 (a CTA barrier lies between). With NB = 4 and rows pipelined (push row j + 1,
+// then collect row j): a CTA pushes row j + 1 only after collecting row j - 1, which each
+// peer pushed in its iteration j - 2, after all its threads had collected row j - 3 in
+// iteration j - 3 (a CTA barrier lies between), and row j - 3 is the row that buffer
+// (j + 1) % 4 held. In both cases no push lands in a buffer before its previous row has
+// been read, and no transaction of row j + NB reaches a barrier phase before the phase of
+// row j has completed.
+template <int NB, int NV>
+__device__ __forceinline__ bool cluster_collect(float (&v)[NV], PushExchange<NB> &px, int j,
+                                                unsigned cn, unsigned rank, bool live) {
+    const int buf = j % NB;
+    const bool ok = live && mbar_wait_cluster_bounded(&px.bar[buf], (unsigned)(j / NB) & 1u);
     float t[NV];
 #pragma unroll
     for (int i = 0; i < NV; ++i) t[i] = 0.f;
@@ -364,6 +391,16 @@ __device__ __forceinline__ bool cluster_push_sum(float (&v)[NV], PushExchange &p
 #pragma unroll
     for (int i = 0; i < NV; ++i) v[i] = t[i];
     return ok;
+}
+
+// Cluster-wide sum of the NV per-CTA totals of the cluster's j-th row: push, then collect.
+// Every thread of every CTA of the cluster calls it once per row, and between two calls
+// every thread of the CTA passes a CTA barrier.
+template <int NV>
+__device__ __forceinline__ bool cluster_push_sum(float (&v)[NV], PushExchange<2> &px, int j,
+                                                 unsigned cn, unsigned rank, bool live) {
+    cluster_push<2, NV>(v, px, j, cn, rank);
+    return cluster_collect<2, NV>(v, px, j, cn, rank, live);
 }
 
 // This CTA's column window and row owner. Not split: columns [0, D) and the plain CTA

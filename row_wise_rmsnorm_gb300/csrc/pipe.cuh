@@ -126,6 +126,10 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
     static_assert(!CLU || RPC == 1, "a split row is one row group per CTA");
     // (the push exchange relies on the CTA barrier inside row_sum: TPR > 32)
     static_assert(!CLU || TPR > 32, "a split row's row group spans several warps");
+    // Split rows read pass 2 from the ring (KEEP = false) with STAGES >= 3: the exchange is
+    // software-pipelined (row j + 1's first pass and push run before row j's collect).
+    constexpr bool PIPEX = CLU && !KEEP && STAGES >= 3;
+    constexpr int NB = PIPEX ? 4 : 2;  // exchange buffers (kernels.cuh, cluster_collect)
     __shared__ float red[2 * RPC * WPR * NV];
     extern __shared__ __align__(16) uint4 ring[];
 
@@ -135,7 +139,7 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
     const float inv_d = 1.0f / (float)D;
     const Window<CLU> win(D, a.slice);
     const unsigned rank = CLU ? cluster_rank() : 0u;
-    if constexpr (CLU) cluster_push_init(push_exchange());
+    if constexpr (CLU) cluster_push_init(push_exchange<NB>());
     bool live = true;  // split rows: no wait of this thread has given up
 
     const int64_t owner = win.owner(), owners = win.owners();
@@ -209,6 +213,99 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
     stats(0, r0, m0);
     stats(1, r1, m1);
 
+    if constexpr (PIPEX) {
+        // Split rows, software-pipelined: iteration j runs row j + 1's first pass, CTA
+        // reduction and push, then collects row j's cluster totals and runs row j's second
+        // pass, so the exchange of row j is in flight while row j + 1 is read. The ring
+        // holds rows j and j + 1 while row j + 2 loads (STAGES >= 3); a thread reads back
+        // only the chunks it copied itself, so the ring needs no barrier.
+        auto pass1 = [&](int j, float mu, float (&vv)[NV]) {
+            const int slot = j % STAGES;
+            const float2 nmu = make_float2(-mu, -mu);
+            float2 v0 = make_float2(0.f, 0.f), v1 = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int k = 0; k < CK; ++k) {
+                if (win.beg + (k * TPR + t) * EPC >= win.end) continue;
+                float2 xk[PPC], dk[PPC], g[PPC];
+                unpack_chunk<XT, PPC>(&ring[R::index(slot, 0, k, tid)], THREADS, xk);
+                unpack_chunk<GT, PPC>(&ring[R::index(slot, 1, k, tid)], THREADS, dk);
+                unpack_chunk<WT, PPC>(&ring[R::param(k, tid)], THREADS, g);
+#pragma unroll
+                for (int p = 0; p < PPC; ++p) {
+                    if constexpr (OP == kLayer) xk[p] = __fadd2_rn(xk[p], nmu);
+                    const float2 gg = __fmul2_rn(dk[p], g[p]);
+                    v0 = __ffma2_rn(gg, xk[p], v0);
+                    if constexpr (OP == kLayer) v1 = __fadd2_rn(v1, gg);
+                }
+            }
+            vv[0] = v0.x + v0.y;
+            if constexpr (OP == kLayer) vv[NV - 1] = v1.x + v1.y;
+        };
+        auto pass2 = [&](int j, float r, float mu, const float (&vv)[NV]) {
+            const int slot = j % STAGES;
+            const int64_t off = (first + (int64_t)j * stride) * (int64_t)D;
+            const float c = r * vv[0] * inv_d;                           // mean_j g*xhat
+            const float am = (OP == kLayer) ? vv[NV - 1] * inv_d : 0.f;  // mean_j g
+            const float2 nmu = make_float2(-mu, -mu);
+            const float2 r2 = make_float2(r, r);
+            const float2 k2 = make_float2(-r * c, -r * c);
+            const float2 ra2 = make_float2(-r * am, -r * am);
+#pragma unroll
+            for (int k = 0; k < CK; ++k) {
+                const int col = win.beg + (k * TPR + t) * EPC;
+                if (col >= win.end) continue;
+                float2 xk[PPC], dk[PPC], g[PPC], o[PPC], sk[PPC];
+                unpack_chunk<XT, PPC>(&ring[R::index(slot, 0, k, tid)], THREADS, xk);
+                unpack_chunk<GT, PPC>(&ring[R::index(slot, 1, k, tid)], THREADS, dk);
+                unpack_chunk<WT, PPC>(&ring[R::param(k, tid)], THREADS, g);
+                if constexpr (HAS_DS) unpack_chunk<GT, PPC>(&ring[R::index(slot, 2, k, tid)], THREADS, sk);
+#pragma unroll
+                for (int p = 0; p < PPC; ++p) {
+                    if constexpr (OP == kLayer) xk[p] = __fadd2_rn(xk[p], nmu);
+                    const float2 xh = __fmul2_rn(xk[p], r2);
+                    const float2 gg = __fmul2_rn(dk[p], g[p]);
+                    const float2 base = (OP == kLayer) ? __ffma2_rn(gg, r2, ra2) : __fmul2_rn(gg, r2);
+                    float2 dx = __ffma2_rn(xh, k2, base);
+                    if constexpr (HAS_DS) dx = __fadd2_rn(dx, sk[p]);
+                    o[p] = dx;
+                    accg[k][p] = __ffma2_rn(dk[p], xh, accg[k][p]);
+                    if constexpr (OP == kLayer) accb[k][p] = __fadd2_rn(accb[k][p], dk[p]);
+                }
+                st_chunk<XT, PPC>(as<XT>(a.dX) + off + col, o);
+            }
+        };
+        PushExchange<NB> &px = push_exchange<NB>();
+        // row 0: first pass and push (a split row's rows all exist: j < iters)
+        float vc[NV];
+        float rc = r0, mc = m0;
+        if (iters > 0) {
+            cp_async_wait<STAGES - 2>();
+            pass1(0, mc, vc);
+            row_sum<TPR, RPC, NV, true>(vc, red, 0, rg, wir, lane);
+            cluster_push<NB, NV>(vc, px, 0, win.cn, rank);
+        }
+        for (int j = 0; j < iters; ++j) {
+            issue(j + STAGES - 1);  // into row j - 1's slot, read by this thread last iteration
+            const float rn = r1, mn = m1;  // row j + 1
+            stats(j + 2, r1, m1);
+            float vn[NV];
+            if (j + 1 < iters) {  // the same for every CTA of the cluster
+                cp_async_wait<STAGES - 2>();
+                pass1(j + 1, mn, vn);
+                row_sum<TPR, RPC, NV, true>(vn, red, (j + 1) & 1, rg, wir, lane);
+                cluster_push<NB, NV>(vn, px, j + 1, win.cn, rank);
+            }
+            if (!cluster_collect<NB, NV>(vc, px, j, win.cn, rank, live) && live) {
+                atomicOr(a.status, kErrClusterWait);
+                live = false;
+            }
+            if (live) pass2(j, rc, mc, vc);
+            rc = rn;
+            mc = mn;
+#pragma unroll
+            for (int i = 0; i < NV; ++i) vc[i] = vn[i];
+        }
+    } else {
     int buf = 0;
     for (int j = 0; j < iters; ++j, buf ^= 1) {
         issue(j + STAGES - 1);
@@ -270,7 +367,7 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
         if constexpr (OP == kLayer) vv[NV - 1] = v1.x + v1.y;
         row_sum<TPR, RPC, NV, true>(vv, red, buf, rg, wir, lane);
         if constexpr (CLU) {
-            if (!cluster_push_sum<NV>(vv, push_exchange(), j, win.cn, rank, live) && live) {
+            if (!cluster_push_sum<NV>(vv, push_exchange<2>(), j, win.cn, rank, live) && live) {
                 atomicOr(a.status, kErrClusterWait);
                 live = false;
             }
@@ -312,6 +409,7 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
             st_chunk<XT, PPC>(as<XT>(a.dX) + off + col, o);
         }
     }
+    }  // (not PIPEX)
     cp_async_wait<0>();
     // split rows: this CTA's pushes are issued; no CTA leaves before the cluster's last
     // pushes into its buffers have landed (waited for below, after the partial rows)
