@@ -207,10 +207,14 @@ mt_status_t run_backward(int op, BwdArgs a, bool vec8, float *dgamma, float *dbe
         if (e != cudaSuccess) sms = 1;
         const int arrays = num_partial_arrays(op);
         const bool wide = (a.D % 4 == 0) && ((a.D + 127) / 128) * arrays >= sms;
+        // wide blocks of 4 warps when each warp's rows still fit one batch of loads (split rows
+        // leave 152 / CL partial rows: 19 for 8-CTA clusters, 38 for 4; measured on GB300:
+        // LayerNorm 1024 x 131072 backward 212.5 -> 206.0 us; 8 warps for 76 rows did not pay)
+        const int ww = (prow <= 4 * kReduceBatch) ? 4 : kReduceWideWarps;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = wide ? dim3((unsigned)((a.D + 127) / 128), (unsigned)arrays)
                            : dim3((unsigned)((a.D + 31) / 32), (unsigned)arrays);
-        cfg.blockDim = dim3(32 * (wide ? kReduceWideWarps : kReduceNarrowWarps));
+        cfg.blockDim = dim3(32 * (wide ? ww : kReduceNarrowWarps));
         cfg.dynamicSmemBytes = 0;
         cfg.stream = stream;
         cudaLaunchAttribute attr[1];
@@ -221,10 +225,12 @@ mt_status_t run_backward(int op, BwdArgs a, bool vec8, float *dgamma, float *dbe
         const float *cpart = part;
         e = launch_hook();
         if (e == cudaSuccess)
-            e = wide ? cudaLaunchKernelEx(&cfg, param_reduce_kernel<4, kReduceWideWarps>, cpart,
-                                          prow, a.D, dgamma, dbeta)
-                     : cudaLaunchKernelEx(&cfg, param_reduce_kernel<1, kReduceNarrowWarps>,
-                                          cpart, prow, a.D, dgamma, dbeta);
+            e = !wide ? cudaLaunchKernelEx(&cfg, param_reduce_kernel<1, kReduceNarrowWarps>, cpart,
+                                           prow, a.D, dgamma, dbeta)
+                : ww == 4 ? cudaLaunchKernelEx(&cfg, param_reduce_kernel<4, 4>, cpart, prow, a.D,
+                                               dgamma, dbeta)
+                          : cudaLaunchKernelEx(&cfg, param_reduce_kernel<4, kReduceWideWarps>, cpart,
+                                               prow, a.D, dgamma, dbeta);
         if (e != cudaSuccess) st = cuda_fail(e);
     }
     if (own_ws) {

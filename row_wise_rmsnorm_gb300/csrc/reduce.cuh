@@ -77,7 +77,8 @@ param_reduce_kernel(const float *__restrict__ part, int P, int D, float *__restr
     }
 }
 
-// Narrow form (32 columns, 32 warps per block) and wide form (128 columns, 16 warps).
+// Narrow form (32 columns, 32 warps per block) and wide form (128 columns, 16 warps; 4 when
+// there are at most 4 batches of partial rows).
 constexpr int kReduceNarrowWarps = 32;
 constexpr int kReduceWideWarps = 16;
 
