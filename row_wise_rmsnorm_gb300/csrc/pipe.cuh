@@ -126,9 +126,10 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
     static_assert(!CLU || RPC == 1, "a split row is one row group per CTA");
     // (the push exchange relies on the CTA barrier inside row_sum: TPR > 32)
     static_assert(!CLU || TPR > 32, "a split row's row group spans several warps");
-    // Split rows read pass 2 from the ring (KEEP = false) with STAGES >= 3: the exchange is
-    // software-pipelined (row j + 1's first pass and push run before row j's collect).
-    constexpr bool PIPEX = CLU && !KEEP && STAGES >= 3;
+    // Split rows with a ring of STAGES >= 3 software-pipeline the exchange (row j + 1's first
+    // pass and push run before row j's collect); both passes then read the row from the ring
+    // (gamma from registers when KEEP, else from the ring).
+    constexpr bool PIPEX = CLU && STAGES >= 3;
     constexpr int NB = PIPEX ? 4 : 2;  // exchange buffers (kernels.cuh, cluster_collect)
     __shared__ float red[2 * RPC * WPR * NV];
     extern __shared__ __align__(16) uint4 ring[];
@@ -229,7 +230,12 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
                 float2 xk[PPC], dk[PPC], g[PPC];
                 unpack_chunk<XT, PPC>(&ring[R::index(slot, 0, k, tid)], THREADS, xk);
                 unpack_chunk<GT, PPC>(&ring[R::index(slot, 1, k, tid)], THREADS, dk);
-                unpack_chunk<WT, PPC>(&ring[R::param(k, tid)], THREADS, g);
+                if constexpr (KEEP) {
+#pragma unroll
+                    for (int p = 0; p < PPC; ++p) g[p] = gam[k][p];
+                } else {
+                    unpack_chunk<WT, PPC>(&ring[R::param(k, tid)], THREADS, g);
+                }
 #pragma unroll
                 for (int p = 0; p < PPC; ++p) {
                     if constexpr (OP == kLayer) xk[p] = __fadd2_rn(xk[p], nmu);
@@ -257,7 +263,12 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
                 float2 xk[PPC], dk[PPC], g[PPC], o[PPC], sk[PPC];
                 unpack_chunk<XT, PPC>(&ring[R::index(slot, 0, k, tid)], THREADS, xk);
                 unpack_chunk<GT, PPC>(&ring[R::index(slot, 1, k, tid)], THREADS, dk);
-                unpack_chunk<WT, PPC>(&ring[R::param(k, tid)], THREADS, g);
+                if constexpr (KEEP) {
+#pragma unroll
+                    for (int p = 0; p < PPC; ++p) g[p] = gam[k][p];
+                } else {
+                    unpack_chunk<WT, PPC>(&ring[R::param(k, tid)], THREADS, g);
+                }
                 if constexpr (HAS_DS) unpack_chunk<GT, PPC>(&ring[R::index(slot, 2, k, tid)], THREADS, sk);
 #pragma unroll
                 for (int p = 0; p < PPC; ++p) {
