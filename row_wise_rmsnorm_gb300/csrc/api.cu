@@ -159,6 +159,15 @@ mt_status_t run_forward(int op, const FwdArgs &a, bool vec8, mt_stream_t stream)
     if (e != cudaSuccess) return cuda_fail(e);
     FwdArgs copy = a;
     copy.slice = p.slice;
+    copy.ahead = 0;
+    if (p.stream) {  // the streamed forward's L2 warm-up distance: its resident CTAs
+        int device = 0, bps = 0, sms = 0;
+        cudaError_t q = cudaGetDevice(&device);
+        if (q == cudaSuccess) q = cached_occupancy(p.kernel, p.threads, p.smem, device, &bps);
+        if (q == cudaSuccess) q = device_sm_count(device, &sms);
+        if (q != cudaSuccess) return cuda_fail(q);
+        copy.ahead = bps * sms;
+    }
     return launch(p, &copy, reinterpret_cast<cudaStream_t>(stream));
 }
 

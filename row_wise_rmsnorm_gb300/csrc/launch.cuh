@@ -239,6 +239,7 @@ struct LaunchPlan {
     int cluster = 1;    // CTAs per cluster (> 1: a row split across the cluster)
     int slice = 0;      // columns per CTA of a split row
     bool waits = false; // the kernel has bounded waits: pass it the device status word
+    bool stream = false;  // streamed forward: pass it its resident CTAs (FwdArgs::ahead)
     // Row owners of a backward, one dgamma/dbeta partial row each.
     int owners() const { return grid / cluster; }
 };
@@ -354,6 +355,7 @@ cudaError_t fwd_stream_shape(int64_t N, LaunchPlan *p) {
     p->smem = 0;
     p->rows_per_cta = 1;
     p->grid = (int)N;
+    p->stream = true;
     return cudaSuccess;
 }
 
