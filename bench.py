@@ -32,6 +32,7 @@ import hashlib
 import io
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -84,14 +85,23 @@ def measured_peak_gbs():
         return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, earlier GB300 measurement)"
 
 
+def _code_only(text: str) -> str:
+    """C++/CUDA source with comments and blank space removed (the sources hold no "//" or
+    "/*" inside string literals)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash() -> str:
-    """Hash of the sources the normalization kernels are built from (the softmax,
-    cross-entropy and norm + GEMV sources are left out: they do not change them)."""
+    """Hash of the code the normalization kernels are built from, comments and blank space
+    left out (the softmax, cross-entropy and norm + GEMV sources are left out too: they do
+    not change these kernels)."""
     h = hashlib.sha256()
     for f in sorted(os.listdir(CSRC)):
         if f.endswith((".cu", ".cuh")) and not f.startswith(("softmax", "gemv")):
-            with open(os.path.join(CSRC, f), "rb") as fh:
-                h.update(f.encode() + b"\0" + fh.read())
+            with open(os.path.join(CSRC, f), encoding="utf-8") as fh:
+                h.update(f.encode() + b"\0" + _code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

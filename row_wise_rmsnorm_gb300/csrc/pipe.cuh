@@ -6,7 +6,10 @@
 // it copied itself, so cp.async.wait_group alone orders the ring: no mbarrier, no
 // cross-thread wait. Bytes in flight per SM are set by the ring depth (STAGES x streamed
 // arrays x row slice), not by registers. A row split across a cluster exchanges its CTAs'
-// row sums by the bounded push exchange of kernels.cuh.
+// row sums by the bounded push exchange of kernels.cuh; with a ring of three or more rows
+// the exchange is software-pipelined (row j + 1's first pass runs while row j's sums are
+// in flight). Before its grid-dependency wait, each CTA asks L2 for the rows its ring is
+// first filled with (prefetch_l2, kernels.cuh).
 //
 // Ownership. Row assignment is static: CTA b runs row slots b*RPC + j*G*RPC
 // (G = gridDim.x, j = 0, 1, ...), row group rg taking slot + rg. Thread t of a row group
