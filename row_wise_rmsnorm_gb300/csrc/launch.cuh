@@ -421,15 +421,25 @@ cudaError_t bwd_pipe_shape(int64_t N, int device, LaunchPlan *p) {
     constexpr int NPAR = (CH <= 2) ? 0 : 1;
     using G = PipeGeom<CH, XT, WT, GT>;
     using R1 = Ring<1, G::CK, TPR * RPC, G::UX, G::UG, HAS_DS, G::UW, NPAR>;
-    constexpr int S = pipe_stages(STAGES, R1::kStageBytes, R1::kParamBytes, CTAS);
+    constexpr int S1 = pipe_stages(STAGES, R1::kStageBytes, R1::kParamBytes, CTAS);
+    // Split rows of the fused op with fp16 dS: read dS into registers instead of through
+    // the ring when that is what makes the ring three deep (and the exchange pipelined).
+    // Measured on GB300 (backward, back to back): fp16 8192 x 16392 239.9 -> 214.3 us,
+    // 1024 x 131072 234.0 -> 216.5 us; with bf16 the same kernel was slower (2048 x 65536
+    // 191.0 -> 262.5 us, every width alike; the cause was not found), so bf16 keeps dS in
+    // a 2-deep ring.
+    using R2 = Ring<1, G::CK, TPR * RPC, G::UX, G::UG, false, G::UW, NPAR>;
+    constexpr int S2 = pipe_stages(STAGES, R2::kStageBytes, R2::kParamBytes, CTAS);
+    constexpr bool DSD = CLU && HAS_DS && GT == kF16 && S1 < 3 && S2 >= 3;
+    constexpr int S = DSD ? S2 : S1;
     if constexpr (S < 2) {
         (void)N; (void)device; (void)p;
         return kNoVectorPlan;
     } else {
-        using R = Ring<S, G::CK, TPR * RPC, G::UX, G::UG, HAS_DS, G::UW, NPAR>;
+        using R = Ring<S, G::CK, TPR * RPC, G::UX, G::UG, HAS_DS && !DSD, G::UW, NPAR>;
         static_assert(R::kBytes <= kMaxDynSmem, "ring too large");
         p->kernel = reinterpret_cast<const void *>(
-            &norm_bwd_pipe_kernel<OP, TPR, RPC, CH, S, HAS_DS, CTAS, XT, WT, GT, CLU>);
+            &norm_bwd_pipe_kernel<OP, TPR, RPC, CH, S, HAS_DS, CTAS, XT, WT, GT, CLU, DSD>);
         p->threads = TPR * RPC;
         p->smem = R::kBytes;
         p->rows_per_cta = RPC;

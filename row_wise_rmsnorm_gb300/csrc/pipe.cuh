@@ -114,8 +114,11 @@ __device__ __forceinline__ int owner_iterations(int64_t N, int rpc, int64_t owne
 // dX are of type XT, gamma of type WT, dY and dS of type GT. CLU: rows split across a
 // cluster (kernels.cuh, "cluster split"); the cluster is the row owner and writes one
 // partial row, each CTA its slice of it.
+// DSD (split rows of the fused op, fp16 dS): dS is loaded straight into registers at the
+// start of its row's iteration instead of through the ring, so that the ring holds two
+// arrays, is three deep and the exchange can be pipelined.
 template <int OP, int TPR, int RPC, int CH, int STAGES, bool HAS_DS, int CTAS, int XT, int WT,
-          int GT, bool CLU = false>
+          int GT, bool CLU = false, bool DSD = false>
 __global__ void __launch_bounds__(TPR * RPC, CTAS)
 norm_bwd_pipe_kernel(const BwdArgs a) {
     constexpr int THREADS = TPR * RPC;
@@ -124,7 +127,8 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
     constexpr bool KEEP = CH <= 2;
     using G = PipeGeom<CH, XT, WT, GT>;
     constexpr int PPC = G::PPC, EPC = G::EPC, CK = G::CK;
-    using R = Ring<STAGES, CK, THREADS, G::UX, G::UG, HAS_DS, G::UW, KEEP ? 0 : 1>;
+    constexpr bool DSR = HAS_DS && !DSD;  // dS through the ring
+    using R = Ring<STAGES, CK, THREADS, G::UX, G::UG, DSR, G::UW, KEEP ? 0 : 1>;
     static_assert(TPR % 32 == 0 && THREADS <= 1024, "bad launch shape");
     static_assert(!CLU || RPC == 1, "a split row is one row group per CTA");
     // (the push exchange relies on the CTA barrier inside row_sum: TPR > 32)
@@ -134,6 +138,7 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
     // (gamma from registers when KEEP, else from the ring).
     constexpr bool PIPEX = CLU && STAGES >= 3;
     constexpr int NB = PIPEX ? 4 : 2;  // exchange buffers (kernels.cuh, cluster_collect)
+    static_assert(!DSD || (PIPEX && HAS_DS && G::UG == 1), "dS in registers: pipelined split rows, 2-byte dS");
     __shared__ float red[2 * RPC * WPR * NV];
     extern __shared__ __align__(16) uint4 ring[];
 
@@ -197,7 +202,7 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
                 if (col < win.end) {
                     cp_chunk<XT, PPC, THREADS>(&ring[R::index(slot, 0, k, tid)], as<XT>(a.X) + off + col);
                     cp_chunk<GT, PPC, THREADS>(&ring[R::index(slot, 1, k, tid)], as<GT>(a.dY) + off + col);
-                    if constexpr (HAS_DS)
+                    if constexpr (DSR)
                         cp_chunk<GT, PPC, THREADS>(&ring[R::index(slot, 2, k, tid)], as<GT>(a.dS) + off + col);
                 }
             }
@@ -250,7 +255,7 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
             vv[0] = v0.x + v0.y;
             if constexpr (OP == kLayer) vv[NV - 1] = v1.x + v1.y;
         };
-        auto pass2 = [&](int j, float r, float mu, const float (&vv)[NV]) {
+        auto pass2 = [&](int j, float r, float mu, const float (&vv)[NV], const uint4 (&dsr)[DSD ? CK : 1]) {
             const int slot = j % STAGES;
             const int64_t off = (first + (int64_t)j * stride) * (int64_t)D;
             const float c = r * vv[0] * inv_d;                           // mean_j g*xhat
@@ -272,7 +277,8 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
                 } else {
                     unpack_chunk<WT, PPC>(&ring[R::param(k, tid)], THREADS, g);
                 }
-                if constexpr (HAS_DS) unpack_chunk<GT, PPC>(&ring[R::index(slot, 2, k, tid)], THREADS, sk);
+                if constexpr (DSD) unpack_chunk<GT, PPC>(&dsr[k], 1, sk);
+                else if constexpr (HAS_DS) unpack_chunk<GT, PPC>(&ring[R::index(slot, 2, k, tid)], THREADS, sk);
 #pragma unroll
                 for (int p = 0; p < PPC; ++p) {
                     if constexpr (OP == kLayer) xk[p] = __fadd2_rn(xk[p], nmu);
@@ -300,6 +306,15 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
         }
         for (int j = 0; j < iters; ++j) {
             issue(j + STAGES - 1);  // into row j - 1's slot, read by this thread last iteration
+            uint4 dsr[DSD ? CK : 1];  // row j's dS, used by its second pass at the end
+            if constexpr (DSD) {
+                const int64_t offd = (first + (int64_t)j * stride) * (int64_t)D;
+#pragma unroll
+                for (int k = 0; k < CK; ++k) {
+                    const int col = win.beg + (k * TPR + t) * EPC;
+                    dsr[k] = col < win.end ? ld_unit<kStream>(as<GT>(a.dS) + offd + col) : make_uint4(0, 0, 0, 0);
+                }
+            }
             const float rn = r1, mn = m1;  // row j + 1
             stats(j + 2, r1, m1);
             float vn[NV];
@@ -313,7 +328,7 @@ norm_bwd_pipe_kernel(const BwdArgs a) {
                 atomicOr(a.status, kErrClusterWait);
                 live = false;
             }
-            if (live) pass2(j, rc, mc, vc);
+            if (live) pass2(j, rc, mc, vc, dsr);
             rc = rn;
             mc = mn;
 #pragma unroll
