@@ -358,13 +358,41 @@ norm_gemv_kernel(const GemvArgs a) {
     __syncthreads();
     if (!last) return;
     __threadfence();
+    // Each thread owns outputs idx = tid + i * THREADS (i < OUTS) and adds each one's KS
+    // partials in slice order; the loads of SB slices of all its outputs are issued before
+    // their adds, so that they are in flight together (the same sums as one add at a time).
+    constexpr int OUTS = (MT * TILE + THREADS - 1) / THREADS;
+    constexpr int SB = (32 / OUTS) > 0 ? 32 / OUTS : 1;
     __half *Y = static_cast<__half *>(a.Y);
-    for (int idx = tid; idx < M * TILE; idx += THREADS) {
+    const size_t step = (size_t)M * N;
+    float sum[OUTS];
+    const float *src[OUTS];
+    bool on[OUTS];
+#pragma unroll
+    for (int i = 0; i < OUTS; ++i) {
+        const int idx = tid + i * THREADS;
         const int m = idx / TILE, n = tile * TILE + idx % TILE;
-        if (n >= N) continue;
-        float sum = 0.f;
-        for (int k = 0; k < a.ks; ++k) sum += __ldcg(&a.part[((size_t)k * M + m) * N + n]);
-        Y[(int64_t)m * N + n] = __float2half_rn(sum);
+        on[i] = idx < M * TILE && n < N;
+        src[i] = a.part + (size_t)(on[i] ? m : 0) * N + (on[i] ? n : 0);
+        sum[i] = 0.f;
+    }
+    for (int k0 = 0; k0 < a.ks; k0 += SB) {
+        float v[OUTS][SB];
+#pragma unroll
+        for (int i = 0; i < OUTS; ++i)
+#pragma unroll
+            for (int b = 0; b < SB; ++b)
+                v[i][b] = (on[i] && k0 + b < a.ks) ? __ldcg(src[i] + (size_t)(k0 + b) * step) : 0.f;
+#pragma unroll
+        for (int i = 0; i < OUTS; ++i)
+#pragma unroll
+            for (int b = 0; b < SB; ++b)
+                if (k0 + b < a.ks) sum[i] += v[i][b];
+    }
+#pragma unroll
+    for (int i = 0; i < OUTS; ++i) {
+        const int idx = tid + i * THREADS;
+        if (on[i]) Y[(int64_t)(idx / TILE) * N + tile * TILE + idx % TILE] = __float2half_rn(sum[i]);
     }
 }
 
