@@ -5,7 +5,7 @@
 //
 // The work is HBM-bound on W: each 2-byte weight feeds M multiply-adds, at most 8 flops per
 // byte for M = 8, two orders of magnitude under the tensor-core ridge. So W is streamed
-// once with 16-byte loads and the products are fp32x2 FMAs on the CUDA cores. Three
+// once with 16-byte loads and the products are fp32x2 FMAs on the CUDA cores. Two
 // launches, chained by programmatic dependent launch:
 //
 //  1. gemv_stats_kernel: the M rows' statistics (RMSNorm: mean of squares; LayerNorm:
@@ -23,11 +23,9 @@
 //     pass 2: normalization applied during the accumulation).
 //     The last CTA to finish a column tile (counted with one atomic increment per CTA on
 //     the tile's counter, after a fence that publishes its partial sums) adds the KS
-//     partial rows of the tile in slice order and writes Y, rounded to fp16. Nothing
+//     partial rows of the tile in slice order and writes Y, rounded to fp16 (the loads of
+//     a batch of slices for all of a thread's outputs are issued before their adds). Nothing
 //     waits on the counter: the other CTAs just exit.
-//
-//  For 3-4 rows and N >= 8192, norm_gemv_wide_kernel (2048-column tiles, each W row read by
-//  a CTA as one 4 KB run) and gemv_reduce_kernel replace step 2.
 //
 // Deterministic sums: per thread, features in ascending order; the G feature groups of a
 // warp by a butterfly; the warps of a CTA in warp order; the slices in slice order (the
@@ -394,113 +392,6 @@ norm_gemv_kernel(const GemvArgs a) {
         const int idx = tid + i * THREADS;
         if (on[i]) Y[(int64_t)(idx / TILE) * N + tile * TILE + idx % TILE] = __float2half_rn(sum[i]);
     }
-}
-
-// 2b. The wide-tile layout, taken for 3-4 rows and N >= 8192: the 8 warps of a CTA sit
-// side by side on a 2048-column tile, so the CTA reads each W row of its slice as one 4 KB
-// run, and every thread streams all of the slice's features (no combination across the
-// CTA's warps). Each thread writes its columns of the (slice, m) partial rows; a third
-// kernel adds them in slice order. Measured on GB300 against norm_gemv_kernel: M = 4,
-// 4096 x 12288: 33.8 us against 43.1 us; 8192 x 14336: 62.8 against 85.2 us; equal at
-// M = 2; slower for M = 1 and for N = 4096 (the extra launch).
-template <int OP, int MT, int S>
-__global__ void __launch_bounds__(kGemvWarps * 32, 2)
-norm_gemv_wide_kernel(const GemvArgs a) {
-    constexpr int THREADS = kGemvWarps * 32;
-    constexpr int TILE = 8 * THREADS;
-    constexpr int MP = gemv_mp<MT>();
-    extern __shared__ __align__(16) float gsm[];
-    const int tid = threadIdx.x;
-    const int M = a.M, N = a.N, K = a.K;
-    const int ntiles = (N + TILE - 1) / TILE;
-    const int tile = (int)(blockIdx.x % ntiles), ks = (int)(blockIdx.x / ntiles);
-    const int kbeg = ks * a.slice, kend = min(K, kbeg + a.slice);
-    const int col = tile * TILE + tid * 8;
-    const int nk = max(0, kend - kbeg);
-    const __half *W = static_cast<const __half *>(a.W);
-    float *xn = gsm;
-    uint4 *ring = reinterpret_cast<uint4 *>(gsm + (size_t)a.slice * MP);
-    auto issue = [&](int i) {
-        if (i < nk && col < N)
-            cp_async16(smem_addr(&ring[(i % S) * THREADS + tid]), W + (int64_t)(kbeg + i) * N + col);
-        cp_async_commit();
-    };
-#pragma unroll
-    for (int i = 0; i < S - 1; ++i) issue(i);
-    pdl_enter();
-    const __half *X = static_cast<const __half *>(a.X);
-    const __half *gam = static_cast<const __half *>(a.gamma);
-    const __half *bet = static_cast<const __half *>(a.beta);
-    float mu[MT], rs[MT];
-#pragma unroll
-    for (int m = 0; m < MT; ++m) {
-        mu[m] = m < M ? a.stats[2 * m] : 0.f;
-        rs[m] = m < M ? a.stats[2 * m + 1] : 0.f;
-    }
-    for (int k = kbeg + tid; k < kend; k += THREADS) {
-        const float g = __half2float(gam[k]);
-        const float b = (OP == kLayer) ? __half2float(bet[k]) : 0.f;
-        float v[MP];
-#pragma unroll
-        for (int m = 0; m < MP; ++m) {
-            v[m] = 0.f;
-            if (m < MT && m < M) v[m] = (__half2float(X[(int64_t)m * K + k]) - mu[m]) * rs[m] * g + b;
-        }
-#pragma unroll
-        for (int qd = 0; qd < MP / 4; ++qd)
-            reinterpret_cast<float4 *>(xn + (size_t)(k - kbeg) * MP)[qd] =
-                make_float4(v[4 * qd], v[4 * qd + 1], v[4 * qd + 2], v[4 * qd + 3]);
-    }
-    __syncthreads();
-    float2 acc[MT][4];
-#pragma unroll
-    for (int m = 0; m < MT; ++m)
-#pragma unroll
-        for (int p = 0; p < 4; ++p) acc[m][p] = make_float2(0.f, 0.f);
-    for (int i = 0; i < nk; ++i) {
-        issue(i + S - 1);
-        cp_async_wait<S - 1>();
-        const uint4 raw = col < N ? ring[(i % S) * THREADS + tid] : make_uint4(0, 0, 0, 0);
-        float2 wf[4];
-        unpack_unit<kF16>(raw, wf);
-        float xv[MP];
-#pragma unroll
-        for (int q = 0; q < MP / 4; ++q) {
-            const float4 t = reinterpret_cast<const float4 *>(xn + (size_t)i * MP)[q];
-            xv[4 * q] = t.x;
-            xv[4 * q + 1] = t.y;
-            xv[4 * q + 2] = t.z;
-            xv[4 * q + 3] = t.w;
-        }
-#pragma unroll
-        for (int m = 0; m < MT; ++m) {
-            const float2 x2 = make_float2(xv[m], xv[m]);
-#pragma unroll
-            for (int p = 0; p < 4; ++p) acc[m][p] = __ffma2_rn(x2, wf[p], acc[m][p]);
-        }
-    }
-    cp_async_wait<0>();
-    if (col < N) {
-#pragma unroll
-        for (int m = 0; m < MT; ++m) {
-            if (m >= M) break;
-            float4 *dst = reinterpret_cast<float4 *>(a.part + ((size_t)ks * M + m) * N + col);
-            dst[0] = make_float4(acc[m][0].x, acc[m][0].y, acc[m][1].x, acc[m][1].y);
-            dst[1] = make_float4(acc[m][2].x, acc[m][2].y, acc[m][3].x, acc[m][3].y);
-        }
-    }
-}
-
-// 3b. Y[m][n] = fp16(sum over slices s = 0, 1, ... of part[s][m][n]) (wide-tile layout).
-__global__ void __launch_bounds__(256)
-gemv_reduce_kernel(const GemvArgs a) {
-    pdl_enter();
-    const int64_t idx = (int64_t)blockIdx.x * 256 + threadIdx.x;
-    const int64_t MN = (int64_t)a.M * a.N;
-    if (idx >= MN) return;
-    float s = 0.f;
-    for (int k = 0; k < a.ks; ++k) s += __ldcg(&a.part[(size_t)k * MN + idx]);
-    static_cast<__half *>(a.Y)[idx] = __float2half_rn(s);
 }
 
 }  // namespace mt

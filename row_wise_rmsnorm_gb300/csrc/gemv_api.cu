@@ -110,36 +110,6 @@ cudaError_t gemv_plan(int op, int M, int N, int K, bool vec, int device, LaunchP
     return cached_occupancy(p->kernel, p->threads, p->smem, device, &per_sm);
 }
 
-// Wide-tile layout (gemv.cuh, 2b) for 3-4 rows and N >= 8192 with 16-byte W rows: 2048-column
-// tiles and the slices that bring the grid to about two CTAs per SM.
-bool gemv_wide(int M, int N, bool vec) { return vec && M >= 3 && M <= 4 && N >= 8192; }
-
-cudaError_t gemv_plan_wide(int op, int M, int N, int K, int device, LaunchPlan *p, int *slice,
-                           int *ks) {
-    int sms = 0;
-    cudaError_t e = device_sm_count(device, &sms);
-    if (e != cudaSuccess) return e;
-    const int wt = (N + 2047) / 2048;
-    int kk = std::max(1, (2 * sms + wt - 1) / wt);
-    int sl = std::min(((K + kk - 1) / kk + 7) / 8 * 8, kGemvMaxSlice);
-    kk = (K + sl - 1) / sl;
-    if (op == kRms) {
-        p->kernel = M == 3 ? reinterpret_cast<const void *>(&norm_gemv_wide_kernel<kRms, 3, kGemvStages>)
-                           : reinterpret_cast<const void *>(&norm_gemv_wide_kernel<kRms, 4, kGemvStages>);
-    } else {
-        p->kernel = M == 3 ? reinterpret_cast<const void *>(&norm_gemv_wide_kernel<kLayer, 3, kGemvStages>)
-                           : reinterpret_cast<const void *>(&norm_gemv_wide_kernel<kLayer, 4, kGemvStages>);
-    }
-    p->threads = kGemvWarps * 32;
-    p->smem = (size_t)sl * gemv_mp<4>() * sizeof(float) + (size_t)kGemvStages * kGemvWarps * 32 * 16;
-    p->grid = wt * kk;
-    p->rows_per_cta = M;
-    *slice = sl;
-    *ks = kk;
-    int per_sm = 0;  // raises the kernel's dynamic shared memory limit to p->smem
-    return cached_occupancy(p->kernel, p->threads, p->smem, device, &per_sm);
-}
-
 mt_status_t norm_gemv_impl(int op, const void *X, const void *gamma, const void *beta,
                            const void *W, void *Y, int64_t M, int64_t N, int64_t K, float eps,
                            mt_stream_t stream_in) {
@@ -163,9 +133,7 @@ mt_status_t norm_gemv_impl(int op, const void *X, const void *gamma, const void 
                       15u) == 0;
     LaunchPlan p;
     int slice = 0, ks = 0, tiles = 0;
-    const bool wide = gemv_wide((int)M, (int)N, vec);
-    e = wide ? gemv_plan_wide(op, (int)M, (int)N, (int)K, device, &p, &slice, &ks)
-             : gemv_plan(op, (int)M, (int)N, (int)K, vec, device, &p, &slice, &ks, &tiles);
+    e = gemv_plan(op, (int)M, (int)N, (int)K, vec, device, &p, &slice, &ks, &tiles);
     if (e != cudaSuccess) return gemv_fail(e);
     // stream-ordered scratch: the statistics, the tile counters, the fp32 partial rows
     const size_t stats_bytes = 256;
@@ -198,13 +166,6 @@ mt_status_t norm_gemv_impl(int op, const void *X, const void *gamma, const void 
     st.grid = (int)M;
     e = launch_pdl(st, &a, stream);
     if (e == cudaSuccess) e = launch_pdl(p, &a, stream);
-    if (e == cudaSuccess && wide) {
-        LaunchPlan rd;
-        rd.kernel = reinterpret_cast<const void *>(&gemv_reduce_kernel);
-        rd.threads = 256;
-        rd.grid = (int)(((int64_t)M * N + 255) / 256);
-        e = launch_pdl(rd, &a, stream);
-    }
     const cudaError_t fe = cudaFreeAsync(ws, stream);
     if (e == cudaSuccess) e = fe;
     return e == cudaSuccess ? MT_OK : gemv_fail(e);
