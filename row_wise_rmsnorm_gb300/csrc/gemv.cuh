@@ -214,17 +214,24 @@ norm_gemv_kernel(const GemvArgs a) {
     };
 #pragma unroll
     for (int i = 0; i < S - 1; ++i) issue(i);
-    pdl_enter();  // the statistics are complete and visible from here on
+    // RMSNorm factors rstd out of the sums: Y = rstd * sum_k (x_k g_k) W_k, so the slice
+    // x * g needs no statistics and the kernel waits for the statistics kernel only before
+    // it counts its tile (the wait also covers the tile counters that kernel zeroes). X is
+    // visible already: this kernel launches only once the statistics kernel has passed its
+    // own wait for the kernel that wrote X. LayerNorm builds the normalized slice, so it
+    // waits here.
+    if constexpr (OP == kRms) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    else pdl_enter();  // the statistics are complete and visible from here on
 
-    // the normalized slice: thread t builds features of chunks t and t + THREADS
+    // the slice: thread t builds features of chunks t and t + THREADS
     const __half *X = static_cast<const __half *>(a.X);
     const __half *gam = static_cast<const __half *>(a.gamma);
     const __half *bet = static_cast<const __half *>(a.beta);
     float mu[MT], rs[MT];
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
-        mu[m] = m < M ? a.stats[2 * m] : 0.f;
-        rs[m] = m < M ? a.stats[2 * m + 1] : 0.f;
+        mu[m] = (OP == kLayer && m < M) ? a.stats[2 * m] : 0.f;
+        rs[m] = (OP == kLayer && m < M) ? a.stats[2 * m + 1] : 1.f;
     }
 #pragma unroll
     for (int c = 0; c < kGemvSliceChunks; ++c) {
@@ -350,6 +357,7 @@ norm_gemv_kernel(const GemvArgs a) {
 
     // the last of the tile's KS CTAs adds the partial rows in slice order
     __shared__ unsigned last;
+    if constexpr (OP == kRms) asm volatile("griddepcontrol.wait;" ::: "memory");
     __threadfence();  // publish this CTA's partial rows before counting it
     __syncthreads();
     if (tid == 0) last = (atomicAdd(&a.count[tile], 1u) == (unsigned)a.ks - 1u);
@@ -390,7 +398,11 @@ norm_gemv_kernel(const GemvArgs a) {
 #pragma unroll
     for (int i = 0; i < OUTS; ++i) {
         const int idx = tid + i * THREADS;
-        if (on[i]) Y[(int64_t)(idx / TILE) * N + tile * TILE + idx % TILE] = __float2half_rn(sum[i]);
+        if (on[i]) {
+            const int m = idx / TILE;
+            const float r = (OP == kRms) ? a.stats[2 * m + 1] : 1.f;  // RMSNorm: rstd applied here
+            Y[(int64_t)m * N + tile * TILE + idx % TILE] = __float2half_rn(sum[i] * r);
+        }
     }
 }
 
