@@ -796,34 +796,51 @@ softmax_stream_bwd_kernel(const SoftmaxArgs a) {
 }
 
 // Fixed-order reduction of the per-row losses for sum/mean: one block; thread i sums rows
-// i, i + B, ... in order and counts the rows whose target is not ignore_index; then a
-// fixed tree. out[0] = sum (reduction 1) or sum / count (2; 0 when no row is valid),
+// i, i + B, ... in order (four rows' loads in flight) and counts the rows whose target is
+// not ignore_index; then each warp's threads by a butterfly and the warps' totals in warp
+// order. out[0] = sum (reduction 1) or sum / count (2; 0 when no row is valid),
 // n_valid[0] = count.
 template <int B>
 __global__ void __launch_bounds__(B)
 ce_loss_reduce_kernel(const float *loss, const int64_t *T, int64_t N, int64_t ignore_index,
                       int reduction, float *out, float *n_valid) {
     pdl_enter();
-    __shared__ float ss[B], sc[B];
+    constexpr int W = B / 32, U = 4;
+    static_assert(W <= 32 && W * 32 == B, "one warp adds the warp totals");
+    __shared__ float ws[W], wc[W];
+    const int lane = threadIdx.x % 32, w = threadIdx.x / 32;
+    // per thread: rows threadIdx.x, + B, + 2B, ... in that order, U rows' loads in flight
     float s = 0.f, c = 0.f;
-    for (int64_t i = threadIdx.x; i < N; i += B) {
-        s += loss[i];
-        c += (T[i] != ignore_index) ? 1.f : 0.f;
-    }
-    ss[threadIdx.x] = s;
-    sc[threadIdx.x] = c;
-    __syncthreads();
-    for (int h = B / 2; h > 0; h >>= 1) {
-        if ((int)threadIdx.x < h) {
-            ss[threadIdx.x] += ss[threadIdx.x + h];
-            sc[threadIdx.x] += sc[threadIdx.x + h];
+    for (int64_t i0 = threadIdx.x; i0 < N; i0 += (int64_t)U * B) {
+        float l[U], v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t i = i0 + (int64_t)u * B;
+            l[u] = i < N ? loss[i] : 0.f;
+            v[u] = (i < N && T[i] != ignore_index) ? 1.f : 0.f;
         }
-        __syncthreads();
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (i0 + (int64_t)u * B < N) {
+                s += l[u];
+                c += v[u];
+            }
     }
-    if (threadIdx.x == 0) {
-        const float tot = ss[0], cnt = sc[0];
-        out[0] = (reduction == 2) ? (cnt > 0.f ? tot / cnt : 0.f) : tot;
-        n_valid[0] = cnt;
+    // the warp's threads by a butterfly, then the warp totals in warp order
+    s = warp_sum(s);
+    c = warp_sum(c);
+    if (lane == 0) {
+        ws[w] = s;
+        wc[w] = c;
+    }
+    __syncthreads();
+    if (w == 0) {
+        float tot = warp_sum(lane < W ? ws[lane] : 0.f);
+        float cnt = warp_sum(lane < W ? wc[lane] : 0.f);
+        if (lane == 0) {
+            out[0] = (reduction == 2) ? (cnt > 0.f ? tot / cnt : 0.f) : tot;
+            n_valid[0] = cnt;
+        }
     }
 }
 
