@@ -160,13 +160,13 @@ mt_status_t run_forward(int op, const FwdArgs &a, bool vec8, mt_stream_t stream)
     FwdArgs copy = a;
     copy.slice = p.slice;
     copy.ahead = 0;
-    if (p.stream) {  // the streamed forward's L2 warm-up distance: its resident CTAs
+    if (p.warm) {  // the L2 warm-up distance: the rows of the launch's resident CTAs
         int device = 0, bps = 0, sms = 0;
         cudaError_t q = cudaGetDevice(&device);
         if (q == cudaSuccess) q = cached_occupancy(p.kernel, p.threads, p.smem, device, &bps);
         if (q == cudaSuccess) q = device_sm_count(device, &sms);
         if (q != cudaSuccess) return cuda_fail(q);
-        copy.ahead = bps * sms;
+        copy.ahead = bps * sms * std::max(p.rows_per_cta, 1);
     }
     return launch(p, &copy, reinterpret_cast<cudaStream_t>(stream));
 }

@@ -57,7 +57,7 @@ struct FwdArgs {
     float eps;
     int xdt, wdt;
     int slice;            // cluster-split kernels: columns per CTA (a multiple of 8)
-    int ahead;            // streamed forward: the launch's resident CTAs (0: no L2 warm-up)
+    int ahead;            // rows of the launch's resident CTAs (the L2 warm-up distance; 0: none)
 };
 
 // X (or the saved S) and dX are stored as xdt, gamma as wdt, dY/dS as gdt.
@@ -680,6 +680,15 @@ norm_fwd_packed_kernel(const FwdArgs a) {
     for (int k = 0; k < CH; ++k) {
         const int col = (k * TPR + t) * 8;
         raw[k] = (ok && col < D) ? ld_unit<kStream>(X + off + col) : make_uint4(0, 0, 0, 0);
+    }
+    // RMSNorm: with its row's loads issued, thread 0 of the row group warms L2 with the row
+    // the next wave takes, `ahead` rows on (one bulk prefetch). Measured on GB300: RMSNorm
+    // 16384 x 4096 forward 40.2 -> 39.2 us, 8192 x 8192 40.3 -> 39.2 us; LayerNorm lost
+    // (2048 x 16384 22.7 -> 23.7 us), so it does not prefetch.
+    if constexpr (OP == kRms) {
+        if (t == 0 && ok && a.ahead > 0 && row + a.ahead < a.N)
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(X + (row + a.ahead) * (int64_t)D),
+                         "r"((unsigned)D * (unsigned)sizeof(*X)) : "memory");
     }
     // Chunk k as fp32 pairs. Each pass widens the chunks again rather than keep fp32
     // copies of the row alive across the reductions. So that the compiler does not merge

@@ -239,7 +239,7 @@ struct LaunchPlan {
     int cluster = 1;    // CTAs per cluster (> 1: a row split across the cluster)
     int slice = 0;      // columns per CTA of a split row
     bool waits = false; // the kernel has bounded waits: pass it the device status word
-    bool stream = false;  // streamed forward: pass it its resident CTAs (FwdArgs::ahead)
+    bool warm = false;  // forward that warms L2 a wave ahead: pass it FwdArgs::ahead
     // Row owners of a backward, one dgamma/dbeta partial row each.
     int owners() const { return grid / cluster; }
 };
@@ -334,10 +334,11 @@ cudaError_t fwd_plan_scalar(int64_t N, int D, LaunchPlan *p) {
 template <int OP, int XT, int WT, int TPR, int RPC, int CH, bool PACK, int MINB>
 cudaError_t fwd_vec_shape(int64_t N, LaunchPlan *p) {
     constexpr int minb = (XT == kF32 || WT == kF32) ? 0 : MINB;
-    if constexpr (PACK && OP != kAddRms && XT != kF32)
+    if constexpr (PACK && OP != kAddRms && XT != kF32) {
         p->kernel = reinterpret_cast<const void *>(
             &norm_fwd_packed_kernel<OP, TPR, RPC, CH, minb, XT, WT>);
-    else
+        p->warm = (OP == kRms);  // (see the kernel)
+    } else
         p->kernel = reinterpret_cast<const void *>(
             &norm_fwd_vec8_kernel<OP, TPR, RPC, CH, minb, XT, WT>);
     p->threads = TPR * RPC;
@@ -355,7 +356,7 @@ cudaError_t fwd_stream_shape(int64_t N, LaunchPlan *p) {
     p->smem = 0;
     p->rows_per_cta = 1;
     p->grid = (int)N;
-    p->stream = true;
+    p->warm = true;
     return cudaSuccess;
 }
 
