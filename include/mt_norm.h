@@ -258,8 +258,10 @@ mt_status_t mt_softmax_backward(mt_dtype_t dtype, const void *Y, const void *dY,
  *            g_i = dloss_i (NONE), dloss (SUM), dloss / n_valid (MEAN), 0 if ignored.
  * logits X / dX: [N, D] of type `dtype`; targets: [N] int64 (device); loss_rows, lse:
  * [N] fp32 (lse is saved for the backward and written for every row); loss_out and
- * n_valid: one fp32 each, written for SUM/MEAN (may be NULL for NONE); the backward's
- * dloss is [N] for NONE and one value otherwise, and n_valid (MEAN) is the forward's.
+ * n_valid: one fp32 each, written for SUM/MEAN (may be NULL for NONE). n_valid is the
+ * number of rows not skipped, counted exactly and rounded to fp32 (exact up to 2^24
+ * rows); MEAN divides the fp32 sum by the exact count. The backward's dloss is [N] for
+ * NONE and one value otherwise, and n_valid (MEAN) is the forward's.
  * A target outside [0, D) that is not ignore_index gives a NaN loss for its row.
  * Bounds: 1 <= D <= MT_MAX_CE_COLS, 0 <= N <= 2^31 - 1; 0 <= label_smoothing <= 1,
  * z_loss >= 0 (both finite), else MT_ERR_INVALID_ARG. N = 0: the forward writes only

@@ -797,9 +797,10 @@ softmax_stream_bwd_kernel(const SoftmaxArgs a) {
 
 // Fixed-order reduction of the per-row losses for sum/mean: one block; thread i sums rows
 // i, i + B, ... in order (four rows' loads in flight) and counts the rows whose target is
-// not ignore_index; then each warp's threads by a butterfly and the warps' totals in warp
-// order. out[0] = sum (reduction 1) or sum / count (2; 0 when no row is valid),
-// n_valid[0] = count.
+// not ignore_index; then each warp's threads by a butterfly, and the warps' totals by a
+// butterfly in warp 0 (the same order every run). The count is an integer (exact for any
+// N < 2^32). out[0] = sum (reduction 1) or sum / count (2, divided in fp64 and rounded
+// once; 0 when no row is valid), n_valid[0] = count rounded to fp32 (exact up to 2^24).
 template <int B>
 __global__ void __launch_bounds__(B)
 ce_loss_reduce_kernel(const float *loss, const int64_t *T, int64_t N, int64_t ignore_index,
@@ -807,17 +808,20 @@ ce_loss_reduce_kernel(const float *loss, const int64_t *T, int64_t N, int64_t ig
     pdl_enter();
     constexpr int W = B / 32, U = 4;
     static_assert(W <= 32 && W * 32 == B, "one warp adds the warp totals");
-    __shared__ float ws[W], wc[W];
+    __shared__ float ws[W];
+    __shared__ unsigned wc[W];
     const int lane = threadIdx.x % 32, w = threadIdx.x / 32;
     // per thread: rows threadIdx.x, + B, + 2B, ... in that order, U rows' loads in flight
-    float s = 0.f, c = 0.f;
+    float s = 0.f;
+    unsigned c = 0u;
     for (int64_t i0 = threadIdx.x; i0 < N; i0 += (int64_t)U * B) {
-        float l[U], v[U];
+        float l[U];
+        unsigned v[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int64_t i = i0 + (int64_t)u * B;
             l[u] = i < N ? loss[i] : 0.f;
-            v[u] = (i < N && T[i] != ignore_index) ? 1.f : 0.f;
+            v[u] = (i < N && T[i] != ignore_index) ? 1u : 0u;
         }
 #pragma unroll
         for (int u = 0; u < U; ++u)
@@ -828,18 +832,18 @@ ce_loss_reduce_kernel(const float *loss, const int64_t *T, int64_t N, int64_t ig
     }
     // the warp's threads by a butterfly, then the warp totals in warp order
     s = warp_sum(s);
-    c = warp_sum(c);
+    c = __reduce_add_sync(0xffffffffu, c);
     if (lane == 0) {
         ws[w] = s;
         wc[w] = c;
     }
     __syncthreads();
     if (w == 0) {
-        float tot = warp_sum(lane < W ? ws[lane] : 0.f);
-        float cnt = warp_sum(lane < W ? wc[lane] : 0.f);
+        const float tot = warp_sum(lane < W ? ws[lane] : 0.f);
+        const unsigned cnt = __reduce_add_sync(0xffffffffu, lane < W ? wc[lane] : 0u);
         if (lane == 0) {
-            out[0] = (reduction == 2) ? (cnt > 0.f ? tot / cnt : 0.f) : tot;
-            n_valid[0] = cnt;
+            out[0] = (reduction == 2) ? (cnt > 0u ? (float)((double)tot / (double)cnt) : 0.f) : tot;
+            n_valid[0] = (float)cnt;
         }
     }
 }

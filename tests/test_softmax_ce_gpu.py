@@ -193,6 +193,29 @@ def test_cross_entropy_edge_cases():
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
 
+def test_cross_entropy_count_past_fp32_integers():
+    """More rows than fp32 counts exactly (2^24): the valid rows are counted as an integer,
+    so n_valid is that count rounded once to fp32, and the mean is the fp32 sum divided by
+    the exact count (rounded once); both reductions match the oracle."""
+    N, D = (1 << 24) + 4100, 2
+    x = _gen((N, D), 2.0, F16, 11)
+    t = torch.zeros(N, dtype=torch.int64, device="cuda")
+    t[1::65536] = -100
+    count = N - int((t == -100).sum().item())
+    assert count > (1 << 24) and count % 2 == 1  # not an fp32 integer
+    mean, _, nv = mt.cross_entropy_forward(x, t, -100, 0.0, 0.0, "mean")
+    tot, _, nv_sum = mt.cross_entropy_forward(x, t, -100, 0.0, 0.0, "sum")
+    torch.cuda.synchronize()
+    assert float(nv.item()) == float(np.float32(count)) == float(nv_sum.item())
+    assert float(mean.item()) == float(np.float32(float(tot.item()) / count))
+    rows, _ = oracle.cross_entropy_forward(f64(x), t.cpu().numpy(), -100, 0.0, 0.0)
+    ref_sum, n_valid = oracle.cross_entropy_reduce(rows, t.cpu().numpy(), -100, "sum")
+    assert n_valid == count
+    tol = 1e-5 * np.sum(np.abs(rows))
+    assert abs(float(tot.item()) - ref_sum) <= tol, f"sum {tot.item()} vs {ref_sum}"
+    assert abs(float(mean.item()) - ref_sum / count) <= tol / count, f"mean {mean.item()}"
+
+
 @pytest.mark.parametrize("shape", [(64, 4096), (17, 1001), (4, 50000)],
                          ids=lambda s: f"{s[0]}x{s[1]}")
 @pytest.mark.parametrize("dtype", [BF16, F32], ids=lambda d: NAMES[d])
