@@ -124,7 +124,10 @@ class ClockSampler:
     NVML (the library nvidia-smi itself uses; read-only queries) every millisecond from a
     background thread, plus one synchronous sample as soon as the timed work is enqueued
     (`mark()`), so that even a region of a few milliseconds carries its own clock record.
-    Falls back to `nvidia-smi -lms 200` when NVML cannot be loaded."""
+    The main thread enqueues the timed calls in Python and holds the interpreter lock
+    between them; at the default 5 ms switch interval the sampler would get one turn in
+    five periods, so the interval is lowered to a quarter period while sampling and
+    restored afterwards. Falls back to `nvidia-smi -lms 200` when NVML cannot be loaded."""
     REASONS = ((0x8, "hw_slowdown"), (0x40, "hw_thermal_slowdown"),
                (0x20, "sw_thermal_slowdown"), (0x4, "sw_power_cap"))
     SMI_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -200,6 +203,8 @@ class ClockSampler:
         import threading
         if self._open_nvml():
             self.source = "nvml, 1 ms"
+            self._switch = sys.getswitchinterval()
+            sys.setswitchinterval(min(self._switch, self.period / 4))
             self._stop = threading.Event()
             self._thread = threading.Thread(target=self._loop, daemon=True)
             self.t0 = time.perf_counter()
@@ -221,6 +226,7 @@ class ClockSampler:
         if self.nvml is not None:
             self._stop.set()
             self._thread.join(timeout=5)
+            sys.setswitchinterval(self._switch)
             self.nvml.nvmlShutdown()
             return
         out = ""
