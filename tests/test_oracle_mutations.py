@@ -3,7 +3,9 @@
 Each mutation is a one-token slip of the kind the pins are meant to catch: a dropped
 term, a flipped sign, a wrong index, a transposed operand, a misplaced eps, the sample
 instead of the population variance. The committed oracle is never modified; each
-mutant is compiled from a patched copy in a temporary directory.
+mutant is compiled from a patched copy in a temporary directory. The cross-entropy
+reductions written in Python (the mean over the rows not ignored, and its gradient) are
+mutated by replacing the function for the duration of one test.
 """
 import pytest
 
@@ -57,6 +59,44 @@ def test_mutation_is_caught(tmp_path, name):
     mutated = tmp_path / "mutant.c"
     mutated.write_text(src.replace(old, new, 1))
     lib = oracle.load_library(oracle.compile_oracle(str(mutated), str(tmp_path / "libmutant.so")))
+    failures = []
+    for pin in ALL_PINS:
+        try:
+            pin(lib)
+        except AssertionError as e:
+            failures.append(f"{pin.__name__}: {str(e).splitlines()[0]}")
+    assert failures, f"no pin caught mutation {name}"
+
+
+# Slips in the Python-level reductions of the cross-entropy oracle, planted by replacing the
+# function for the duration of the test.
+def _mean_over_all_rows(orig):
+    def reduce(loss, T, ignore_index, reduction):
+        val, n_valid = orig(loss, T, ignore_index, reduction)
+        if reduction == "mean":
+            return float(sum(loss)) / len(loss), n_valid
+        return val, n_valid
+    return "cross_entropy_reduce", reduce
+
+
+def _mean_grad_without_count(orig):
+    def row_grad(dloss, N, n_valid, reduction):
+        return orig(dloss, N, n_valid, "sum" if reduction == "mean" else reduction)
+    return "cross_entropy_row_grad", row_grad
+
+
+PY_MUTATIONS = {
+    "ce_mean_over_all_rows": (_mean_over_all_rows, "cross_entropy_reduce"),
+    "ce_mean_grad_without_count": (_mean_grad_without_count, "cross_entropy_row_grad"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PY_MUTATIONS))
+def test_python_mutation_is_caught(monkeypatch, name):
+    make, attr = PY_MUTATIONS[name]
+    target, fn = make(getattr(oracle, attr))
+    monkeypatch.setattr(oracle, target, fn)
+    lib = oracle.load_library()
     failures = []
     for pin in ALL_PINS:
         try:
