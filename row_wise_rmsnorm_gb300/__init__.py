@@ -4,67 +4,24 @@ RMSNorm, forward and backward, behind the C ABI of include/mt_norm.h.
 The package holds the CUDA kernels and the C ABI (csrc/), the build step (build.py)
 and a thin ctypes binding (_binding.py) with the C entry points' names plus
 allocating convenience wrappers. PyTorch is used only for device memory and streams.
+
+The package's names are the binding's public ones: the C entry points (mt_*), the
+header's constants (MT_*), the allocating wrappers (rmsnorm_forward, ...), EXPORTED,
+MtNormError, load and library_path.
 """
-from ._binding import (  # noqa: F401
-    EXPORTED,
-    MT_ERR_CUDA,
-    MT_ERR_INVALID_ARG,
-    MT_DTYPE_BF16,
-    MT_DTYPE_F16,
-    MT_DTYPE_F32,
-    MT_ERR_UNSUPPORTED,
-    MT_MAX_COLS,
-    MT_MAX_SOFTMAX_COLS,
-    MT_MAX_GEMV_ROWS,
-    MT_MAX_GEMV_K,
-    MT_NOALLOC_SCRATCH_BYTES,
-    MT_MAX_CE_COLS,
-    MT_OK,
-    MT_OP_ADD_RMSNORM,
-    MT_OP_LAYERNORM,
-    MT_OP_RMSNORM,
-    MT_REDUCTION_MEAN,
-    MT_REDUCTION_NONE,
-    MT_REDUCTION_SUM,
-    MT_WAIT_ERR_CLUSTER,
-    MtNormError,
-    add_rmsnorm_backward,
-    add_rmsnorm_forward,
-    cross_entropy_backward,
-    cross_entropy_forward,
-    dtype_code,
-    layernorm_backward,
-    layernorm_forward,
-    library_path,
-    load,
-    mt_add_rmsnorm_backward,
-    mt_add_rmsnorm_backward_ws,
-    mt_add_rmsnorm_forward,
-    mt_cross_entropy_backward,
-    mt_cross_entropy_forward,
-    mt_device_wait_errors,
-    mt_fused_layernorm_gemv,
-    mt_fused_rmsnorm_gemv,
-    mt_last_cuda_error,
-    mt_layernorm_backward,
-    mt_layernorm_backward_ws,
-    mt_layernorm_forward,
-    mt_norm_backward_ex,
-    mt_norm_backward_workspace_size,
-    mt_norm_forward_ex,
-    mt_norm_version,
-    mt_rmsnorm_backward,
-    mt_rmsnorm_backward_noalloc,
-    mt_rmsnorm_backward_ws,
-    mt_rmsnorm_forward,
-    mt_softmax_backward,
-    mt_softmax_forward,
-    mt_status_string,
-    norm_backward,
-    norm_forward,
-    norm_gemv,
-    rmsnorm_backward,
-    rmsnorm_forward,
-    softmax_backward,
-    softmax_forward,
-)
+import types as _types
+
+from . import _binding
+
+
+def __getattr__(name):
+    if not name.startswith("_"):
+        value = getattr(_binding, name, _binding)
+        if value is not _binding and not isinstance(value, _types.ModuleType):
+            return value
+    raise AttributeError(f"module {__name__!r} has no attribute {name!r}")
+
+
+def __dir__():
+    return sorted(set(globals()) | {n for n in dir(_binding) if not n.startswith("_")
+                                    and not isinstance(getattr(_binding, n), _types.ModuleType)})
