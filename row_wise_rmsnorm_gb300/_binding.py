@@ -18,9 +18,10 @@ from __future__ import annotations
 import ctypes
 import os
 
-from . import build as _build
 
-LIB_PATH = _build.LIB
+# the library build.py writes (build.LIB; not imported here, so that
+# `python -m row_wise_rmsnorm_gb300.build` runs a module nothing has imported yet)
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libmt_norm.so")
 
 MT_OK, MT_ERR_INVALID_ARG, MT_ERR_UNSUPPORTED, MT_ERR_CUDA = 0, 1, 2, 3
 MT_OP_RMSNORM, MT_OP_LAYERNORM, MT_OP_ADD_RMSNORM = 0, 1, 2

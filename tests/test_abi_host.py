@@ -35,6 +35,10 @@ def declared_functions():
                                  re.M)))
 
 
+def test_binding_loads_the_library_the_build_writes():
+    assert mt.library_path() == mtbuild.LIB
+
+
 def test_header_is_plain_c():
     subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-fsyntax-only", "-x", "c", HEADER],
                    check=True)
